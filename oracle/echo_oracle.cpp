@@ -1,0 +1,379 @@
+// echo_oracle.cpp -- TEST INFRASTRUCTURE ONLY.
+//
+// A plain, slow, single-threaded CPU restatement of the per-call arithmetic of
+// Echo, the error-compensated 4-bit tensor-parallel all-reduce described in
+// "Echo: Error-Compensated 4-Bit Tensor-Parallel Communication for LLM Training
+// and Inference" (arXiv 2610.14277) and in the article "Your All-Reduce Is 4x
+// Overpriced: Echo's 4-Bit Error-Feedback Trick for Tensor-Parallel Training".
+//
+// It exists so that the GPU library can be checked against something obviously
+// correct.  Only the test suite, the smoke check and the bench's CPU-baseline
+// leg load it.  It shares no source, header, table or helper with the GPU
+// library, and it never reads anything the GPU library produced.
+//
+// Numerics: every floating-point step is a single IEEE-754 binary32 operation
+// rounded to nearest-even.  The file is compiled with -O2 -ffp-contract=off so
+// that no multiply and add are fused.  Conversions to binary16 and bfloat16 are
+// written below from the definitions of those formats, not taken from a library.
+//
+// Where the pages leave a step open, the reading taken here is stated at the
+// step (the quantizer formula itself, "Eqn. (8)" in the paper's appendix, is not
+// printed on the pages):
+//   * quantizer: zero-aware asymmetric min/max quantizer with an integer zero
+//     point; the range [lo, hi] is widened to contain 0 so that 0 is encoded
+//     exactly (Table 8 row "zero-aware asymmetric, g=128", against the ablation
+//     rows "naive zero-point" and "symmetric grid");
+//   * per-group parameters in half precision: an fp16 scale and an fp16 zero
+//     point, 4 bytes per group (article, section "The cancellation rule": 4-bit
+//     integers with half-precision quantization parameters per group);
+//   * the scale is rounded toward +infinity to fp16, so that no code is clamped
+//     by more than half a step; an all-zero group gets scale 1;
+//   * codes are rint (half-to-even) of v/s plus the zero point, clamped to
+//     [0, 2^b - 1];
+//   * owner segments are contiguous: rank o owns elements [o*m, (o+1)*m) with
+//     m = n/P; groups are consecutive runs of g elements inside a segment, the
+//     last one shorter when g does not divide m (Fig. 2(a), Fig. 4);
+//   * the owner's high-precision sum is an fp32 sum in ascending rank order,
+//     starting from rank 0's term (Fig. 2(a): "sums them ... in high precision");
+//   * compensator: full error feedback, each error held where it is revealed.
+//     A sender keeps, for each element it quantized for the push, the stage-1
+//     error v - deq(q); the owner keeps, for each element of its segment, the
+//     stage-2 error sum - bf16 output.  The next call adds the held error to the
+//     input before quantizing (the "entry pass"); the update itself does not
+//     change the values computed by the call (article, "The cancellation rule";
+//     paper abstract: "the summation reveals each injected error, and Echo feeds
+//     it back into later calls").
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <vector>
+
+namespace {
+
+uint32_t f32_bits(float x) {
+  uint32_t u;
+  std::memcpy(&u, &x, 4);
+  return u;
+}
+
+float bits_f32(uint32_t u) {
+  float x;
+  std::memcpy(&x, &u, 4);
+  return x;
+}
+
+}  // namespace
+
+extern "C" {
+
+// ---------------------------------------------------------------------------
+// Number formats.
+// ---------------------------------------------------------------------------
+
+// IEEE 754 binary16 -> binary32 (exact).
+float oracle_f16_to_f32(uint16_t h) {
+  const int sign = (h >> 15) & 1;
+  const int ex = (h >> 10) & 0x1F;
+  const int man = h & 0x3FF;
+  float mag;
+  if (ex == 0) {
+    mag = std::ldexp((float)man, -24);                 // subnormal: man * 2^-24
+  } else if (ex == 31) {
+    mag = man ? NAN : INFINITY;
+  } else {
+    mag = std::ldexp((float)(1024 + man), ex - 25);    // (1.man) * 2^(ex-15)
+  }
+  return sign ? -mag : mag;
+}
+
+// binary32 -> binary16, rounding toward +infinity.
+// The magnitude is first truncated to the binary16 grid, remembering whether
+// any bits were dropped; a positive inexact value then moves one binary16 step
+// up, a negative one keeps the truncated magnitude (which is the larger value).
+uint16_t oracle_f32_to_f16_ru(float x) {
+  const uint32_t u = f32_bits(x);
+  const uint16_t sign = (uint16_t)((u >> 16) & 0x8000);
+  const uint32_t a = u & 0x7FFFFFFF;
+  const int ex32 = (int)(a >> 23);
+  const uint32_t man32 = a & 0x7FFFFF;
+  if (ex32 == 0xFF) {                          // inf or NaN
+    return (uint16_t)(sign | (man32 ? 0x7E00 : 0x7C00));
+  }
+  uint16_t trunc;   // binary16 magnitude bits, rounded toward zero
+  bool inexact;
+  if (ex32 == 0) {                             // binary32 zero or subnormal: below 2^-126
+    trunc = 0;
+    inexact = man32 != 0;
+  } else {
+    const int e = ex32 - 127;                  // unbiased exponent
+    const uint32_t M = (1u << 23) | man32;     // 24-bit significand, value M * 2^(e-23)
+    if (e > 15) {                              // at least 2^16: beyond the largest finite
+      trunc = 0x7BFF;                          // 65504
+      inexact = true;
+    } else if (e >= -14) {                     // binary16 normal range
+      trunc = (uint16_t)(((e + 15) << 10) | (man32 >> 13));
+      inexact = (man32 & 0x1FFF) != 0;
+    } else {                                   // binary16 subnormal: units of 2^-24
+      const int shift = -(e + 1);              // value / 2^-24 = M * 2^(e+1)
+      if (shift >= 32) {
+        trunc = 0;
+        inexact = true;
+      } else {
+        trunc = (uint16_t)(M >> shift);
+        inexact = (M & ((1u << shift) - 1)) != 0;
+      }
+    }
+  }
+  if (sign) {
+    return (uint16_t)(sign | trunc);           // toward +inf = toward zero for negatives
+  }
+  return (uint16_t)(trunc + (inexact ? 1 : 0));  // 0x7BFF + 1 carries into +inf
+}
+
+float oracle_bf16_to_f32(uint16_t b) { return bits_f32((uint32_t)b << 16); }
+
+// binary32 -> bfloat16, round to nearest, ties to even.
+uint16_t oracle_f32_to_bf16_rn(float x) {
+  const uint32_t u = f32_bits(x);
+  if ((u & 0x7FFFFFFF) > 0x7F800000) {         // NaN: keep sign, force quiet
+    return (uint16_t)((u >> 16) | 0x0040);
+  }
+  const uint32_t kept_lsb = (u >> 16) & 1;
+  return (uint16_t)((u + 0x7FFF + kept_lsb) >> 16);
+}
+
+// Element-wise array forms of the conversions above.
+void oracle_f32_to_f16_ru_n(const float* x, int64_t count, uint16_t* out) {
+  for (int64_t i = 0; i < count; ++i) out[i] = oracle_f32_to_f16_ru(x[i]);
+}
+
+void oracle_f16_to_f32_n(const uint16_t* h, int64_t count, float* out) {
+  for (int64_t i = 0; i < count; ++i) out[i] = oracle_f16_to_f32(h[i]);
+}
+
+void oracle_f32_to_bf16_rn_n(const float* x, int64_t count, uint16_t* out) {
+  for (int64_t i = 0; i < count; ++i) out[i] = oracle_f32_to_bf16_rn(x[i]);
+}
+
+// ---------------------------------------------------------------------------
+// The quantizer Q_b on one group of `len` fp32 values.
+//
+// Returns 1 when the group holds a non-finite value or its scale does not fit
+// fp16 (the results are then unspecified), else 0.  Writes the codes q[i] in
+// [0, 2^b-1], the fp16 scale bits and the fp16 zero-point bits.
+// ---------------------------------------------------------------------------
+int oracle_quantize_group(const float* v, int len, int bits, uint8_t* q,
+                          uint16_t* s_bits, uint16_t* z_bits,
+                          int64_t* ties) {
+  const int L = (1 << bits) - 1;
+  const float Lf = (float)L;
+  int bad = 0;
+
+  // Step 1: the zero-aware range always contains 0.
+  float lo = 0.0f, hi = 0.0f;
+  for (int i = 0; i < len; ++i) {
+    if (!std::isfinite(v[i])) bad = 1;
+    lo = std::fmin(lo, v[i]);
+    hi = std::fmax(hi, v[i]);
+  }
+
+  // Steps 2-3: step size, rounded up to fp16; an all-zero group gets 1.
+  const float s32 = (hi - lo) / Lf;
+  uint16_t sb = oracle_f32_to_f16_ru(s32);
+  float s = oracle_f16_to_f32(sb);
+  if (s == 0.0f) {
+    sb = 0x3C00;
+    s = 1.0f;
+  }
+  if (!std::isfinite(s)) bad = 1;
+
+  // Step 4: integer zero point, the code that decodes to exactly 0.
+  float zf = std::rint(-lo / s);
+  zf = std::fmin(std::fmax(zf, 0.0f), Lf);
+  const int z = (int)zf;
+
+  // Step 5: codes.
+  for (int i = 0; i < len; ++i) {
+    const float r = v[i] / s;
+    if (ties && std::isfinite(r) && (r - std::floor(r)) == 0.5f) ++*ties;
+    float c = std::rint(r) + (float)z;
+    c = std::fmin(std::fmax(c, 0.0f), Lf);
+    q[i] = (uint8_t)(int)c;
+  }
+  *s_bits = sb;
+  *z_bits = oracle_f32_to_f16_ru((float)z);    // exact: a small integer
+  return bad;
+}
+
+// Step 6: deq(q) = s * (q - z): integer difference, exact conversion, one multiply.
+void oracle_dequantize_group(const uint8_t* q, int len, uint16_t s_bits,
+                             uint16_t z_bits, float* out) {
+  const float s = oracle_f16_to_f32(s_bits);
+  const int z = (int)oracle_f16_to_f32(z_bits);
+  for (int i = 0; i < len; ++i) out[i] = (float)((int)q[i] - z) * s;
+}
+
+// Wire packing of codes.  b=4: element 2i in the low nibble of byte i, element
+// 2i+1 in its high nibble (an odd count leaves the last high nibble 0).  b=8:
+// one byte per element.
+void oracle_pack_codes(const uint8_t* q, int64_t count, int bits, uint8_t* out) {
+  if (bits == 8) {
+    for (int64_t i = 0; i < count; ++i) out[i] = q[i];
+    return;
+  }
+  for (int64_t i = 0; i < (count + 1) / 2; ++i) {
+    const uint8_t lo = q[2 * i] & 0xF;
+    const uint8_t hi = (2 * i + 1 < count) ? (q[2 * i + 1] & 0xF) : 0;
+    out[i] = (uint8_t)(lo | (hi << 4));
+  }
+}
+
+// ---------------------------------------------------------------------------
+// One group position: the same `len` elements of all P ranks, in the segment
+// owned by rank `o`.  Group positions are independent of one another, so a
+// whole call is this function applied to every position (oracle_allreduce),
+// and a sample of positions can be checked on its own.
+//
+//   x      [P][len]  bf16 bits of each rank's input
+//   e      [P][len]  compensator state (updated in place), or NULL for an
+//                    uncompensated call (no state is read or written)
+//   y      [len]     bf16 bits of the value every rank receives
+//   q1     [P][len]  stage-1 codes of each sender (row o untouched), or NULL
+//   m1     [P]       stage-1 meta (fp16 s | fp16 z << 16) per sender, or NULL
+//   q2     [len]     stage-2 codes, or NULL;  m2 [1] stage-2 meta, or NULL
+//   acc    [len]     the owner's fp32 sum, or NULL
+//   nq     [P][len]  number of quantizations each rank's contribution went
+//                    through before reaching y, or NULL
+//   ties   counter of exact rounding ties (v/s exactly k + 1/2), or NULL
+// Returns the number of quantizations flagged non-finite (0 when all is fine).
+// ---------------------------------------------------------------------------
+int oracle_group_position(int P, int o, int len, int bits, const uint16_t* x,
+                          float* e, uint16_t* y, uint8_t* q1, uint32_t* m1,
+                          uint8_t* q2, uint32_t* m2, float* acc_out,
+                          uint8_t* nq, int64_t* ties) {
+  int bad = 0;
+  std::vector<float> v(len), d((size_t)P * len), acc(len);
+  std::vector<uint8_t> q(len);
+  uint16_t sb, zb;
+  if (nq) std::memset(nq, 0, (size_t)P * len);
+
+  // Fig. 2(a), push: every rank other than the owner quantizes its copy of the
+  // segment.  The entry pass first adds the error that rank holds.
+  for (int p = 0; p < P; ++p) {
+    if (p == o) continue;
+    const uint16_t* xp = x + (size_t)p * len;
+    float* ep = e ? e + (size_t)p * len : nullptr;
+    for (int i = 0; i < len; ++i) {
+      v[i] = ep ? oracle_bf16_to_f32(xp[i]) + ep[i] : oracle_bf16_to_f32(xp[i]);
+    }
+    bad += oracle_quantize_group(v.data(), len, bits, q.data(), &sb, &zb, ties);
+    float* dp = d.data() + (size_t)p * len;
+    oracle_dequantize_group(q.data(), len, sb, zb, dp);
+    if (q1) std::memcpy(q1 + (size_t)p * len, q.data(), len);
+    if (m1) m1[p] = (uint32_t)sb | ((uint32_t)zb << 16);
+    if (nq) for (int i = 0; i < len; ++i) nq[(size_t)p * len + i] += 1;
+    // The push reveals this rank's stage-1 error; the rank keeps it.
+    if (ep) for (int i = 0; i < len; ++i) ep[i] = v[i] - dp[i];
+  }
+
+  // The owner's own copy is not quantized; its entry pass adds its held error.
+  {
+    const uint16_t* xo = x + (size_t)o * len;
+    const float* eo = e ? e + (size_t)o * len : nullptr;
+    float* dst = d.data() + (size_t)o * len;
+    for (int i = 0; i < len; ++i) {
+      dst[i] = eo ? oracle_bf16_to_f32(xo[i]) + eo[i] : oracle_bf16_to_f32(xo[i]);
+    }
+  }
+
+  // Reduce: fp32 sum in ascending rank order, starting from rank 0's term.
+  for (int i = 0; i < len; ++i) {
+    float a = d[i];
+    for (int p = 1; p < P; ++p) a = a + d[(size_t)p * len + i];
+    acc[i] = a;
+  }
+
+  // Gather: the sum is quantized once; every rank decodes the same code.
+  bad += oracle_quantize_group(acc.data(), len, bits, q.data(), &sb, &zb, ties);
+  oracle_dequantize_group(q.data(), len, sb, zb, v.data());
+  for (int i = 0; i < len; ++i) y[i] = oracle_f32_to_bf16_rn(v[i]);
+  if (q2) std::memcpy(q2, q.data(), len);
+  if (m2) m2[0] = (uint32_t)sb | ((uint32_t)zb << 16);
+  if (nq) for (size_t k = 0; k < (size_t)P * len; ++k) nq[k] += 1;
+  if (acc_out) std::memcpy(acc_out, acc.data(), sizeof(float) * len);
+
+  // The owner keeps the stage-2 error, measured against what ranks receive.
+  if (e) {
+    float* eo = e + (size_t)o * len;
+    for (int i = 0; i < len; ++i) eo[i] = acc[i] - oracle_bf16_to_f32(y[i]);
+  }
+  return bad;
+}
+
+// ---------------------------------------------------------------------------
+// One whole call over P ranks of n elements each (n a multiple of P; g need
+// not divide m = n/P, the last group of a segment is then shorter).
+//
+//   x    [P][n] bf16 bits;  out [P][n] bf16 bits (every row equal)
+//   e    [P][n] fp32 state, updated in place, or NULL (uncompensated)
+//   q1   [P][n]        stage-1 code of element i sent by rank p (own segment
+//                      entries 0), or NULL
+//   m1   [P][P][Gs]    stage-1 meta of rank p for group j of segment o
+//                      (entries with p == o are 0), or NULL; Gs = ceil(m/g)
+//   q2   [n]           stage-2 codes, or NULL;  m2 [P][Gs] stage-2 meta, or NULL
+//   acc  [n]           the owners' fp32 sums, or NULL
+//   nq   [P][n]        quantization counts, or NULL
+//   ties               exact-tie counter, or NULL
+// Returns the number of flagged quantizations, or -1 for invalid arguments.
+// ---------------------------------------------------------------------------
+int64_t oracle_allreduce(int P, int64_t n, int g, int bits, const uint16_t* x,
+                         uint16_t* out, float* e, uint8_t* q1, uint32_t* m1,
+                         uint8_t* q2, uint32_t* m2, float* acc, uint8_t* nq,
+                         int64_t* ties) {
+  if (P < 1 || n < 0 || g < 1 || (bits != 4 && bits != 8) || n % P != 0) return -1;
+  const int64_t m = n / P;
+  const int64_t Gs = (m + g - 1) / g;
+  if (q1) std::memset(q1, 0, (size_t)(P * n));
+  if (m1) std::memset(m1, 0, sizeof(uint32_t) * (size_t)(P * P * Gs));
+
+  std::vector<uint16_t> xg((size_t)P * g), yg(g);
+  std::vector<float> eg((size_t)P * g), accg(g);
+  std::vector<uint8_t> q1g((size_t)P * g), q2g(g), nqg((size_t)P * g);
+  std::vector<uint32_t> m1g(P);
+  int64_t bad = 0;
+
+  for (int o = 0; o < P; ++o) {
+    for (int64_t j = 0; j < Gs; ++j) {
+      const int64_t start = o * m + j * g;
+      const int len = (int)std::min<int64_t>(g, m - j * g);
+      for (int p = 0; p < P; ++p) {
+        for (int i = 0; i < len; ++i) {
+          xg[(size_t)p * len + i] = x[p * n + start + i];
+          if (e) eg[(size_t)p * len + i] = e[p * n + start + i];
+        }
+      }
+      uint32_t m2g = 0;
+      bad += oracle_group_position(P, o, len, bits, xg.data(), e ? eg.data() : nullptr,
+                                   yg.data(), q1g.data(), m1g.data(), q2g.data(), &m2g,
+                                   accg.data(), nqg.data(), ties);
+      for (int p = 0; p < P; ++p) {
+        for (int i = 0; i < len; ++i) {
+          out[p * n + start + i] = yg[i];
+          if (e) e[p * n + start + i] = eg[(size_t)p * len + i];
+          if (nq) nq[p * n + start + i] = nqg[(size_t)p * len + i];
+          if (q1 && p != o) q1[p * n + start + i] = q1g[(size_t)p * len + i];
+        }
+        if (m1 && p != o) m1[((int64_t)p * P + o) * Gs + j] = m1g[p];
+      }
+      for (int i = 0; i < len; ++i) {
+        if (q2) q2[start + i] = q2g[i];
+        if (acc) acc[start + i] = accg[i];
+      }
+      if (m2) m2[o * Gs + j] = m2g;
+    }
+  }
+  return bad;
+}
+
+}  // extern "C"
