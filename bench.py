@@ -1,0 +1,555 @@
+#!/usr/bin/env python
+"""Throughput of the Echo emulated all-reduce on one GB300.
+
+Metric: bf16-input GB/s per emulated all-reduce call (P ranks x n bf16
+elements per call / time per call), with the fraction of the HBM roofline.
+
+A step is one pass of the whole hot path over the workload's call sequence:
+for the default workload (P=4, 2048 x 4096 per rank, per-channel LogNormal
+scales with 1% x20 outlier channels) that is 64 compensated calls (32 layers x
+attention+MLP sites), each on its own inputs, all resident in HBM before the
+timed region.  Every call runs the push, reduce and gather kernels of
+libecho.so through its C ABI.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+With --gpus N > 1 (one process per GPU under torchrun) every rank runs an
+independent replica of the workload on its own GPU (the emulated all-reduce
+has no cross-GPU exchange); the value is the work of all ranks over the
+slowest rank's time.  `--impl reference` times the CPU oracle (the plain
+single-threaded restatement the GPU path is checked against) on the host
+cores, on a sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "bf16-input GB/s per emulated all-reduce call; % of GB300 HBM roofline"
+G = 128
+FALLBACK_HBM_GBS = 6800.0
+SPEC_HBM_GBS = 7900.0
+L2_BYTES = 126 * 2 ** 20
+
+
+# ------------------------------------------------------------- byte model ----
+
+def code_bytes_per_elem(bits: int) -> float:
+    """Codes plus the 4-byte meta word of each 128-element group."""
+    return bits / 8 + 4 / G
+
+
+def kernel_bytes(P: int, n: int, bits: int, compensated: bool, fused: bool) -> dict:
+    """Algorithmic bytes each kernel must move per call (one call = P ranks x n).
+
+    push:   reads the non-owned bf16 input, reads+writes its fp32 state, writes
+            codes + meta:                  (P-1) n (2 + 8 + c)
+    reduce: reads P-1 code tiles + meta, the owner's bf16 input and state
+            (read+write), writes gather codes + meta:
+                                           (P-1) n c + n (2 + 8 + c)
+            (+ 2 P n when it also writes the P outputs)
+    gather: reads gather codes + meta, writes P bf16 outputs:  n c + 2 P n
+    The state terms (8 B per element) drop out when uncompensated."""
+    c = code_bytes_per_elem(bits)
+    st = 8 if compensated else 0
+    d = {"push": (P - 1) * n * (2 + st + c),
+         "reduce": (P - 1) * n * c + n * (2 + st + c) + (2 * P * n if fused else 0)}
+    if not fused:
+        d["gather"] = n * c + 2 * P * n
+    if P == 1:
+        d["push"] = 0
+    return d
+
+
+def call_model_bytes(P, n, bits, compensated, fused):
+    return sum(kernel_bytes(P, n, bits, compensated, fused).values())
+
+
+# ---------------------------------------------------------------- helpers ----
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return float(pk["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs)"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback 6.8 TB/s (MEASURED_PEAKS.json absent)"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "bit_error_compensated_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, or None
+    when there is none or the kernel sources changed since it was taken."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except Exception:
+        return None
+    ent = rec.get(workload, {}).get(kernel)
+    if not ent or ent.get("source_hash") != kernel_source_hash():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.lines = []
+        try:
+            import torch
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            sel = ["-i", uuid if uuid.startswith("GPU-") else "GPU-" + uuid]
+        except Exception:
+            sel = []
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200", *sel], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if world <= 1:
+        return 0, 0, 1
+    import torch
+    import torch.distributed as dist
+    rank = int(os.environ["RANK"])
+    local = int(os.environ.get("LOCAL_RANK", rank))
+    backend = "nccl" if torch.cuda.is_available() else "gloo"
+    if backend == "nccl":
+        torch.cuda.set_device(local)
+    dist.init_process_group(backend)
+    return rank, local, world
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(value: float, world: int) -> float:
+    """The largest `value` over all ranks (the slowest rank's time)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(bytes_per_rank_per_step: float, steps: int, world: int, max_ms: float) -> float:
+    """Work of all ranks over the slowest rank's time, in GB/s."""
+    return bytes_per_rank_per_step * steps * world / (max_ms / 1e3) / 1e9
+
+
+# ------------------------------------------------------------- our arm -------
+
+def build_inputs(number, seq, distinct, device):
+    import torch
+    from bit_error_compensated_gb300.workloads import WORKLOADS, rank_inputs
+    w = WORKLOADS[number]
+    xs = torch.empty((distinct, w.P, w.n), dtype=torch.bfloat16, device=device)
+    for k in range(distinct):
+        rank_inputs(number, seq[k], device, out=xs[k])
+    return xs
+
+
+def run_ours(args, rank, local, world):
+    import torch
+    from bit_error_compensated_gb300 import echo
+    from bit_error_compensated_gb300.workloads import WORKLOADS, call_sequence
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+    number, bits, fused = args.workload, args.bits, args.fused
+    w = WORKLOADS[number]
+    P, n = w.P, w.n
+    seq = call_sequence(number, steps=1)
+    calls = len(seq)
+    xs = build_inputs(number, seq, calls, dev)
+    out = torch.empty((P, n), dtype=torch.bfloat16, device=dev)
+    plan = echo.echo_plan(P, n, G, bits)
+    echo.echo_set_fused(plan, fused)
+    states = {"fwd": echo.COMP_DEFAULT,
+              "bwd": torch.zeros((P, n), dtype=torch.float32, device=dev) if any(
+                  c.state == "bwd" for c in seq) else None,
+              "none": None}
+    out_rows = list(out)
+    call_args = [(list(xs[k]), states[c.state]) for k, c in enumerate(seq)]
+
+    def step():
+        for ins, comp in call_args:
+            echo.echo_allreduce(plan, ins, out_rows, comp, stream)
+
+    launches_per_call = (2 if fused else 3) - (1 if P == 1 else 0)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    if echo.echo_get_status(plan, stream) != 0:
+        raise RuntimeError("device status word set during warm-up")
+
+    # Timed region: K steps, CUDA events on the launching stream.
+    clocks = ClockSampler(local)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(args.steps):
+        step()
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    clk = clocks.stop()
+    ms = t0.elapsed_time(t1)
+    max_ms = max_over_ranks(ms, world)
+
+    bytes_in_per_call = P * n * 2
+    value = whole_job_gbs(bytes_in_per_call * calls, args.steps, world, max_ms)
+    per_call_s = max_ms / 1e3 / (args.steps * calls)
+    compensated_calls = sum(1 for c in seq if c.state != "none")
+    model = (compensated_calls * call_model_bytes(P, n, bits, True, fused) +
+             (calls - compensated_calls) * call_model_bytes(P, n, bits, False, fused)) / calls
+    hbm, hbm_src = load_peaks()
+
+    # Per-kernel durations: the same K steps again, with events around each
+    # kernel of every call (this makes each launch stream-serialised).
+    per_kernel_ms = {"push": 0.0, "reduce": 0.0, "gather": 0.0}
+    ev_sets = []
+    torch.cuda.synchronize(dev)
+    for _ in range(args.steps):
+        for ins, comp in call_args:
+            evs = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+            for e in evs:
+                e.record(stream)
+            echo.echo_set_timing(plan, evs)
+            echo.echo_allreduce(plan, ins, out_rows, comp, stream)
+            ev_sets.append(evs)
+    echo.echo_set_timing(plan, None)
+    torch.cuda.synchronize(dev)
+    for evs in ev_sets:
+        per_kernel_ms["push"] += evs[0].elapsed_time(evs[1])
+        per_kernel_ms["reduce"] += evs[1].elapsed_time(evs[2])
+        per_kernel_ms["gather"] += evs[2].elapsed_time(evs[3])
+    nlaunch = len(ev_sets)
+    kb_comp = kernel_bytes(P, n, bits, True, fused)
+    kb_unc = kernel_bytes(P, n, bits, False, fused)
+    ran = [k for k in ("push", "reduce", "gather") if k in kb_comp and (k != "push" or P > 1)]
+    avg_us = {k: per_kernel_ms[k] / nlaunch * 1e3 for k in ran}
+    dominant = max(avg_us, key=lambda k: avg_us[k])
+    kbytes = (compensated_calls * kb_comp[dominant] + (calls - compensated_calls) * kb_unc[dominant]) / calls
+    achieved = kbytes / (avg_us[dominant] / 1e6) / 1e9
+    kname = {"push": "push_kernel", "reduce": "reduce_kernel", "gather": "gather_kernel"}[dominant]
+    traffic = profiled_traffic(kname, w.name)
+    roofline = {"bound": "hbm", "kernel": kname, "achieved": round(achieved, 1), "peak": hbm,
+                "unit": "GB/s", "frac": round(achieved / hbm, 4), "traffic": traffic,
+                "algorithmic_bytes_per_launch": int(kbytes), "avg_launch_us": round(avg_us[dominant], 2),
+                "peak_source": hbm_src}
+
+    result = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(max_ms / args.steps, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded; shapes and distributions of the workload, no dataset)",
+        "config": {"workload": w.name, "P": P, "n_per_rank": n, "bits": bits, "g": G,
+                   "calls_per_step": calls, "compensated": compensated_calls == calls,
+                   "fused_gather": bool(fused), "io": "bf16 in/out, fp32 arithmetic, "
+                   f"{bits}-bit codes, fp32 state",
+                   "l2": f"inputs distinct per call ({calls} x {P * n * 2 >> 20} MiB resident); "
+                         f"per-call working set {(P * n * (2 + 2 + 8)) >> 20} MiB > L2",
+                   "parallelism": f"replicas x{world}" if world > 1 else "1 GPU, P ranks emulated"},
+        "hbm_roofline_frac": round(model / per_call_s / 1e9 / hbm, 4),
+        "hbm_roofline_frac_spec": round(model / per_call_s / 1e9 / SPEC_HBM_GBS, 4),
+        "model_bytes_per_call": int(model),
+        "us_per_call": round(per_call_s * 1e6, 2),
+        "per_kernel_us": {k: round(v, 2) for k, v in avg_us.items()},
+        "roofline": roofline,
+        "gpu_launches": launches_per_call * calls * args.steps,
+        "clocks": clk,
+    }
+
+    if not args.no_e2e:
+        result["e2e"] = run_e2e(args, echo, plan, xs, seq, states, dev, world)
+    if args.also:
+        result["also"] = {}
+        for num in [int(v) for v in args.also.split(",") if v]:
+            result["also"][WORKLOADS[num].name] = time_other(echo, num, bits, fused, dev)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline_oracle(number, bits, budget_s=args.cpu_budget)
+    del plan
+    return result
+
+
+def run_e2e(args, echo, plan, xs, seq, states, dev, world):
+    """The same call sequence from pinned host memory: every call copies its
+    inputs host->device and its result (the reduced tensor, identical on every
+    rank) device->host inside the timed region.  Copies run on their own
+    streams, double-buffered, so the copy of call k+1 overlaps call k."""
+    import torch
+    P, n = xs.shape[1], xs.shape[2]
+    distinct = min(8, xs.shape[0])
+    host_in = [xs[k].cpu().pin_memory() for k in range(distinct)]
+    host_out = torch.empty((2, n), dtype=torch.bfloat16).pin_memory()
+    dev_in = [torch.empty((P, n), dtype=torch.bfloat16, device=dev) for _ in range(2)]
+    dev_out = [torch.empty((P, n), dtype=torch.bfloat16, device=dev) for _ in range(2)]
+    s_comp = torch.cuda.current_stream(dev)
+    s_h2d = torch.cuda.Stream(dev)
+    s_d2h = torch.cuda.Stream(dev)
+    ev_loaded = [torch.cuda.Event() for _ in range(2)]
+    ev_done = [torch.cuda.Event() for _ in range(2)]
+    ev_read = [torch.cuda.Event() for _ in range(2)]
+    calls = len(seq)
+    comps = [states[c.state] for c in seq]
+
+    def step(first):
+        for k in range(calls):
+            b = k & 1
+            with torch.cuda.stream(s_h2d):
+                if not (first and k < 2):
+                    s_h2d.wait_event(ev_done[b])          # dev_in[b] no longer read
+                dev_in[b].copy_(host_in[k % distinct], non_blocking=True)
+                ev_loaded[b].record(s_h2d)
+            s_comp.wait_event(ev_loaded[b])
+            if not (first and k < 2):
+                s_comp.wait_event(ev_read[b])             # dev_out[b] copied out
+            echo.echo_allreduce(plan, list(dev_in[b]), list(dev_out[b]), comps[k], s_comp)
+            ev_done[b].record(s_comp)
+            with torch.cuda.stream(s_d2h):
+                s_d2h.wait_event(ev_done[b])
+                host_out[b].copy_(dev_out[b][0], non_blocking=True)
+                ev_read[b].record(s_d2h)
+
+    for i in range(max(1, args.warmup)):
+        step(i == 0)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        step(False)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    wall_ms = (time.perf_counter() - t) * 1e3
+    max_ms = max_over_ranks(wall_ms, world)
+    v = whole_job_gbs(P * n * 2 * calls, args.steps, world, max_ms)
+    return {"value": round(v, 2), "unit": "GB/s", "h2d_bytes_per_step": P * n * 2 * calls,
+            "d2h_bytes_per_step": n * 2 * calls, "ms_per_step": round(max_ms / args.steps, 3),
+            "timing": "host wall clock around K steps, synchronized at both ends",
+            "host_inputs": f"{distinct} distinct pinned input sets cycled over the {calls} calls"}
+
+
+def time_other(echo, number, bits, fused, dev, reps=3):
+    """Time another workload's call sequence (8 distinct inputs cycled): GB/s
+    and the pipeline's fraction of the HBM roofline.  No parity here: the
+    GPU tests check these workloads against the oracle."""
+    import torch
+    from bit_error_compensated_gb300.workloads import WORKLOADS, call_sequence
+    w = WORKLOADS[number]
+    seq = call_sequence(number, steps=1)
+    distinct = min(8, len(seq))
+    xs = build_inputs(number, seq, distinct, dev)
+    out = torch.empty((w.P, w.n), dtype=torch.bfloat16, device=dev)
+    plan = echo.echo_plan(w.P, w.n, G, bits)
+    echo.echo_set_fused(plan, fused)
+    bwd = torch.zeros((w.P, w.n), dtype=torch.float32, device=dev)
+    comps = [{"fwd": echo.COMP_DEFAULT, "bwd": bwd, "none": None}[c.state] for c in seq]
+    rows = [list(xs[k]) for k in range(distinct)]
+    out_rows = list(out)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        for k in range(len(seq)):
+            echo.echo_allreduce(plan, rows[k % distinct], out_rows, comps[k], stream)
+
+    step()
+    torch.cuda.synchronize(dev)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(reps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    per_call_s = a.elapsed_time(b) / 1e3 / (reps * len(seq))
+    hbm, _ = load_peaks()
+    comp_calls = sum(1 for c in seq if c.state != "none")
+    model = (comp_calls * call_model_bytes(w.P, w.n, bits, True, fused) +
+             (len(seq) - comp_calls) * call_model_bytes(w.P, w.n, bits, False, fused)) / len(seq)
+    del plan, xs
+    torch.cuda.empty_cache()
+    return {"gbs": round(w.P * w.n * 2 / per_call_s / 1e9, 2), "us_per_call": round(per_call_s * 1e6, 2),
+            "hbm_roofline_frac": round(model / per_call_s / 1e9 / hbm, 4), "calls": len(seq) * reps}
+
+
+# ------------------------------------------------------------- the oracle ----
+
+def cpu_baseline_oracle(number, bits, budget_s=12.0):
+    """The oracle as it stands, single-threaded on a host core, over the first
+    calls of the workload's sequence until about `budget_s` seconds of oracle
+    time have passed (input generation and copies are not timed)."""
+    import numpy as np
+    import torch
+    import oracle
+    from bit_error_compensated_gb300.workloads import WORKLOADS, call_sequence, rank_inputs
+    w = WORKLOADS[number]
+    seq = call_sequence(number, steps=1)
+    states = {}
+    spent, done = 0.0, 0
+    for c in seq:
+        x = rank_inputs(number, c, "cpu").view(torch.int16).numpy().view(np.uint16)
+        e = None if c.state == "none" else states.setdefault(c.state, np.zeros(x.shape, np.float32))
+        t = time.perf_counter()
+        oracle.allreduce(x, G, bits, e=e)
+        spent += time.perf_counter() - t
+        done += 1
+        if spent >= budget_s:
+            break
+    v = done * w.P * w.n * 2 / spent / 1e9
+    return {"value": round(v, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"first {done} of the {len(seq)} calls of {w.name}, whole tensors "
+                      f"({spent:.1f} s of single-threaded oracle time)"}
+
+
+def run_reference(args, rank, world):
+    """The oracle on the host cores: each step is one call of the workload's
+    sequence restricted to a fixed 1/8 sample of its group positions (exactly
+    the oracle's work on those positions), state carried across steps."""
+    import numpy as np
+    import torch
+    import oracle
+    from bit_error_compensated_gb300.workloads import WORKLOADS, call_sequence, rank_inputs
+    number, bits = args.workload, args.bits
+    w = WORKLOADS[number]
+    P, n = w.P, w.n
+    seq = call_sequence(number, steps=1)
+    Gs = n // P // G
+    rng = np.random.default_rng(number)
+    pos = np.sort(rng.choice(P * Gs, size=max(1, P * Gs // 8), replace=False))
+    owners = (pos // Gs).astype(np.int32)
+    idx = (pos[:, None] * G + np.arange(G)[None, :]).ravel()
+    e = np.zeros((pos.size, P, G), np.float32)
+    prepared = []
+    for k in range(min(len(seq), 4)):
+        x = rank_inputs(number, seq[k], "cpu").view(torch.int16).numpy().view(np.uint16)
+        prepared.append(np.ascontiguousarray(x[:, idx].reshape(P, pos.size, G).transpose(1, 0, 2)))
+
+    def step(i):
+        oracle.group_positions(P, owners, bits, prepared[i % len(prepared)], e)
+
+    for i in range(args.warmup):
+        step(i)
+    t = time.perf_counter()
+    for i in range(args.steps):
+        step(i)
+    sec = time.perf_counter() - t
+    bytes_per_step = pos.size * P * G * 2
+    v = bytes_per_step * args.steps / sec / 1e9
+    sample = (f"each step: one call of {w.name} on a fixed 1/8 sample of its group positions "
+              f"({pos.size} of {P * Gs}), 4 distinct inputs cycled, state carried")
+    return {"impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": "GB/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(sec / args.steps * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (seeded; shapes and distributions of the workload, no dataset)",
+            "config": {"workload": w.name, "P": P, "n_per_rank": n, "bits": bits, "g": G,
+                       "compensated": True},
+            "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+# ------------------------------------------------------------------- main ----
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", type=int, default=2, help="1..5 (default 2: P=4, 2048x4096, 64 calls)")
+    ap.add_argument("--bits", type=int, default=4, choices=[4, 8])
+    ap.add_argument("--fused", action="store_true", help="reduce kernel writes the outputs itself")
+    ap.add_argument("--also", default="4", help="other workloads to time, comma-separated ('' for none)")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3 and args.impl == "ours":
+        ap.error("--warmup must be at least 3")
+
+    rank, local, world = dist_setup()
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args, rank, world)), flush=True)
+        return 0
+    res = run_ours(args, rank, local, world)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,284 @@
+// echo_api.cu -- host side of libecho.so: plans, argument checks, launches.
+// The operation and every call's contract are described in include/echo.h.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+#include <new>
+
+#include "echo_internal.h"
+
+using echo::CallArgs;
+
+struct echo_plan_s {
+  int P = 0, g = 0, bits = 0, device = 0;
+  int64_t n = 0, m = 0, Gs = 0, Gs_pad = 0, CB = 0;
+  uint8_t* wire = nullptr;          // one allocation: push codes/meta, gather codes/meta
+  size_t wire_bytes = 0;
+  int64_t off[4] = {0, 0, 0, 0};
+  float* comp = nullptr;            // the plan's own compensator state
+  size_t comp_bytes = 0;
+  int* status = nullptr;            // device status word
+  cudaStream_t last_stream = nullptr;
+  int fused = 0;
+  cudaEvent_t ev[4] = {nullptr, nullptr, nullptr, nullptr};
+  int timing = 0;
+};
+
+namespace {
+
+thread_local cudaError_t g_last_cuda = cudaSuccess;
+
+int cuda_fail(cudaError_t e) {
+  g_last_cuda = e;
+  return ECHO_ERR_CUDA;
+}
+
+#define ECHO_CUDA(call)                              \
+  do {                                               \
+    cudaError_t e_ = (call);                         \
+    if (e_ != cudaSuccess) return cuda_fail(e_);     \
+  } while (0)
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+bool overlap(uintptr_t a, uintptr_t b, size_t bytes) {
+  return a < b + bytes && b < a + bytes;
+}
+
+int check_device(const echo_plan_s* plan) {
+  int dev = -1;
+  ECHO_CUDA(cudaGetDevice(&dev));
+  return dev == plan->device ? ECHO_OK : ECHO_ERR_ARG;
+}
+
+bool g_kernels_prepared[64] = {false};
+
+}  // namespace
+
+extern "C" {
+
+int echo_plan(int P, int64_t n, int g, int bits, echo_plan_t* out) {
+  if (out == nullptr) return ECHO_ERR_ARG;
+  *out = nullptr;
+  if (P < 1 || P > ECHO_MAX_RANKS || g < 1) return ECHO_ERR_ARG;
+  if (bits != 4 && bits != 8) return ECHO_ERR_UNSUPPORTED;
+  if (g != echo::kGroup) return ECHO_ERR_UNSUPPORTED;
+  if (n < 0 || n % ((int64_t)P * g) != 0) return ECHO_ERR_SHAPE;
+  if (n > ((int64_t)1 << 40)) return ECHO_ERR_SHAPE;
+
+  echo_plan_s* p = new (std::nothrow) echo_plan_s();
+  if (p == nullptr) return ECHO_ERR_ARG;
+  p->P = P;
+  p->g = g;
+  p->bits = bits;
+  p->n = n;
+  p->m = n / P;
+  p->Gs = p->m / g;
+  p->Gs_pad = (p->Gs + 3) / 4 * 4;
+  p->CB = (int64_t)g * bits / 8;
+
+  const size_t codes1 = (size_t)P * (P - 1) * p->Gs * p->CB;
+  const size_t meta1 = (size_t)P * (P - 1) * p->Gs_pad * 4;
+  const size_t codes2 = (size_t)P * p->Gs * p->CB;
+  const size_t meta2 = (size_t)P * p->Gs_pad * 4;
+  p->off[0] = 0;
+  p->off[1] = (int64_t)align_up(p->off[0] + codes1, 256);
+  p->off[2] = (int64_t)align_up(p->off[1] + meta1, 256);
+  p->off[3] = (int64_t)align_up(p->off[2] + codes2, 256);
+  p->wire_bytes = align_up(p->off[3] + meta2, 256);
+  p->comp_bytes = (size_t)P * n * sizeof(float);
+
+  cudaError_t e = cudaGetDevice(&p->device);
+  if (e == cudaSuccess && p->device >= 0 && p->device < 64 && !g_kernels_prepared[p->device]) {
+    e = echo::prepare_kernels();
+    if (e == cudaSuccess) g_kernels_prepared[p->device] = true;
+  }
+  if (e == cudaSuccess && p->wire_bytes > 0) e = cudaMalloc((void**)&p->wire, p->wire_bytes);
+  if (e == cudaSuccess && p->comp_bytes > 0) e = cudaMalloc((void**)&p->comp, p->comp_bytes);
+  if (e == cudaSuccess) e = cudaMalloc((void**)&p->status, sizeof(int));
+  if (e == cudaSuccess && p->wire_bytes > 0) e = cudaMemset(p->wire, 0, p->wire_bytes);
+  if (e == cudaSuccess && p->comp_bytes > 0) e = cudaMemset(p->comp, 0, p->comp_bytes);
+  if (e == cudaSuccess) e = cudaMemset(p->status, 0, sizeof(int));
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) {
+    echo_plan_destroy(p);
+    return cuda_fail(e);
+  }
+  *out = p;
+  return ECHO_OK;
+}
+
+int echo_allreduce(echo_plan_t plan, const void* const* in, void* const* out,
+                   void* comp_state, void* stream) {
+  if (plan == nullptr || in == nullptr || out == nullptr) return ECHO_ERR_ARG;
+  const int P = plan->P;
+  const size_t bytes = (size_t)plan->n * 2;
+  for (int p = 0; p < P; ++p) {
+    if (in[p] == nullptr || out[p] == nullptr) return ECHO_ERR_ARG;
+    if (!aligned16(in[p]) || !aligned16(out[p])) return ECHO_ERR_ALIGN;
+  }
+  float* comp = nullptr;
+  if (comp_state == ECHO_COMP_DEFAULT) {
+    comp = plan->comp;
+  } else if (comp_state != nullptr) {
+    if (!aligned16(comp_state)) return ECHO_ERR_ALIGN;
+    comp = static_cast<float*>(comp_state);
+  }
+  // Aliasing: out[p] may be in[p]; otherwise outputs overlap nothing, and the
+  // state overlaps no input or output.
+  for (int p = 0; p < P; ++p) {
+    const uintptr_t op = (uintptr_t)out[p];
+    for (int q = 0; q < P; ++q) {
+      const uintptr_t iq = (uintptr_t)in[q];
+      if (op == iq && p == q) continue;
+      if (overlap(op, iq, bytes)) return ECHO_ERR_ARG;
+      if (q != p && overlap(op, (uintptr_t)out[q], bytes)) return ECHO_ERR_ARG;
+    }
+    if (comp != nullptr && plan->comp_bytes > 0) {
+      const uintptr_t c = (uintptr_t)comp;
+      if (c < op + bytes && op < c + plan->comp_bytes) return ECHO_ERR_ARG;
+      if (c < (uintptr_t)in[p] + bytes && (uintptr_t)in[p] < c + plan->comp_bytes) return ECHO_ERR_ARG;
+    }
+  }
+  int rc = check_device(plan);
+  if (rc != ECHO_OK) return rc;
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  plan->last_stream = s;
+  if (plan->n == 0) return ECHO_OK;
+
+  CallArgs a;
+  std::memset(&a, 0, sizeof(a));
+  for (int p = 0; p < P; ++p) {
+    a.in[p] = static_cast<const __nv_bfloat16*>(in[p]);
+    a.out[p] = static_cast<__nv_bfloat16*>(out[p]);
+  }
+  a.comp = comp;
+  a.codes1 = plan->wire + plan->off[0];
+  a.meta1 = reinterpret_cast<uint32_t*>(plan->wire + plan->off[1]);
+  a.codes2 = plan->wire + plan->off[2];
+  a.meta2 = reinterpret_cast<uint32_t*>(plan->wire + plan->off[3]);
+  a.status = plan->status;
+  a.n = plan->n;
+  a.Gs = plan->Gs;
+  a.Gs_pad = plan->Gs_pad;
+  a.P = P;
+
+  // Programmatic dependent launch lets each kernel's blocks be scheduled while
+  // the previous kernel drains; every kernel waits (griddepcontrol.wait) before
+  // touching data the previous one wrote.  Timing events in between make each
+  // launch an ordinary stream-ordered one.
+  const bool pdl = plan->timing == 0;
+  if (plan->timing) ECHO_CUDA(cudaEventRecord(plan->ev[0], s));
+  if (P > 1) ECHO_CUDA(echo::launch_push(a, plan->bits, s, pdl));
+  if (plan->timing) ECHO_CUDA(cudaEventRecord(plan->ev[1], s));
+  ECHO_CUDA(echo::launch_reduce(a, plan->bits, plan->fused != 0, s, pdl));
+  if (plan->timing) ECHO_CUDA(cudaEventRecord(plan->ev[2], s));
+  if (!plan->fused) ECHO_CUDA(echo::launch_gather(a, plan->bits, s, pdl));
+  if (plan->timing) ECHO_CUDA(cudaEventRecord(plan->ev[3], s));
+  return ECHO_OK;
+}
+
+int echo_reset_comp(echo_plan_t plan) {
+  if (plan == nullptr) return ECHO_ERR_ARG;
+  return echo_reset_comp_async(plan, ECHO_COMP_DEFAULT, plan->last_stream);
+}
+
+int echo_reset_comp_async(echo_plan_t plan, void* comp_state, void* stream) {
+  if (plan == nullptr || comp_state == nullptr) return ECHO_ERR_ARG;
+  void* dst = comp_state == ECHO_COMP_DEFAULT ? (void*)plan->comp : comp_state;
+  if (plan->comp_bytes == 0) return ECHO_OK;
+  int rc = check_device(plan);
+  if (rc != ECHO_OK) return rc;
+  ECHO_CUDA(cudaMemsetAsync(dst, 0, plan->comp_bytes, static_cast<cudaStream_t>(stream)));
+  return ECHO_OK;
+}
+
+size_t echo_comp_bytes(echo_plan_t plan) { return plan ? plan->comp_bytes : 0; }
+
+size_t echo_wire_bytes(echo_plan_t plan) { return plan ? plan->wire_bytes : 0; }
+
+int echo_wire_layout(echo_plan_t plan, int64_t* desc) {
+  if (plan == nullptr || desc == nullptr) return ECHO_ERR_ARG;
+  for (int k = 0; k < 4; ++k) desc[k] = plan->off[k];
+  desc[4] = plan->Gs;
+  desc[5] = plan->Gs_pad;
+  desc[6] = plan->CB;
+  desc[7] = (int64_t)plan->wire_bytes;
+  return ECHO_OK;
+}
+
+int echo_get_status(echo_plan_t plan, void* stream, int* status) {
+  if (plan == nullptr || status == nullptr) return ECHO_ERR_ARG;
+  int rc = check_device(plan);
+  if (rc != ECHO_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int word = 0;
+  ECHO_CUDA(cudaMemcpyAsync(&word, plan->status, sizeof(int), cudaMemcpyDeviceToHost, s));
+  ECHO_CUDA(cudaMemsetAsync(plan->status, 0, sizeof(int), s));
+  ECHO_CUDA(cudaStreamSynchronize(s));
+  *status = (word & echo::kStatusTimeout) ? ECHO_ERR_TIMEOUT
+            : (word & echo::kStatusOverflow) ? ECHO_ERR_OVERFLOW : ECHO_OK;
+  return ECHO_OK;
+}
+
+int echo_debug_wire(echo_plan_t plan, void* host_dst, size_t bytes, void* stream) {
+  if (plan == nullptr || host_dst == nullptr) return ECHO_ERR_ARG;
+  if (bytes < plan->wire_bytes) return ECHO_ERR_ARG;
+  if (plan->wire_bytes == 0) return ECHO_OK;
+  int rc = check_device(plan);
+  if (rc != ECHO_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  ECHO_CUDA(cudaMemcpyAsync(host_dst, plan->wire, plan->wire_bytes, cudaMemcpyDeviceToHost, s));
+  ECHO_CUDA(cudaStreamSynchronize(s));
+  return ECHO_OK;
+}
+
+int echo_set_fused(echo_plan_t plan, int fused) {
+  if (plan == nullptr || (fused != 0 && fused != 1)) return ECHO_ERR_ARG;
+  plan->fused = fused;
+  return ECHO_OK;
+}
+
+int echo_set_timing(echo_plan_t plan, void* const* events, int count) {
+  if (plan == nullptr) return ECHO_ERR_ARG;
+  if (count == 0) {
+    plan->timing = 0;
+    return ECHO_OK;
+  }
+  if (count != 4 || events == nullptr) return ECHO_ERR_ARG;
+  for (int k = 0; k < 4; ++k) {
+    if (events[k] == nullptr) return ECHO_ERR_ARG;
+    plan->ev[k] = static_cast<cudaEvent_t>(events[k]);
+  }
+  plan->timing = 1;
+  return ECHO_OK;
+}
+
+void echo_plan_destroy(echo_plan_t plan) {
+  if (plan == nullptr) return;
+  if (plan->wire) cudaFree(plan->wire);
+  if (plan->comp) cudaFree(plan->comp);
+  if (plan->status) cudaFree(plan->status);
+  delete plan;
+}
+
+const char* echo_strerror(int status) {
+  switch (status) {
+    case ECHO_OK: return "ok";
+    case ECHO_ERR_ARG: return "invalid argument";
+    case ECHO_ERR_SHAPE: return "n must be a non-negative multiple of P*g";
+    case ECHO_ERR_UNSUPPORTED: return "unsupported configuration (bits must be 4 or 8, g must be 128)";
+    case ECHO_ERR_ALIGN: return "device pointer not 16-byte aligned";
+    case ECHO_ERR_CUDA: return cudaGetErrorString(g_last_cuda);
+    case ECHO_ERR_OVERFLOW: return "non-finite input or fp16 step overflow in some group";
+    case ECHO_ERR_TIMEOUT: return "a device-side wait gave up";
+    default: return "unknown status";
+  }
+}
+
+}  // extern "C"

@@ -1,0 +1,47 @@
+// echo_internal.h -- types shared by the host side of libecho.so and its
+// kernels.  Not part of the public ABI (include/echo.h is).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "../../include/echo.h"
+
+namespace echo {
+
+// Elements per quantization group on the GPU.
+constexpr int kGroup = 128;
+// Groups per reduce tile (one thread block of the reduce kernel).
+constexpr int kReduceTile = 32;
+// Threads per block of every kernel.
+constexpr int kThreads = 256;
+
+// Status-word bits written by the kernels (read by echo_get_status).
+constexpr int kStatusOverflow = 1;
+constexpr int kStatusTimeout = 2;
+
+// Everything a kernel needs about one call, passed by value.
+struct CallArgs {
+  const __nv_bfloat16* in[ECHO_MAX_RANKS];   // rank p's input, n elements
+  __nv_bfloat16* out[ECHO_MAX_RANKS];        // rank p's output, n elements
+  float* comp;         // [P][n] compensator state, or nullptr (uncompensated)
+  uint8_t* codes1;     // push codes  [P owners][P-1 senders][Gs][CB]
+  uint32_t* meta1;     // push meta   [P owners][P-1 senders][Gs_pad]
+  uint8_t* codes2;     // gather codes [P owners][Gs][CB]
+  uint32_t* meta2;     // gather meta  [P owners][Gs_pad]
+  int* status;         // device status word
+  int64_t n;           // elements per rank
+  int64_t Gs;          // groups per owner segment (m / 128)
+  int64_t Gs_pad;      // Gs rounded up to a multiple of 4
+  int P;
+};
+
+// Launchers (one translation unit each).  They return the launch error.
+cudaError_t launch_push(const CallArgs& a, int bits, cudaStream_t s, bool pdl);
+cudaError_t launch_reduce(const CallArgs& a, int bits, bool fused, cudaStream_t s, bool pdl);
+cudaError_t launch_gather(const CallArgs& a, int bits, cudaStream_t s, bool pdl);
+// One-time per-device set-up of kernel attributes (dynamic shared memory).
+cudaError_t prepare_kernels();
+
+}  // namespace echo

@@ -1,0 +1,183 @@
+"""ctypes binding of libecho.so (include/echo.h), with the same call names.
+
+Argument marshalling only: tensors become device pointers, torch streams become
+cudaStream_t handles, status codes become exceptions.  Every step of the
+all-reduce runs in the library's CUDA kernels; there is no fallback.  Importing
+this module raises if the library has not been built
+(``python -m bit_error_compensated_gb300.build``).
+"""
+from __future__ import annotations
+
+import ctypes
+from pathlib import Path
+
+_LIB_PATH = Path(__file__).resolve().parent / "lib" / "libecho.so"
+if not _LIB_PATH.exists():
+    raise ImportError(f"{_LIB_PATH} is missing: build it with "
+                      "`python -m bit_error_compensated_gb300.build` (needs nvcc)")
+_lib = ctypes.CDLL(str(_LIB_PATH))
+
+ECHO_OK = 0
+ECHO_ERR_ARG = 1
+ECHO_ERR_SHAPE = 2
+ECHO_ERR_UNSUPPORTED = 3
+ECHO_ERR_ALIGN = 4
+ECHO_ERR_CUDA = 5
+ECHO_ERR_OVERFLOW = 6
+ECHO_ERR_TIMEOUT = 7
+ECHO_MAX_RANKS = 16
+COMP_DEFAULT = ctypes.c_void_p(-1 & (2 ** 64 - 1))   # ECHO_COMP_DEFAULT
+
+_vp, _i32, _i64, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
+_SIGS = {
+    "echo_plan": (_i32, [_i32, _i64, _i32, _i32, ctypes.POINTER(_vp)]),
+    "echo_allreduce": (_i32, [_vp, ctypes.POINTER(_vp), ctypes.POINTER(_vp), _vp, _vp]),
+    "echo_reset_comp": (_i32, [_vp]),
+    "echo_reset_comp_async": (_i32, [_vp, _vp, _vp]),
+    "echo_comp_bytes": (_sz, [_vp]),
+    "echo_wire_bytes": (_sz, [_vp]),
+    "echo_wire_layout": (_i32, [_vp, ctypes.POINTER(_i64)]),
+    "echo_get_status": (_i32, [_vp, _vp, ctypes.POINTER(_i32)]),
+    "echo_debug_wire": (_i32, [_vp, _vp, _sz, _vp]),
+    "echo_set_fused": (_i32, [_vp, _i32]),
+    "echo_set_timing": (_i32, [_vp, ctypes.POINTER(_vp), _i32]),
+    "echo_plan_destroy": (None, [_vp]),
+    "echo_strerror": (ctypes.c_char_p, [_i32]),
+}
+for _name, (_res, _args) in _SIGS.items():
+    _fn = getattr(_lib, _name)
+    _fn.restype = _res
+    _fn.argtypes = _args
+
+EXPORTED = tuple(_SIGS)
+
+
+class EchoError(RuntimeError):
+    def __init__(self, status: int, call: str):
+        self.status = status
+        super().__init__(f"{call}: {_lib.echo_strerror(status).decode()} (status {status})")
+
+
+def _check(status: int, call: str):
+    if status != ECHO_OK:
+        raise EchoError(status, call)
+
+
+def _ptr(x) -> int | None:
+    """A device pointer from a tensor, an int address, or None."""
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    if isinstance(x, ctypes.c_void_p):
+        return x.value
+    return x.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+class Plan:
+    """Owning handle of an echo_plan_t; frees the plan when collected."""
+
+    def __init__(self, handle: int, P: int, n: int, g: int, bits: int):
+        self.handle = handle
+        self.P, self.n, self.g, self.bits = P, n, g, bits
+
+    def __del__(self):
+        h, self.handle = getattr(self, "handle", None), None
+        if h:
+            _lib.echo_plan_destroy(h)
+
+    @property
+    def _as_parameter_(self):
+        return ctypes.c_void_p(self.handle)
+
+
+def echo_plan(P: int, n: int, g: int = 128, bits: int = 4) -> Plan:
+    h = _vp()
+    _check(_lib.echo_plan(P, n, g, bits, ctypes.byref(h)), "echo_plan")
+    return Plan(h.value, P, n, g, bits)
+
+
+def echo_allreduce(plan: Plan, ins, outs, comp_state=None, stream=None) -> None:
+    """ins/outs: sequences of P device tensors (or int addresses); comp_state:
+    None (uncompensated), COMP_DEFAULT (the plan's own state) or a device
+    buffer of echo_comp_bytes(plan) bytes."""
+    P = plan.P
+    if len(ins) != P or len(outs) != P:
+        raise ValueError(f"expected {P} input and {P} output buffers")
+    arr_in = (_vp * P)(*[_ptr(t) for t in ins])
+    arr_out = (_vp * P)(*[_ptr(t) for t in outs])
+    comp = COMP_DEFAULT if comp_state is COMP_DEFAULT else _ptr(comp_state)
+    _check(_lib.echo_allreduce(plan, arr_in, arr_out, comp, _stream(stream)), "echo_allreduce")
+
+
+def echo_reset_comp(plan: Plan) -> None:
+    _check(_lib.echo_reset_comp(plan), "echo_reset_comp")
+
+
+def echo_reset_comp_async(plan: Plan, comp_state=COMP_DEFAULT, stream=None) -> None:
+    comp = COMP_DEFAULT if comp_state is COMP_DEFAULT else _ptr(comp_state)
+    _check(_lib.echo_reset_comp_async(plan, comp, _stream(stream)), "echo_reset_comp_async")
+
+
+def echo_comp_bytes(plan: Plan) -> int:
+    return int(_lib.echo_comp_bytes(plan))
+
+
+def echo_wire_bytes(plan: Plan) -> int:
+    return int(_lib.echo_wire_bytes(plan))
+
+
+def echo_wire_layout(plan: Plan) -> dict:
+    d = (_i64 * 8)()
+    _check(_lib.echo_wire_layout(plan, d), "echo_wire_layout")
+    keys = ("codes1", "meta1", "codes2", "meta2", "Gs", "Gs_pad", "code_bytes", "total")
+    return dict(zip(keys, [int(v) for v in d]))
+
+
+def echo_get_status(plan: Plan, stream=None) -> int:
+    st = _i32(0)
+    _check(_lib.echo_get_status(plan, _stream(stream), ctypes.byref(st)), "echo_get_status")
+    return st.value
+
+
+def echo_debug_wire(plan: Plan, stream=None) -> bytes:
+    nbytes = echo_wire_bytes(plan)
+    buf = (ctypes.c_uint8 * max(nbytes, 1))()
+    _check(_lib.echo_debug_wire(plan, buf, nbytes, _stream(stream)), "echo_debug_wire")
+    return bytes(buf)[:nbytes]
+
+
+def echo_set_fused(plan: Plan, fused: bool) -> None:
+    _check(_lib.echo_set_fused(plan, 1 if fused else 0), "echo_set_fused")
+
+
+def echo_set_timing(plan: Plan, events) -> None:
+    """events: four torch.cuda.Event (enable_timing=True), or None to disable."""
+    if not events:
+        _check(_lib.echo_set_timing(plan, None, 0), "echo_set_timing")
+        return
+    arr = (_vp * 4)(*[ev.cuda_event for ev in events])
+    _check(_lib.echo_set_timing(plan, arr, 4), "echo_set_timing")
+
+
+def echo_plan_destroy(plan: Plan) -> None:
+    h, plan.handle = plan.handle, None
+    if h:
+        _lib.echo_plan_destroy(h)
+
+
+def echo_strerror(status: int) -> str:
+    return _lib.echo_strerror(status).decode()
+
+
+def library_path() -> str:
+    return str(_LIB_PATH)

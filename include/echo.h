@@ -1,0 +1,192 @@
+/*
+ * echo.h -- C ABI of libecho.so: the Echo error-compensated low-bit all-reduce,
+ * with P tensor-parallel ranks emulated as P buffers in one GPU's memory.
+ *
+ * The operation is the quantized P2P all-reduce of "Echo: Error-Compensated
+ * 4-Bit Tensor-Parallel Communication for LLM Training and Inference" (arXiv
+ * 2610.14277), Fig. 2(a), with the error feedback described in its abstract and
+ * in the article "Your All-Reduce Is 4x Overpriced: Echo's 4-Bit Error-Feedback
+ * Trick for Tensor-Parallel Training" (section "The cancellation rule"):
+ *
+ *   push    every rank p quantizes each segment it does not own (after adding
+ *           the error it holds for those elements) to b-bit codes with one fp16
+ *           step and one fp16 zero point per group of g elements, and writes
+ *           them to that segment owner's receive slot;
+ *   reduce  the owner of segment o decodes the P-1 received code tiles and sums
+ *           them with its own segment (plus its held error) in fp32, in
+ *           ascending rank order;
+ *   gather  the owner quantizes the sum once; every rank, the owner included,
+ *           decodes the same codes, so all P outputs are bit-identical and every
+ *           element passes through at most two quantizers for any P;
+ *   feedback each error the call reveals is kept where it arose (the sender's
+ *           stage-1 error v - deq(q) on its non-owned elements, the owner's
+ *           stage-2 error sum - output on its own segment) and is added back by
+ *           the next call's entry pass.
+ *
+ * The quantizer (zero-aware asymmetric, the paper's Table 8 "full" row; its
+ * formula is not printed on the pages) is read as: lo = min(0, min v),
+ * hi = max(0, max v), s = fp16 round-up of (hi - lo) / (2^b - 1) (1 for an
+ * all-zero group), z = clamp(rint(-lo / s), 0, 2^b - 1),
+ * q = clamp(rint(v / s) + z, 0, 2^b - 1), decoded as s * (q - z); all in IEEE
+ * fp32 with no fused multiply-add.  Outputs are rounded to bf16 (nearest even).
+ *
+ * ---------------------------------------------------------------------------
+ * Conventions for every call
+ *   - Device pointers are plain CUDA device addresses on the device that was
+ *     current when the plan was made; that device must be current at each call.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *     stream).  Work is enqueued on it and the call returns without waiting,
+ *     except where a call says it synchronizes.
+ *   - Every call returns an ECHO_* status; 0 is success.  On ECHO_ERR_CUDA the
+ *     CUDA error is kept and echo_strerror(ECHO_ERR_CUDA) names it.
+ *   - A plan serves one stream at a time: its receive slots are shared by all
+ *     calls made with it, so calls on different streams must be ordered by the
+ *     caller.  Distinct plans are independent.
+ * ---------------------------------------------------------------------------
+ */
+#ifndef ECHO_H_
+#define ECHO_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes. */
+#define ECHO_OK              0
+#define ECHO_ERR_ARG         1  /* NULL pointer, P outside 1..ECHO_MAX_RANKS, g < 1,
+                                   aliasing other than out[p] == in[p], wrong device */
+#define ECHO_ERR_SHAPE       2  /* n < 0, or n not a multiple of P*g */
+#define ECHO_ERR_UNSUPPORTED 3  /* bits not 4 or 8, or g other than 128 */
+#define ECHO_ERR_ALIGN       4  /* a device pointer not 16-byte aligned */
+#define ECHO_ERR_CUDA        5  /* a CUDA runtime call failed */
+#define ECHO_ERR_OVERFLOW    6  /* (status word) a non-finite input or an fp16 step overflow */
+#define ECHO_ERR_TIMEOUT     7  /* (status word) a device-side wait gave up */
+
+#define ECHO_MAX_RANKS 16
+
+/* Pass as `comp_state` to use the compensator state owned by the plan. */
+#define ECHO_COMP_DEFAULT ((void*)(intptr_t)-1)
+
+typedef struct echo_plan_s* echo_plan_t;
+
+/*
+ * echo_plan -- build the layout for P emulated ranks of n bf16 elements each,
+ * groups of g elements and b-bit codes, and allocate (cudaMalloc, on the
+ * current device) the plan's receive slots and its own compensator state
+ * (P*n fp32, zeroed).  Synchronizes the device once.
+ *   P     1..ECHO_MAX_RANKS
+ *   n     elements per rank, a multiple of P*g (n = 0 gives an empty plan)
+ *   g     group size; 128 on the GPU
+ *   bits  4 or 8
+ *   out   receives the plan handle; the caller frees it with echo_plan_destroy.
+ * Segments are contiguous: rank o owns elements [o*m, (o+1)*m), m = n/P
+ * (Fig. 2(a) and Fig. 4 of the paper show contiguous segments).
+ */
+int echo_plan(int P, int64_t n, int g, int bits, echo_plan_t* out);
+
+/*
+ * echo_allreduce -- one emulated all-reduce call (Fig. 2(a)).
+ *   in[P]       host array of P device pointers, each to n bf16 values (rank p's
+ *               partial tensor), 16-byte aligned, caller-owned, read-only.
+ *   out[P]      host array of P device pointers, each to n bf16 outputs, 16-byte
+ *               aligned, caller-owned.  All P rows receive the same bits.
+ *               out[p] may equal in[p] (in place); any other overlap between an
+ *               out buffer and another in/out buffer is rejected (ECHO_ERR_ARG).
+ *   comp_state  NULL: uncompensated call (no state read or written);
+ *               ECHO_COMP_DEFAULT: the plan's own state;
+ *               otherwise a caller device buffer of echo_comp_bytes(plan) bytes,
+ *               16-byte aligned, fp32 laid out [P][n] (rank p's error for its
+ *               element i at p*n + i), zero before the first call of a sequence;
+ *               read and updated in place.
+ *   stream      cudaStream_t as void*.
+ * Enqueues three kernels (push, reduce, gather; or two when the fused gather is
+ * selected with echo_set_fused) and returns.  Inputs must stay valid and
+ * unmodified until the work completes.  Non-finite inputs or an fp16 step
+ * overflow do not fail the call: they set the plan's status word (see
+ * echo_get_status) and leave the affected groups' results unspecified.
+ */
+int echo_allreduce(echo_plan_t plan, const void* const* in, void* const* out,
+                   void* comp_state, void* stream);
+
+/*
+ * echo_reset_comp -- zero the plan's own compensator state, ordered on the
+ * stream of the plan's last echo_allreduce (the legacy default stream if none).
+ */
+int echo_reset_comp(echo_plan_t plan);
+
+/*
+ * echo_reset_comp_async -- zero a compensator state on `stream`.
+ * comp_state is ECHO_COMP_DEFAULT or a caller buffer of echo_comp_bytes bytes.
+ */
+int echo_reset_comp_async(echo_plan_t plan, void* comp_state, void* stream);
+
+/* Bytes of one compensator state: P * n * 4.  0 for a NULL plan. */
+size_t echo_comp_bytes(echo_plan_t plan);
+
+/* Bytes of the plan's receive-slot workspace (what echo_debug_wire copies). */
+size_t echo_wire_bytes(echo_plan_t plan);
+
+/*
+ * echo_wire_layout -- describe the receive-slot workspace, for tests and tools.
+ * Writes 8 int64 values to `desc`:
+ *   [0] byte offset of the push codes    [P owners][P-1 senders][Gs groups][g*b/8 bytes]
+ *   [1] byte offset of the push meta     [P owners][P-1 senders][Gs_pad] uint32
+ *   [2] byte offset of the gather codes  [P owners][Gs groups][g*b/8 bytes]
+ *   [3] byte offset of the gather meta   [P owners][Gs_pad] uint32
+ *   [4] Gs     groups per segment (m / g)
+ *   [5] Gs_pad Gs rounded up to a multiple of 4
+ *   [6] bytes of codes per group (g * b / 8)
+ *   [7] total bytes (echo_wire_bytes)
+ * Sender slot index: rank p's slot at owner o is p if p < o, else p - 1.
+ * A meta word holds the fp16 step in its low 16 bits and the fp16 zero point
+ * (an integer value) in its high 16 bits.  Codes of 4 bits: element 2i of a
+ * group in the low nibble of byte i, element 2i+1 in the high nibble.
+ */
+int echo_wire_layout(echo_plan_t plan, int64_t* desc);
+
+/*
+ * echo_get_status -- read and clear the plan's device status word.
+ * Synchronizes `stream`, then writes ECHO_OK, ECHO_ERR_OVERFLOW or
+ * ECHO_ERR_TIMEOUT (the latter wins if both occurred) to *status.
+ */
+int echo_get_status(echo_plan_t plan, void* stream, int* status);
+
+/*
+ * echo_debug_wire -- copy the whole receive-slot workspace (layout as in
+ * echo_wire_layout) to host memory `host_dst` of at least `bytes` bytes, after
+ * the work already on `stream`.  Synchronizes `stream`.  For tests.
+ */
+int echo_debug_wire(echo_plan_t plan, void* host_dst, size_t bytes, void* stream);
+
+/*
+ * echo_set_fused -- 0 (default): the gather is its own kernel, which reads the
+ * gather codes back and writes all P outputs.  1: the reduce kernel writes the
+ * P outputs itself from the values it just encoded (the gather codes are
+ * still written); this skips one kernel and one read of the gather codes.
+ * Both give bit-identical outputs, state and codes.
+ */
+int echo_set_fused(echo_plan_t plan, int fused);
+
+/*
+ * echo_set_timing -- events (cudaEvent_t as void*) that echo_allreduce records
+ * around its kernels: ev[0] before the push kernel, ev[1] after it, ev[2] after
+ * the reduce kernel, ev[3] after the gather kernel (== after reduce when
+ * fused).  count 4 enables, count 0 disables.  The caller owns the events.
+ */
+int echo_set_timing(echo_plan_t plan, void* const* events, int count);
+
+/* Free everything the plan allocated.  NULL is accepted. */
+void echo_plan_destroy(echo_plan_t plan);
+
+/* A static description of a status code; for ECHO_ERR_CUDA, of the last CUDA
+ * error seen by the library in this thread. */
+const char* echo_strerror(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ECHO_H_ */

@@ -1,0 +1,78 @@
+"""The C-ABI library builds, loads, and exports every entry point include/echo.h
+declares; host-side argument checks that need no GPU."""
+import ctypes
+import re
+from pathlib import Path
+
+import pytest
+
+ROOT = Path(__file__).resolve().parents[1]
+HEADERS = sorted((ROOT / "include").glob("*.h"))
+
+
+def _declared():
+    names = set()
+    for h in HEADERS:
+        text = re.sub(r"/\*.*?\*/", "", h.read_text(), flags=re.S)
+        for m in re.finditer(r"^\s*[A-Za-z_][\w\s\*]*?\b(echo_\w+)\s*\(", text, flags=re.M):
+            names.add(m.group(1))
+    return names
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from bit_error_compensated_gb300.build import build_library
+    return ctypes.CDLL(str(build_library()))
+
+
+def test_headers_declare_the_north_star_calls():
+    d = _declared()
+    assert {"echo_plan", "echo_allreduce", "echo_reset_comp"} <= d
+    assert len(d) >= 12
+
+
+def test_every_declared_symbol_is_exported(lib):
+    missing = [n for n in sorted(_declared()) if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_binding_wraps_every_declared_call(lib):
+    from bit_error_compensated_gb300 import echo
+    assert set(echo.EXPORTED) == _declared()
+    assert echo.library_path().endswith("libecho.so")
+
+
+def test_host_argument_checks_without_gpu(lib):
+    from bit_error_compensated_gb300 import echo
+    h = ctypes.c_void_p()
+    lib.echo_plan.argtypes = [ctypes.c_int, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
+                              ctypes.POINTER(ctypes.c_void_p)]
+    # argument errors are reported before any CUDA call
+    assert lib.echo_plan(0, 128, 128, 4, ctypes.byref(h)) == echo.ECHO_ERR_ARG
+    assert lib.echo_plan(17, 17 * 128, 128, 4, ctypes.byref(h)) == echo.ECHO_ERR_ARG
+    assert lib.echo_plan(2, 256, 0, 4, ctypes.byref(h)) == echo.ECHO_ERR_ARG
+    assert lib.echo_plan(2, 256, 128, 5, ctypes.byref(h)) == echo.ECHO_ERR_UNSUPPORTED
+    assert lib.echo_plan(2, 256, 64, 4, ctypes.byref(h)) == echo.ECHO_ERR_UNSUPPORTED
+    assert lib.echo_plan(2, 300, 128, 4, ctypes.byref(h)) == echo.ECHO_ERR_SHAPE
+    assert lib.echo_plan(2, -256, 128, 4, ctypes.byref(h)) == echo.ECHO_ERR_SHAPE
+    assert lib.echo_plan(2, 256, 128, 4, None) == echo.ECHO_ERR_ARG
+    assert h.value is None
+    assert lib.echo_allreduce(None, None, None, None, None) == echo.ECHO_ERR_ARG
+    assert lib.echo_reset_comp(None) == echo.ECHO_ERR_ARG
+    lib.echo_comp_bytes.restype = ctypes.c_size_t
+    assert lib.echo_comp_bytes(None) == 0
+    lib.echo_plan_destroy(None)
+    for code, word in [(0, "ok"), (2, "multiple"), (4, "aligned"), (7, "wait")]:
+        assert word in echo.echo_strerror(code)
+
+
+def test_comp_default_sentinel_matches_header():
+    from bit_error_compensated_gb300 import echo
+    text = (ROOT / "include" / "echo.h").read_text()
+    assert "#define ECHO_COMP_DEFAULT ((void*)(intptr_t)-1)" in text
+    assert echo.COMP_DEFAULT.value == 2 ** 64 - 1
+    for name in ("ECHO_OK", "ECHO_ERR_ARG", "ECHO_ERR_SHAPE", "ECHO_ERR_UNSUPPORTED",
+                 "ECHO_ERR_ALIGN", "ECHO_ERR_CUDA", "ECHO_ERR_OVERFLOW", "ECHO_ERR_TIMEOUT",
+                 "ECHO_MAX_RANKS"):
+        m = re.search(rf"#define {name}\s+(\d+)", text)
+        assert m and int(m.group(1)) == getattr(echo, name), name

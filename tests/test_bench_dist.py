@@ -1,0 +1,67 @@
+"""Host logic of `bench.py --gpus N`: with N > 1 every rank runs an independent
+replica, the timed value is the slowest rank's time, and the reported
+throughput is the work of all ranks over that time.  Checked with two gloo
+ranks on the CPU (no GPU involved)."""
+import os
+import socket
+
+import pytest
+import torch.multiprocessing as mp
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    import bench
+    r, local, w = bench.dist_setup()
+    try:
+        mine = 10.0 + 5.0 * r                     # rank 1 is the slow one
+        slowest = bench.max_over_ranks(mine, w)
+        bench.barrier(w)
+        gbs = bench.whole_job_gbs(1e9, steps=2, world=w, max_ms=slowest)
+        q.put((r, local, w, slowest, gbs))
+    finally:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def test_two_gloo_ranks_take_the_slowest_time():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = sorted(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert [r[0] for r in res] == [0, 1]
+    assert all(r[2] == 2 for r in res)
+    assert all(r[3] == pytest.approx(15.0) for r in res)
+    # 2 ranks x 2 steps x 1 GB over 15 ms
+    assert all(r[4] == pytest.approx(2 * 2 * 1.0 / 0.015) for r in res)
+
+
+def test_single_process_needs_no_process_group():
+    import bench
+    assert bench.dist_setup() == (0, 0, 1)
+    assert bench.max_over_ranks(3.5, 1) == 3.5
+
+
+def test_byte_model_matches_the_per_element_totals():
+    import bench
+    c = bench.code_bytes_per_elem(4)
+    assert c == 0.53125
+    P, n = 4, 1 << 20
+    assert bench.call_model_bytes(P, n, 4, True, False) == pytest.approx(P * n * (12 + 2 * c))
+    assert bench.call_model_bytes(P, n, 4, False, False) == pytest.approx(P * n * (4 + 2 * c))
+    assert bench.call_model_bytes(P, n, 8, True, False) == pytest.approx(P * n * (12 + 2 * 1.03125))
+    # the fused gather skips one read of the gather codes
+    assert bench.call_model_bytes(P, n, 4, True, True) == pytest.approx(P * n * (12 + 2 * c) - n * c)

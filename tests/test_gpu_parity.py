@@ -1,0 +1,212 @@
+"""Parity of the CUDA path (called through the C ABI) with the CPU oracle.
+
+Small and mid sizes, compared element by element: outputs of every rank, the
+compensator state, and every push and gather code and meta word.  Sizes span
+several reduce tiles (32 groups each) with a ragged last tile (37 groups per
+segment), P from 1 to 16, 4- and 8-bit codes, the three compensator modes and
+both gather variants, over a sequence of calls that carries the state.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from _parity import assert_state_close, assert_wire_equal, bits, wire_to_canonical
+
+pytestmark = pytest.mark.gpu
+
+G = 128
+
+
+@pytest.fixture(scope="module")
+def echo():
+    from bit_error_compensated_gb300 import echo as mod
+    return mod
+
+
+def _inputs(P, n, seed, scale=1.0):
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(seed)
+    x = torch.randn((P, n), generator=gen, device="cuda") * scale
+    # a per-element spread shared by the ranks, like the channel scales of a
+    # TP partial sum
+    spread = torch.exp(torch.randn(n, generator=gen, device="cuda"))
+    return (x * spread).to(torch.bfloat16)
+
+
+def _run_sequence(echo, P, Gs, bits_, mode, fused, calls=3, seed=0, inplace=False):
+    n = P * G * Gs
+    plan = echo.echo_plan(P, n, G, bits_)
+    echo.echo_set_fused(plan, fused)
+    lay = echo.echo_wire_layout(plan)
+    comp_t = torch.zeros((P, n), dtype=torch.float32, device="cuda") if mode == "caller" else None
+    comp_arg = {"none": None, "default": echo.COMP_DEFAULT, "caller": comp_t}[mode]
+    e_ref = None if mode == "none" else np.zeros((P, n), np.float32)
+    for k in range(calls):
+        x = _inputs(P, n, seed * 100 + k)
+        xb = bits(x)
+        out = x if inplace else torch.empty_like(x)
+        echo.echo_allreduce(plan, list(x), list(out), comp_arg)
+        torch.cuda.synchronize()
+        assert echo.echo_get_status(plan) == 0
+        ref = oracle.allreduce(xb, G, bits_, e=e_ref, want_wire=True)
+        got = bits(out)
+        assert np.array_equal(got, ref["out"]), f"outputs differ at call {k}"
+        wire = wire_to_canonical(echo.echo_debug_wire(plan), lay, P, n, bits_)
+        assert_wire_equal(wire, ref, P)
+        if mode == "caller":
+            assert_state_close(comp_t.cpu().numpy(), e_ref, f"state after call {k}")
+    return plan
+
+
+@pytest.mark.parametrize("fused", [0, 1])
+@pytest.mark.parametrize("mode", ["none", "default", "caller"])
+@pytest.mark.parametrize("bits_", [4, 8])
+@pytest.mark.parametrize("P", [1, 2, 3, 4, 8, 16])
+def test_matches_oracle(echo, P, bits_, mode, fused):
+    _run_sequence(echo, P, 37, bits_, mode, fused, seed=P * 10 + bits_)
+
+
+@pytest.mark.parametrize("Gs", [1, 4, 31, 32, 33, 64, 129])
+def test_tile_boundaries(echo, Gs):
+    _run_sequence(echo, 4, Gs, 4, "caller", 0, calls=2, seed=Gs)
+
+
+@pytest.mark.parametrize("fused", [0, 1])
+def test_in_place(echo, fused):
+    _run_sequence(echo, 4, 40, 4, "caller", fused, calls=3, seed=7, inplace=True)
+
+
+def test_fused_and_unfused_identical(echo):
+    P, Gs, n = 4, 50, 4 * G * 50
+    outs = []
+    for fused in (0, 1):
+        plan = echo.echo_plan(P, n, G, 4)
+        echo.echo_set_fused(plan, fused)
+        comp = torch.zeros((P, n), device="cuda")
+        o = []
+        for k in range(4):
+            x = _inputs(P, n, 900 + k)
+            out = torch.empty_like(x)
+            echo.echo_allreduce(plan, list(x), list(out), comp)
+            o.append(bits(out))
+        outs.append((o, comp.cpu().numpy(), echo.echo_debug_wire(plan)))
+    assert all(np.array_equal(a, b) for a, b in zip(outs[0][0], outs[1][0]))
+    assert np.array_equal(outs[0][1].view(np.uint32), outs[1][1].view(np.uint32))
+    assert outs[0][2] == outs[1][2]
+
+
+def test_deterministic_run_twice(echo):
+    P, n = 8, 8 * G * 45
+    res = []
+    for _ in range(2):
+        plan = echo.echo_plan(P, n, G, 4)
+        comp = torch.zeros((P, n), device="cuda")
+        for k in range(3):
+            x = _inputs(P, n, 50 + k)
+            out = torch.empty_like(x)
+            echo.echo_allreduce(plan, list(x), list(out), comp)
+        res.append((bits(out), comp.cpu().numpy().view(np.uint32), echo.echo_debug_wire(plan)))
+    assert np.array_equal(res[0][0], res[1][0])
+    assert np.array_equal(res[0][1], res[1][1])
+    assert res[0][2] == res[1][2]
+
+
+def test_all_outputs_identical_across_ranks(echo):
+    P, n = 8, 8 * G * 33
+    plan = echo.echo_plan(P, n, G, 4)
+    x = _inputs(P, n, 3)
+    out = torch.empty_like(x)
+    echo.echo_allreduce(plan, list(x), list(out), echo.COMP_DEFAULT)
+    o = bits(out)
+    assert all(np.array_equal(o[p], o[0]) for p in range(P))
+
+
+def test_reset_and_resume(echo):
+    """Checkpoint/resume of the only cross-call state: K calls, save the state,
+    M more calls; then restore and replay the M calls -- bitwise equal."""
+    P, n = 4, 4 * G * 34
+    plan = echo.echo_plan(P, n, G, 4)
+    comp = torch.zeros((P, n), device="cuda")
+    for k in range(3):
+        x = _inputs(P, n, 200 + k)
+        echo.echo_allreduce(plan, list(x), list(torch.empty_like(x)), comp)
+    saved = comp.clone()
+    outs_a = []
+    for k in range(3, 6):
+        x = _inputs(P, n, 200 + k)
+        out = torch.empty_like(x)
+        echo.echo_allreduce(plan, list(x), list(out), comp)
+        outs_a.append(bits(out))
+    state_a = comp.clone()
+    comp.copy_(saved)
+    for i, k in enumerate(range(3, 6)):
+        x = _inputs(P, n, 200 + k)
+        out = torch.empty_like(x)
+        echo.echo_allreduce(plan, list(x), list(out), comp)
+        assert np.array_equal(bits(out), outs_a[i])
+    assert torch.equal(comp.view(torch.int32), state_a.view(torch.int32))
+    # reset: the plan's own state back to zero gives a fresh start
+    echo.echo_allreduce(plan, list(x), list(torch.empty_like(x)), echo.COMP_DEFAULT)
+    echo.echo_reset_comp(plan)
+    out1 = torch.empty_like(x)
+    echo.echo_allreduce(plan, list(x), list(out1), echo.COMP_DEFAULT)
+    out2 = torch.empty_like(x)
+    echo.echo_allreduce(plan, list(x), list(out2), torch.zeros((P, n), device="cuda"))
+    assert torch.equal(out1, out2)
+    comp.zero_()
+    echo.echo_reset_comp_async(plan, comp)
+    assert not comp.any()
+
+
+def test_overflow_flag(echo):
+    P, n = 2, 2 * G * 4
+    plan = echo.echo_plan(P, n, G, 4)
+    x = _inputs(P, n, 1)
+    x[1, 300] = float("inf")
+    echo.echo_allreduce(plan, list(x), list(torch.empty_like(x)), None)
+    assert echo.echo_get_status(plan) == echo.ECHO_ERR_OVERFLOW
+    assert echo.echo_get_status(plan) == 0          # read-and-clear
+    x = _inputs(P, n, 1) * 1e6                       # step beyond fp16
+    x = x.to(torch.bfloat16)
+    echo.echo_allreduce(plan, list(x), list(torch.empty_like(x)), None)
+    assert echo.echo_get_status(plan) == echo.ECHO_ERR_OVERFLOW
+    assert oracle.allreduce(bits(x), G, 4)["flagged"] > 0
+
+
+def test_empty_and_degenerate(echo):
+    plan = echo.echo_plan(4, 0, G, 4)
+    e = torch.empty((4, 0), dtype=torch.bfloat16, device="cuda")
+    ptrs = [torch.empty(8, dtype=torch.bfloat16, device="cuda") for _ in range(4)]
+    echo.echo_allreduce(plan, ptrs, [torch.empty(8, dtype=torch.bfloat16, device="cuda")
+                                     for _ in range(4)], echo.COMP_DEFAULT)
+    assert echo.echo_comp_bytes(plan) == 0 and e.numel() == 0
+    # all-zero input: step 1, zero point 0, outputs exactly zero
+    P, n = 4, 4 * G * 3
+    plan = echo.echo_plan(P, n, G, 4)
+    x = torch.zeros((P, n), dtype=torch.bfloat16, device="cuda")
+    out = torch.ones_like(x)
+    echo.echo_allreduce(plan, list(x), list(out), echo.COMP_DEFAULT)
+    assert not out.any()
+
+
+def test_argument_errors(echo):
+    P, n = 2, 2 * G * 2
+    plan = echo.echo_plan(P, n, G, 4)
+    x = torch.zeros((P, n + 8), dtype=torch.bfloat16, device="cuda")
+    out = torch.zeros((P, n + 8), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(echo.EchoError) as ei:          # misaligned by 2 bytes
+        echo.echo_allreduce(plan, [x[0, 1:], x[1]], [out[0], out[1]], None)
+    assert ei.value.status == echo.ECHO_ERR_ALIGN
+    with pytest.raises(echo.EchoError) as ei:          # out[0] overlaps in[1]
+        echo.echo_allreduce(plan, [x[0], x[1]], [x[1], out[1]], None)
+    assert ei.value.status == echo.ECHO_ERR_ARG
+    with pytest.raises(echo.EchoError) as ei:          # two outputs overlap
+        echo.echo_allreduce(plan, [x[0], x[1]], [out[0], out[0]], None)
+    assert ei.value.status == echo.ECHO_ERR_ARG
+    with pytest.raises(echo.EchoError) as ei:
+        echo.echo_plan(3, 3 * G * 2 + 1, G, 4)
+    assert ei.value.status == echo.ECHO_ERR_SHAPE
+    with pytest.raises(echo.EchoError) as ei:
+        echo.echo_plan(2, 2 * G, G, 6)
+    assert ei.value.status == echo.ECHO_ERR_UNSUPPORTED

@@ -1,0 +1,105 @@
+"""The five workloads at their full sizes, in the launch configuration the bench
+times, checked against the oracle on a fixed sample of group positions carried
+through every call of the sequence (positions are independent, so the oracle on
+a sample is exactly the oracle's whole call restricted to it).  The two-rank
+workload is small enough to compare in full, wire codes included.
+
+Sample sizes keep each test within tens of seconds of oracle time; every sample
+includes the first and last group of every owner segment.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from _parity import (SampledOracle, assert_state_close, assert_wire_equal, bits,
+                     sample_groups, sampled_wire, wire_to_canonical)
+from bit_error_compensated_gb300.workloads import WORKLOADS, call_sequence, rank_inputs
+
+pytestmark = pytest.mark.gpu
+G = 128
+
+
+@pytest.fixture(scope="module")
+def echo():
+    from bit_error_compensated_gb300 import echo as mod
+    return mod
+
+
+def test_p2_n4096_full(echo):
+    w = WORKLOADS[1]
+    plan = echo.echo_plan(w.P, w.n, G, 4)
+    lay = echo.echo_wire_layout(plan)
+    comp = torch.zeros((w.P, w.n), device="cuda")
+    e_ref = np.zeros((w.P, w.n), np.float32)
+    ties = 0
+    for c in call_sequence(1):
+        x = rank_inputs(1, c, "cuda")
+        out = torch.empty_like(x)
+        compensated = c.state != "none"
+        echo.echo_allreduce(plan, list(x), list(out), comp if compensated else None)
+        ref = oracle.allreduce(bits(x), G, 4, e=e_ref if compensated else None, want_wire=True)
+        ties += ref["ties"]
+        assert np.array_equal(bits(out), ref["out"])
+        assert_wire_equal(wire_to_canonical(echo.echo_debug_wire(plan), lay, w.P, w.n, 4), ref, w.P)
+        assert_state_close(comp.cpu().numpy(), e_ref)
+    print(f"p2_n4096: exact rounding ties in the oracle: {ties}; code mismatches: 0")
+
+
+def _sampled_sequence(echo, number, bits_, sample, calls=None, wire_calls=(0,)):
+    w = WORKLOADS[number]
+    P, n = w.P, w.n
+    plan = echo.echo_plan(P, n, G, bits_)
+    lay = echo.echo_wire_layout(plan)
+    Gs = lay["Gs"]
+    groups = sample_groups(P, Gs, sample, seed=number)
+    so = SampledOracle(P, Gs, groups, bits_)
+    states = {}
+    x = torch.empty((P, n), dtype=torch.bfloat16, device="cuda")
+    out = torch.empty_like(x)
+    seq = call_sequence(number)
+    if calls is not None:
+        seq = seq[:calls]
+    ties = 0
+    for k, c in enumerate(seq):
+        rank_inputs(number, c, "cuda", out=x)
+        comp = None
+        if c.state != "none":
+            comp = states.setdefault(c.state, torch.zeros((P, n), device="cuda"))
+        echo.echo_allreduce(plan, list(x), list(out), comp)
+        xs = bits(so.gather(x))
+        check_wire = k in wire_calls or k == len(seq) - 1
+        ref = so.call(xs, c.state if comp is not None else None, want_wire=check_wire)
+        ties += ref["ties"]
+        got = bits(so.gather(out))
+        for p in range(P):
+            assert np.array_equal(got[p], ref["y_rows"]), f"call {k} rank {p}"
+        if comp is not None:
+            assert_state_close(so.gather(comp).numpy(), so.state_rows(c.state), f"state call {k}")
+        if check_wire:
+            wire = sampled_wire(echo.echo_debug_wire(plan), lay, P, groups, bits_)
+            for p in range(P):
+                mask = so.owners != p
+                assert np.array_equal(wire["q1"][mask, p], ref["q1"][mask, p]), f"push codes, call {k}"
+                assert np.array_equal(wire["m1"][mask, p], ref["m1"][mask, p]), f"push meta, call {k}"
+            assert np.array_equal(wire["q2"], ref["q2"]), f"gather codes, call {k}"
+            assert np.array_equal(wire["m2"], ref["m2"]), f"gather meta, call {k}"
+    print(f"workload {number} ({bits_}-bit): {len(seq)} calls, {groups.size} sampled positions, "
+          f"exact rounding ties in the oracle: {ties}; code mismatches: 0")
+
+
+def test_p4_2048x4096_sampled(echo):
+    _sampled_sequence(echo, 2, 4, sample=1024)
+
+
+@pytest.mark.parametrize("bits_", [4, 8])
+def test_p8_1gib_sampled(echo, bits_):
+    _sampled_sequence(echo, 3, bits_, sample=4096)
+
+
+def test_p4_8192x4096_sampled(echo):
+    _sampled_sequence(echo, 4, 4, sample=1024)
+
+
+def test_p4_32768x1024_sampled(echo):
+    _sampled_sequence(echo, 5, 4, sample=384)
