@@ -65,6 +65,8 @@ def _load():
         lib.oracle_pack_codes.restype = None
         lib.oracle_group_position.argtypes = [i32, i32, i32, i32, P, P, P, P, P, P, P, P, P, P]
         lib.oracle_group_position.restype = i32
+        lib.oracle_group_positions.argtypes = [i32, i64, P, i32, i32, P, P, P, P, P, P, P, P]
+        lib.oracle_group_positions.restype = i64
         lib.oracle_allreduce.argtypes = [i32, i64, i32, i32, P, P, P, P, P, P, P, P, P, P]
         lib.oracle_allreduce.restype = i64
         _lib = lib
@@ -156,6 +158,36 @@ def group_position(P: int, owner: int, bits: int, x: np.ndarray, e: np.ndarray |
     r["flagged"] = lib.oracle_group_position(
         P, owner, ln, bits, _ptr(x), _ptr(e), _ptr(r["y"]), _ptr(r["q1"]), _ptr(r["m1"]),
         _ptr(r["q2"]), _ptr(r["m2"]), _ptr(r["acc"]), _ptr(r["nq"]), ctypes.byref(ties))
+    r["ties"] = ties.value
+    return r
+
+
+def group_positions(P: int, owners: np.ndarray, bits: int, x: np.ndarray,
+                    e: np.ndarray | None, want_wire: bool = False):
+    """Many independent group positions at once.
+
+    owners [npos] int; x [npos, P, len] bf16 bits; e [npos, P, len] float32
+    (updated in place) or None.  Returns a dict with y [npos, len] and, on
+    request, q1 [npos, P, len], m1 [npos, P], q2 [npos, len], m2 [npos]; plus
+    ``flagged`` and ``ties``."""
+    lib = _load()
+    owners = np.ascontiguousarray(owners, dtype=np.int32)
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    npos, P_, ln = x.shape
+    assert P_ == P and owners.shape == (npos,)
+    if e is not None:
+        assert e.dtype == np.float32 and e.flags.c_contiguous and e.shape == x.shape
+    r = dict(y=np.zeros((npos, ln), np.uint16))
+    if want_wire:
+        r.update(q1=np.zeros((npos, P, ln), np.uint8), m1=np.zeros((npos, P), np.uint32),
+                 q2=np.zeros((npos, ln), np.uint8), m2=np.zeros(npos, np.uint32))
+    ties = ctypes.c_int64(0)
+    bad = lib.oracle_group_positions(P, npos, _ptr(owners), ln, bits, _ptr(x), _ptr(e),
+                                     _ptr(r["y"]), _ptr(r.get("q1")), _ptr(r.get("m1")),
+                                     _ptr(r.get("q2")), _ptr(r.get("m2")), ctypes.byref(ties))
+    if bad < 0:
+        raise ValueError("oracle_group_positions rejected its arguments")
+    r["flagged"] = int(bad)
     r["ties"] = ties.value
     return r
 

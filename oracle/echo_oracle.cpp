@@ -311,6 +311,29 @@ int oracle_group_position(int P, int o, int len, int bits, const uint16_t* x,
   return bad;
 }
 
+// A list of independent group positions, each of `len` elements, processed one
+// after the other by oracle_group_position.  Arrays are position-major:
+//   owners [npos]; x [npos][P][len]; e [npos][P][len] or NULL; y [npos][len];
+//   q1 [npos][P][len], m1 [npos][P], q2 [npos][len], m2 [npos] (each or NULL).
+// Returns the number of flagged quantizations, or -1 for invalid arguments.
+int64_t oracle_group_positions(int P, int64_t npos, const int* owners, int len,
+                               int bits, const uint16_t* x, float* e, uint16_t* y,
+                               uint8_t* q1, uint32_t* m1, uint8_t* q2,
+                               uint32_t* m2, int64_t* ties) {
+  if (P < 1 || npos < 0 || len < 1 || (bits != 4 && bits != 8)) return -1;
+  const size_t blk = (size_t)P * len;
+  int64_t bad = 0;
+  for (int64_t k = 0; k < npos; ++k) {
+    if (owners[k] < 0 || owners[k] >= P) return -1;
+    bad += oracle_group_position(P, owners[k], len, bits, x + k * blk,
+                                 e ? e + k * blk : nullptr, y + k * len,
+                                 q1 ? q1 + k * blk : nullptr, m1 ? m1 + k * P : nullptr,
+                                 q2 ? q2 + k * len : nullptr, m2 ? m2 + k : nullptr,
+                                 nullptr, nullptr, ties);
+  }
+  return bad;
+}
+
 // ---------------------------------------------------------------------------
 // One whole call over P ranks of n elements each (n a multiple of P; g need
 // not divide m = n/P, the last group of a segment is then shorter).
