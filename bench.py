@@ -226,6 +226,8 @@ def run_ours(args, rank, local, world):
     w = WORKLOADS[number]
     P, n = w.P, w.n
     seq = call_sequence(number, steps=1)
+    if args.calls:
+        seq = seq[:args.calls]
     calls = len(seq)
     xs = build_inputs(number, seq, calls, dev)
     out = torch.empty((P, n), dtype=torch.bfloat16, device=dev)
@@ -442,78 +444,77 @@ def time_other(echo, number, bits, fused, dev, reps=3):
 
 # ------------------------------------------------------------- the oracle ----
 
+class OracleSample:
+    """The oracle on a fixed 1/8 sample of one workload's group positions.
+
+    Each step is one call of the workload's sequence restricted to those
+    positions -- exactly the oracle's work on them, since positions are
+    independent -- with 4 distinct inputs cycled and the state carried."""
+
+    def __init__(self, number, bits):
+        import numpy as np
+        import torch
+        from bit_error_compensated_gb300.workloads import WORKLOADS, call_sequence, rank_inputs
+        w = WORKLOADS[number]
+        self.w, self.bits, self.P = w, bits, w.P
+        seq = call_sequence(number, steps=1)
+        Gs = w.n // w.P // G
+        rng = np.random.default_rng(number)
+        pos = np.sort(rng.choice(w.P * Gs, size=max(1, w.P * Gs // 8), replace=False))
+        self.owners = (pos // Gs).astype(np.int32)
+        idx = (pos[:, None] * G + np.arange(G)[None, :]).ravel()
+        self.e = np.zeros((pos.size, w.P, G), np.float32)
+        self.inputs = []
+        for k in range(min(len(seq), 4)):
+            x = rank_inputs(number, seq[k], "cpu").view(torch.int16).numpy().view(np.uint16)
+            self.inputs.append(np.ascontiguousarray(x[:, idx].reshape(w.P, pos.size, G).transpose(1, 0, 2)))
+        self.bytes_per_step = pos.size * w.P * G * 2
+        self.sample = (f"each step: one call of {w.name} on a fixed 1/8 sample of its group "
+                       f"positions ({pos.size} of {w.P * Gs}), 4 distinct inputs cycled, state carried; "
+                       f"single-threaded")
+        self.i = 0
+
+    def step(self):
+        import oracle
+        oracle.group_positions(self.P, self.owners, self.bits, self.inputs[self.i % len(self.inputs)], self.e)
+        self.i += 1
+
+
 def cpu_baseline_oracle(number, bits, budget_s=12.0):
-    """The oracle as it stands, single-threaded on a host core, over the first
-    calls of the workload's sequence until about `budget_s` seconds of oracle
-    time have passed (input generation and copies are not timed)."""
-    import numpy as np
-    import torch
-    import oracle
-    from bit_error_compensated_gb300.workloads import WORKLOADS, call_sequence, rank_inputs
-    w = WORKLOADS[number]
-    seq = call_sequence(number, steps=1)
-    states = {}
-    spent, done = 0.0, 0
-    for c in seq:
-        x = rank_inputs(number, c, "cpu").view(torch.int16).numpy().view(np.uint16)
-        e = None if c.state == "none" else states.setdefault(c.state, np.zeros(x.shape, np.float32))
-        t = time.perf_counter()
-        oracle.allreduce(x, G, bits, e=e)
-        spent += time.perf_counter() - t
-        done += 1
-        if spent >= budget_s:
-            break
-    v = done * w.P * w.n * 2 / spent / 1e9
-    return {"value": round(v, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"first {done} of the {len(seq)} calls of {w.name}, whole tensors "
-                      f"({spent:.1f} s of single-threaded oracle time)"}
+    """The oracle as it stands, single-threaded on one host core, for about
+    `budget_s` seconds of steps of OracleSample."""
+    s = OracleSample(number, bits)
+    s.step()
+    steps, t = 0, time.perf_counter()
+    while time.perf_counter() - t < budget_s:
+        s.step()
+        steps += 1
+    sec = time.perf_counter() - t
+    return {"value": round(s.bytes_per_step * steps / sec / 1e9, 4), "unit": "GB/s", "cores": 1,
+            "kind": "oracle", "sample": f"{steps} steps; " + s.sample}
 
 
 def run_reference(args, rank, world):
-    """The oracle on the host cores: each step is one call of the workload's
-    sequence restricted to a fixed 1/8 sample of its group positions (exactly
-    the oracle's work on those positions), state carried across steps."""
-    import numpy as np
-    import torch
-    import oracle
-    from bit_error_compensated_gb300.workloads import WORKLOADS, call_sequence, rank_inputs
-    number, bits = args.workload, args.bits
-    w = WORKLOADS[number]
-    P, n = w.P, w.n
-    seq = call_sequence(number, steps=1)
-    Gs = n // P // G
-    rng = np.random.default_rng(number)
-    pos = np.sort(rng.choice(P * Gs, size=max(1, P * Gs // 8), replace=False))
-    owners = (pos // Gs).astype(np.int32)
-    idx = (pos[:, None] * G + np.arange(G)[None, :]).ravel()
-    e = np.zeros((pos.size, P, G), np.float32)
-    prepared = []
-    for k in range(min(len(seq), 4)):
-        x = rank_inputs(number, seq[k], "cpu").view(torch.int16).numpy().view(np.uint16)
-        prepared.append(np.ascontiguousarray(x[:, idx].reshape(P, pos.size, G).transpose(1, 0, 2)))
-
-    def step(i):
-        oracle.group_positions(P, owners, bits, prepared[i % len(prepared)], e)
-
-    for i in range(args.warmup):
-        step(i)
+    """`--impl reference`: the oracle on the host cores, K timed steps of
+    OracleSample after W warm-up steps."""
+    s = OracleSample(args.workload, args.bits)
+    for _ in range(args.warmup):
+        s.step()
     t = time.perf_counter()
-    for i in range(args.steps):
-        step(i)
+    for _ in range(args.steps):
+        s.step()
     sec = time.perf_counter() - t
-    bytes_per_step = pos.size * P * G * 2
-    v = bytes_per_step * args.steps / sec / 1e9
-    sample = (f"each step: one call of {w.name} on a fixed 1/8 sample of its group positions "
-              f"({pos.size} of {P * Gs}), 4 distinct inputs cycled, state carried")
+    v = s.bytes_per_step * args.steps / sec / 1e9
+    w = s.w
     return {"impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": "GB/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(sec / args.steps * 1e3, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic (seeded; shapes and distributions of the workload, no dataset)",
-            "config": {"workload": w.name, "P": P, "n_per_rank": n, "bits": bits, "g": G,
+            "config": {"workload": w.name, "P": w.P, "n_per_rank": w.n, "bits": args.bits, "g": G,
                        "compensated": True},
             "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                             "sample": sample},
+                             "sample": s.sample},
             "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
 
@@ -530,6 +531,8 @@ def main(argv=None):
     ap.add_argument("--bits", type=int, default=4, choices=[4, 8])
     ap.add_argument("--fused", action="store_true", help="reduce kernel writes the outputs itself")
     ap.add_argument("--also", default="4", help="other workloads to time, comma-separated ('' for none)")
+    ap.add_argument("--calls", type=int, default=0,
+                    help="time only the first N calls of the sequence (profiling runs)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
