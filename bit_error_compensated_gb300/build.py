@@ -19,7 +19,7 @@ ROOT = PKG.parent
 CSRC = PKG / "csrc"
 LIBDIR = PKG / "lib"
 LIB = LIBDIR / "libecho.so"
-SOURCES = ["echo_api.cu", "k_push.cu", "k_reduce.cu", "k_gather.cu"]
+SOURCES = ["echo_api.cu", "k_push.cu", "k_reduce.cu", "k_gather.cu", "echo_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

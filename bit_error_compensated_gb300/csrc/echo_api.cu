@@ -59,6 +59,10 @@ bool g_kernels_prepared[64] = {false};
 
 }  // namespace
 
+namespace echo {
+int note_cuda_error(cudaError_t e) { return cuda_fail(e); }
+}  // namespace echo
+
 extern "C" {
 
 int echo_plan(int P, int64_t n, int g, int bits, echo_plan_t* out) {
@@ -277,6 +281,8 @@ const char* echo_strerror(int status) {
     case ECHO_ERR_CUDA: return cudaGetErrorString(g_last_cuda);
     case ECHO_ERR_OVERFLOW: return "non-finite input or fp16 step overflow in some group";
     case ECHO_ERR_TIMEOUT: return "a device-side wait gave up";
+    case ECHO_ERR_TOO_LARGE:
+      return "problem needs more receive-slot space than the fixed no-allocation area holds";
     default: return "unknown status";
   }
 }

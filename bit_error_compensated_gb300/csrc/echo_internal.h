@@ -43,5 +43,8 @@ cudaError_t launch_reduce(const CallArgs& a, int bits, bool fused, cudaStream_t 
 cudaError_t launch_gather(const CallArgs& a, int bits, cudaStream_t s, bool pdl);
 // One-time per-device set-up of kernel attributes (dynamic shared memory).
 cudaError_t prepare_kernels();
+// Records `e` as the error echo_strerror(ECHO_ERR_CUDA) reports in this thread
+// and returns ECHO_ERR_CUDA.
+int note_cuda_error(cudaError_t e);
 
 }  // namespace echo

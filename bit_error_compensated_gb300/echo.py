@@ -25,6 +25,8 @@ ECHO_ERR_ALIGN = 4
 ECHO_ERR_CUDA = 5
 ECHO_ERR_OVERFLOW = 6
 ECHO_ERR_TIMEOUT = 7
+ECHO_ERR_TOO_LARGE = 8
+ECHO_NOALLOC_SCRATCH_BYTES = 32 << 20
 ECHO_MAX_RANKS = 16
 COMP_DEFAULT = ctypes.c_void_p(-1 & (2 ** 64 - 1))   # ECHO_COMP_DEFAULT
 
@@ -41,6 +43,8 @@ _SIGS = {
     "echo_debug_wire": (_i32, [_vp, _vp, _sz, _vp]),
     "echo_set_fused": (_i32, [_vp, _i32]),
     "echo_set_timing": (_i32, [_vp, ctypes.POINTER(_vp), _i32]),
+    "echo_allreduce_noalloc": (_i32, [_i32, _i64, _i32, ctypes.POINTER(_vp), ctypes.POINTER(_vp),
+                                      _vp, _vp]),
     "echo_plan_destroy": (None, [_vp]),
     "echo_strerror": (ctypes.c_char_p, [_i32]),
 }
@@ -167,6 +171,18 @@ def echo_set_timing(plan: Plan, events) -> None:
         return
     arr = (_vp * 4)(*[ev.cuda_event for ev in events])
     _check(_lib.echo_set_timing(plan, arr, 4), "echo_set_timing")
+
+
+def echo_allreduce_noalloc(P: int, n: int, bits: int, ins, outs, comp_state=None,
+                           stream=None) -> None:
+    """The no-allocation call (see include/echo.h): no plan, receive slots in
+    the library's fixed device array; comp_state is None or a caller buffer."""
+    if len(ins) != P or len(outs) != P:
+        raise ValueError(f"expected {P} input and {P} output buffers")
+    arr_in = (_vp * P)(*[_ptr(t) for t in ins])
+    arr_out = (_vp * P)(*[_ptr(t) for t in outs])
+    _check(_lib.echo_allreduce_noalloc(P, n, bits, arr_in, arr_out, _ptr(comp_state),
+                                       _stream(stream)), "echo_allreduce_noalloc")
 
 
 def echo_plan_destroy(plan: Plan) -> None:

@@ -64,6 +64,7 @@ extern "C" {
 #define ECHO_ERR_CUDA        5  /* a CUDA runtime call failed */
 #define ECHO_ERR_OVERFLOW    6  /* (status word) a non-finite input or an fp16 step overflow */
 #define ECHO_ERR_TIMEOUT     7  /* (status word) a device-side wait gave up */
+#define ECHO_ERR_TOO_LARGE   8  /* echo_allreduce_noalloc: beyond its fixed scratch area */
 
 #define ECHO_MAX_RANKS 16
 
@@ -177,6 +178,46 @@ int echo_set_fused(echo_plan_t plan, int fused);
  * fused).  count 4 enables, count 0 disables.  The caller owns the events.
  */
 int echo_set_timing(echo_plan_t plan, void* const* events, int count);
+
+/*
+ * echo_allreduce_noalloc -- the same call as echo_allreduce, for callers that
+ * must not allocate device memory.  The paper has no counterpart: this is an
+ * interface of this library only.
+ *
+ * Who needs it: code that runs where another component owns the device memory
+ * budget and forbids allocation on the execution path (a plugin inside an
+ * inference runtime, for one), and latency-critical loops where cudaMalloc's
+ * implicit device synchronization, or an allocation failing late on a nearly
+ * full device, is not acceptable.  echo_plan allocates its receive slots and
+ * state with cudaMalloc; this entry point needs no plan and allocates nothing.
+ *
+ * Scratch: the receive slots live in one file-scope __device__ array of
+ * ECHO_NOALLOC_SCRATCH_BYTES (32 MiB).  Every GPU that loads the library's
+ * device code holds it until the process exits (with CUDA's default lazy
+ * module loading, from this entry point's first call on that GPU).  The first call on a device looks the array's
+ * device address up (cudaGetSymbolAddress) and sets the kernels' attributes,
+ * with that device current; make that first call before any stream capture.
+ * Every call on a device shares the array and leaves the last call's codes in
+ * it (the call clears what must start at zero itself), so calls whose work
+ * overlaps on the GPU -- on different streams, or from different threads
+ * without ordering -- race.  Calls on one stream are ordered and safe.
+ *
+ *   P, n, bits  as for echo_plan, with g = 128.  A problem whose receive slots
+ *               (about P*n*(b/8 + 4/128) bytes, see echo_wire_layout) do not
+ *               fit the array returns ECHO_ERR_TOO_LARGE; for example P=4 with
+ *               4-bit codes fits up to 2048 x 4096 elements per rank.
+ *   in, out     as for echo_allreduce (same alignment and aliasing rules).
+ *   comp_state  NULL (uncompensated) or a caller device buffer of P*n*4 bytes,
+ *               fp32 [P][n], as for echo_allreduce; ECHO_COMP_DEFAULT is
+ *               rejected (ECHO_ERR_ARG) since there is no plan.
+ *   stream      cudaStream_t as void*.
+ * Outputs, state and codes are bit-identical to echo_allreduce's (unfused
+ * gather).  Non-finite inputs are not reported: there is no status word to
+ * read back.
+ */
+#define ECHO_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+int echo_allreduce_noalloc(int P, int64_t n, int bits, const void* const* in,
+                           void* const* out, void* comp_state, void* stream);
 
 /* Free everything the plan allocated.  NULL is accepted. */
 void echo_plan_destroy(echo_plan_t plan);
