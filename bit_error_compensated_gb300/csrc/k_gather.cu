@@ -5,10 +5,11 @@
 // all-gather is one read of each segment's codes and P writes of the decoded
 // bf16 values.
 //
-// One warp per group, 4 elements per lane: a warp reads 64 B (4-bit) or 128 B
-// (8-bit) of codes plus one meta word and writes P x 256 B of bf16 with
-// streaming stores.  U groups per warp are read before any is written, to keep
-// several code reads in flight.  Write-bound: P * 2 bytes out per element.
+// Half a warp per group, 8 elements per lane (quant.cuh): a warp reads the
+// codes and meta words of two adjacent groups and writes P x 2 x 256 B of bf16
+// with streaming stores.  U group pairs per warp are read before any is
+// written, to keep several code reads in flight.  Write-bound: P * 2 bytes out
+// per element.
 #include "echo_internal.h"
 #include "quant.cuh"
 
@@ -21,42 +22,53 @@ gather_kernel(const CallArgs a) {
   constexpr int CB = 16 * BITS;
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int lane = threadIdx.x & 31;
-  const int64_t warp = ((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5;
-  const int64_t nwarp = ((int64_t)gridDim.x * kThreads) >> 5;
+  const int half = lane >> 4;
+  const int h = lane & 15;
+  const int64_t wg = (int64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
+  const int64_t nw = (int64_t)gridDim.x * (kThreads / 32);
   const int P = a.P;
-  const int64_t W = (int64_t)P * a.Gs;    // groups of one rank tensor
+  const int o = blockIdx.y;                       // owner segment
+  const int64_t Gs = a.Gs;
+  const uint8_t* cs = a.codes2 + (int64_t)o * Gs * CB;
+  const uint32_t* ms = a.meta2 + (int64_t)o * a.Gs_pad;
+  const int64_t W = Gs;
 
-  for (int64_t base = warp; base < W; base += nwarp * U) {
-    uint32_t word[U], meta[U];
+  // Two adjacent groups per warp (half a warp each), U pairs in flight.
+  for (int64_t pair0 = wg; 2 * pair0 < W; pair0 += nw * U) {
+    uint32_t wa[U], wb[U], meta[U];
+    int64_t w[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      const int64_t w = base + (int64_t)u * nwarp;
-      if (w < W) {
-        const int64_t o = w / a.Gs;
-        const int64_t j = w - o * a.Gs;
-        meta[u] = a.meta2[o * a.Gs_pad + j];
+      w[u] = 2 * (pair0 + (int64_t)u * nw) + half;
+      if (w[u] < W) {
+        meta[u] = ms[w[u]];
+        const uint8_t* cg = cs + w[u] * CB;
         if (BITS == 4) {
-          word[u] = reinterpret_cast<const uint16_t*>(a.codes2 + w * CB)[lane];
+          wa[u] = reinterpret_cast<const uint16_t*>(cg)[h];
+          wb[u] = reinterpret_cast<const uint16_t*>(cg + 32)[h];
         } else {
-          word[u] = reinterpret_cast<const uint32_t*>(a.codes2 + w * CB)[lane];
+          wa[u] = reinterpret_cast<const uint32_t*>(cg)[h];
+          wb[u] = reinterpret_cast<const uint32_t*>(cg + 64)[h];
         }
       }
     }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      const int64_t w = base + (int64_t)u * nwarp;
-      if (w >= W) break;                      // warp-uniform
-      float s;
-      int z;
-      unpack_meta(meta[u], s, z);
-      int q[4];
-      unpack4<BITS>(word[u], q);
-      float deq[4], yb[4];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) deq[k] = decode(q[k], z, s);
-      const uint2 y = f32x4_to_bf16(deq, yb);
-      const int64_t elem = w * kGroup + 4 * lane;
-      for (int r = 0; r < P; ++r) __stcs(reinterpret_cast<uint2*>(a.out[r] + elem), y);
+      if (w[u] >= W) continue;
+      float s, zf;
+      unpack_meta(meta[u], s, zf);
+      float deq[8], yb[8];
+      decode4<BITS>(wa[u], s, zf, deq);
+      decode4<BITS>(wb[u], s, zf, deq + 4);
+      const uint2 ya = f32x4_to_bf16(deq, yb);
+      const uint2 yv = f32x4_to_bf16(deq + 4, yb + 4);
+      const int64_t grp = (int64_t)o * Gs + w[u];  // group index in the rank tensor
+      const int64_t ea = grp * kGroup + chunk_a(h);
+      const int64_t eb = grp * kGroup + chunk_b(h);
+      for (int r = 0; r < P; ++r) {
+        __stcs(reinterpret_cast<uint2*>(a.out[r] + ea), ya);
+        __stcs(reinterpret_cast<uint2*>(a.out[r] + eb), yv);
+      }
     }
   }
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -77,13 +89,16 @@ cudaError_t launch_t(const CallArgs& a, cudaStream_t s, bool pdl) {
                                                   kThreads, 0);
     grid = sms * (per_sm > 0 ? per_sm : 1);
   }
-  const int64_t W = (int64_t)a.P * a.Gs;
-  const int64_t warps_needed = (W + kGatherUnroll - 1) / kGatherUnroll;
-  const int64_t blocks_needed = (warps_needed + (kThreads / 32) - 1) / (kThreads / 32);
-  const int blocks = (int)(blocks_needed < grid ? blocks_needed : grid);
+  // Blocks per owner segment: enough to fill the GPU once across the P
+  // segments, but no more than the segment has group pairs for.
+  const int64_t per_block = (int64_t)(kThreads / 32) * kGatherUnroll * 2;
+  const int64_t need = (a.Gs + per_block - 1) / per_block;
+  int64_t bx = (grid + a.P - 1) / a.P;
+  if (bx > need) bx = need;
+  if (bx < 1) bx = 1;
 
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(blocks);
+  cfg.gridDim = dim3((unsigned)bx, (unsigned)a.P);
   cfg.blockDim = dim3(kThreads);
   cfg.stream = s;
   cudaLaunchAttribute attr[1];

@@ -8,126 +8,203 @@
 // element is added before quantizing, and the error this quantization reveals,
 // v - deq(q), replaces it (the update changes nothing this call computes).
 //
-// Work unit: one group of 128 elements of one rank's non-owned segment, one
-// warp per group, 4 consecutive elements per lane, so each warp-wide access is
-// contiguous: 256 B of bf16 input, 512 B of fp32 state, 64 B (4-bit) or 128 B
-// (8-bit) of codes.  U groups per warp are loaded before any is processed to
-// keep enough bytes in flight for HBM.  HBM-bound: per group the kernel reads
-// 256 B + 512 B and writes 512 B + codes + 4 B of meta.
+// Grid: blockIdx.y is a (sender p, owner o) segment pair, blockIdx.x strides
+// over the segment's groups, so no division is needed per group.  Half a warp
+// per 128-element group (quant.cuh); a warp works on two adjacent groups at a
+// time (a "pair": 512 B of bf16 input and 1 KB of fp32 state, contiguous).
+//
+// Each warp runs its own kPushStages-deep pipeline: lane 0 issues 1-D bulk
+// copies (cp.async.bulk, the TMA engine) of the next pairs' input and state
+// into the warp's shared-memory stages, each stage completing on its own
+// mbarrier, while the warp quantizes the current pair from shared memory and
+// stores codes, meta and the new state straight to global memory.  Loads stay
+// in flight during compute without holding registers.  The waits are bounded:
+// on timeout the warp records ECHO_ERR_TIMEOUT, waits once more (bounded) for
+// each copy it still has in flight, and returns.  HBM-bound: per group
+// 256 B + 512 B read, 512 B + codes + 4 B of meta written.
 #include "echo_internal.h"
 #include "quant.cuh"
+#include "tma.cuh"
 
 namespace echo {
 namespace {
 
-template <int BITS, bool COMP, int U>
+constexpr int kPushStages = 4;
+constexpr int kPairX = 2 * kGroup * 2;      // bf16 bytes of a pair
+constexpr int kPairE = 2 * kGroup * 4;      // fp32 state bytes of a pair
+
+template <bool COMP>
+constexpr int push_stage_bytes() { return kPairX + (COMP ? kPairE : 0); }
+
+template <bool COMP>
+constexpr size_t push_smem_bytes() {
+  return (size_t)(kThreads / 32) * kPushStages * push_stage_bytes<COMP>();
+}
+
+template <int BITS, bool COMP>
 __global__ void __launch_bounds__(kThreads)
 push_kernel(const CallArgs a) {
   constexpr float L = (float)((1 << BITS) - 1);
-  constexpr int CB = 16 * BITS;                 // code bytes per group
+  constexpr int CB = 16 * BITS;                     // code bytes per group
+  constexpr int S = kPushStages;
+  constexpr int SB = push_stage_bytes<COMP>();
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ __align__(8) uint64_t bars[kThreads / 32][S];
+
+  const int P = a.P;
+  const int p = (int)blockIdx.y / (P - 1);          // sender
+  const int oi = (int)blockIdx.y - p * (P - 1);
+  const int o = oi + (oi >= p ? 1 : 0);             // owner of the segment
+  const int slot = o * (P - 1) + (p < o ? p : p - 1);
+  const int64_t Gs = a.Gs;
+  const __nv_bfloat16* xs = a.in[p] + (int64_t)o * Gs * kGroup;
+  float* es = COMP ? a.comp + (int64_t)p * a.n + (int64_t)o * Gs * kGroup : nullptr;
+  uint8_t* cs = a.codes1 + (int64_t)slot * Gs * CB;
+  uint32_t* ms = a.meta1 + (int64_t)slot * a.Gs_pad;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int half = lane >> 4;
+  const int h = lane & 15;
+  const int64_t wg = (int64_t)blockIdx.x * (kThreads / 32) + warp;
+  const int64_t nw = (int64_t)gridDim.x * (kThreads / 32);
+  const int64_t npairs = (Gs + 1) / 2;
+  uint8_t* wbuf = smem + (size_t)warp * S * SB;
+  const uint32_t bar0 = smem_addr(&bars[warp][0]);
+
+  if (lane == 0) {
+#pragma unroll
+    for (int st = 0; st < S; ++st) mbar_init(bar0 + 8 * st, 1);
+    fence_barrier_init();
+  }
+  __syncwarp();
   asm volatile("griddepcontrol.wait;" ::: "memory");
 
-  const int lane = threadIdx.x & 31;
-  const int64_t warp = ((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5;
-  const int64_t nwarp = ((int64_t)gridDim.x * kThreads) >> 5;
-  const int P = a.P;
-  const int64_t Gs = a.Gs;
-  const int64_t per_rank = (int64_t)(P - 1) * Gs;  // non-owned groups of a rank
-  const int64_t W = (int64_t)P * per_rank;
+  uint64_t pol = 0;
+  if (lane == 0) pol = policy_evict_first();        // input and state are read once per call
+  // Lane 0: start the copies of iteration i into stage st.
+  auto issue = [&](int64_t i, int st) {
+    const int64_t pr = wg + i * nw;
+    if (pr >= npairs) return;
+    const int64_t g0 = 2 * pr;
+    const uint32_t ng = (uint32_t)((Gs - g0) < 2 ? (Gs - g0) : 2);
+    const uint32_t bar = bar0 + 8 * st;
+    mbar_expect_tx(bar, ng * (COMP ? 768u : 256u));
+    bulk_g2s(smem_addr(wbuf + st * SB), xs + g0 * kGroup, ng * 256u, bar, pol);
+    if (COMP) bulk_g2s(smem_addr(wbuf + st * SB + kPairX), es + g0 * kGroup, ng * 512u, bar, pol);
+  };
+  if (lane == 0) {
+#pragma unroll
+    for (int st = 0; st < S; ++st) issue(st, st);
+  }
 
-  for (int64_t base = warp; base < W; base += nwarp * U) {
-    float v[U][4];
-    int64_t elem[U];      // first element of the group within the rank's tensor
-    int64_t dst[U];       // group index in the push-code array
-    int64_t midx[U];      // index in the push-meta array
-    int prank[U];
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int64_t w = base + (int64_t)u * nwarp;
-      prank[u] = -1;
-      if (w < W) {
-        const int p = (int)(w / per_rank);
-        const int64_t r = w - (int64_t)p * per_rank;
-        const int oi = (int)(r / Gs);
-        const int64_t j = r - (int64_t)oi * Gs;
-        const int o = oi + (oi >= p ? 1 : 0);         // owner of the segment
-        const int slot = o * (P - 1) + (p < o ? p : p - 1);
-        prank[u] = p;
-        elem[u] = ((int64_t)o * Gs + j) * kGroup + 4 * lane;
-        dst[u] = (int64_t)slot * Gs + j;
-        midx[u] = (int64_t)slot * a.Gs_pad + j;
-        const uint2 xr = __ldcs(reinterpret_cast<const uint2*>(a.in[p] + elem[u]));
-        bf16x4_to_f32(xr, v[u]);
-        if (COMP) {
-          const float4 e = __ldcs(reinterpret_cast<const float4*>(a.comp + (int64_t)p * a.n + elem[u]));
-          v[u][0] = __fadd_rn(v[u][0], e.x);
-          v[u][1] = __fadd_rn(v[u][1], e.y);
-          v[u][2] = __fadd_rn(v[u][2], e.z);
-          v[u][3] = __fadd_rn(v[u][3], e.w);
-        }
+  for (int64_t i = 0; wg + i * nw < npairs; ++i) {
+    const int st = (int)(i % S);
+    const uint32_t parity = (uint32_t)((i / S) & 1);
+    if (!mbar_wait_bounded(bar0 + 8 * st, parity)) {
+      if (lane == 0) atomicOr(a.status, kStatusTimeout);
+      for (int k = 0; k < S; ++k) {               // copies still in flight
+        const int64_t ii = i + k;
+        if (wg + ii * nw < npairs) mbar_wait_bounded(bar0 + 8 * (int)(ii % S), (uint32_t)((ii / S) & 1));
       }
+      return;
     }
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      if (prank[u] < 0) break;                       // warp-uniform
-      float lo, hi;
-      warp_range(v[u], lo, hi);
-      const GroupGrid gg = make_grid(lo, hi, L);
-      int q[4];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) q[k] = encode(v[u][k], gg, L);
-      const uint32_t word = pack4<BITS>(q);
-      if (BITS == 4) {
-        reinterpret_cast<uint16_t*>(a.codes1 + dst[u] * CB)[lane] = (uint16_t)word;
-      } else {
-        reinterpret_cast<uint32_t*>(a.codes1 + dst[u] * CB)[lane] = word;
-      }
-      if (lane == 0) a.meta1[midx[u]] = gg.meta;
+    const int64_t j = 2 * (wg + i * nw) + half;      // this half's group
+    const bool valid = j < Gs;
+    float v[8];
+    if (valid) {
+      const uint2* sx = reinterpret_cast<const uint2*>(wbuf + st * SB) + half * 32;
+      bf16x4_to_f32(sx[h], v);
+      bf16x4_to_f32(sx[16 + h], v + 4);
       if (COMP) {
-        float4 en;
-        en.x = __fsub_rn(v[u][0], decode(q[0], gg.z, gg.s));
-        en.y = __fsub_rn(v[u][1], decode(q[1], gg.z, gg.s));
-        en.z = __fsub_rn(v[u][2], decode(q[2], gg.z, gg.s));
-        en.w = __fsub_rn(v[u][3], decode(q[3], gg.z, gg.s));
-        *reinterpret_cast<float4*>(a.comp + (int64_t)prank[u] * a.n + elem[u]) = en;
+        const float4* se = reinterpret_cast<const float4*>(wbuf + st * SB + kPairX) + half * 32;
+        const float4 ea = se[h];
+        const float4 eb = se[16 + h];
+        v[0] = __fadd_rn(v[0], ea.x);
+        v[1] = __fadd_rn(v[1], ea.y);
+        v[2] = __fadd_rn(v[2], ea.z);
+        v[3] = __fadd_rn(v[3], ea.w);
+        v[4] = __fadd_rn(v[4], eb.x);
+        v[5] = __fadd_rn(v[5], eb.y);
+        v[6] = __fadd_rn(v[6], eb.z);
+        v[7] = __fadd_rn(v[7], eb.w);
       }
-      const bool bad = !gg.finite || !all_finite4(v[u]);
-      if (__any_sync(kFull, bad) && lane == 0) atomicOr(a.status, kStatusOverflow);
+    } else {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) v[k] = 0.0f;       // idle half of a one-group pair
+    }
+    // The stage has been read into registers: hand it back to the copy engine.
+    __syncwarp();
+    if (lane == 0) {
+      fence_proxy_async();
+      issue(i + S, st);
+    }
+
+    float lo, hi;
+    half_range(v, lo, hi);
+    const GroupGrid gg = make_grid(lo, hi, L);
+    float c[8], d[8];
+    quantize8(v, gg, L, c, d);
+    if (valid) {
+      uint8_t* cg = cs + j * CB;
+      if (BITS == 4) {
+        reinterpret_cast<uint16_t*>(cg)[h] = (uint16_t)pack4<4>(c);
+        reinterpret_cast<uint16_t*>(cg + 32)[h] = (uint16_t)pack4<4>(c + 4);
+      } else {
+        reinterpret_cast<uint32_t*>(cg)[h] = pack4<8>(c);
+        reinterpret_cast<uint32_t*>(cg + 64)[h] = pack4<8>(c + 4);
+      }
+      if (h == 0) ms[j] = gg.meta;
+      if (COMP) {
+        float* eg = es + j * kGroup;
+        *reinterpret_cast<float4*>(eg + chunk_a(h)) =
+            make_float4(__fsub_rn(v[0], d[0]), __fsub_rn(v[1], d[1]),
+                        __fsub_rn(v[2], d[2]), __fsub_rn(v[3], d[3]));
+        *reinterpret_cast<float4*>(eg + chunk_b(h)) =
+            make_float4(__fsub_rn(v[4], d[4]), __fsub_rn(v[5], d[5]),
+                        __fsub_rn(v[6], d[6]), __fsub_rn(v[7], d[7]));
+      }
+      if (!gg.finite && h == 0) atomicOr(a.status, kStatusOverflow);
     }
   }
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-constexpr int kPushUnroll = 4;
-
 template <int BITS, bool COMP>
 cudaError_t launch_t(const CallArgs& a, cudaStream_t s, bool pdl) {
-  static int grid_cache[64] = {0};
+  static int resident_cache[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
-  int& grid = grid_cache[dev & 63];
-  if (grid == 0) {
+  int& resident = resident_cache[dev & 63];
+  if (resident == 0) {
     int sms = 0, per_sm = 0;
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, push_kernel<BITS, COMP, kPushUnroll>,
-                                                  kThreads, 0);
-    grid = sms * (per_sm > 0 ? per_sm : 1);
+    cudaFuncSetAttribute(push_kernel<BITS, COMP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         (int)push_smem_bytes<COMP>());
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, push_kernel<BITS, COMP>, kThreads,
+                                                  push_smem_bytes<COMP>());
+    resident = sms * (per_sm > 0 ? per_sm : 1);
   }
-  const int64_t W = (int64_t)a.P * (a.P - 1) * a.Gs;
-  const int64_t warps_needed = (W + kPushUnroll - 1) / kPushUnroll;
-  const int64_t blocks_needed = (warps_needed + (kThreads / 32) - 1) / (kThreads / 32);
-  const int blocks = (int)(blocks_needed < grid ? blocks_needed : grid);
+  const int pairs = a.P * (a.P - 1);
+  // Blocks per segment: enough to fill the GPU once across all segments, but
+  // no more than the segment has group pairs for (8 warps x U pairs each).
+  const int64_t per_block = (int64_t)(kThreads / 32) * 2;
+  const int64_t need = (a.Gs + per_block - 1) / per_block;
+  int64_t bx = (resident + pairs - 1) / pairs;
+  if (bx > need) bx = need;
+  if (bx < 1) bx = 1;
 
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(blocks);
+  cfg.gridDim = dim3((unsigned)bx, (unsigned)pairs);
   cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = push_smem_bytes<COMP>();
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, push_kernel<BITS, COMP, kPushUnroll>, a);
+  return cudaLaunchKernelEx(&cfg, push_kernel<BITS, COMP>, a);
 }
 
 }  // namespace

@@ -19,47 +19,10 @@
 // buffers, so the separate gather kernel is skipped.
 #include "echo_internal.h"
 #include "quant.cuh"
+#include "tma.cuh"
 
 namespace echo {
 namespace {
-
-constexpr uint64_t kWaitLimitNs = 1000ull * 1000ull * 1000ull;  // 1 s
-
-__device__ __forceinline__ uint32_t smem_addr(const void* p) {
-  return (uint32_t)__cvta_generic_to_shared(p);
-}
-
-__device__ __forceinline__ uint64_t global_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-      :: "r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-  uint32_t done;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(done) : "r"(bar), "r"(parity) : "memory");
-  return done != 0;
-}
-
-// Wait for phase `parity` of the barrier, giving up after kWaitLimitNs.
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = global_ns();
-  while (!mbar_try_wait(bar, parity)) {
-    if (global_ns() - t0 > kWaitLimitNs) return false;
-  }
-  return true;
-}
 
 template <int BITS, bool COMP, bool FUSED>
 __global__ void __launch_bounds__(kThreads)
@@ -83,9 +46,8 @@ reduce_kernel(const CallArgs a, int64_t tiles_per_seg) {
   const uint32_t bar_a = smem_addr(&bar);
   const int64_t seg_group0 = (int64_t)o * a.Gs + j0;           // first group of the tile in the rank tensor
   if (threadIdx.x == 0) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" :: "r"(bar_a) : "memory");
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    mbar_init(bar_a, 1);
+    fence_barrier_init();
   }
   __syncthreads();
 
@@ -98,18 +60,19 @@ reduce_kernel(const CallArgs a, int64_t tiles_per_seg) {
     if (P == 1) asm volatile("griddepcontrol.wait;" ::: "memory");
     const uint32_t meta_bytes = (uint32_t)(((t + 3) & ~3) * 4);
     const uint32_t total = (uint32_t)((P - 1) * (t * CB + meta_bytes) + t * 256 + (COMP ? t * 512 : 0));
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
-                 :: "r"(bar_a), "r"(total) : "memory");
-    bulk_g2s(smem_addr(s_x), a.in[o] + seg_group0 * kGroup, (uint32_t)(t * 256), bar_a);
+    const uint64_t pol = policy_evict_first();     // every byte here is read once per call
+    mbar_expect_tx(bar_a, total);
+    bulk_g2s(smem_addr(s_x), a.in[o] + seg_group0 * kGroup, (uint32_t)(t * 256), bar_a, pol);
     if (COMP) {
-      bulk_g2s(smem_addr(s_e), a.comp + (int64_t)o * a.n + seg_group0 * kGroup, (uint32_t)(t * 512), bar_a);
+      bulk_g2s(smem_addr(s_e), a.comp + (int64_t)o * a.n + seg_group0 * kGroup, (uint32_t)(t * 512),
+               bar_a, pol);
     }
     asm volatile("griddepcontrol.wait;" ::: "memory");
     for (int js = 0; js < P - 1; ++js) {
       const int64_t slot = (int64_t)o * (P - 1) + js;
       bulk_g2s(smem_addr(s_codes + js * T * CB), a.codes1 + (slot * a.Gs + j0) * CB,
-               (uint32_t)(t * CB), bar_a);
-      bulk_g2s(smem_addr(s_meta + js * T), a.meta1 + slot * a.Gs_pad + j0, meta_bytes, bar_a);
+               (uint32_t)(t * CB), bar_a, pol);
+      bulk_g2s(smem_addr(s_meta + js * T), a.meta1 + slot * a.Gs_pad + j0, meta_bytes, bar_a, pol);
     }
   } else {
     asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -123,81 +86,96 @@ reduce_kernel(const CallArgs a, int64_t tiles_per_seg) {
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  for (int gl = warp; gl < t; gl += kThreads / 32) {
-    float acc[4];
-#pragma unroll 1
+  const int half = lane >> 4;
+  const int h = lane & 15;
+  // Two groups per warp per pass (half a warp each, see quant.cuh).
+  for (int gp = 2 * warp; gp < t; gp += 2 * (kThreads / 32)) {
+    const int gl = gp + half;                      // group within the tile
+    const bool valid = gl < t;
+    const int gs = valid ? gl : gp;                // idle half reads a valid group
+    float acc[8];
+#pragma unroll 4
     for (int p = 0; p < P; ++p) {
-      float term[4];
+      float term[8];
       if (p == o) {
-        bf16x4_to_f32(s_x[gl * 32 + lane], term);
+        bf16x4_to_f32(s_x[gs * 32 + h], term);
+        bf16x4_to_f32(s_x[gs * 32 + 16 + h], term + 4);
         if (COMP) {
-          const float4 e = s_e[gl * 32 + lane];
-          term[0] = __fadd_rn(term[0], e.x);
-          term[1] = __fadd_rn(term[1], e.y);
-          term[2] = __fadd_rn(term[2], e.z);
-          term[3] = __fadd_rn(term[3], e.w);
+          const float4 ea = s_e[gs * 32 + h];
+          const float4 eb = s_e[gs * 32 + 16 + h];
+          term[0] = __fadd_rn(term[0], ea.x);
+          term[1] = __fadd_rn(term[1], ea.y);
+          term[2] = __fadd_rn(term[2], ea.z);
+          term[3] = __fadd_rn(term[3], ea.w);
+          term[4] = __fadd_rn(term[4], eb.x);
+          term[5] = __fadd_rn(term[5], eb.y);
+          term[6] = __fadd_rn(term[6], eb.z);
+          term[7] = __fadd_rn(term[7], eb.w);
         }
       } else {
         const int js = p < o ? p : p - 1;
-        float s;
-        int z;
-        unpack_meta(s_meta[js * T + gl], s, z);
-        uint32_t w;
+        float s, zf;
+        unpack_meta(s_meta[js * T + gs], s, zf);
+        const uint8_t* cg = s_codes + (js * T + gs) * CB;
+        uint32_t wa, wb;
         if (BITS == 4) {
-          w = reinterpret_cast<const uint16_t*>(s_codes + (js * T + gl) * CB)[lane];
+          wa = reinterpret_cast<const uint16_t*>(cg)[h];
+          wb = reinterpret_cast<const uint16_t*>(cg + 32)[h];
         } else {
-          w = reinterpret_cast<const uint32_t*>(s_codes + (js * T + gl) * CB)[lane];
+          wa = reinterpret_cast<const uint32_t*>(cg)[h];
+          wb = reinterpret_cast<const uint32_t*>(cg + 64)[h];
         }
-        int q[4];
-        unpack4<BITS>(w, q);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) term[k] = decode(q[k], z, s);
+        decode4<BITS>(wa, s, zf, term);
+        decode4<BITS>(wb, s, zf, term + 4);
       }
       if (p == 0) {
 #pragma unroll
-        for (int k = 0; k < 4; ++k) acc[k] = term[k];
+        for (int k = 0; k < 8; ++k) acc[k] = term[k];
       } else {
 #pragma unroll
-        for (int k = 0; k < 4; ++k) acc[k] = __fadd_rn(acc[k], term[k]);
+        for (int k = 0; k < 8; ++k) acc[k] = __fadd_rn(acc[k], term[k]);
       }
     }
 
     // Quantize the sum once for the gather.
     float lo, hi;
-    warp_range(acc, lo, hi);
+    half_range(acc, lo, hi);
     const GroupGrid gg = make_grid(lo, hi, L);
-    int q[4];
-    float deq[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      q[k] = encode(acc[k], gg, L);
-      deq[k] = decode(q[k], gg.z, gg.s);
-    }
+    float c[8], deq[8];
+    quantize8(acc, gg, L, c, deq);
+    if (!valid) continue;
     const int64_t grp = seg_group0 + gl;           // group index in the rank tensor
-    const uint32_t word = pack4<BITS>(q);
+    uint8_t* cg = a.codes2 + grp * CB;
     if (BITS == 4) {
-      reinterpret_cast<uint16_t*>(a.codes2 + grp * CB)[lane] = (uint16_t)word;
+      reinterpret_cast<uint16_t*>(cg)[h] = (uint16_t)pack4<4>(c);
+      reinterpret_cast<uint16_t*>(cg + 32)[h] = (uint16_t)pack4<4>(c + 4);
     } else {
-      reinterpret_cast<uint32_t*>(a.codes2 + grp * CB)[lane] = word;
+      reinterpret_cast<uint32_t*>(cg)[h] = pack4<8>(c);
+      reinterpret_cast<uint32_t*>(cg + 64)[h] = pack4<8>(c + 4);
     }
-    if (lane == 0) a.meta2[(int64_t)o * a.Gs_pad + j0 + gl] = gg.meta;
+    if (h == 0) a.meta2[(int64_t)o * a.Gs_pad + j0 + gl] = gg.meta;
 
-    float yb[4];
-    const uint2 y = f32x4_to_bf16(deq, yb);
-    const int64_t elem = grp * kGroup + 4 * lane;
+    float yb[8];
+    const uint2 ya = f32x4_to_bf16(deq, yb);
+    const uint2 yv = f32x4_to_bf16(deq + 4, yb + 4);
+    const int64_t ea = grp * kGroup + chunk_a(h);
+    const int64_t eb = grp * kGroup + chunk_b(h);
     if (COMP) {
-      float4 en;
-      en.x = __fsub_rn(acc[0], yb[0]);
-      en.y = __fsub_rn(acc[1], yb[1]);
-      en.z = __fsub_rn(acc[2], yb[2]);
-      en.w = __fsub_rn(acc[3], yb[3]);
-      *reinterpret_cast<float4*>(a.comp + (int64_t)o * a.n + elem) = en;
+      float* eo = a.comp + (int64_t)o * a.n;
+      *reinterpret_cast<float4*>(eo + ea) =
+          make_float4(__fsub_rn(acc[0], yb[0]), __fsub_rn(acc[1], yb[1]),
+                      __fsub_rn(acc[2], yb[2]), __fsub_rn(acc[3], yb[3]));
+      *reinterpret_cast<float4*>(eo + eb) =
+          make_float4(__fsub_rn(acc[4], yb[4]), __fsub_rn(acc[5], yb[5]),
+                      __fsub_rn(acc[6], yb[6]), __fsub_rn(acc[7], yb[7]));
     }
     if (FUSED) {
-      for (int r = 0; r < P; ++r) __stcs(reinterpret_cast<uint2*>(a.out[r] + elem), y);
+      for (int r = 0; r < P; ++r) {
+        __stcs(reinterpret_cast<uint2*>(a.out[r] + ea), ya);
+        __stcs(reinterpret_cast<uint2*>(a.out[r] + eb), yv);
+      }
     }
-    const bool bad = !gg.finite || !all_finite4(acc);
-    if (__any_sync(kFull, bad) && lane == 0) atomicOr(a.status, kStatusOverflow);
+    if (!gg.finite && h == 0) atomicOr(a.status, kStatusOverflow);
   }
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }

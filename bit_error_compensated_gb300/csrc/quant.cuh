@@ -10,7 +10,10 @@
 // decoded value s * (q - z).  Each step is one IEEE fp32 operation with
 // explicit round-to-nearest intrinsics, so no multiply-add is ever fused.
 //
-// One warp handles one group of 128 values, 4 consecutive values per lane.
+// Thread mapping: half a warp (16 lanes) per group of 128 values; lane h of the
+// half holds 8 values, elements [4h, 4h+4) ("chunk A") and [64+4h, 64+4h+4)
+// ("chunk B"), so that every warp-wide load or store of a chunk covers two
+// contiguous runs, one per group.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -21,25 +24,43 @@ namespace echo {
 
 constexpr unsigned kFull = 0xFFFFFFFFu;
 
-struct GroupGrid {
-  float s;        // step (an fp16 value)
-  float zf;       // zero point as a float (an integer value)
-  int z;          // zero point
-  uint32_t meta;  // fp16 step bits | fp16 zero-point bits << 16
-  bool finite;    // false when the step overflowed fp16 (or the range was NaN)
-};
+// NaN-propagating min / max (PTX min.NaN / max.NaN).  For finite and infinite
+// values they equal fminf / fmaxf; a NaN anywhere in a group makes its range,
+// hence its step, NaN, which flags the group (see make_grid).
+__device__ __forceinline__ float min_nan(float a, float b) {
+  float r;
+  asm("min.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ float max_nan(float a, float b) {
+  float r;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+  return r;
+}
 
-// Warp-wide zero-aware range: every lane passes its 4 values, all lanes get
-// (lo, hi) with lo <= 0 <= hi.
-__device__ __forceinline__ void warp_range(const float v[4], float& lo, float& hi) {
-  lo = fminf(fminf(fminf(0.0f, v[0]), fminf(v[1], v[2])), v[3]);
-  hi = fmaxf(fmaxf(fmaxf(0.0f, v[0]), fmaxf(v[1], v[2])), v[3]);
+// Zero-aware range of a group over the 16 lanes of a half warp (all 32 lanes
+// must call it; each half reduces its own group).
+__device__ __forceinline__ void half_range(const float v[8], float& lo, float& hi) {
+  float a = min_nan(min_nan(v[0], v[1]), min_nan(v[2], v[3]));
+  float b = min_nan(min_nan(v[4], v[5]), min_nan(v[6], v[7]));
+  lo = min_nan(min_nan(a, b), 0.0f);
+  a = max_nan(max_nan(v[0], v[1]), max_nan(v[2], v[3]));
+  b = max_nan(max_nan(v[4], v[5]), max_nan(v[6], v[7]));
+  hi = max_nan(max_nan(a, b), 0.0f);
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) {
-    lo = fminf(lo, __shfl_xor_sync(kFull, lo, off));
-    hi = fmaxf(hi, __shfl_xor_sync(kFull, hi, off));
+  for (int off = 8; off > 0; off >>= 1) {
+    lo = min_nan(lo, __shfl_xor_sync(kFull, lo, off));
+    hi = max_nan(hi, __shfl_xor_sync(kFull, hi, off));
   }
 }
+
+struct GroupGrid {
+  float s;        // step (an fp16 value)
+  float inv;      // 1/s rounded to nearest (fast path of v/s, see encode)
+  float zf;       // zero point as a float (an integer value)
+  uint32_t meta;  // fp16 step bits | fp16 zero-point bits << 16
+  bool finite;    // false: non-finite input or step overflow; results unspecified
+};
 
 // Step and zero point of a group from its range.
 __device__ __forceinline__ GroupGrid make_grid(float lo, float hi, float L) {
@@ -52,54 +73,84 @@ __device__ __forceinline__ GroupGrid make_grid(float lo, float hi, float L) {
   }
   float zf = rintf(__fdiv_rn(-lo, s));
   zf = fminf(fmaxf(zf, 0.0f), L);
+  const int z = (int)zf;
   GroupGrid gg;
-  gg.z = (int)zf;
-  gg.zf = (float)gg.z;
   gg.s = s;
+  gg.inv = __frcp_rn(s);
+  gg.zf = (float)z;
   gg.meta = (uint32_t)__half_as_ushort(sh) |
-            ((uint32_t)__half_as_ushort(__int2half_rn(gg.z)) << 16);
+            ((uint32_t)__half_as_ushort(__int2half_rn(z)) << 16);
   gg.finite = isfinite(s);
   return gg;
 }
 
-__device__ __forceinline__ int encode(float v, const GroupGrid& gg, float L) {
-  float c = __fadd_rn(rintf(__fdiv_rn(v, gg.s)), gg.zf);
-  c = fminf(fmaxf(c, 0.0f), L);
-  return (int)c;
-}
+// Largest distance from an integer at which rint(v * (1/s)) is taken as
+// rint(v / s).  For a finite group |v / s| < 256, so the correctly rounded
+// reciprocal and product are within 256 * 3 * 2^-24 < 2^-13 of the correctly
+// rounded quotient; when the product lies farther than that from every
+// half-integer, both round to the same integer.  Otherwise the quotient itself
+// is computed (IEEE division).
+constexpr float kFastRintLimit = 0.5f - 1.0f / 8192.0f;
 
-// s * (q - z): an integer difference, an exact conversion, one multiply.
-__device__ __forceinline__ float decode(int q, int z, float s) {
-  return __fmul_rn((float)(q - z), s);
-}
-
-// Meta word -> (step, zero point).
-__device__ __forceinline__ void unpack_meta(uint32_t meta, float& s, int& z) {
-  s = __half2float(__ushort_as_half((unsigned short)(meta & 0xFFFFu)));
-  z = (int)__half2float(__ushort_as_half((unsigned short)(meta >> 16)));
-}
-
-// 4 codes of one lane <-> its slice of the packed group.  4-bit: element 2i in
-// the low nibble of byte i, so 4 consecutive codes form one little-endian
-// 16-bit word; 8-bit: one byte each, one 32-bit word.
-template <int BITS>
-__device__ __forceinline__ uint32_t pack4(const int q[4]) {
-  if (BITS == 4) {
-    return (uint32_t)q[0] | ((uint32_t)q[1] << 4) | ((uint32_t)q[2] << 8) | ((uint32_t)q[3] << 12);
-  } else {
-    return (uint32_t)q[0] | ((uint32_t)q[1] << 8) | ((uint32_t)q[2] << 16) | ((uint32_t)q[3] << 24);
+// rint(v / s) for 8 values, identical to rintf(__fdiv_rn(v, s)).
+__device__ __forceinline__ void rint_quotients(const float v[8], const GroupGrid& gg, float r[8]) {
+  unsigned near = 0;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const float t = __fmul_rn(v[k], gg.inv);
+    r[k] = rintf(t);
+    near |= (fabsf(__fsub_rn(t, r[k])) >= kFastRintLimit) ? (1u << k) : 0u;
+  }
+  if (near) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      if (near & (1u << k)) r[k] = rintf(__fdiv_rn(v[k], gg.s));
+    }
   }
 }
 
-template <int BITS>
-__device__ __forceinline__ void unpack4(uint32_t w, int q[4]) {
-  constexpr int SH = BITS;
-  constexpr uint32_t MASK = (1u << BITS) - 1;
+// Codes (as floats, integer-valued in [0, L]) and decoded values of 8 values.
+__device__ __forceinline__ void quantize8(const float v[8], const GroupGrid& gg, float L,
+                                          float c[8], float d[8]) {
+  float r[8];
+  rint_quotients(v, gg, r);
 #pragma unroll
-  for (int k = 0; k < 4; ++k) q[k] = (int)((w >> (SH * k)) & MASK);
+  for (int k = 0; k < 8; ++k) {
+    c[k] = fminf(fmaxf(__fadd_rn(r[k], gg.zf), 0.0f), L);
+    d[k] = __fmul_rn(__fsub_rn(c[k], gg.zf), gg.s);   // (q - z) exact, times s
+  }
 }
 
-// 4 bf16 values in 8 bytes <-> floats.
+// Meta word -> (step, zero point as float).
+__device__ __forceinline__ void unpack_meta(uint32_t meta, float& s, float& zf) {
+  s = __half2float(__ushort_as_half((unsigned short)(meta & 0xFFFFu)));
+  zf = __half2float(__ushort_as_half((unsigned short)(meta >> 16)));
+}
+
+// Packing of 4 consecutive codes of a chunk.  4-bit: element 2i in the low
+// nibble of byte i, so 4 codes form one little-endian 16-bit word; 8-bit: one
+// byte each, one 32-bit word.
+template <int BITS>
+__device__ __forceinline__ uint32_t pack4(const float c[4]) {
+  const uint32_t q0 = (uint32_t)c[0], q1 = (uint32_t)c[1], q2 = (uint32_t)c[2], q3 = (uint32_t)c[3];
+  if (BITS == 4) return q0 | (q1 << 4) | (q2 << 8) | (q3 << 12);
+  return q0 | (q1 << 8) | (q2 << 16) | (q3 << 24);
+}
+
+// Decoding of a packed chunk word: (q - z) * s for its 4 codes.  The code is
+// turned into a float exactly by placing it in the mantissa of 2^23.
+template <int BITS>
+__device__ __forceinline__ void decode4(uint32_t w, float s, float zf, float d[4]) {
+  constexpr uint32_t MASK = (1u << BITS) - 1;
+  const float bias = __fadd_rn(8388608.0f, zf);   // 2^23 + z, exact
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float q23 = __uint_as_float(0x4B000000u | ((w >> (BITS * k)) & MASK));  // 2^23 + q
+    d[k] = __fmul_rn(__fsub_rn(q23, bias), s);    // q - z exact
+  }
+}
+
+// bf16 <-> f32 for a chunk of 4 values held in 8 bytes.
 __device__ __forceinline__ void bf16x4_to_f32(uint2 r, float f[4]) {
   f[0] = __uint_as_float(r.x << 16);
   f[1] = __uint_as_float(r.x & 0xFFFF0000u);
@@ -122,8 +173,8 @@ __device__ __forceinline__ uint2 f32x4_to_bf16(const float f[4], float back[4]) 
   return r;
 }
 
-__device__ __forceinline__ bool all_finite4(const float v[4]) {
-  return isfinite(v[0]) && isfinite(v[1]) && isfinite(v[2]) && isfinite(v[3]);
-}
+// Element offsets, within a group, of the two chunks of lane h (0..15).
+__device__ __forceinline__ int chunk_a(int h) { return 4 * h; }
+__device__ __forceinline__ int chunk_b(int h) { return 64 + 4 * h; }
 
 }  // namespace echo

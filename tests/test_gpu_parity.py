@@ -210,3 +210,36 @@ def test_argument_errors(echo):
     with pytest.raises(echo.EchoError) as ei:
         echo.echo_plan(2, 2 * G, G, 6)
     assert ei.value.status == echo.ECHO_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("bits_", [4, 8])
+def test_exact_and_near_rounding_ties(echo, bits_):
+    """Inputs on a half-step grid make v/s land exactly on half-integers (ties
+    to even) or, with a tiny held error added, within 2^-10..2^-22 of them --
+    the cases where the kernels' reciprocal fast path must defer to the exact
+    quotient.  Outputs, state and codes must still equal the oracle's."""
+    P, Gs = 2, 64
+    n = P * G * Gs
+    L = (1 << bits_) - 1
+    rng = np.random.default_rng(bits_)
+    s = 0.125                                     # the step every group gets
+    i = rng.integers(0, min(2 * L, 255) + 1, (P, n)).astype(np.float64)
+    vals = i * (s / 2)
+    vals[:, ::G] = L * s                          # each group's maximum: range [0, L*s]
+    x = torch.from_numpy(vals.astype(np.float32)).to(torch.bfloat16)
+    assert np.array_equal(x.float().numpy(), vals.astype(np.float32))   # exact in bf16
+    near = rng.random((P, n)) < 0.5
+    delta = (2.0 ** -rng.integers(10, 23, (P, n))) * s
+    e0 = np.where(near & (vals < L * s), delta, 0.0).astype(np.float32)
+    x = x.cuda()
+    comp = torch.from_numpy(e0.copy()).cuda()
+    plan = echo.echo_plan(P, n, G, bits_)
+    lay = echo.echo_wire_layout(plan)
+    out = torch.empty_like(x)
+    echo.echo_allreduce(plan, list(x), list(out), comp)
+    e_ref = e0.copy()
+    ref = oracle.allreduce(bits(x), G, bits_, e=e_ref, want_wire=True)
+    assert ref["ties"] > 100                      # the grid does produce exact ties
+    assert np.array_equal(bits(out), ref["out"])
+    assert_wire_equal(wire_to_canonical(echo.echo_debug_wire(plan), lay, P, n, bits_), ref, P)
+    assert_state_close(comp.cpu().numpy(), e_ref)
