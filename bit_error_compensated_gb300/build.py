@@ -35,6 +35,8 @@ def _flags(ptxas_verbose: bool):
                 "-I", str(ROOT / "include"), "--expt-relaxed-constexpr"]
     if ptxas_verbose:
         f += ["-Xptxas", "-v"]
+    # tuning overrides, e.g. ECHO_NVCC_FLAGS="-DECHO_REDUCE_TILE=16"
+    f += os.environ.get("ECHO_NVCC_FLAGS", "").split()
     return f
 
 

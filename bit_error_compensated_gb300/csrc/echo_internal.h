@@ -12,8 +12,13 @@ namespace echo {
 
 // Elements per quantization group on the GPU.
 constexpr int kGroup = 128;
-// Groups per reduce tile (one thread block of the reduce kernel).
-constexpr int kReduceTile = 32;
+// Groups per reduce tile (one thread block of the reduce kernel); a multiple
+// of 4 so that every tile's meta words form a 16-byte-aligned bulk copy.
+#ifndef ECHO_REDUCE_TILE
+#define ECHO_REDUCE_TILE 32
+#endif
+constexpr int kReduceTile = ECHO_REDUCE_TILE;
+static_assert(kReduceTile % 4 == 0 && kReduceTile >= 4, "reduce tile: multiple of 4 groups");
 // Threads per block of every kernel.
 constexpr int kThreads = 256;
 

@@ -5,9 +5,9 @@
 // all-gather is one read of each segment's codes and P writes of the decoded
 // bf16 values.
 //
-// Half a warp per group, 8 elements per lane (quant.cuh): a warp reads the
-// codes and meta words of two adjacent groups and writes P x 2 x 256 B of bf16
-// with streaming stores.  U group pairs per warp are read before any is
+// Half a warp per group, 8 consecutive elements per lane: a warp reads the
+// codes and meta words of two adjacent groups and writes, per rank, one
+// 16-byte streaming store per lane (2 x 256 B per warp).  U group pairs per warp are read before any is
 // written, to keep several code reads in flight.  Write-bound: P * 2 bytes out
 // per element.
 #include "echo_internal.h"
@@ -23,7 +23,7 @@ gather_kernel(const CallArgs a) {
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int lane = threadIdx.x & 31;
   const int half = lane >> 4;
-  const int h = lane & 15;
+  const int h = lane & 15;          // lane h of a half decodes elements [8h, 8h+8)
   const int64_t wg = (int64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
   const int64_t nw = (int64_t)gridDim.x * (kThreads / 32);
   const int P = a.P;
@@ -31,50 +31,53 @@ gather_kernel(const CallArgs a) {
   const int64_t Gs = a.Gs;
   const uint8_t* cs = a.codes2 + (int64_t)o * Gs * CB;
   const uint32_t* ms = a.meta2 + (int64_t)o * a.Gs_pad;
-  const int64_t W = Gs;
 
   // Two adjacent groups per warp (half a warp each), U pairs in flight.
-  for (int64_t pair0 = wg; 2 * pair0 < W; pair0 += nw * U) {
-    uint32_t wa[U], wb[U], meta[U];
+  for (int64_t pair0 = wg; 2 * pair0 < Gs; pair0 += nw * U) {
+    uint2 word[U];
+    uint32_t meta[U];
     int64_t w[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       w[u] = 2 * (pair0 + (int64_t)u * nw) + half;
-      if (w[u] < W) {
+      if (w[u] < Gs) {
         meta[u] = ms[w[u]];
         const uint8_t* cg = cs + w[u] * CB;
         if (BITS == 4) {
-          wa[u] = reinterpret_cast<const uint16_t*>(cg)[h];
-          wb[u] = reinterpret_cast<const uint16_t*>(cg + 32)[h];
+          word[u].x = reinterpret_cast<const uint32_t*>(cg)[h];
+          word[u].y = 0;
         } else {
-          wa[u] = reinterpret_cast<const uint32_t*>(cg)[h];
-          wb[u] = reinterpret_cast<const uint32_t*>(cg + 64)[h];
+          word[u] = reinterpret_cast<const uint2*>(cg)[h];
         }
       }
     }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      if (w[u] >= W) continue;
+      if (w[u] >= Gs) continue;
       float s, zf;
       unpack_meta(meta[u], s, zf);
       float deq[8], yb[8];
-      decode4<BITS>(wa[u], s, zf, deq);
-      decode4<BITS>(wb[u], s, zf, deq + 4);
+      if (BITS == 4) {
+        decode4<4>(word[u].x, s, zf, deq);
+        decode4<4>(word[u].x >> 16, s, zf, deq + 4);
+      } else {
+        decode4<8>(word[u].x, s, zf, deq);
+        decode4<8>(word[u].y, s, zf, deq + 4);
+      }
       const uint2 ya = f32x4_to_bf16(deq, yb);
       const uint2 yv = f32x4_to_bf16(deq + 4, yb + 4);
-      const int64_t grp = (int64_t)o * Gs + w[u];  // group index in the rank tensor
-      const int64_t ea = grp * kGroup + chunk_a(h);
-      const int64_t eb = grp * kGroup + chunk_b(h);
-      for (int r = 0; r < P; ++r) {
-        __stcs(reinterpret_cast<uint2*>(a.out[r] + ea), ya);
-        __stcs(reinterpret_cast<uint2*>(a.out[r] + eb), yv);
-      }
+      const uint4 y = make_uint4(ya.x, ya.y, yv.x, yv.y);
+      const int64_t e0 = ((int64_t)o * Gs + w[u]) * kGroup + 8 * h;
+      for (int r = 0; r < P; ++r) __stcs(reinterpret_cast<uint4*>(a.out[r] + e0), y);
     }
   }
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-constexpr int kGatherUnroll = 4;
+#ifndef ECHO_GATHER_UNROLL
+#define ECHO_GATHER_UNROLL 4
+#endif
+constexpr int kGatherUnroll = ECHO_GATHER_UNROLL;  // group pairs in flight per warp
 
 template <int BITS>
 cudaError_t launch_t(const CallArgs& a, cudaStream_t s, bool pdl) {

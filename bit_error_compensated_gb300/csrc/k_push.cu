@@ -29,7 +29,10 @@
 namespace echo {
 namespace {
 
-constexpr int kPushStages = 4;
+#ifndef ECHO_PUSH_STAGES
+#define ECHO_PUSH_STAGES 4
+#endif
+constexpr int kPushStages = ECHO_PUSH_STAGES;      // pairs in flight per warp
 constexpr int kPairX = 2 * kGroup * 2;      // bf16 bytes of a pair
 constexpr int kPairE = 2 * kGroup * 4;      // fp32 state bytes of a pair
 
@@ -101,11 +104,14 @@ push_kernel(const CallArgs a) {
   for (int64_t i = 0; wg + i * nw < npairs; ++i) {
     const int st = (int)(i % S);
     const uint32_t parity = (uint32_t)((i / S) & 1);
-    if (!mbar_wait_bounded(bar0 + 8 * st, parity)) {
-      if (lane == 0) atomicOr(a.status, kStatusTimeout);
-      for (int k = 0; k < S; ++k) {               // copies still in flight
-        const int64_t ii = i + k;
-        if (wg + ii * nw < npairs) mbar_wait_bounded(bar0 + 8 * (int)(ii % S), (uint32_t)((ii / S) & 1));
+    if (!mbar_wait_warp(bar0 + 8 * st, parity)) {        // same outcome for every lane
+      if (lane == 0) {
+        atomicOr(a.status, kStatusTimeout);
+        for (int k = 0; k < S; ++k) {             // copies still in flight
+          const int64_t ii = i + k;
+          if (wg + ii * nw < npairs)
+            mbar_wait_bounded(bar0 + 8 * (int)(ii % S), (uint32_t)((ii / S) & 1));
+        }
       }
       return;
     }

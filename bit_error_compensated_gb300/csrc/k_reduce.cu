@@ -11,9 +11,10 @@
 // 1-D bulk copies (cp.async.bulk, the TMA engine) of the P-1 received code
 // tiles, their meta words, the owner's bf16 tile and its fp32 state tile into
 // shared memory, all completing on one mbarrier; the block then works from
-// shared memory, one warp per group.  The wait on the mbarrier is bounded: if
-// it gives up, the block records ECHO_ERR_TIMEOUT in the status word, waits
-// once more (also bounded) for its copies, and returns.
+// shared memory, half a warp per group.  The wait on the mbarrier is bounded
+// and its outcome is the same for the whole block: if it gives up, the block
+// records ECHO_ERR_TIMEOUT in the status word, waits once more (also bounded)
+// for its copies, and returns.
 //
 // With `FUSED` the block also writes the decoded gather value to all P output
 // buffers, so the separate gather kernel is skipped.
@@ -78,9 +79,11 @@ reduce_kernel(const CallArgs a, int64_t tiles_per_seg) {
     asm volatile("griddepcontrol.wait;" ::: "memory");
   }
 
-  if (!mbar_wait_bounded(bar_a, 0)) {
-    if (threadIdx.x == 0) atomicOr(a.status, kStatusTimeout);
-    mbar_wait_bounded(bar_a, 0);   // let copies in flight land before leaving
+  if (!mbar_wait_block(bar_a, 0)) {                // same outcome for the whole block
+    if (threadIdx.x == 0) {
+      atomicOr(a.status, kStatusTimeout);
+      mbar_wait_bounded(bar_a, 0);                 // let copies in flight land before leaving
+    }
     return;
   }
 

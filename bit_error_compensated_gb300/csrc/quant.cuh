@@ -62,6 +62,21 @@ struct GroupGrid {
   bool finite;    // false: non-finite input or step overflow; results unspecified
 };
 
+// rint(t) for |t| < 2^22 with two fp32 adds: at 1.5 * 2^23 the fp32 spacing
+// is 1, so the first add rounds t to an integer (to nearest, ties to even)
+// and the second removes the offset exactly.  Runs on the FMA pipe.
+__device__ __forceinline__ float rint_small(float t) {
+  return __fsub_rn(__fadd_rn(t, 12582912.0f), 12582912.0f);
+}
+
+// Largest distance from an integer at which rint(x * (1/s)) is taken as
+// rint(x / s).  For a finite group |x / s| < 256, so the correctly rounded
+// reciprocal and product are within 256 * 3 * 2^-24 < 2^-13 of the correctly
+// rounded quotient; when the product lies farther than that from every
+// half-integer, both round to the same integer.  Otherwise the quotient itself
+// is computed (IEEE division).
+constexpr float kFastRintLimit = 0.5f - 1.0f / 8192.0f;
+
 // Step and zero point of a group from its range.
 __device__ __forceinline__ GroupGrid make_grid(float lo, float hi, float L) {
   const float s32 = __fdiv_rn(__fsub_rn(hi, lo), L);
@@ -71,52 +86,48 @@ __device__ __forceinline__ GroupGrid make_grid(float lo, float hi, float L) {
     sh = __ushort_as_half((unsigned short)0x3C00);  // 1.0
     s = 1.0f;
   }
-  float zf = rintf(__fdiv_rn(-lo, s));
+  const float inv = __frcp_rn(s);
+  // z = rint(-lo / s); -lo / s lies in [0, L(1 + 2^-22)] for a finite group.
+  const float t = __fmul_rn(-lo, inv);
+  float zf = rint_small(t);
+  if (!(fabsf(__fsub_rn(t, zf)) < kFastRintLimit)) zf = rintf(__fdiv_rn(-lo, s));
   zf = fminf(fmaxf(zf, 0.0f), L);
-  const int z = (int)zf;
   GroupGrid gg;
   gg.s = s;
-  gg.inv = __frcp_rn(s);
-  gg.zf = (float)z;
+  gg.inv = inv;
+  gg.zf = zf;
   gg.meta = (uint32_t)__half_as_ushort(sh) |
-            ((uint32_t)__half_as_ushort(__int2half_rn(z)) << 16);
+            ((uint32_t)__half_as_ushort(__float2half_rn(zf)) << 16);
   gg.finite = isfinite(s);
   return gg;
 }
 
-// Largest distance from an integer at which rint(v * (1/s)) is taken as
-// rint(v / s).  For a finite group |v / s| < 256, so the correctly rounded
-// reciprocal and product are within 256 * 3 * 2^-24 < 2^-13 of the correctly
-// rounded quotient; when the product lies farther than that from every
-// half-integer, both round to the same integer.  Otherwise the quotient itself
-// is computed (IEEE division).
-constexpr float kFastRintLimit = 0.5f - 1.0f / 8192.0f;
-
-// rint(v / s) for 8 values, identical to rintf(__fdiv_rn(v, s)).
-__device__ __forceinline__ void rint_quotients(const float v[8], const GroupGrid& gg, float r[8]) {
-  unsigned near = 0;
-#pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    const float t = __fmul_rn(v[k], gg.inv);
-    r[k] = rintf(t);
-    near |= (fabsf(__fsub_rn(t, r[k])) >= kFastRintLimit) ? (1u << k) : 0u;
-  }
-  if (near) {
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      if (near & (1u << k)) r[k] = rintf(__fdiv_rn(v[k], gg.s));
-    }
-  }
-}
-
-// Codes (as floats, integer-valued in [0, L]) and decoded values of 8 values.
+// Codes (as integer-valued floats in [0, L]) and decoded values of 8 values:
+// c = clamp(rint(v / s) + z, 0, L), d = (c - z) * s.
+//
+// rint(v / s) comes from the product with the reciprocal unless some value of
+// the 8 lies near a rounding boundary, in which case all 8 are recomputed with
+// IEEE division.  Only the upper clamp is applied: for a finite group v >= lo,
+// so rint(fl(v / s)) >= rint(fl(lo / s)) = -z (division and rint are monotonic
+// and odd-symmetric), and c >= 0 already.  (For a non-finite group the codes
+// are unspecified; pack4 still confines each packed word to its own bytes.)
 __device__ __forceinline__ void quantize8(const float v[8], const GroupGrid& gg, float L,
                                           float c[8], float d[8]) {
   float r[8];
-  rint_quotients(v, gg, r);
+  float dev = 0.0f;
 #pragma unroll
   for (int k = 0; k < 8; ++k) {
-    c[k] = fminf(fmaxf(__fadd_rn(r[k], gg.zf), 0.0f), L);
+    const float t = __fmul_rn(v[k], gg.inv);
+    r[k] = rint_small(t);
+    dev = fmaxf(dev, fabsf(__fsub_rn(t, r[k])));
+  }
+  if (dev >= kFastRintLimit) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) r[k] = rintf(__fdiv_rn(v[k], gg.s));
+  }
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    c[k] = fminf(__fadd_rn(r[k], gg.zf), L);
     d[k] = __fmul_rn(__fsub_rn(c[k], gg.zf), gg.s);   // (q - z) exact, times s
   }
 }
@@ -129,12 +140,22 @@ __device__ __forceinline__ void unpack_meta(uint32_t meta, float& s, float& zf) 
 
 // Packing of 4 consecutive codes of a chunk.  4-bit: element 2i in the low
 // nibble of byte i, so 4 codes form one little-endian 16-bit word; 8-bit: one
-// byte each, one 32-bit word.
+// byte each, one 32-bit word.  The codes are integer-valued floats, so the
+// word is built with exact fp arithmetic (every intermediate is an integer
+// below 2^16) and read out of the mantissa of 2^23 + word.
+__device__ __forceinline__ uint32_t small_int_bits(float w) {
+  return __float_as_uint(__fadd_rn(w, 8388608.0f)) & 0xFFFFu;
+}
+
 template <int BITS>
 __device__ __forceinline__ uint32_t pack4(const float c[4]) {
-  const uint32_t q0 = (uint32_t)c[0], q1 = (uint32_t)c[1], q2 = (uint32_t)c[2], q3 = (uint32_t)c[3];
-  if (BITS == 4) return q0 | (q1 << 4) | (q2 << 8) | (q3 << 12);
-  return q0 | (q1 << 8) | (q2 << 16) | (q3 << 24);
+  if (BITS == 4) {
+    const float w = __fmaf_rn(c[3], 4096.0f, __fmaf_rn(c[2], 256.0f, __fmaf_rn(c[1], 16.0f, c[0])));
+    return small_int_bits(w);
+  }
+  const uint32_t lo = small_int_bits(__fmaf_rn(c[1], 256.0f, c[0]));
+  const uint32_t hi = small_int_bits(__fmaf_rn(c[3], 256.0f, c[2]));
+  return __byte_perm(lo, hi, 0x5410);
 }
 
 // Decoding of a packed chunk word: (q - z) * s for its 4 codes.  The code is

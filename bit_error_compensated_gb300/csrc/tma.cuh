@@ -86,4 +86,17 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity)
   return true;
 }
 
+// Bounded wait whose outcome is the same for the whole warp: every lane waits
+// (bounded) and the lanes then agree by vote, so that if any lane gave up,
+// all of them take the give-up path together.
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity) {
+  return __all_sync(0xFFFFFFFFu, mbar_wait_bounded(bar, parity)) != 0;
+}
+
+// The same for the whole block (contains a __syncthreads: every thread of the
+// block must call it).
+__device__ __forceinline__ bool mbar_wait_block(uint32_t bar, uint32_t parity) {
+  return __syncthreads_and(mbar_wait_bounded(bar, parity) ? 1 : 0) != 0;
+}
+
 }  // namespace echo
