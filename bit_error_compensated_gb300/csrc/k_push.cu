@@ -9,19 +9,21 @@
 // v - deq(q), replaces it (the update changes nothing this call computes).
 //
 // Grid: blockIdx.y is a (sender p, owner o) segment pair, blockIdx.x strides
-// over the segment's groups, so no division is needed per group.  Half a warp
-// per 128-element group (quant.cuh); a warp works on two adjacent groups at a
-// time (a "pair": 512 B of bf16 input and 1 KB of fp32 state, contiguous).
+// over the segment's groups, so no division is needed per group.  A quarter
+// warp per 128-element group (quant.cuh); a warp works on four adjacent
+// groups at a time (a "quad": 1 KB of bf16 input and 2 KB of fp32 state,
+// contiguous).
 //
 // Each warp runs its own kPushStages-deep pipeline: lane 0 issues 1-D bulk
-// copies (cp.async.bulk, the TMA engine) of the next pairs' input and state
+// copies (cp.async.bulk, the TMA engine) of the next quads' input and state
 // into the warp's shared-memory stages, each stage completing on its own
-// mbarrier, while the warp quantizes the current pair from shared memory and
+// mbarrier, while the warp quantizes the current quad from shared memory and
 // stores codes, meta and the new state straight to global memory.  Loads stay
-// in flight during compute without holding registers.  The waits are bounded:
-// on timeout the warp records ECHO_ERR_TIMEOUT, waits once more (bounded) for
-// each copy it still has in flight, and returns.  HBM-bound: per group
-// 256 B + 512 B read, 512 B + codes + 4 B of meta written.
+// in flight during compute without holding registers.  The waits are bounded
+// and their outcome is the same for the whole warp: on timeout the warp
+// records ECHO_ERR_TIMEOUT, waits once more (bounded) for each copy it still
+// has in flight, and returns.  HBM-bound: per group 256 B + 512 B read,
+// 512 B + codes + 4 B of meta written.
 #include "echo_internal.h"
 #include "quant.cuh"
 #include "tma.cuh"
@@ -30,14 +32,14 @@ namespace echo {
 namespace {
 
 #ifndef ECHO_PUSH_STAGES
-#define ECHO_PUSH_STAGES 4
+#define ECHO_PUSH_STAGES 2
 #endif
-constexpr int kPushStages = ECHO_PUSH_STAGES;      // pairs in flight per warp
-constexpr int kPairX = 2 * kGroup * 2;      // bf16 bytes of a pair
-constexpr int kPairE = 2 * kGroup * 4;      // fp32 state bytes of a pair
+constexpr int kPushStages = ECHO_PUSH_STAGES;      // quads in flight per warp
+constexpr int kQuadX = 4 * kGroup * 2;      // bf16 bytes of a quad
+constexpr int kQuadE = 4 * kGroup * 4;      // fp32 state bytes of a quad
 
 template <bool COMP>
-constexpr int push_stage_bytes() { return kPairX + (COMP ? kPairE : 0); }
+constexpr int push_stage_bytes() { return kQuadX + (COMP ? kQuadE : 0); }
 
 template <bool COMP>
 constexpr size_t push_smem_bytes() {
@@ -67,11 +69,11 @@ push_kernel(const CallArgs a) {
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int half = lane >> 4;
-  const int h = lane & 15;
+  const int quarter = lane >> 3;                    // group within the quad
+  const int q = lane & 7;
   const int64_t wg = (int64_t)blockIdx.x * (kThreads / 32) + warp;
   const int64_t nw = (int64_t)gridDim.x * (kThreads / 32);
-  const int64_t npairs = (Gs + 1) / 2;
+  const int64_t nquads = (Gs + 3) / 4;
   uint8_t* wbuf = smem + (size_t)warp * S * SB;
   const uint32_t bar0 = smem_addr(&bars[warp][0]);
 
@@ -87,21 +89,21 @@ push_kernel(const CallArgs a) {
   if (lane == 0) pol = policy_evict_first();        // input and state are read once per call
   // Lane 0: start the copies of iteration i into stage st.
   auto issue = [&](int64_t i, int st) {
-    const int64_t pr = wg + i * nw;
-    if (pr >= npairs) return;
-    const int64_t g0 = 2 * pr;
-    const uint32_t ng = (uint32_t)((Gs - g0) < 2 ? (Gs - g0) : 2);
+    const int64_t qd = wg + i * nw;
+    if (qd >= nquads) return;
+    const int64_t g0 = 4 * qd;
+    const uint32_t ng = (uint32_t)((Gs - g0) < 4 ? (Gs - g0) : 4);
     const uint32_t bar = bar0 + 8 * st;
     mbar_expect_tx(bar, ng * (COMP ? 768u : 256u));
     bulk_g2s(smem_addr(wbuf + st * SB), xs + g0 * kGroup, ng * 256u, bar, pol);
-    if (COMP) bulk_g2s(smem_addr(wbuf + st * SB + kPairX), es + g0 * kGroup, ng * 512u, bar, pol);
+    if (COMP) bulk_g2s(smem_addr(wbuf + st * SB + kQuadX), es + g0 * kGroup, ng * 512u, bar, pol);
   };
   if (lane == 0) {
 #pragma unroll
     for (int st = 0; st < S; ++st) issue(st, st);
   }
 
-  for (int64_t i = 0; wg + i * nw < npairs; ++i) {
+  for (int64_t i = 0; wg + i * nw < nquads; ++i) {
     const int st = (int)(i % S);
     const uint32_t parity = (uint32_t)((i / S) & 1);
     if (!mbar_wait_warp(bar0 + 8 * st, parity)) {        // same outcome for every lane
@@ -109,35 +111,33 @@ push_kernel(const CallArgs a) {
         atomicOr(a.status, kStatusTimeout);
         for (int k = 0; k < S; ++k) {             // copies still in flight
           const int64_t ii = i + k;
-          if (wg + ii * nw < npairs)
+          if (wg + ii * nw < nquads)
             mbar_wait_bounded(bar0 + 8 * (int)(ii % S), (uint32_t)((ii / S) & 1));
         }
       }
       return;
     }
-    const int64_t j = 2 * (wg + i * nw) + half;      // this half's group
+    const int64_t j = 4 * (wg + i * nw) + quarter;   // this quarter's group
     const bool valid = j < Gs;
-    float v[8];
+    float v[16];
     if (valid) {
-      const uint2* sx = reinterpret_cast<const uint2*>(wbuf + st * SB) + half * 32;
-      bf16x4_to_f32(sx[h], v);
-      bf16x4_to_f32(sx[16 + h], v + 4);
+      const uint2* sx = reinterpret_cast<const uint2*>(wbuf + st * SB) + quarter * 32;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) bf16x4_to_f32(sx[8 * c + q], v + 4 * c);
       if (COMP) {
-        const float4* se = reinterpret_cast<const float4*>(wbuf + st * SB + kPairX) + half * 32;
-        const float4 ea = se[h];
-        const float4 eb = se[16 + h];
-        v[0] = __fadd_rn(v[0], ea.x);
-        v[1] = __fadd_rn(v[1], ea.y);
-        v[2] = __fadd_rn(v[2], ea.z);
-        v[3] = __fadd_rn(v[3], ea.w);
-        v[4] = __fadd_rn(v[4], eb.x);
-        v[5] = __fadd_rn(v[5], eb.y);
-        v[6] = __fadd_rn(v[6], eb.z);
-        v[7] = __fadd_rn(v[7], eb.w);
+        const float4* se = reinterpret_cast<const float4*>(wbuf + st * SB + kQuadX) + quarter * 32;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const float4 e = se[8 * c + q];
+          v[4 * c + 0] = __fadd_rn(v[4 * c + 0], e.x);
+          v[4 * c + 1] = __fadd_rn(v[4 * c + 1], e.y);
+          v[4 * c + 2] = __fadd_rn(v[4 * c + 2], e.z);
+          v[4 * c + 3] = __fadd_rn(v[4 * c + 3], e.w);
+        }
       }
     } else {
 #pragma unroll
-      for (int k = 0; k < 8; ++k) v[k] = 0.0f;       // idle half of a one-group pair
+      for (int k = 0; k < 16; ++k) v[k] = 0.0f;      // idle quarter of a short quad
     }
     // The stage has been read into registers: hand it back to the copy engine.
     __syncwarp();
@@ -147,30 +147,36 @@ push_kernel(const CallArgs a) {
     }
 
     float lo, hi;
-    half_range(v, lo, hi);
+    quarter_range(v, lo, hi);
     const GroupGrid gg = make_grid(lo, hi, L);
-    float c[8], d[8];
-    quantize8(v, gg, L, c, d);
-    if (valid) {
-      uint8_t* cg = cs + j * CB;
-      if (BITS == 4) {
-        reinterpret_cast<uint16_t*>(cg)[h] = (uint16_t)pack4<4>(c);
-        reinterpret_cast<uint16_t*>(cg + 32)[h] = (uint16_t)pack4<4>(c + 4);
-      } else {
-        reinterpret_cast<uint32_t*>(cg)[h] = pack4<8>(c);
-        reinterpret_cast<uint32_t*>(cg + 64)[h] = pack4<8>(c + 4);
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {                 // chunks 2hh and 2hh+1
+      float c[8], d[8];
+      quantize8(v + 8 * hh, gg, L, c, d);
+      if (valid) {
+        uint8_t* cg = cs + j * CB;
+        if (BITS == 4) {
+          reinterpret_cast<uint16_t*>(cg + 32 * hh)[q] = (uint16_t)pack4<4>(c);
+          reinterpret_cast<uint16_t*>(cg + 32 * hh + 16)[q] = (uint16_t)pack4<4>(c + 4);
+        } else {
+          reinterpret_cast<uint32_t*>(cg + 64 * hh)[q] = pack4<8>(c);
+          reinterpret_cast<uint32_t*>(cg + 64 * hh + 32)[q] = pack4<8>(c + 4);
+        }
+        if (COMP) {
+          float* eg = es + j * kGroup;
+          const float* vv = v + 8 * hh;
+          *reinterpret_cast<float4*>(eg + chunk_at(2 * hh, q)) =
+              make_float4(__fsub_rn(vv[0], d[0]), __fsub_rn(vv[1], d[1]),
+                          __fsub_rn(vv[2], d[2]), __fsub_rn(vv[3], d[3]));
+          *reinterpret_cast<float4*>(eg + chunk_at(2 * hh + 1, q)) =
+              make_float4(__fsub_rn(vv[4], d[4]), __fsub_rn(vv[5], d[5]),
+                          __fsub_rn(vv[6], d[6]), __fsub_rn(vv[7], d[7]));
+        }
       }
-      if (h == 0) ms[j] = gg.meta;
-      if (COMP) {
-        float* eg = es + j * kGroup;
-        *reinterpret_cast<float4*>(eg + chunk_a(h)) =
-            make_float4(__fsub_rn(v[0], d[0]), __fsub_rn(v[1], d[1]),
-                        __fsub_rn(v[2], d[2]), __fsub_rn(v[3], d[3]));
-        *reinterpret_cast<float4*>(eg + chunk_b(h)) =
-            make_float4(__fsub_rn(v[4], d[4]), __fsub_rn(v[5], d[5]),
-                        __fsub_rn(v[6], d[6]), __fsub_rn(v[7], d[7]));
-      }
-      if (!gg.finite && h == 0) atomicOr(a.status, kStatusOverflow);
+    }
+    if (valid && q == 0) {
+      ms[j] = gg.meta;
+      if (!gg.finite) atomicOr(a.status, kStatusOverflow);
     }
   }
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -193,8 +199,8 @@ cudaError_t launch_t(const CallArgs& a, cudaStream_t s, bool pdl) {
   }
   const int pairs = a.P * (a.P - 1);
   // Blocks per segment: enough to fill the GPU once across all segments, but
-  // no more than the segment has group pairs for (8 warps x U pairs each).
-  const int64_t per_block = (int64_t)(kThreads / 32) * 2;
+  // no more than the segment has quads for (8 warps x 1 quad each).
+  const int64_t per_block = (int64_t)(kThreads / 32) * 4;
   const int64_t need = (a.Gs + per_block - 1) / per_block;
   int64_t bx = (resident + pairs - 1) / pairs;
   if (bx > need) bx = need;

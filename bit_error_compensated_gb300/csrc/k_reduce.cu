@@ -11,7 +11,7 @@
 // 1-D bulk copies (cp.async.bulk, the TMA engine) of the P-1 received code
 // tiles, their meta words, the owner's bf16 tile and its fp32 state tile into
 // shared memory, all completing on one mbarrier; the block then works from
-// shared memory, half a warp per group.  The wait on the mbarrier is bounded
+// shared memory, a quarter warp per group.  The wait on the mbarrier is bounded
 // and its outcome is the same for the whole block: if it gives up, the block
 // records ECHO_ERR_TIMEOUT in the status word, waits once more (also bounded)
 // for its copies, and returns.
@@ -89,96 +89,106 @@ reduce_kernel(const CallArgs a, int64_t tiles_per_seg) {
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int half = lane >> 4;
-  const int h = lane & 15;
-  // Two groups per warp per pass (half a warp each, see quant.cuh).
-  for (int gp = 2 * warp; gp < t; gp += 2 * (kThreads / 32)) {
-    const int gl = gp + half;                      // group within the tile
+  const int quarter = lane >> 3;
+  const int q = lane & 7;
+  // Four groups per warp per pass (a quarter warp each, see quant.cuh).
+  for (int gq = 4 * warp; gq < t; gq += 4 * (kThreads / 32)) {
+    const int gl = gq + quarter;                   // group within the tile
     const bool valid = gl < t;
-    const int gs = valid ? gl : gp;                // idle half reads a valid group
-    float acc[8];
-#pragma unroll 4
-    for (int p = 0; p < P; ++p) {
-      float term[8];
-      if (p == o) {
-        bf16x4_to_f32(s_x[gs * 32 + h], term);
-        bf16x4_to_f32(s_x[gs * 32 + 16 + h], term + 4);
+    const int gs = valid ? gl : gq;                // idle quarter reads a valid group
+    // Decoded term of sender p (p != o), from its receive slot.
+    auto sender_term = [&](int p, float term[16]) {
+      const int js = p < o ? p : p - 1;
+      float s, zf;
+      unpack_meta(s_meta[js * T + gs], s, zf);
+      const uint8_t* cg = s_codes + (js * T + gs) * CB;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const uint32_t w = BITS == 4 ? (uint32_t)reinterpret_cast<const uint16_t*>(cg + 16 * c)[q]
+                                     : reinterpret_cast<const uint32_t*>(cg + 32 * c)[q];
+        decode4<BITS>(w, s, zf, term + 4 * c);
+      }
+    };
+    // The owner's own term: its bf16 input plus (compensated) its held error.
+    auto own_term = [&](float term[16]) {
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        bf16x4_to_f32(s_x[gs * 32 + 8 * c + q], term + 4 * c);
         if (COMP) {
-          const float4 ea = s_e[gs * 32 + h];
-          const float4 eb = s_e[gs * 32 + 16 + h];
-          term[0] = __fadd_rn(term[0], ea.x);
-          term[1] = __fadd_rn(term[1], ea.y);
-          term[2] = __fadd_rn(term[2], ea.z);
-          term[3] = __fadd_rn(term[3], ea.w);
-          term[4] = __fadd_rn(term[4], eb.x);
-          term[5] = __fadd_rn(term[5], eb.y);
-          term[6] = __fadd_rn(term[6], eb.z);
-          term[7] = __fadd_rn(term[7], eb.w);
+          const float4 e = s_e[gs * 32 + 8 * c + q];
+          term[4 * c + 0] = __fadd_rn(term[4 * c + 0], e.x);
+          term[4 * c + 1] = __fadd_rn(term[4 * c + 1], e.y);
+          term[4 * c + 2] = __fadd_rn(term[4 * c + 2], e.z);
+          term[4 * c + 3] = __fadd_rn(term[4 * c + 3], e.w);
         }
-      } else {
-        const int js = p < o ? p : p - 1;
-        float s, zf;
-        unpack_meta(s_meta[js * T + gs], s, zf);
-        const uint8_t* cg = s_codes + (js * T + gs) * CB;
-        uint32_t wa, wb;
-        if (BITS == 4) {
-          wa = reinterpret_cast<const uint16_t*>(cg)[h];
-          wb = reinterpret_cast<const uint16_t*>(cg + 32)[h];
-        } else {
-          wa = reinterpret_cast<const uint32_t*>(cg)[h];
-          wb = reinterpret_cast<const uint32_t*>(cg + 64)[h];
-        }
-        decode4<BITS>(wa, s, zf, term);
-        decode4<BITS>(wb, s, zf, term + 4);
       }
-      if (p == 0) {
+    };
+    // Ascending rank order, starting from rank 0's term: the senders below
+    // the owner, the owner's own term, the senders above.
+    float acc[16], term[16];
+    if (o == 0) {
+      own_term(acc);
+    } else {
+      sender_term(0, acc);
+      for (int p = 1; p < o; ++p) {
+        sender_term(p, term);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) acc[k] = term[k];
-      } else {
-#pragma unroll
-        for (int k = 0; k < 8; ++k) acc[k] = __fadd_rn(acc[k], term[k]);
+        for (int k = 0; k < 16; ++k) acc[k] = __fadd_rn(acc[k], term[k]);
       }
+      own_term(term);
+#pragma unroll
+      for (int k = 0; k < 16; ++k) acc[k] = __fadd_rn(acc[k], term[k]);
+    }
+    for (int p = o + 1; p < P; ++p) {
+      sender_term(p, term);
+#pragma unroll
+      for (int k = 0; k < 16; ++k) acc[k] = __fadd_rn(acc[k], term[k]);
     }
 
     // Quantize the sum once for the gather.
     float lo, hi;
-    half_range(acc, lo, hi);
+    quarter_range(acc, lo, hi);
     const GroupGrid gg = make_grid(lo, hi, L);
-    float c[8], deq[8];
-    quantize8(acc, gg, L, c, deq);
-    if (!valid) continue;
     const int64_t grp = seg_group0 + gl;           // group index in the rank tensor
-    uint8_t* cg = a.codes2 + grp * CB;
-    if (BITS == 4) {
-      reinterpret_cast<uint16_t*>(cg)[h] = (uint16_t)pack4<4>(c);
-      reinterpret_cast<uint16_t*>(cg + 32)[h] = (uint16_t)pack4<4>(c + 4);
-    } else {
-      reinterpret_cast<uint32_t*>(cg)[h] = pack4<8>(c);
-      reinterpret_cast<uint32_t*>(cg + 64)[h] = pack4<8>(c + 4);
-    }
-    if (h == 0) a.meta2[(int64_t)o * a.Gs_pad + j0 + gl] = gg.meta;
-
-    float yb[8];
-    const uint2 ya = f32x4_to_bf16(deq, yb);
-    const uint2 yv = f32x4_to_bf16(deq + 4, yb + 4);
-    const int64_t ea = grp * kGroup + chunk_a(h);
-    const int64_t eb = grp * kGroup + chunk_b(h);
-    if (COMP) {
-      float* eo = a.comp + (int64_t)o * a.n;
-      *reinterpret_cast<float4*>(eo + ea) =
-          make_float4(__fsub_rn(acc[0], yb[0]), __fsub_rn(acc[1], yb[1]),
-                      __fsub_rn(acc[2], yb[2]), __fsub_rn(acc[3], yb[3]));
-      *reinterpret_cast<float4*>(eo + eb) =
-          make_float4(__fsub_rn(acc[4], yb[4]), __fsub_rn(acc[5], yb[5]),
-                      __fsub_rn(acc[6], yb[6]), __fsub_rn(acc[7], yb[7]));
-    }
-    if (FUSED) {
-      for (int r = 0; r < P; ++r) {
-        __stcs(reinterpret_cast<uint2*>(a.out[r] + ea), ya);
-        __stcs(reinterpret_cast<uint2*>(a.out[r] + eb), yv);
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {               // chunks 2hh and 2hh+1
+      float c[8], deq[8];
+      quantize8(acc + 8 * hh, gg, L, c, deq);
+      if (!valid) continue;
+      uint8_t* cg = a.codes2 + grp * CB;
+      if (BITS == 4) {
+        reinterpret_cast<uint16_t*>(cg + 32 * hh)[q] = (uint16_t)pack4<4>(c);
+        reinterpret_cast<uint16_t*>(cg + 32 * hh + 16)[q] = (uint16_t)pack4<4>(c + 4);
+      } else {
+        reinterpret_cast<uint32_t*>(cg + 64 * hh)[q] = pack4<8>(c);
+        reinterpret_cast<uint32_t*>(cg + 64 * hh + 32)[q] = pack4<8>(c + 4);
+      }
+      float yb[8];
+      const uint2 ya = f32x4_to_bf16(deq, yb);
+      const uint2 yv = f32x4_to_bf16(deq + 4, yb + 4);
+      const int64_t ea = grp * kGroup + chunk_at(2 * hh, q);
+      const int64_t eb = grp * kGroup + chunk_at(2 * hh + 1, q);
+      if (COMP) {
+        float* eo = a.comp + (int64_t)o * a.n;
+        const float* aa = acc + 8 * hh;
+        *reinterpret_cast<float4*>(eo + ea) =
+            make_float4(__fsub_rn(aa[0], yb[0]), __fsub_rn(aa[1], yb[1]),
+                        __fsub_rn(aa[2], yb[2]), __fsub_rn(aa[3], yb[3]));
+        *reinterpret_cast<float4*>(eo + eb) =
+            make_float4(__fsub_rn(aa[4], yb[4]), __fsub_rn(aa[5], yb[5]),
+                        __fsub_rn(aa[6], yb[6]), __fsub_rn(aa[7], yb[7]));
+      }
+      if (FUSED) {
+        for (int r = 0; r < P; ++r) {
+          __stcs(reinterpret_cast<uint2*>(a.out[r] + ea), ya);
+          __stcs(reinterpret_cast<uint2*>(a.out[r] + eb), yv);
+        }
       }
     }
-    if (!gg.finite && h == 0) atomicOr(a.status, kStatusOverflow);
+    if (valid && q == 0) {
+      a.meta2[(int64_t)o * a.Gs_pad + j0 + gl] = gg.meta;
+      if (!gg.finite) atomicOr(a.status, kStatusOverflow);
+    }
   }
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }

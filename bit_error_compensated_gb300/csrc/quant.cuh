@@ -10,10 +10,10 @@
 // decoded value s * (q - z).  Each step is one IEEE fp32 operation with
 // explicit round-to-nearest intrinsics, so no multiply-add is ever fused.
 //
-// Thread mapping: half a warp (16 lanes) per group of 128 values; lane h of the
-// half holds 8 values, elements [4h, 4h+4) ("chunk A") and [64+4h, 64+4h+4)
-// ("chunk B"), so that every warp-wide load or store of a chunk covers two
-// contiguous runs, one per group.
+// Thread mapping: a quarter warp (8 lanes) per group of 128 values; lane q of
+// the quarter holds 16 values in four chunks of 4 consecutive elements,
+// chunk c being elements [32c + 4q, 32c + 4q + 4), so that every warp-wide
+// load or store of a chunk covers four contiguous runs, one per group.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -38,17 +38,19 @@ __device__ __forceinline__ float max_nan(float a, float b) {
   return r;
 }
 
-// Zero-aware range of a group over the 16 lanes of a half warp (all 32 lanes
-// must call it; each half reduces its own group).
-__device__ __forceinline__ void half_range(const float v[8], float& lo, float& hi) {
-  float a = min_nan(min_nan(v[0], v[1]), min_nan(v[2], v[3]));
-  float b = min_nan(min_nan(v[4], v[5]), min_nan(v[6], v[7]));
-  lo = min_nan(min_nan(a, b), 0.0f);
-  a = max_nan(max_nan(v[0], v[1]), max_nan(v[2], v[3]));
-  b = max_nan(max_nan(v[4], v[5]), max_nan(v[6], v[7]));
-  hi = max_nan(max_nan(a, b), 0.0f);
+// Zero-aware range of a group over the 8 lanes of a quarter warp (all 32
+// lanes must call it; each quarter reduces its own group).
+__device__ __forceinline__ void quarter_range(const float v[16], float& lo, float& hi) {
+  float a[4], b[4];
 #pragma unroll
-  for (int off = 8; off > 0; off >>= 1) {
+  for (int k = 0; k < 4; ++k) {
+    a[k] = min_nan(min_nan(v[4 * k], v[4 * k + 1]), min_nan(v[4 * k + 2], v[4 * k + 3]));
+    b[k] = max_nan(max_nan(v[4 * k], v[4 * k + 1]), max_nan(v[4 * k + 2], v[4 * k + 3]));
+  }
+  lo = min_nan(min_nan(min_nan(a[0], a[1]), min_nan(a[2], a[3])), 0.0f);
+  hi = max_nan(max_nan(max_nan(b[0], b[1]), max_nan(b[2], b[3])), 0.0f);
+#pragma unroll
+  for (int off = 4; off > 0; off >>= 1) {
     lo = min_nan(lo, __shfl_xor_sync(kFull, lo, off));
     hi = max_nan(hi, __shfl_xor_sync(kFull, hi, off));
   }
@@ -194,8 +196,7 @@ __device__ __forceinline__ uint2 f32x4_to_bf16(const float f[4], float back[4]) 
   return r;
 }
 
-// Element offsets, within a group, of the two chunks of lane h (0..15).
-__device__ __forceinline__ int chunk_a(int h) { return 4 * h; }
-__device__ __forceinline__ int chunk_b(int h) { return 64 + 4 * h; }
+// Element offset, within a group, of chunk c (0..3) of quarter lane q (0..7).
+__device__ __forceinline__ int chunk_at(int c, int q) { return 32 * c + 4 * q; }
 
 }  // namespace echo
