@@ -7,14 +7,18 @@
 // The entry pass of the compensator (adding the owner's held error to its own
 // segment) is fused in as well.
 //
-// One thread block per owner tile of kReduceTile groups.  One thread issues
-// 1-D bulk copies (cp.async.bulk, the TMA engine) of the P-1 received code
-// tiles, their meta words, the owner's bf16 tile and its fp32 state tile into
-// shared memory, all completing on one mbarrier; the block then works from
-// shared memory, a quarter warp per group.  The wait on the mbarrier is bounded
-// and its outcome is the same for the whole block: if it gives up, the block
-// records ECHO_ERR_TIMEOUT in the status word, waits once more (also bounded)
-// for its copies, and returns.
+// Blocks walk owner tiles of kReduceTile groups through a ring of
+// kReduceRing shared-memory stages.  Thread 0 fills a stage with 1-D bulk
+// copies (cp.async.bulk, the TMA engine) of the tile's P-1 received code
+// tiles, their meta words, the owner's bf16 tile and its fp32 state tile, all
+// completing on the stage's mbarrier; the block works from shared memory (a
+// quarter warp per group) and stores its results straight to global memory,
+// and thread 0 refills the stage with the block's next tile as soon as every
+// thread is done reading it, so the next tile loads while this one is
+// computed.  With a ring of 1 every block takes exactly one tile.  The waits
+// on the mbarriers are bounded and their outcome is the same for the whole
+// block: if one gives up, the block records ECHO_ERR_TIMEOUT in the status
+// word, waits once more (also bounded) for its copies in flight, and returns.
 //
 // With `FUSED` the block also writes the decoded gather value to all P output
 // buffers, so the separate gather kernel is skipped.
@@ -22,71 +26,37 @@
 #include "quant.cuh"
 #include "tma.cuh"
 
+#ifndef ECHO_REDUCE_RING
+#define ECHO_REDUCE_RING 2
+#endif
+
 namespace echo {
 namespace {
 
+constexpr int kReduceRing = ECHO_REDUCE_RING;   // tiles in flight per block
+
+// Shared-memory stage of one tile: [P-1][T][CB] received codes, [P-1][T] meta
+// words, [T] x 256 B owner bf16 input, [T] x 512 B owner state (compensated).
+template <int BITS, bool COMP>
+__host__ __device__ inline uint32_t stage_bytes(int P) {
+  return (uint32_t)((P - 1) * kReduceTile * (16 * BITS + 4) + kReduceTile * 256 +
+                    (COMP ? kReduceTile * 512 : 0));
+}
+
+// Computes one owner tile (t groups from j0 of segment o) held in a stage,
+// writing the gather codes, meta, new owner state and (FUSED) all P outputs
+// to global memory.  Every thread of the block takes part.
 template <int BITS, bool COMP, bool FUSED>
-__global__ void __launch_bounds__(kThreads)
-reduce_kernel(const CallArgs a, int64_t tiles_per_seg) {
+__device__ __forceinline__ void reduce_tile(const CallArgs& a, const uint8_t* stage, int o,
+                                            int64_t j0, int t) {
   constexpr float L = (float)((1 << BITS) - 1);
-  constexpr int CB = 16 * BITS;            // code bytes per group
+  constexpr int CB = 16 * BITS;
   constexpr int T = kReduceTile;
-  extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ __align__(8) uint64_t bar;
-
   const int P = a.P;
-  const int o = (int)(blockIdx.x / tiles_per_seg);
-  const int64_t j0 = (blockIdx.x - (int64_t)o * tiles_per_seg) * T;
-  const int t = (int)((a.Gs - j0) < T ? (a.Gs - j0) : T);   // groups in this tile
-
-  uint8_t* s_codes = smem;                                     // [P-1][T][CB]
-  uint32_t* s_meta = reinterpret_cast<uint32_t*>(smem + (P - 1) * T * CB);   // [P-1][T]
-  uint2* s_x = reinterpret_cast<uint2*>(smem + (P - 1) * T * (CB + 4));      // [T][32] of 4 bf16
-  float4* s_e = reinterpret_cast<float4*>(smem + (P - 1) * T * (CB + 4) + T * 256);  // [T][32]
-
-  const uint32_t bar_a = smem_addr(&bar);
-  const int64_t seg_group0 = (int64_t)o * a.Gs + j0;           // first group of the tile in the rank tensor
-  if (threadIdx.x == 0) {
-    mbar_init(bar_a, 1);
-    fence_barrier_init();
-  }
-  __syncthreads();
-
-  if (threadIdx.x == 0) {
-    // The owner's own tile does not depend on the push kernel, so with P > 1
-    // its copies are issued before waiting for the push to finish.  (The push
-    // kernel itself waited for everything before it, so what it did not write
-    // is already final.)  With P == 1 there is no push kernel and the
-    // preceding kernel may still be writing that tile: wait first.
-    if (P == 1) asm volatile("griddepcontrol.wait;" ::: "memory");
-    const uint32_t meta_bytes = (uint32_t)(((t + 3) & ~3) * 4);
-    const uint32_t total = (uint32_t)((P - 1) * (t * CB + meta_bytes) + t * 256 + (COMP ? t * 512 : 0));
-    const uint64_t pol = policy_evict_first();     // every byte here is read once per call
-    mbar_expect_tx(bar_a, total);
-    bulk_g2s(smem_addr(s_x), a.in[o] + seg_group0 * kGroup, (uint32_t)(t * 256), bar_a, pol);
-    if (COMP) {
-      bulk_g2s(smem_addr(s_e), a.comp + (int64_t)o * a.n + seg_group0 * kGroup, (uint32_t)(t * 512),
-               bar_a, pol);
-    }
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    for (int js = 0; js < P - 1; ++js) {
-      const int64_t slot = (int64_t)o * (P - 1) + js;
-      bulk_g2s(smem_addr(s_codes + js * T * CB), a.codes1 + (slot * a.Gs + j0) * CB,
-               (uint32_t)(t * CB), bar_a, pol);
-      bulk_g2s(smem_addr(s_meta + js * T), a.meta1 + slot * a.Gs_pad + j0, meta_bytes, bar_a, pol);
-    }
-  } else {
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-  }
-
-  if (!mbar_wait_block(bar_a, 0)) {                // same outcome for the whole block
-    if (threadIdx.x == 0) {
-      atomicOr(a.status, kStatusTimeout);
-      mbar_wait_bounded(bar_a, 0);                 // let copies in flight land before leaving
-    }
-    return;
-  }
-
+  const uint8_t* s_codes = stage;
+  const uint32_t* s_meta = reinterpret_cast<const uint32_t*>(stage + (P - 1) * T * CB);
+  const uint2* s_x = reinterpret_cast<const uint2*>(stage + (P - 1) * T * (CB + 4));
+  const float4* s_e = reinterpret_cast<const float4*>(stage + (P - 1) * T * (CB + 4) + T * 256);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int quarter = lane >> 3;
@@ -149,7 +119,7 @@ reduce_kernel(const CallArgs a, int64_t tiles_per_seg) {
     float lo, hi;
     quarter_range(acc, lo, hi);
     const GroupGrid gg = make_grid(lo, hi, L);
-    const int64_t grp = seg_group0 + gl;           // group index in the rank tensor
+    const int64_t grp = (int64_t)o * a.Gs + j0 + gl;           // group index in the rank tensor
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {               // chunks 2hh and 2hh+1
       float c[8], deq[8];
@@ -190,13 +160,110 @@ reduce_kernel(const CallArgs a, int64_t tiles_per_seg) {
       if (!gg.finite) atomicOr(a.status, kStatusOverflow);
     }
   }
+}
+
+template <int BITS, bool COMP, bool FUSED>
+__global__ void __launch_bounds__(kThreads)
+reduce_kernel(const CallArgs a, int64_t tiles_per_seg, int64_t ntiles) {
+  constexpr int CB = 16 * BITS;            // code bytes per group
+  constexpr int T = kReduceTile;
+  constexpr int R = kReduceRing;
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ __align__(8) uint64_t full[R];
+
+  const int P = a.P;
+  const uint32_t sbytes = stage_bytes<BITS, COMP>(P);
+  const uint32_t full0 = smem_addr(&full[0]);
+  if (threadIdx.x == 0) {
+    for (int st = 0; st < R; ++st) mbar_init(full0 + 8 * st, 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+
+  auto tile_of = [&](int64_t k, int& o, int64_t& j0, int& t) {
+    const int64_t tile = (int64_t)blockIdx.x + k * gridDim.x;
+    o = (int)(tile / tiles_per_seg);
+    j0 = (tile - (int64_t)o * tiles_per_seg) * T;
+    t = (int)((a.Gs - j0) < T ? (a.Gs - j0) : T);
+  };
+  auto exists = [&](int64_t k) { return (int64_t)blockIdx.x + k * gridDim.x < ntiles; };
+  uint64_t pol = 0;
+  // Thread 0: the owner's own input and state of block tile k into stage st
+  // (arming the stage's barrier for the whole tile), then its received codes.
+  auto issue_own = [&](int64_t k, int st) {
+    int o, t;
+    int64_t j0;
+    tile_of(k, o, j0, t);
+    const uint32_t meta_bytes = (uint32_t)(((t + 3) & ~3) * 4);
+    const uint32_t bar = full0 + 8 * st;
+    uint8_t* stage = smem + (size_t)st * sbytes;
+    const int64_t g0 = (int64_t)o * a.Gs + j0;
+    mbar_expect_tx(bar, (uint32_t)((P - 1) * (t * CB + meta_bytes) + t * 256 + (COMP ? t * 512 : 0)));
+    bulk_g2s(smem_addr(stage + (P - 1) * T * (CB + 4)), a.in[o] + g0 * kGroup, (uint32_t)(t * 256),
+             bar, pol);
+    if (COMP) bulk_g2s(smem_addr(stage + (P - 1) * T * (CB + 4) + T * 256),
+                       a.comp + (int64_t)o * a.n + g0 * kGroup, (uint32_t)(t * 512), bar, pol);
+  };
+  auto issue_codes = [&](int64_t k, int st) {
+    int o, t;
+    int64_t j0;
+    tile_of(k, o, j0, t);
+    const uint32_t meta_bytes = (uint32_t)(((t + 3) & ~3) * 4);
+    const uint32_t bar = full0 + 8 * st;
+    uint8_t* stage = smem + (size_t)st * sbytes;
+    for (int js = 0; js < P - 1; ++js) {
+      const int64_t slot = (int64_t)o * (P - 1) + js;
+      bulk_g2s(smem_addr(stage + js * T * CB), a.codes1 + (slot * a.Gs + j0) * CB,
+               (uint32_t)(t * CB), bar, pol);
+      bulk_g2s(smem_addr(stage + (P - 1) * T * CB + js * T * 4), a.meta1 + slot * a.Gs_pad + j0,
+               meta_bytes, bar, pol);
+    }
+  };
+
+  if (threadIdx.x == 0) {
+    pol = policy_evict_first();                    // every byte loaded is read once per call
+    // The owner's own tiles do not depend on the push kernel, so with P > 1
+    // their copies are issued before waiting for the push to finish.  (The
+    // push kernel itself waited for everything before it, so what it did not
+    // write is already final.)  With P == 1 there is no push kernel and the
+    // preceding kernel may still be writing them: wait first.
+    if (P == 1) asm volatile("griddepcontrol.wait;" ::: "memory");
+    for (int st = 0; st < R; ++st) if (exists(st)) issue_own(st, st);
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    for (int st = 0; st < R; ++st) if (exists(st)) issue_codes(st, st);
+  } else {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+  }
+
+  for (int64_t k = 0; exists(k); ++k) {
+    const int st = (int)(k % R);
+    if (!mbar_wait_block(full0 + 8 * st, (uint32_t)((k / R) & 1))) {   // same outcome for all
+      if (threadIdx.x == 0) {
+        atomicOr(a.status, kStatusTimeout);
+        for (int64_t kk = k; kk < k + R && exists(kk); ++kk)   // copies still in flight
+          mbar_wait_bounded(full0 + 8 * (int)(kk % R), (uint32_t)((kk / R) & 1));
+      }
+      return;
+    }
+    int o, t;
+    int64_t j0;
+    tile_of(k, o, j0, t);
+    reduce_tile<BITS, COMP, FUSED>(a, smem + (size_t)st * sbytes, o, j0, t);
+    if (exists(k + R)) {                           // block-uniform
+      fence_proxy_async();                         // this thread's reads before the refill
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        issue_own(k + R, st);
+        issue_codes(k + R, st);
+      }
+    }
+  }
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 template <int BITS, bool COMP, bool FUSED>
 size_t smem_bytes(int P) {
-  constexpr int CB = 16 * BITS;
-  return (size_t)(P - 1) * kReduceTile * (CB + 4) + kReduceTile * 256 + (COMP ? kReduceTile * 512 : 0);
+  return (size_t)kReduceRing * stage_bytes<BITS, COMP>(P);
 }
 
 template <int BITS, bool COMP, bool FUSED>
@@ -208,18 +275,33 @@ cudaError_t set_attr() {
 
 template <int BITS, bool COMP, bool FUSED>
 cudaError_t launch_t(const CallArgs& a, cudaStream_t s, bool pdl) {
+  static int resident_cache[64][ECHO_MAX_RANKS + 1] = {{0}};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const size_t smem = smem_bytes<BITS, COMP, FUSED>(a.P);
+  int& resident = resident_cache[dev & 63][a.P];
+  if (resident == 0) {
+    int sms = 0, per_sm = 0;
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, reduce_kernel<BITS, COMP, FUSED>,
+                                                  kThreads, smem);
+    resident = sms * (per_sm > 0 ? per_sm : 1);
+  }
   const int64_t tiles_per_seg = (a.Gs + kReduceTile - 1) / kReduceTile;
+  const int64_t ntiles = tiles_per_seg * a.P;
+  // A ring of 1 is one tile per block; otherwise one resident wave of blocks.
+  const int64_t blocks = (kReduceRing == 1 || ntiles < resident) ? ntiles : resident;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(tiles_per_seg * a.P));
+  cfg.gridDim = dim3((unsigned)blocks);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = smem_bytes<BITS, COMP, FUSED>(a.P);
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, reduce_kernel<BITS, COMP, FUSED>, a, tiles_per_seg);
+  return cudaLaunchKernelEx(&cfg, reduce_kernel<BITS, COMP, FUSED>, a, tiles_per_seg, ntiles);
 }
 
 }  // namespace
