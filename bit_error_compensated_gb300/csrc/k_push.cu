@@ -87,6 +87,7 @@ push_kernel(const CallArgs a) {
 
   uint64_t pol = 0;
   if (lane == 0) pol = policy_evict_first();        // input and state are read once per call
+  const uint64_t codes_pol = kCodesPolicyLast ? policy_evict_last() : policy_evict_normal();
   // Lane 0: start the copies of iteration i into stage st.
   auto issue = [&](int64_t i, int st) {
     const int64_t qd = wg + i * nw;
@@ -156,11 +157,11 @@ push_kernel(const CallArgs a) {
       if (valid) {
         uint8_t* cg = cs + j * CB;
         if (BITS == 4) {
-          reinterpret_cast<uint16_t*>(cg + 32 * hh)[q] = (uint16_t)pack4<4>(c);
-          reinterpret_cast<uint16_t*>(cg + 32 * hh + 16)[q] = (uint16_t)pack4<4>(c + 4);
+          st_hint_u16(cg + 32 * hh + 2 * q, pack4<4>(c), codes_pol);
+          st_hint_u16(cg + 32 * hh + 16 + 2 * q, pack4<4>(c + 4), codes_pol);
         } else {
-          reinterpret_cast<uint32_t*>(cg + 64 * hh)[q] = pack4<8>(c);
-          reinterpret_cast<uint32_t*>(cg + 64 * hh + 32)[q] = pack4<8>(c + 4);
+          st_hint_u32(cg + 64 * hh + 4 * q, pack4<8>(c), codes_pol);
+          st_hint_u32(cg + 64 * hh + 32 + 4 * q, pack4<8>(c + 4), codes_pol);
         }
         if (COMP) {
           float* eg = es + j * kGroup;
@@ -175,7 +176,7 @@ push_kernel(const CallArgs a) {
       }
     }
     if (valid && q == 0) {
-      ms[j] = gg.meta;
+      st_hint_u32(ms + j, gg.meta, codes_pol);
       if (!gg.finite) atomicOr(a.status, kStatusOverflow);
     }
   }

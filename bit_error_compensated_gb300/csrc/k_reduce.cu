@@ -57,6 +57,8 @@ __device__ __forceinline__ void reduce_tile(const CallArgs& a, const uint8_t* st
   const uint32_t* s_meta = reinterpret_cast<const uint32_t*>(stage + (P - 1) * T * CB);
   const uint2* s_x = reinterpret_cast<const uint2*>(stage + (P - 1) * T * (CB + 4));
   const float4* s_e = reinterpret_cast<const float4*>(stage + (P - 1) * T * (CB + 4) + T * 256);
+  // The gather kernel reads these codes next: keep them in L2.
+  const uint64_t codes_pol = kCodesPolicyLast ? policy_evict_last() : policy_evict_normal();
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int quarter = lane >> 3;
@@ -127,11 +129,11 @@ __device__ __forceinline__ void reduce_tile(const CallArgs& a, const uint8_t* st
       if (!valid) continue;
       uint8_t* cg = a.codes2 + grp * CB;
       if (BITS == 4) {
-        reinterpret_cast<uint16_t*>(cg + 32 * hh)[q] = (uint16_t)pack4<4>(c);
-        reinterpret_cast<uint16_t*>(cg + 32 * hh + 16)[q] = (uint16_t)pack4<4>(c + 4);
+        st_hint_u16(cg + 32 * hh + 2 * q, pack4<4>(c), codes_pol);
+        st_hint_u16(cg + 32 * hh + 16 + 2 * q, pack4<4>(c + 4), codes_pol);
       } else {
-        reinterpret_cast<uint32_t*>(cg + 64 * hh)[q] = pack4<8>(c);
-        reinterpret_cast<uint32_t*>(cg + 64 * hh + 32)[q] = pack4<8>(c + 4);
+        st_hint_u32(cg + 64 * hh + 4 * q, pack4<8>(c), codes_pol);
+        st_hint_u32(cg + 64 * hh + 32 + 4 * q, pack4<8>(c + 4), codes_pol);
       }
       float yb[8];
       const uint2 ya = f32x4_to_bf16(deq, yb);
@@ -156,7 +158,7 @@ __device__ __forceinline__ void reduce_tile(const CallArgs& a, const uint8_t* st
       }
     }
     if (valid && q == 0) {
-      a.meta2[(int64_t)o * a.Gs_pad + j0 + gl] = gg.meta;
+      st_hint_u32(a.meta2 + (int64_t)o * a.Gs_pad + j0 + gl, gg.meta, codes_pol);
       if (!gg.finite) atomicOr(a.status, kStatusOverflow);
     }
   }

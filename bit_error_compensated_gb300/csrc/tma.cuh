@@ -60,6 +60,18 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
   return p;
 }
 
+__device__ __forceinline__ uint64_t policy_evict_normal() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+#ifndef ECHO_CODES_EVICT_LAST
+#define ECHO_CODES_EVICT_LAST 1
+#endif
+// Codes written by one kernel for the next are stored with L2 evict_last.
+constexpr bool kCodesPolicyLast = ECHO_CODES_EVICT_LAST != 0;
+
 __device__ __forceinline__ uint64_t policy_evict_last() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
@@ -97,6 +109,16 @@ __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity) {
 // block must call it).
 __device__ __forceinline__ bool mbar_wait_block(uint32_t bar, uint32_t parity) {
   return __syncthreads_and(mbar_wait_bounded(bar, parity) ? 1 : 0) != 0;
+}
+
+// Global stores with an L2 cache policy (createpolicy): the codes written by
+// one kernel and read by the next are kept in L2 with evict_last.
+__device__ __forceinline__ void st_hint_u16(void* p, uint32_t v, uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.b16 [%0], %1, %2;"
+               :: "l"(p), "h"((unsigned short)v), "l"(pol) : "memory");
+}
+__device__ __forceinline__ void st_hint_u32(void* p, uint32_t v, uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.b32 [%0], %1, %2;" :: "l"(p), "r"(v), "l"(pol) : "memory");
 }
 
 }  // namespace echo
