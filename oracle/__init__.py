@@ -54,7 +54,8 @@ def _load():
         lib.oracle_bf16_to_f32.restype = ctypes.c_float
         lib.oracle_f32_to_bf16_rn.argtypes = [ctypes.c_float]
         lib.oracle_f32_to_bf16_rn.restype = ctypes.c_uint16
-        for fn in ("oracle_f32_to_f16_ru_n", "oracle_f16_to_f32_n", "oracle_f32_to_bf16_rn_n"):
+        for fn in ("oracle_f32_to_f16_ru_n", "oracle_f16_to_f32_n", "oracle_f32_to_bf16_rn_n",
+                   "oracle_f32_to_f16_rd_n"):
             getattr(lib, fn).argtypes = [P, i64, P]
             getattr(lib, fn).restype = None
         lib.oracle_quantize_group.argtypes = [P, i32, i32, P, P, P, P]
@@ -67,6 +68,14 @@ def _load():
         lib.oracle_group_position.restype = i32
         lib.oracle_group_positions.argtypes = [i32, i64, P, i32, i32, P, P, P, P, P, P, P, P]
         lib.oracle_group_positions.restype = i64
+        lib.oracle_quantize_group_mode.argtypes = [P, i32, i32, i32, P, P, P, P]
+        lib.oracle_quantize_group_mode.restype = i32
+        lib.oracle_dequantize_group_mode.argtypes = [P, i32, i32, ctypes.c_uint16, ctypes.c_uint16, P]
+        lib.oracle_dequantize_group_mode.restype = None
+        lib.oracle_group_positions_mode.argtypes = [i32, i64, P, i32, i32, i32, P, P, P, P, P, P, P, P]
+        lib.oracle_group_positions_mode.restype = i64
+        lib.oracle_allreduce_mode.argtypes = [i32, i64, i32, i32, i32, P, P, P, P, P, P, P, P, P, P]
+        lib.oracle_allreduce_mode.restype = i64
         lib.oracle_allreduce.argtypes = [i32, i64, i32, i32, P, P, P, P, P, P, P, P, P, P]
         lib.oracle_allreduce.restype = i64
         _lib = lib
@@ -84,6 +93,14 @@ def f32_to_f16_ru(x: np.ndarray) -> np.ndarray:
     x = np.ascontiguousarray(x, dtype=np.float32).ravel()
     out = np.zeros(x.size, dtype=np.uint16)
     _load().oracle_f32_to_f16_ru_n(_ptr(x), x.size, _ptr(out))
+    return out
+
+
+def f32_to_f16_rd(x: np.ndarray) -> np.ndarray:
+    """binary32 -> binary16 bits, rounding toward -infinity (element-wise)."""
+    x = np.ascontiguousarray(x, dtype=np.float32).ravel()
+    out = np.zeros(x.size, dtype=np.uint16)
+    _load().oracle_f32_to_f16_rd_n(_ptr(x), x.size, _ptr(out))
     return out
 
 
@@ -111,24 +128,36 @@ def bf16_to_f32(b: np.ndarray) -> np.ndarray:
 
 # -------------------------------------------------------------- quantizer ----
 
-def quantize_group(v: np.ndarray, bits: int):
-    """Q_b on one group.  Returns (codes uint8, s_bits, z_bits, flagged, ties)."""
+# Quantizer variants: the method's zero-aware asymmetric quantizer and the two
+# ablations of Table 8 ("naive zero-point", "symmetric grid").
+ZERO_AWARE, NAIVE_ZERO_POINT, SYMMETRIC = 0, 1, 2
+
+def quantize_group(v: np.ndarray, bits: int, mode: int = ZERO_AWARE):
+    """Q_b on one group.  Returns (codes uint8, s_bits, z_bits, flagged, ties);
+    for the naive zero-point mode z_bits is the fp16 offset m."""
     lib = _load()
     v = np.ascontiguousarray(v, dtype=np.float32)
     q = np.zeros(v.size, dtype=np.uint8)
     sb = ctypes.c_uint16()
     zb = ctypes.c_uint16()
     ties = ctypes.c_int64(0)
-    bad = lib.oracle_quantize_group(_ptr(v), v.size, bits, _ptr(q), ctypes.byref(sb),
-                                    ctypes.byref(zb), ctypes.byref(ties))
+    if mode == ZERO_AWARE:
+        bad = lib.oracle_quantize_group(_ptr(v), v.size, bits, _ptr(q), ctypes.byref(sb),
+                                        ctypes.byref(zb), ctypes.byref(ties))
+    else:
+        bad = lib.oracle_quantize_group_mode(_ptr(v), v.size, bits, mode, _ptr(q), ctypes.byref(sb),
+                                             ctypes.byref(zb), ctypes.byref(ties))
     return q, sb.value, zb.value, bad, ties.value
 
 
-def dequantize_group(q: np.ndarray, s_bits: int, z_bits: int) -> np.ndarray:
+def dequantize_group(q: np.ndarray, s_bits: int, z_bits: int, mode: int = ZERO_AWARE) -> np.ndarray:
     lib = _load()
     q = np.ascontiguousarray(q, dtype=np.uint8)
     out = np.zeros(q.size, dtype=np.float32)
-    lib.oracle_dequantize_group(_ptr(q), q.size, s_bits, z_bits, _ptr(out))
+    if mode == ZERO_AWARE:
+        lib.oracle_dequantize_group(_ptr(q), q.size, s_bits, z_bits, _ptr(out))
+    else:
+        lib.oracle_dequantize_group_mode(_ptr(q), q.size, mode, s_bits, z_bits, _ptr(out))
     return out
 
 
@@ -163,7 +192,7 @@ def group_position(P: int, owner: int, bits: int, x: np.ndarray, e: np.ndarray |
 
 
 def group_positions(P: int, owners: np.ndarray, bits: int, x: np.ndarray,
-                    e: np.ndarray | None, want_wire: bool = False):
+                    e: np.ndarray | None, want_wire: bool = False, mode: int = ZERO_AWARE):
     """Many independent group positions at once.
 
     owners [npos] int; x [npos, P, len] bf16 bits; e [npos, P, len] float32
@@ -182,9 +211,9 @@ def group_positions(P: int, owners: np.ndarray, bits: int, x: np.ndarray,
         r.update(q1=np.zeros((npos, P, ln), np.uint8), m1=np.zeros((npos, P), np.uint32),
                  q2=np.zeros((npos, ln), np.uint8), m2=np.zeros(npos, np.uint32))
     ties = ctypes.c_int64(0)
-    bad = lib.oracle_group_positions(P, npos, _ptr(owners), ln, bits, _ptr(x), _ptr(e),
-                                     _ptr(r["y"]), _ptr(r.get("q1")), _ptr(r.get("m1")),
-                                     _ptr(r.get("q2")), _ptr(r.get("m2")), ctypes.byref(ties))
+    bad = lib.oracle_group_positions_mode(P, npos, _ptr(owners), ln, bits, mode, _ptr(x), _ptr(e),
+                                          _ptr(r["y"]), _ptr(r.get("q1")), _ptr(r.get("m1")),
+                                          _ptr(r.get("q2")), _ptr(r.get("m2")), ctypes.byref(ties))
     if bad < 0:
         raise ValueError("oracle_group_positions rejected its arguments")
     r["flagged"] = int(bad)
@@ -193,7 +222,8 @@ def group_positions(P: int, owners: np.ndarray, bits: int, x: np.ndarray,
 
 
 def allreduce(x: np.ndarray, g: int, bits: int, e: np.ndarray | None = None,
-              want_wire: bool = False, want_acc: bool = False, want_nq: bool = False):
+              want_wire: bool = False, want_acc: bool = False, want_nq: bool = False,
+              mode: int = ZERO_AWARE):
     """One emulated all-reduce call.
 
     x: [P, n] uint16 bf16 bits.  e: [P, n] float32 compensator state, updated IN
@@ -218,12 +248,12 @@ def allreduce(x: np.ndarray, g: int, bits: int, e: np.ndarray | None = None,
     if want_nq:
         r["nq"] = np.zeros((P, n), np.uint8)
     ties = ctypes.c_int64(0)
-    bad = lib.oracle_allreduce(P, n, g, bits, _ptr(x), _ptr(r["out"]), _ptr(e),
-                               _ptr(r.get("q1")), _ptr(r.get("m1")), _ptr(r.get("q2")),
-                               _ptr(r.get("m2")), _ptr(r.get("acc")), _ptr(r.get("nq")),
-                               ctypes.byref(ties))
+    bad = lib.oracle_allreduce_mode(P, n, g, bits, mode, _ptr(x), _ptr(r["out"]), _ptr(e),
+                                    _ptr(r.get("q1")), _ptr(r.get("m1")), _ptr(r.get("q2")),
+                                    _ptr(r.get("m2")), _ptr(r.get("acc")), _ptr(r.get("nq")),
+                                    ctypes.byref(ties))
     if bad < 0:
-        raise ValueError(f"oracle_allreduce rejected P={P} n={n} g={g} bits={bits}")
+        raise ValueError(f"oracle_allreduce rejected P={P} n={n} g={g} bits={bits} mode={mode}")
     r["flagged"] = int(bad)
     r["ties"] = ties.value
     return r

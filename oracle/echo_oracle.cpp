@@ -30,6 +30,12 @@
 //     by more than half a step; an all-zero group gets scale 1;
 //   * codes are rint (half-to-even) of v/s plus the zero point, clamped to
 //     [0, 2^b - 1];
+//   * the two quantizers of the ablation in Table 8 (their formulas are not
+//     printed either) are read as: "naive zero-point" -- range [min v, max v]
+//     without 0, a float offset m (fp16, rounded down from min v) stored where
+//     the zero point goes, codes rint((v - m)/s), decoded m + s*q, so 0 is in
+//     general not exactly representable; "symmetric grid" -- s from max|v| over
+//     2^(b-1) - 1 levels, a fixed zero point 2^(b-1), codes rint(v/s) + 2^(b-1);
 //   * owner segments are contiguous: rank o owns elements [o*m, (o+1)*m) with
 //     m = n/P; groups are consecutive runs of g elements inside a segment, the
 //     last one shorter when g does not divide m (Fig. 2(a), Fig. 4);
@@ -156,6 +162,19 @@ void oracle_f32_to_bf16_rn_n(const float* x, int64_t count, uint16_t* out) {
   for (int64_t i = 0; i < count; ++i) out[i] = oracle_f32_to_bf16_rn(x[i]);
 }
 
+// binary32 -> binary16, rounding toward -infinity: the negation of rounding
+// the negated value toward +infinity.
+uint16_t oracle_f32_to_f16_rd(float x) {
+  return (uint16_t)(oracle_f32_to_f16_ru(-x) ^ 0x8000);
+}
+
+void oracle_f32_to_f16_rd_n(const float* x, int64_t count, uint16_t* out) {
+  for (int64_t i = 0; i < count; ++i) out[i] = oracle_f32_to_f16_rd(x[i]);
+}
+
+// Quantizer variants (a mode argument where the functions take one).
+enum { kZeroAware = 0, kNaiveZeroPoint = 1, kSymmetric = 2 };
+
 // ---------------------------------------------------------------------------
 // The quantizer Q_b on one group of `len` fp32 values.
 //
@@ -163,6 +182,11 @@ void oracle_f32_to_bf16_rn_n(const float* x, int64_t count, uint16_t* out) {
 // fp16 (the results are then unspecified), else 0.  Writes the codes q[i] in
 // [0, 2^b-1], the fp16 scale bits and the fp16 zero-point bits.
 // ---------------------------------------------------------------------------
+static int quantize_naive(const float* v, int len, int bits, uint8_t* q, uint16_t* s_bits,
+                          uint16_t* z_bits, int64_t* ties);
+static int quantize_symmetric(const float* v, int len, int bits, uint8_t* q, uint16_t* s_bits,
+                              uint16_t* z_bits, int64_t* ties);
+
 int oracle_quantize_group(const float* v, int len, int bits, uint8_t* q,
                           uint16_t* s_bits, uint16_t* z_bits,
                           int64_t* ties) {
@@ -214,6 +238,91 @@ void oracle_dequantize_group(const uint8_t* q, int len, uint16_t s_bits,
   for (int i = 0; i < len; ++i) out[i] = (float)((int)q[i] - z) * s;
 }
 
+// Ablation "naive zero-point" (Table 8): the group's own range, no 0 in it; a
+// float offset m = fp16 rounding of min v toward -inf, so that v - m >= 0; step
+// (max v - m) / L rounded up to fp16; codes rint((v - m) / s) in [0, L].  The
+// meta word carries m where the zero point otherwise goes.
+static int quantize_naive(const float* v, int len, int bits, uint8_t* q, uint16_t* s_bits,
+                          uint16_t* z_bits, int64_t* ties) {
+  const float Lf = (float)((1 << bits) - 1);
+  int bad = 0;
+  float lo = INFINITY, hi = -INFINITY;
+  for (int i = 0; i < len; ++i) {
+    if (!std::isfinite(v[i])) bad = 1;
+    lo = std::fmin(lo, v[i]);
+    hi = std::fmax(hi, v[i]);
+  }
+  const uint16_t mb = oracle_f32_to_f16_rd(lo);
+  const float m = oracle_f16_to_f32(mb);
+  uint16_t sb = oracle_f32_to_f16_ru((hi - m) / Lf);
+  float s = oracle_f16_to_f32(sb);
+  if (s == 0.0f) {
+    sb = 0x3C00;
+    s = 1.0f;
+  }
+  if (!std::isfinite(s) || !std::isfinite(m)) bad = 1;
+  for (int i = 0; i < len; ++i) {
+    const float r = (v[i] - m) / s;
+    if (ties && std::isfinite(r) && (r - std::floor(r)) == 0.5f) ++*ties;
+    const float c = std::fmin(std::fmax(std::rint(r), 0.0f), Lf);
+    q[i] = (uint8_t)(int)c;
+  }
+  *s_bits = sb;
+  *z_bits = mb;
+  return bad;
+}
+
+// Ablation "symmetric grid" (Table 8): step max|v| / (2^(b-1) - 1) rounded up
+// to fp16, fixed zero point 2^(b-1), codes rint(v/s) clamped to
+// [-(2^(b-1) - 1), 2^(b-1) - 1] plus the zero point; decoded as s * (q - z).
+static int quantize_symmetric(const float* v, int len, int bits, uint8_t* q, uint16_t* s_bits,
+                              uint16_t* z_bits, int64_t* ties) {
+  const int half = 1 << (bits - 1);
+  const float Lh = (float)(half - 1);
+  int bad = 0;
+  float a = 0.0f;
+  for (int i = 0; i < len; ++i) {
+    if (!std::isfinite(v[i])) bad = 1;
+    a = std::fmax(a, std::fabs(v[i]));
+  }
+  uint16_t sb = oracle_f32_to_f16_ru(a / Lh);
+  float s = oracle_f16_to_f32(sb);
+  if (s == 0.0f) {
+    sb = 0x3C00;
+    s = 1.0f;
+  }
+  if (!std::isfinite(s)) bad = 1;
+  for (int i = 0; i < len; ++i) {
+    const float r = v[i] / s;
+    if (ties && std::isfinite(r) && (r - std::floor(r)) == 0.5f) ++*ties;
+    const float c = std::fmin(std::fmax(std::rint(r), -Lh), Lh) + (float)half;
+    q[i] = (uint8_t)(int)c;
+  }
+  *s_bits = sb;
+  *z_bits = oracle_f32_to_f16_ru((float)half);   // exact: a small integer
+  return bad;
+}
+
+int oracle_quantize_group_mode(const float* v, int len, int bits, int mode, uint8_t* q,
+                               uint16_t* s_bits, uint16_t* z_bits, int64_t* ties) {
+  if (mode == kNaiveZeroPoint) return quantize_naive(v, len, bits, q, s_bits, z_bits, ties);
+  if (mode == kSymmetric) return quantize_symmetric(v, len, bits, q, s_bits, z_bits, ties);
+  return oracle_quantize_group(v, len, bits, q, s_bits, z_bits, ties);
+}
+
+// Decoding for any mode: s * (q - z), or m + s * q for the naive zero point
+// (one multiply, then one add).
+void oracle_dequantize_group_mode(const uint8_t* q, int len, int mode, uint16_t s_bits,
+                                  uint16_t z_bits, float* out) {
+  if (mode != kNaiveZeroPoint) {
+    oracle_dequantize_group(q, len, s_bits, z_bits, out);
+    return;
+  }
+  const float s = oracle_f16_to_f32(s_bits);
+  const float m = oracle_f16_to_f32(z_bits);
+  for (int i = 0; i < len; ++i) out[i] = (float)q[i] * s + m;
+}
+
 // Wire packing of codes.  b=4: element 2i in the low nibble of byte i, element
 // 2i+1 in its high nibble (an odd count leaves the last high nibble 0).  b=8:
 // one byte per element.
@@ -248,10 +357,10 @@ void oracle_pack_codes(const uint8_t* q, int64_t count, int bits, uint8_t* out) 
 //   ties   counter of exact rounding ties (v/s exactly k + 1/2), or NULL
 // Returns the number of quantizations flagged non-finite (0 when all is fine).
 // ---------------------------------------------------------------------------
-int oracle_group_position(int P, int o, int len, int bits, const uint16_t* x,
-                          float* e, uint16_t* y, uint8_t* q1, uint32_t* m1,
-                          uint8_t* q2, uint32_t* m2, float* acc_out,
-                          uint8_t* nq, int64_t* ties) {
+int oracle_group_position_mode(int P, int o, int len, int bits, int mode, const uint16_t* x,
+                               float* e, uint16_t* y, uint8_t* q1, uint32_t* m1,
+                               uint8_t* q2, uint32_t* m2, float* acc_out,
+                               uint8_t* nq, int64_t* ties) {
   int bad = 0;
   std::vector<float> v(len), d((size_t)P * len), acc(len);
   std::vector<uint8_t> q(len);
@@ -267,9 +376,9 @@ int oracle_group_position(int P, int o, int len, int bits, const uint16_t* x,
     for (int i = 0; i < len; ++i) {
       v[i] = ep ? oracle_bf16_to_f32(xp[i]) + ep[i] : oracle_bf16_to_f32(xp[i]);
     }
-    bad += oracle_quantize_group(v.data(), len, bits, q.data(), &sb, &zb, ties);
+    bad += oracle_quantize_group_mode(v.data(), len, bits, mode, q.data(), &sb, &zb, ties);
     float* dp = d.data() + (size_t)p * len;
-    oracle_dequantize_group(q.data(), len, sb, zb, dp);
+    oracle_dequantize_group_mode(q.data(), len, mode, sb, zb, dp);
     if (q1) std::memcpy(q1 + (size_t)p * len, q.data(), len);
     if (m1) m1[p] = (uint32_t)sb | ((uint32_t)zb << 16);
     if (nq) for (int i = 0; i < len; ++i) nq[(size_t)p * len + i] += 1;
@@ -295,8 +404,8 @@ int oracle_group_position(int P, int o, int len, int bits, const uint16_t* x,
   }
 
   // Gather: the sum is quantized once; every rank decodes the same code.
-  bad += oracle_quantize_group(acc.data(), len, bits, q.data(), &sb, &zb, ties);
-  oracle_dequantize_group(q.data(), len, sb, zb, v.data());
+  bad += oracle_quantize_group_mode(acc.data(), len, bits, mode, q.data(), &sb, &zb, ties);
+  oracle_dequantize_group_mode(q.data(), len, mode, sb, zb, v.data());
   for (int i = 0; i < len; ++i) y[i] = oracle_f32_to_bf16_rn(v[i]);
   if (q2) std::memcpy(q2, q.data(), len);
   if (m2) m2[0] = (uint32_t)sb | ((uint32_t)zb << 16);
@@ -311,27 +420,43 @@ int oracle_group_position(int P, int o, int len, int bits, const uint16_t* x,
   return bad;
 }
 
+int oracle_group_position(int P, int o, int len, int bits, const uint16_t* x,
+                          float* e, uint16_t* y, uint8_t* q1, uint32_t* m1,
+                          uint8_t* q2, uint32_t* m2, float* acc_out,
+                          uint8_t* nq, int64_t* ties) {
+  return oracle_group_position_mode(P, o, len, bits, kZeroAware, x, e, y, q1, m1, q2, m2,
+                                    acc_out, nq, ties);
+}
+
 // A list of independent group positions, each of `len` elements, processed one
 // after the other by oracle_group_position.  Arrays are position-major:
 //   owners [npos]; x [npos][P][len]; e [npos][P][len] or NULL; y [npos][len];
 //   q1 [npos][P][len], m1 [npos][P], q2 [npos][len], m2 [npos] (each or NULL).
 // Returns the number of flagged quantizations, or -1 for invalid arguments.
-int64_t oracle_group_positions(int P, int64_t npos, const int* owners, int len,
-                               int bits, const uint16_t* x, float* e, uint16_t* y,
-                               uint8_t* q1, uint32_t* m1, uint8_t* q2,
-                               uint32_t* m2, int64_t* ties) {
-  if (P < 1 || npos < 0 || len < 1 || (bits != 4 && bits != 8)) return -1;
+int64_t oracle_group_positions_mode(int P, int64_t npos, const int* owners, int len,
+                                    int bits, int mode, const uint16_t* x, float* e, uint16_t* y,
+                                    uint8_t* q1, uint32_t* m1, uint8_t* q2,
+                                    uint32_t* m2, int64_t* ties) {
+  if (P < 1 || npos < 0 || len < 1 || (bits != 4 && bits != 8) || mode < 0 || mode > 2) return -1;
   const size_t blk = (size_t)P * len;
   int64_t bad = 0;
   for (int64_t k = 0; k < npos; ++k) {
     if (owners[k] < 0 || owners[k] >= P) return -1;
-    bad += oracle_group_position(P, owners[k], len, bits, x + k * blk,
-                                 e ? e + k * blk : nullptr, y + k * len,
-                                 q1 ? q1 + k * blk : nullptr, m1 ? m1 + k * P : nullptr,
-                                 q2 ? q2 + k * len : nullptr, m2 ? m2 + k : nullptr,
-                                 nullptr, nullptr, ties);
+    bad += oracle_group_position_mode(P, owners[k], len, bits, mode, x + k * blk,
+                                      e ? e + k * blk : nullptr, y + k * len,
+                                      q1 ? q1 + k * blk : nullptr, m1 ? m1 + k * P : nullptr,
+                                      q2 ? q2 + k * len : nullptr, m2 ? m2 + k : nullptr,
+                                      nullptr, nullptr, ties);
   }
   return bad;
+}
+
+int64_t oracle_group_positions(int P, int64_t npos, const int* owners, int len,
+                               int bits, const uint16_t* x, float* e, uint16_t* y,
+                               uint8_t* q1, uint32_t* m1, uint8_t* q2,
+                               uint32_t* m2, int64_t* ties) {
+  return oracle_group_positions_mode(P, npos, owners, len, bits, kZeroAware, x, e, y, q1, m1,
+                                     q2, m2, ties);
 }
 
 // ---------------------------------------------------------------------------
@@ -350,11 +475,12 @@ int64_t oracle_group_positions(int P, int64_t npos, const int* owners, int len,
 //   ties               exact-tie counter, or NULL
 // Returns the number of flagged quantizations, or -1 for invalid arguments.
 // ---------------------------------------------------------------------------
-int64_t oracle_allreduce(int P, int64_t n, int g, int bits, const uint16_t* x,
-                         uint16_t* out, float* e, uint8_t* q1, uint32_t* m1,
-                         uint8_t* q2, uint32_t* m2, float* acc, uint8_t* nq,
-                         int64_t* ties) {
+int64_t oracle_allreduce_mode(int P, int64_t n, int g, int bits, int mode, const uint16_t* x,
+                              uint16_t* out, float* e, uint8_t* q1, uint32_t* m1,
+                              uint8_t* q2, uint32_t* m2, float* acc, uint8_t* nq,
+                              int64_t* ties) {
   if (P < 1 || n < 0 || g < 1 || (bits != 4 && bits != 8) || n % P != 0) return -1;
+  if (mode < 0 || mode > 2) return -1;
   const int64_t m = n / P;
   const int64_t Gs = (m + g - 1) / g;
   if (q1) std::memset(q1, 0, (size_t)(P * n));
@@ -377,9 +503,9 @@ int64_t oracle_allreduce(int P, int64_t n, int g, int bits, const uint16_t* x,
         }
       }
       uint32_t m2g = 0;
-      bad += oracle_group_position(P, o, len, bits, xg.data(), e ? eg.data() : nullptr,
-                                   yg.data(), q1g.data(), m1g.data(), q2g.data(), &m2g,
-                                   accg.data(), nqg.data(), ties);
+      bad += oracle_group_position_mode(P, o, len, bits, mode, xg.data(), e ? eg.data() : nullptr,
+                                        yg.data(), q1g.data(), m1g.data(), q2g.data(), &m2g,
+                                        accg.data(), nqg.data(), ties);
       for (int p = 0; p < P; ++p) {
         for (int i = 0; i < len; ++i) {
           out[p * n + start + i] = yg[i];
@@ -397,6 +523,14 @@ int64_t oracle_allreduce(int P, int64_t n, int g, int bits, const uint16_t* x,
     }
   }
   return bad;
+}
+
+int64_t oracle_allreduce(int P, int64_t n, int g, int bits, const uint16_t* x,
+                         uint16_t* out, float* e, uint8_t* q1, uint32_t* m1,
+                         uint8_t* q2, uint32_t* m2, float* acc, uint8_t* nq,
+                         int64_t* ties) {
+  return oracle_allreduce_mode(P, n, g, bits, kZeroAware, x, out, e, q1, m1, q2, m2, acc, nq,
+                               ties);
 }
 
 }  // extern "C"
