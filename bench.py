@@ -36,6 +36,8 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "bf16-input GB/s per emulated all-reduce call; % of GB300 HBM roofline"
+QUANTIZERS = {0: "zero-aware asymmetric", 1: "naive zero-point (ablation)",
+              2: "symmetric grid (ablation)"}
 G = 128
 FALLBACK_HBM_GBS = 6800.0
 SPEC_HBM_GBS = 7900.0
@@ -233,6 +235,7 @@ def run_ours(args, rank, local, world):
     out = torch.empty((P, n), dtype=torch.bfloat16, device=dev)
     plan = echo.echo_plan(P, n, G, bits)
     echo.echo_set_fused(plan, fused)
+    echo.echo_set_quantizer(plan, args.quantizer)
     states = {"fwd": echo.COMP_DEFAULT,
               "bwd": torch.zeros((P, n), dtype=torch.float32, device=dev) if any(
                   c.state == "bwd" for c in seq) else None,
@@ -316,7 +319,8 @@ def run_ours(args, rank, local, world):
         "data": "synthetic (seeded; shapes and distributions of the workload, no dataset)",
         "config": {"workload": w.name, "P": P, "n_per_rank": n, "bits": bits, "g": G,
                    "calls_per_step": calls, "compensated": compensated_calls == calls,
-                   "fused_gather": bool(fused), "io": "bf16 in/out, fp32 arithmetic, "
+                   "fused_gather": bool(fused), "quantizer": QUANTIZERS[args.quantizer],
+                   "io": "bf16 in/out, fp32 arithmetic, "
                    f"{bits}-bit codes, fp32 state",
                    "l2": f"inputs distinct per call ({calls} x {P * n * 2 >> 20} MiB resident); "
                          f"per-call working set {(P * n * (2 + 2 + 8)) >> 20} MiB > L2",
@@ -519,6 +523,59 @@ def run_reference(args, rank, world):
                     "d2h_bytes_per_step": 0}}
 
 
+# --------------------------------------------------- accuracy (Table 8) ----
+
+def run_accuracy(args):
+    """A synthetic stand-in for the paper's Table 6 / Table 8 comparisons, which
+    need models and datasets: for each quantizer, with and without the
+    compensator, run the workload's call sequence and measure, against the
+    exact sum of the bf16 inputs (fp64),
+      per_call_rel_rms  RMS error of one call's output / RMS of the exact sum
+                        (mean over calls), and
+      drift_rel_rms     RMS of the error accumulated over the whole sequence /
+                        RMS of one call's exact sum,
+    the quantity whose growth the compensator is meant to stop."""
+    import torch
+    from bit_error_compensated_gb300 import echo
+    from bit_error_compensated_gb300.workloads import WORKLOADS, call_sequence, rank_inputs
+    number, bits = args.workload, args.bits
+    w = WORKLOADS[number]
+    P, n = w.P, w.n
+    seq = call_sequence(number, steps=1)
+    if args.calls:
+        seq = seq[:args.calls]
+    dev = torch.device("cuda", 0)
+    x = torch.empty((P, n), dtype=torch.bfloat16, device=dev)
+    out = torch.empty_like(x)
+    rows = {}
+    for qz in (0, 1, 2):
+        for compensated in (True, False):
+            plan = echo.echo_plan(P, n, G, bits)
+            echo.echo_set_quantizer(plan, qz)
+            states = {}
+            drift = torch.zeros(n, dtype=torch.float64, device=dev)
+            rel, scale = [], None
+            for c in seq:
+                rank_inputs(number, c, dev, out=x)
+                comp = None
+                if compensated and c.state != "none":
+                    comp = states.setdefault(c.state, torch.zeros((P, n), device=dev))
+                echo.echo_allreduce(plan, list(x), list(out), comp)
+                exact = x.double().sum(0)
+                err = out[0].double() - exact
+                drift += err
+                ex_rms = float(exact.square().mean().sqrt())
+                scale = scale or ex_rms
+                rel.append(float(err.square().mean().sqrt()) / ex_rms)
+            if echo.echo_get_status(plan) != 0:
+                raise RuntimeError("status word set")
+            rows[f"{QUANTIZERS[qz]}, {'compensated' if compensated else 'uncompensated'}"] = {
+                "per_call_rel_rms": round(sum(rel) / len(rel), 6),
+                "drift_rel_rms": round(float(drift.square().mean().sqrt()) / scale, 6)}
+            del plan
+    return {"workload": w.name, "bits": bits, "calls": len(seq), "results": rows}
+
+
 # ------------------------------------------------------------------- main ----
 
 def main(argv=None):
@@ -530,9 +587,13 @@ def main(argv=None):
     ap.add_argument("--workload", type=int, default=2, help="1..5 (default 2: P=4, 2048x4096, 64 calls)")
     ap.add_argument("--bits", type=int, default=4, choices=[4, 8])
     ap.add_argument("--fused", action="store_true", help="reduce kernel writes the outputs itself")
+    ap.add_argument("--quantizer", type=int, default=0, choices=[0, 1, 2],
+                    help="0 zero-aware (the method), 1 naive zero-point, 2 symmetric grid")
     ap.add_argument("--also", default="4", help="other workloads to time, comma-separated ('' for none)")
     ap.add_argument("--calls", type=int, default=0,
                     help="time only the first N calls of the sequence (profiling runs)")
+    ap.add_argument("--accuracy", action="store_true",
+                    help="report output error and accumulated drift per quantizer instead of timing")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
@@ -540,6 +601,9 @@ def main(argv=None):
     if args.warmup < 3 and args.impl == "ours":
         ap.error("--warmup must be at least 3")
 
+    if args.accuracy:
+        print(json.dumps(run_accuracy(args)), flush=True)
+        return 0
     rank, local, world = dist_setup()
     if args.impl == "reference":
         if rank == 0:

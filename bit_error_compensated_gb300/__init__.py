@@ -9,7 +9,8 @@ _BINDING_NAMES = (
     "echo_plan", "echo_allreduce", "echo_reset_comp", "echo_reset_comp_async",
     "echo_comp_bytes", "echo_wire_bytes", "echo_wire_layout", "echo_get_status",
     "echo_debug_wire", "echo_plan_destroy", "echo_strerror", "echo_set_fused",
-    "echo_set_timing", "Plan", "EchoError", "COMP_DEFAULT",
+    "echo_set_timing", "echo_set_quantizer", "echo_allreduce_noalloc", "Plan", "EchoError",
+    "COMP_DEFAULT",
 )
 
 

@@ -22,6 +22,7 @@ struct echo_plan_s {
   int* status = nullptr;            // device status word
   cudaStream_t last_stream = nullptr;
   int fused = 0;
+  int mode = ECHO_QUANT_ZERO_AWARE;
   cudaEvent_t ev[4] = {nullptr, nullptr, nullptr, nullptr};
   int timing = 0;
 };
@@ -171,6 +172,7 @@ int echo_allreduce(echo_plan_t plan, const void* const* in, void* const* out,
   a.Gs = plan->Gs;
   a.Gs_pad = plan->Gs_pad;
   a.P = P;
+  a.mode = plan->mode;
 
   // Programmatic dependent launch lets each kernel's blocks be scheduled while
   // the previous kernel drains; every kernel waits (griddepcontrol.wait) before
@@ -245,6 +247,12 @@ int echo_debug_wire(echo_plan_t plan, void* host_dst, size_t bytes, void* stream
 int echo_set_fused(echo_plan_t plan, int fused) {
   if (plan == nullptr || (fused != 0 && fused != 1)) return ECHO_ERR_ARG;
   plan->fused = fused;
+  return ECHO_OK;
+}
+
+int echo_set_quantizer(echo_plan_t plan, int mode) {
+  if (plan == nullptr || mode < ECHO_QUANT_ZERO_AWARE || mode > ECHO_QUANT_SYMMETRIC) return ECHO_ERR_ARG;
+  plan->mode = mode;
   return ECHO_OK;
 }
 

@@ -40,6 +40,7 @@ struct CallArgs {
   int64_t Gs;          // groups per owner segment (m / 128)
   int64_t Gs_pad;      // Gs rounded up to a multiple of 4
   int P;
+  int mode;            // quantizer: 0 zero-aware (the method), 1 naive zero point, 2 symmetric
 };
 
 // Launchers (one translation unit each).  They return the launch error.

@@ -16,7 +16,7 @@
 namespace echo {
 namespace {
 
-template <int BITS, int U>
+template <int BITS, int U, int MODE>
 __global__ void __launch_bounds__(kThreads)
 gather_kernel(const CallArgs a) {
   constexpr int CB = 16 * BITS;
@@ -58,11 +58,11 @@ gather_kernel(const CallArgs a) {
       unpack_meta(meta[u], s, zf);
       float deq[8], yb[8];
       if (BITS == 4) {
-        decode4<4>(word[u].x, s, zf, deq);
-        decode4<4>(word[u].x >> 16, s, zf, deq + 4);
+        decode4_mode<4, MODE>(word[u].x, s, zf, deq);
+        decode4_mode<4, MODE>(word[u].x >> 16, s, zf, deq + 4);
       } else {
-        decode4<8>(word[u].x, s, zf, deq);
-        decode4<8>(word[u].y, s, zf, deq + 4);
+        decode4_mode<8, MODE>(word[u].x, s, zf, deq);
+        decode4_mode<8, MODE>(word[u].y, s, zf, deq + 4);
       }
       const uint2 ya = f32x4_to_bf16(deq, yb);
       const uint2 yv = f32x4_to_bf16(deq + 4, yb + 4);
@@ -79,7 +79,7 @@ gather_kernel(const CallArgs a) {
 #endif
 constexpr int kGatherUnroll = ECHO_GATHER_UNROLL;  // group pairs in flight per warp
 
-template <int BITS>
+template <int BITS, int MODE>
 cudaError_t launch_t(const CallArgs& a, cudaStream_t s, bool pdl) {
   static int grid_cache[64] = {0};
   int dev = 0;
@@ -88,7 +88,7 @@ cudaError_t launch_t(const CallArgs& a, cudaStream_t s, bool pdl) {
   if (grid == 0) {
     int sms = 0, per_sm = 0;
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gather_kernel<BITS, kGatherUnroll>,
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gather_kernel<BITS, kGatherUnroll, MODE>,
                                                   kThreads, 0);
     grid = sms * (per_sm > 0 ? per_sm : 1);
   }
@@ -109,13 +109,17 @@ cudaError_t launch_t(const CallArgs& a, cudaStream_t s, bool pdl) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, gather_kernel<BITS, kGatherUnroll>, a);
+  return cudaLaunchKernelEx(&cfg, gather_kernel<BITS, kGatherUnroll, MODE>, a);
 }
 
 }  // namespace
 
 cudaError_t launch_gather(const CallArgs& a, int bits, cudaStream_t s, bool pdl) {
-  return bits == 4 ? launch_t<4>(a, s, pdl) : launch_t<8>(a, s, pdl);
+  if (a.mode == kNaiveZeroPoint)
+    return bits == 4 ? launch_t<4, kNaiveZeroPoint>(a, s, pdl) : launch_t<8, kNaiveZeroPoint>(a, s, pdl);
+  if (a.mode == kSymmetric)
+    return bits == 4 ? launch_t<4, kSymmetric>(a, s, pdl) : launch_t<8, kSymmetric>(a, s, pdl);
+  return bits == 4 ? launch_t<4, kZeroAware>(a, s, pdl) : launch_t<8, kZeroAware>(a, s, pdl);
 }
 
 }  // namespace echo

@@ -46,7 +46,7 @@ constexpr size_t push_smem_bytes() {
   return (size_t)(kThreads / 32) * kPushStages * push_stage_bytes<COMP>();
 }
 
-template <int BITS, bool COMP>
+template <int BITS, bool COMP, int MODE>
 __global__ void __launch_bounds__(kThreads)
 push_kernel(const CallArgs a) {
   constexpr float L = (float)((1 << BITS) - 1);
@@ -147,13 +147,11 @@ push_kernel(const CallArgs a) {
       issue(i + S, st);
     }
 
-    float lo, hi;
-    quarter_range(v, lo, hi);
-    const GroupGrid gg = make_grid(lo, hi, L);
+    const GroupGrid gg = group_grid<MODE>(v, L);
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {                 // chunks 2hh and 2hh+1
       float c[8], d[8];
-      quantize8(v + 8 * hh, gg, L, c, d);
+      quantize8_mode<MODE>(v + 8 * hh, gg, L, c, d);
       if (valid) {
         uint8_t* cg = cs + j * CB;
         if (BITS == 4) {
@@ -183,7 +181,7 @@ push_kernel(const CallArgs a) {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-template <int BITS, bool COMP>
+template <int BITS, bool COMP, int MODE>
 cudaError_t launch_t(const CallArgs& a, cudaStream_t s, bool pdl) {
   static int resident_cache[64] = {0};
   int dev = 0;
@@ -192,9 +190,9 @@ cudaError_t launch_t(const CallArgs& a, cudaStream_t s, bool pdl) {
   if (resident == 0) {
     int sms = 0, per_sm = 0;
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    cudaFuncSetAttribute(push_kernel<BITS, COMP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaFuncSetAttribute(push_kernel<BITS, COMP, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          (int)push_smem_bytes<COMP>());
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, push_kernel<BITS, COMP>, kThreads,
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, push_kernel<BITS, COMP, MODE>, kThreads,
                                                   push_smem_bytes<COMP>());
     resident = sms * (per_sm > 0 ? per_sm : 1);
   }
@@ -217,15 +215,20 @@ cudaError_t launch_t(const CallArgs& a, cudaStream_t s, bool pdl) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, push_kernel<BITS, COMP>, a);
+  return cudaLaunchKernelEx(&cfg, push_kernel<BITS, COMP, MODE>, a);
 }
 
 }  // namespace
 
 cudaError_t launch_push(const CallArgs& a, int bits, cudaStream_t s, bool pdl) {
   const bool comp = a.comp != nullptr;
-  if (bits == 4) return comp ? launch_t<4, true>(a, s, pdl) : launch_t<4, false>(a, s, pdl);
-  return comp ? launch_t<8, true>(a, s, pdl) : launch_t<8, false>(a, s, pdl);
+#define ECHO_PUSH_MODE(M)                                                         \
+  if (bits == 4) return comp ? launch_t<4, true, M>(a, s, pdl) : launch_t<4, false, M>(a, s, pdl); \
+  return comp ? launch_t<8, true, M>(a, s, pdl) : launch_t<8, false, M>(a, s, pdl);
+  if (a.mode == kNaiveZeroPoint) { ECHO_PUSH_MODE(kNaiveZeroPoint) }
+  if (a.mode == kSymmetric) { ECHO_PUSH_MODE(kSymmetric) }
+  ECHO_PUSH_MODE(kZeroAware)
+#undef ECHO_PUSH_MODE
 }
 
 }  // namespace echo

@@ -46,7 +46,7 @@ __host__ __device__ inline uint32_t stage_bytes(int P) {
 // Computes one owner tile (t groups from j0 of segment o) held in a stage,
 // writing the gather codes, meta, new owner state and (FUSED) all P outputs
 // to global memory.  Every thread of the block takes part.
-template <int BITS, bool COMP, bool FUSED>
+template <int BITS, bool COMP, bool FUSED, int MODE>
 __device__ __forceinline__ void reduce_tile(const CallArgs& a, const uint8_t* stage, int o,
                                             int64_t j0, int t) {
   constexpr float L = (float)((1 << BITS) - 1);
@@ -78,7 +78,7 @@ __device__ __forceinline__ void reduce_tile(const CallArgs& a, const uint8_t* st
       for (int c = 0; c < 4; ++c) {
         const uint32_t w = BITS == 4 ? (uint32_t)reinterpret_cast<const uint16_t*>(cg + 16 * c)[q]
                                      : reinterpret_cast<const uint32_t*>(cg + 32 * c)[q];
-        decode4<BITS>(w, s, zf, term + 4 * c);
+        decode4_mode<BITS, MODE>(w, s, zf, term + 4 * c);
       }
     };
     // The owner's own term: its bf16 input plus (compensated) its held error.
@@ -118,14 +118,12 @@ __device__ __forceinline__ void reduce_tile(const CallArgs& a, const uint8_t* st
     }
 
     // Quantize the sum once for the gather.
-    float lo, hi;
-    quarter_range(acc, lo, hi);
-    const GroupGrid gg = make_grid(lo, hi, L);
+    const GroupGrid gg = group_grid<MODE>(acc, L);
     const int64_t grp = (int64_t)o * a.Gs + j0 + gl;           // group index in the rank tensor
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {               // chunks 2hh and 2hh+1
       float c[8], deq[8];
-      quantize8(acc + 8 * hh, gg, L, c, deq);
+      quantize8_mode<MODE>(acc + 8 * hh, gg, L, c, deq);
       if (!valid) continue;
       uint8_t* cg = a.codes2 + grp * CB;
       if (BITS == 4) {
@@ -164,7 +162,7 @@ __device__ __forceinline__ void reduce_tile(const CallArgs& a, const uint8_t* st
   }
 }
 
-template <int BITS, bool COMP, bool FUSED>
+template <int BITS, bool COMP, bool FUSED, int MODE>
 __global__ void __launch_bounds__(kThreads)
 reduce_kernel(const CallArgs a, int64_t tiles_per_seg, int64_t ntiles) {
   constexpr int CB = 16 * BITS;            // code bytes per group
@@ -250,7 +248,7 @@ reduce_kernel(const CallArgs a, int64_t tiles_per_seg, int64_t ntiles) {
     int o, t;
     int64_t j0;
     tile_of(k, o, j0, t);
-    reduce_tile<BITS, COMP, FUSED>(a, smem + (size_t)st * sbytes, o, j0, t);
+    reduce_tile<BITS, COMP, FUSED, MODE>(a, smem + (size_t)st * sbytes, o, j0, t);
     if (exists(k + R)) {                           // block-uniform
       fence_proxy_async();                         // this thread's reads before the refill
       __syncthreads();
@@ -268,14 +266,7 @@ size_t smem_bytes(int P) {
   return (size_t)kReduceRing * stage_bytes<BITS, COMP>(P);
 }
 
-template <int BITS, bool COMP, bool FUSED>
-cudaError_t set_attr() {
-  return cudaFuncSetAttribute(reduce_kernel<BITS, COMP, FUSED>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)smem_bytes<BITS, COMP, FUSED>(ECHO_MAX_RANKS));
-}
-
-template <int BITS, bool COMP, bool FUSED>
+template <int BITS, bool COMP, bool FUSED, int MODE>
 cudaError_t launch_t(const CallArgs& a, cudaStream_t s, bool pdl) {
   static int resident_cache[64][ECHO_MAX_RANKS + 1] = {{0}};
   int dev = 0;
@@ -285,7 +276,7 @@ cudaError_t launch_t(const CallArgs& a, cudaStream_t s, bool pdl) {
   if (resident == 0) {
     int sms = 0, per_sm = 0;
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, reduce_kernel<BITS, COMP, FUSED>,
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, reduce_kernel<BITS, COMP, FUSED, MODE>,
                                                   kThreads, smem);
     resident = sms * (per_sm > 0 ? per_sm : 1);
   }
@@ -303,31 +294,53 @@ cudaError_t launch_t(const CallArgs& a, cudaStream_t s, bool pdl) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, reduce_kernel<BITS, COMP, FUSED>, a, tiles_per_seg, ntiles);
+  return cudaLaunchKernelEx(&cfg, reduce_kernel<BITS, COMP, FUSED, MODE>, a, tiles_per_seg, ntiles);
+}
+
+template <int BITS, bool COMP, bool FUSED, int MODE>
+cudaError_t set_attr() {
+  return cudaFuncSetAttribute(reduce_kernel<BITS, COMP, FUSED, MODE>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)smem_bytes<BITS, COMP, FUSED>(ECHO_MAX_RANKS));
+}
+
+template <int MODE>
+cudaError_t launch_mode(const CallArgs& a, int bits, bool fused, cudaStream_t s, bool pdl) {
+  const bool comp = a.comp != nullptr;
+  if (bits == 4) {
+    if (comp) return fused ? launch_t<4, true, true, MODE>(a, s, pdl) : launch_t<4, true, false, MODE>(a, s, pdl);
+    return fused ? launch_t<4, false, true, MODE>(a, s, pdl) : launch_t<4, false, false, MODE>(a, s, pdl);
+  }
+  if (comp) return fused ? launch_t<8, true, true, MODE>(a, s, pdl) : launch_t<8, true, false, MODE>(a, s, pdl);
+  return fused ? launch_t<8, false, true, MODE>(a, s, pdl) : launch_t<8, false, false, MODE>(a, s, pdl);
+}
+
+template <int MODE>
+cudaError_t prepare_mode() {
+  cudaError_t e = cudaSuccess, r;
+  if ((r = set_attr<4, true, true, MODE>()) != cudaSuccess) e = r;
+  if ((r = set_attr<4, true, false, MODE>()) != cudaSuccess) e = r;
+  if ((r = set_attr<4, false, true, MODE>()) != cudaSuccess) e = r;
+  if ((r = set_attr<4, false, false, MODE>()) != cudaSuccess) e = r;
+  if ((r = set_attr<8, true, true, MODE>()) != cudaSuccess) e = r;
+  if ((r = set_attr<8, true, false, MODE>()) != cudaSuccess) e = r;
+  if ((r = set_attr<8, false, true, MODE>()) != cudaSuccess) e = r;
+  if ((r = set_attr<8, false, false, MODE>()) != cudaSuccess) e = r;
+  return e;
 }
 
 }  // namespace
 
 cudaError_t launch_reduce(const CallArgs& a, int bits, bool fused, cudaStream_t s, bool pdl) {
-  const bool comp = a.comp != nullptr;
-  if (bits == 4) {
-    if (comp) return fused ? launch_t<4, true, true>(a, s, pdl) : launch_t<4, true, false>(a, s, pdl);
-    return fused ? launch_t<4, false, true>(a, s, pdl) : launch_t<4, false, false>(a, s, pdl);
-  }
-  if (comp) return fused ? launch_t<8, true, true>(a, s, pdl) : launch_t<8, true, false>(a, s, pdl);
-  return fused ? launch_t<8, false, true>(a, s, pdl) : launch_t<8, false, false>(a, s, pdl);
+  if (a.mode == kNaiveZeroPoint) return launch_mode<kNaiveZeroPoint>(a, bits, fused, s, pdl);
+  if (a.mode == kSymmetric) return launch_mode<kSymmetric>(a, bits, fused, s, pdl);
+  return launch_mode<kZeroAware>(a, bits, fused, s, pdl);
 }
 
 cudaError_t prepare_kernels() {
-  cudaError_t e = cudaSuccess, r;
-  if ((r = set_attr<4, true, true>()) != cudaSuccess) e = r;
-  if ((r = set_attr<4, true, false>()) != cudaSuccess) e = r;
-  if ((r = set_attr<4, false, true>()) != cudaSuccess) e = r;
-  if ((r = set_attr<4, false, false>()) != cudaSuccess) e = r;
-  if ((r = set_attr<8, true, true>()) != cudaSuccess) e = r;
-  if ((r = set_attr<8, true, false>()) != cudaSuccess) e = r;
-  if ((r = set_attr<8, false, true>()) != cudaSuccess) e = r;
-  if ((r = set_attr<8, false, false>()) != cudaSuccess) e = r;
+  cudaError_t e = prepare_mode<kZeroAware>(), r;
+  if ((r = prepare_mode<kNaiveZeroPoint>()) != cudaSuccess) e = r;
+  if ((r = prepare_mode<kSymmetric>()) != cudaSuccess) e = r;
   return e;
 }
 

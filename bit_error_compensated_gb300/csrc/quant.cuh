@@ -134,6 +134,110 @@ __device__ __forceinline__ void quantize8(const float v[8], const GroupGrid& gg,
   }
 }
 
+// Quantizer variants: the method's zero-aware asymmetric quantizer and the two
+// ablations of Table 8.  Readings of the unprinted formulas:
+//   kNaiveZeroPoint  range [min v, max v] without 0; offset m = fp16 rounding
+//                    of min v toward -inf, carried in the meta word's zero-point
+//                    half; s = (max v - m) / (2^b - 1) rounded up to fp16;
+//                    q = clamp(rint((v - m) / s), 0, 2^b - 1); decoded m + s*q.
+//   kSymmetric       s = max|v| / (2^(b-1) - 1) rounded up to fp16; zero point
+//                    2^(b-1); q = clamp(rint(v / s), +-(2^(b-1) - 1)) + 2^(b-1).
+enum QuantMode : int { kZeroAware = 0, kNaiveZeroPoint = 1, kSymmetric = 2 };
+
+// The grid of one group held by a quarter warp (16 values per lane); every
+// lane of the warp must call it.  For kNaiveZeroPoint, zf holds the offset m.
+template <int MODE>
+__device__ __forceinline__ GroupGrid group_grid(const float v[16], float L) {
+  if constexpr (MODE == kZeroAware) {
+    float lo, hi;
+    quarter_range(v, lo, hi);
+    return make_grid(lo, hi, L);
+  } else if constexpr (MODE == kSymmetric) {
+    float a = 0.0f;
+#pragma unroll
+    for (int k = 0; k < 16; ++k) a = max_nan(a, fabsf(v[k]));
+#pragma unroll
+    for (int off = 4; off > 0; off >>= 1) a = max_nan(a, __shfl_xor_sync(kFull, a, off));
+    const float zf = __fadd_rn(__fmul_rn(L, 0.5f), 0.5f);   // 2^(b-1), exact
+    __half sh = __float2half_ru(__fdiv_rn(a, __fsub_rn(zf, 1.0f)));
+    float s = __half2float(sh);
+    if (s == 0.0f) {
+      sh = __ushort_as_half((unsigned short)0x3C00);
+      s = 1.0f;
+    }
+    GroupGrid gg;
+    gg.s = s;
+    gg.inv = __frcp_rn(s);
+    gg.zf = zf;
+    gg.meta = (uint32_t)__half_as_ushort(sh) | ((uint32_t)__half_as_ushort(__float2half_rn(zf)) << 16);
+    gg.finite = isfinite(s);
+    return gg;
+  } else {
+    float lo = v[0], hi = v[0];
+#pragma unroll
+    for (int k = 1; k < 16; ++k) {
+      lo = min_nan(lo, v[k]);
+      hi = max_nan(hi, v[k]);
+    }
+#pragma unroll
+    for (int off = 4; off > 0; off >>= 1) {
+      lo = min_nan(lo, __shfl_xor_sync(kFull, lo, off));
+      hi = max_nan(hi, __shfl_xor_sync(kFull, hi, off));
+    }
+    const __half mh = __float2half_rd(lo);
+    const float m = __half2float(mh);
+    __half sh = __float2half_ru(__fdiv_rn(__fsub_rn(hi, m), L));
+    float s = __half2float(sh);
+    if (s == 0.0f) {
+      sh = __ushort_as_half((unsigned short)0x3C00);
+      s = 1.0f;
+    }
+    GroupGrid gg;
+    gg.s = s;
+    gg.inv = __frcp_rn(s);
+    gg.zf = m;
+    gg.meta = (uint32_t)__half_as_ushort(sh) | ((uint32_t)__half_as_ushort(mh) << 16);
+    gg.finite = isfinite(s) && isfinite(m);
+    return gg;
+  }
+}
+
+// Codes (integer-valued floats) and decoded values of 8 values in any mode.
+// The quotient is rint(x / s) with x = v (or v - m for the naive offset),
+// taken through the reciprocal as in quantize8; |x / s| < 256 in every mode.
+template <int MODE>
+__device__ __forceinline__ void quantize8_mode(const float v[8], const GroupGrid& gg, float L,
+                                               float c[8], float d[8]) {
+  if constexpr (MODE == kZeroAware) {
+    quantize8(v, gg, L, c, d);
+  } else {
+    float x[8], r[8];
+    float dev = 0.0f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      x[k] = MODE == kNaiveZeroPoint ? __fsub_rn(v[k], gg.zf) : v[k];
+      const float t = __fmul_rn(x[k], gg.inv);
+      r[k] = rint_small(t);
+      dev = fmaxf(dev, fabsf(__fsub_rn(t, r[k])));
+    }
+    if (dev >= kFastRintLimit) {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) r[k] = rintf(__fdiv_rn(x[k], gg.s));
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      if constexpr (MODE == kSymmetric) {
+        const float lh = __fsub_rn(gg.zf, 1.0f);
+        c[k] = __fadd_rn(fminf(fmaxf(r[k], -lh), lh), gg.zf);
+        d[k] = __fmul_rn(__fsub_rn(c[k], gg.zf), gg.s);
+      } else {
+        c[k] = fminf(fmaxf(r[k], 0.0f), L);
+        d[k] = __fadd_rn(__fmul_rn(c[k], gg.s), gg.zf);   // m + s*q
+      }
+    }
+  }
+}
+
 // Meta word -> (step, zero point as float).
 __device__ __forceinline__ void unpack_meta(uint32_t meta, float& s, float& zf) {
   s = __half2float(__ushort_as_half((unsigned short)(meta & 0xFFFFu)));
@@ -170,6 +274,22 @@ __device__ __forceinline__ void decode4(uint32_t w, float s, float zf, float d[4
   for (int k = 0; k < 4; ++k) {
     const float q23 = __uint_as_float(0x4B000000u | ((w >> (BITS * k)) & MASK));  // 2^23 + q
     d[k] = __fmul_rn(__fsub_rn(q23, bias), s);    // q - z exact
+  }
+}
+
+// Decoding in any mode: s * (q - z), or m + s * q for the naive offset
+// (zf then holds m).
+template <int BITS, int MODE>
+__device__ __forceinline__ void decode4_mode(uint32_t w, float s, float zf, float d[4]) {
+  if constexpr (MODE != kNaiveZeroPoint) {
+    decode4<BITS>(w, s, zf, d);
+  } else {
+    constexpr uint32_t MASK = (1u << BITS) - 1;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float q = __fsub_rn(__uint_as_float(0x4B000000u | ((w >> (BITS * k)) & MASK)), 8388608.0f);
+      d[k] = __fadd_rn(__fmul_rn(q, s), zf);
+    }
   }
 }
 

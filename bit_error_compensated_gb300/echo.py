@@ -28,6 +28,9 @@ ECHO_ERR_TIMEOUT = 7
 ECHO_ERR_TOO_LARGE = 8
 ECHO_NOALLOC_SCRATCH_BYTES = 32 << 20
 ECHO_MAX_RANKS = 16
+ECHO_QUANT_ZERO_AWARE = 0
+ECHO_QUANT_NAIVE_ZERO_POINT = 1
+ECHO_QUANT_SYMMETRIC = 2
 COMP_DEFAULT = ctypes.c_void_p(-1 & (2 ** 64 - 1))   # ECHO_COMP_DEFAULT
 
 _vp, _i32, _i64, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
@@ -43,6 +46,7 @@ _SIGS = {
     "echo_debug_wire": (_i32, [_vp, _vp, _sz, _vp]),
     "echo_set_fused": (_i32, [_vp, _i32]),
     "echo_set_timing": (_i32, [_vp, ctypes.POINTER(_vp), _i32]),
+    "echo_set_quantizer": (_i32, [_vp, _i32]),
     "echo_allreduce_noalloc": (_i32, [_i32, _i64, _i32, ctypes.POINTER(_vp), ctypes.POINTER(_vp),
                                       _vp, _vp]),
     "echo_plan_destroy": (None, [_vp]),
@@ -162,6 +166,10 @@ def echo_debug_wire(plan: Plan, stream=None) -> bytes:
 
 def echo_set_fused(plan: Plan, fused: bool) -> None:
     _check(_lib.echo_set_fused(plan, 1 if fused else 0), "echo_set_fused")
+
+
+def echo_set_quantizer(plan: Plan, mode: int) -> None:
+    _check(_lib.echo_set_quantizer(plan, mode), "echo_set_quantizer")
 
 
 def echo_set_timing(plan: Plan, events) -> None:

@@ -219,6 +219,28 @@ int echo_set_timing(echo_plan_t plan, void* const* events, int count);
 int echo_allreduce_noalloc(int P, int64_t n, int bits, const void* const* in,
                            void* const* out, void* comp_state, void* stream);
 
+/*
+ * echo_set_quantizer -- choose the group quantizer of a plan's calls.
+ *   ECHO_QUANT_ZERO_AWARE (default): the method's zero-aware asymmetric
+ *     quantizer (the "full" row of the paper's Table 8), as described at the
+ *     top of this header.
+ *   ECHO_QUANT_NAIVE_ZERO_POINT, ECHO_QUANT_SYMMETRIC: the two ablation rows of
+ *     Table 8 ("naive zero-point", "symmetric grid"), whose formulas are not
+ *     printed either; read as
+ *       naive:     range [min v, max v] without 0, an fp16 offset m rounded
+ *                  down from min v (carried in the meta word's zero-point
+ *                  half), s = (max v - m)/(2^b - 1) rounded up to fp16,
+ *                  q = clamp(rint((v - m)/s), 0, 2^b - 1), decoded m + s*q;
+ *       symmetric: s = max|v|/(2^(b-1) - 1) rounded up to fp16, zero point
+ *                  2^(b-1), q = clamp(rint(v/s), +-(2^(b-1) - 1)) + 2^(b-1).
+ * Applies to both quantizations of every later echo_allreduce of the plan;
+ * the wire layout is unchanged.  Any other value returns ECHO_ERR_ARG.
+ */
+#define ECHO_QUANT_ZERO_AWARE       0
+#define ECHO_QUANT_NAIVE_ZERO_POINT 1
+#define ECHO_QUANT_SYMMETRIC        2
+int echo_set_quantizer(echo_plan_t plan, int mode);
+
 /* Free everything the plan allocated.  NULL is accepted. */
 void echo_plan_destroy(echo_plan_t plan);
 

@@ -93,8 +93,10 @@ class SampledOracle:
     position's compensator state from call to call (positions are independent,
     so this is exactly the oracle's whole call restricted to them)."""
 
-    def __init__(self, P: int, Gs: int, groups: np.ndarray, bits_: int, g: int = 128):
+    def __init__(self, P: int, Gs: int, groups: np.ndarray, bits_: int, g: int = 128,
+                 mode: int = 0):
         self.P, self.Gs, self.groups, self.bits, self.g = P, Gs, groups, bits_, g
+        self.mode = mode
         self.owners = (groups // Gs).astype(np.int32)
         self.idx = group_element_index(groups, g)
         self.idx_t = None
@@ -113,7 +115,8 @@ class SampledOracle:
         e = None
         if state is not None:
             e = self.states.setdefault(state, np.zeros((npos, self.P, self.g), np.float32))
-        r = oracle.group_positions(self.P, self.owners, self.bits, x, e, want_wire=want_wire)
+        r = oracle.group_positions(self.P, self.owners, self.bits, x, e, want_wire=want_wire,
+                                   mode=self.mode)
         r["y_rows"] = r["y"].reshape(-1)          # [npos*g], same for every rank
         return r
 

@@ -34,10 +34,11 @@ def _inputs(P, n, seed, scale=1.0):
     return (x * spread).to(torch.bfloat16)
 
 
-def _run_sequence(echo, P, Gs, bits_, mode, fused, calls=3, seed=0, inplace=False):
+def _run_sequence(echo, P, Gs, bits_, mode, fused, calls=3, seed=0, inplace=False, quant=0):
     n = P * G * Gs
     plan = echo.echo_plan(P, n, G, bits_)
     echo.echo_set_fused(plan, fused)
+    echo.echo_set_quantizer(plan, quant)
     lay = echo.echo_wire_layout(plan)
     comp_t = torch.zeros((P, n), dtype=torch.float32, device="cuda") if mode == "caller" else None
     comp_arg = {"none": None, "default": echo.COMP_DEFAULT, "caller": comp_t}[mode]
@@ -49,7 +50,7 @@ def _run_sequence(echo, P, Gs, bits_, mode, fused, calls=3, seed=0, inplace=Fals
         echo.echo_allreduce(plan, list(x), list(out), comp_arg)
         torch.cuda.synchronize()
         assert echo.echo_get_status(plan) == 0
-        ref = oracle.allreduce(xb, G, bits_, e=e_ref, want_wire=True)
+        ref = oracle.allreduce(xb, G, bits_, e=e_ref, want_wire=True, mode=quant)
         got = bits(out)
         assert np.array_equal(got, ref["out"]), f"outputs differ at call {k}"
         wire = wire_to_canonical(echo.echo_debug_wire(plan), lay, P, n, bits_)
@@ -65,6 +66,17 @@ def _run_sequence(echo, P, Gs, bits_, mode, fused, calls=3, seed=0, inplace=Fals
 @pytest.mark.parametrize("P", [1, 2, 3, 4, 8, 16])
 def test_matches_oracle(echo, P, bits_, mode, fused):
     _run_sequence(echo, P, 37, bits_, mode, fused, seed=P * 10 + bits_)
+
+
+@pytest.mark.parametrize("quant", [1, 2])
+@pytest.mark.parametrize("fused", [0, 1])
+@pytest.mark.parametrize("mode", ["none", "caller"])
+@pytest.mark.parametrize("bits_", [4, 8])
+@pytest.mark.parametrize("P", [1, 3, 4, 8])
+def test_ablation_quantizers_match_oracle(echo, P, bits_, mode, fused, quant):
+    """The two quantizers of the paper's Table 8 ablation ("naive zero-point",
+    "symmetric grid"), selected with echo_set_quantizer."""
+    _run_sequence(echo, P, 37, bits_, mode, fused, seed=500 + 10 * P + bits_, quant=quant)
 
 
 @pytest.mark.parametrize("Gs", [1, 4, 31, 32, 33, 64, 129])
@@ -210,6 +222,9 @@ def test_argument_errors(echo):
     with pytest.raises(echo.EchoError) as ei:
         echo.echo_plan(2, 2 * G, G, 6)
     assert ei.value.status == echo.ECHO_ERR_UNSUPPORTED
+    with pytest.raises(echo.EchoError) as ei:
+        echo.echo_set_quantizer(plan, 3)
+    assert ei.value.status == echo.ECHO_ERR_ARG
 
 
 @pytest.mark.parametrize("bits_", [4, 8])

@@ -46,14 +46,15 @@ def test_p2_n4096_full(echo):
     print(f"p2_n4096: exact rounding ties in the oracle: {ties}; code mismatches: 0")
 
 
-def _sampled_sequence(echo, number, bits_, sample, calls=None, wire_calls=(0,)):
+def _sampled_sequence(echo, number, bits_, sample, calls=None, wire_calls=(0,), quant=0):
     w = WORKLOADS[number]
     P, n = w.P, w.n
     plan = echo.echo_plan(P, n, G, bits_)
+    echo.echo_set_quantizer(plan, quant)
     lay = echo.echo_wire_layout(plan)
     Gs = lay["Gs"]
     groups = sample_groups(P, Gs, sample, seed=number)
-    so = SampledOracle(P, Gs, groups, bits_)
+    so = SampledOracle(P, Gs, groups, bits_, mode=quant)
     states = {}
     x = torch.empty((P, n), dtype=torch.bfloat16, device="cuda")
     out = torch.empty_like(x)
@@ -103,3 +104,10 @@ def test_p4_8192x4096_sampled(echo):
 
 def test_p4_32768x1024_sampled(echo):
     _sampled_sequence(echo, 5, 4, sample=384)
+
+
+@pytest.mark.parametrize("quant", [1, 2])
+def test_p4_2048x4096_ablation_quantizers_sampled(echo, quant):
+    """The Table 8 ablation quantizers over the first 16 calls of the 64-call
+    workload, at full size."""
+    _sampled_sequence(echo, 2, 4, sample=512, calls=16, quant=quant)
