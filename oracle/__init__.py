@@ -76,6 +76,12 @@ def _load():
         lib.oracle_group_positions_mode.restype = i64
         lib.oracle_allreduce_mode.argtypes = [i32, i64, i32, i32, i32, P, P, P, P, P, P, P, P, P, P]
         lib.oracle_allreduce_mode.restype = i64
+        lib.oracle_group_positions_ex.argtypes = [i32, i64, P, i32, i32, i32, i32, ctypes.c_float,
+                                                  P, P, P, P, P, P, P, P]
+        lib.oracle_group_positions_ex.restype = i64
+        lib.oracle_allreduce_ex.argtypes = [i32, i64, i32, i32, i32, i32, ctypes.c_float,
+                                            P, P, P, P, P, P, P, P, P, P]
+        lib.oracle_allreduce_ex.restype = i64
         lib.oracle_allreduce.argtypes = [i32, i64, i32, i32, P, P, P, P, P, P, P, P, P, P]
         lib.oracle_allreduce.restype = i64
         _lib = lib
@@ -192,7 +198,8 @@ def group_position(P: int, owner: int, bits: int, x: np.ndarray, e: np.ndarray |
 
 
 def group_positions(P: int, owners: np.ndarray, bits: int, x: np.ndarray,
-                    e: np.ndarray | None, want_wire: bool = False, mode: int = ZERO_AWARE):
+                    e: np.ndarray | None, want_wire: bool = False, mode: int = ZERO_AWARE,
+                    bf16_state: bool = False, decay: float = 1.0):
     """Many independent group positions at once.
 
     owners [npos] int; x [npos, P, len] bf16 bits; e [npos, P, len] float32
@@ -211,9 +218,10 @@ def group_positions(P: int, owners: np.ndarray, bits: int, x: np.ndarray,
         r.update(q1=np.zeros((npos, P, ln), np.uint8), m1=np.zeros((npos, P), np.uint32),
                  q2=np.zeros((npos, ln), np.uint8), m2=np.zeros(npos, np.uint32))
     ties = ctypes.c_int64(0)
-    bad = lib.oracle_group_positions_mode(P, npos, _ptr(owners), ln, bits, mode, _ptr(x), _ptr(e),
-                                          _ptr(r["y"]), _ptr(r.get("q1")), _ptr(r.get("m1")),
-                                          _ptr(r.get("q2")), _ptr(r.get("m2")), ctypes.byref(ties))
+    bad = lib.oracle_group_positions_ex(P, npos, _ptr(owners), ln, bits, mode, int(bf16_state),
+                                        decay, _ptr(x), _ptr(e), _ptr(r["y"]), _ptr(r.get("q1")),
+                                        _ptr(r.get("m1")), _ptr(r.get("q2")), _ptr(r.get("m2")),
+                                        ctypes.byref(ties))
     if bad < 0:
         raise ValueError("oracle_group_positions rejected its arguments")
     r["flagged"] = int(bad)
@@ -223,11 +231,13 @@ def group_positions(P: int, owners: np.ndarray, bits: int, x: np.ndarray,
 
 def allreduce(x: np.ndarray, g: int, bits: int, e: np.ndarray | None = None,
               want_wire: bool = False, want_acc: bool = False, want_nq: bool = False,
-              mode: int = ZERO_AWARE):
+              mode: int = ZERO_AWARE, bf16_state: bool = False, decay: float = 1.0):
     """One emulated all-reduce call.
 
     x: [P, n] uint16 bf16 bits.  e: [P, n] float32 compensator state, updated IN
-    PLACE, or None for an uncompensated call.  Returns a dict with ``out``
+    PLACE, or None for an uncompensated call.  With bf16_state the state keeps
+    bf16-rounded values (still in the float32 array); decay scales each revealed
+    error before it is kept.  Returns a dict with ``out``
     ([P, n] bf16 bits), ``flagged``, ``ties`` and, on request, the wire codes in
     the oracle's canonical layout (q1 [P, n], m1 [P, P, Gs], q2 [n], m2 [P, Gs]),
     the owner sums ``acc`` [n] and the quantization counts ``nq`` [P, n].
@@ -248,7 +258,8 @@ def allreduce(x: np.ndarray, g: int, bits: int, e: np.ndarray | None = None,
     if want_nq:
         r["nq"] = np.zeros((P, n), np.uint8)
     ties = ctypes.c_int64(0)
-    bad = lib.oracle_allreduce_mode(P, n, g, bits, mode, _ptr(x), _ptr(r["out"]), _ptr(e),
+    bad = lib.oracle_allreduce_ex(P, n, g, bits, mode, int(bf16_state), decay, _ptr(x),
+                                  _ptr(r["out"]), _ptr(e),
                                     _ptr(r.get("q1")), _ptr(r.get("m1")), _ptr(r.get("q2")),
                                     _ptr(r.get("m2")), _ptr(r.get("acc")), _ptr(r.get("nq")),
                                     ctypes.byref(ties))

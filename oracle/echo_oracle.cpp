@@ -36,6 +36,10 @@
 //     the zero point goes, codes rint((v - m)/s), decoded m + s*q, so 0 is in
 //     general not exactly representable; "symmetric grid" -- s from max|v| over
 //     2^(b-1) - 1 levels, a fixed zero point 2^(b-1), codes rint(v/s) + 2^(b-1);
+//   * options of the compensator (the pages print none of its constants): the
+//     held error may be stored in bf16 (rounded to nearest even) instead of
+//     fp32, and it may be decayed, e' = decay * (revealed error), before it is
+//     stored; decay 1 with fp32 storage is the plain error feedback above;
 //   * owner segments are contiguous: rank o owns elements [o*m, (o+1)*m) with
 //     m = n/P; groups are consecutive runs of g elements inside a segment, the
 //     last one shorter when g does not divide m (Fig. 2(a), Fig. 4);
@@ -357,10 +361,18 @@ void oracle_pack_codes(const uint8_t* q, int64_t count, int bits, uint8_t* out) 
 //   ties   counter of exact rounding ties (v/s exactly k + 1/2), or NULL
 // Returns the number of quantizations flagged non-finite (0 when all is fine).
 // ---------------------------------------------------------------------------
-int oracle_group_position_mode(int P, int o, int len, int bits, int mode, const uint16_t* x,
-                               float* e, uint16_t* y, uint8_t* q1, uint32_t* m1,
-                               uint8_t* q2, uint32_t* m2, float* acc_out,
-                               uint8_t* nq, int64_t* ties) {
+// The value the state keeps for a revealed error r: decay * r (one fp32
+// multiply), rounded to bf16 when the state is stored in bf16.  The state
+// array itself stays fp32 (holding bf16 values in that case).
+static float keep_error(float r, int bf16_state, float decay) {
+  const float t = decay * r;
+  return bf16_state ? oracle_bf16_to_f32(oracle_f32_to_bf16_rn(t)) : t;
+}
+
+int oracle_group_position_ex(int P, int o, int len, int bits, int mode, int bf16_state,
+                             float decay, const uint16_t* x, float* e, uint16_t* y,
+                             uint8_t* q1, uint32_t* m1, uint8_t* q2, uint32_t* m2,
+                             float* acc_out, uint8_t* nq, int64_t* ties) {
   int bad = 0;
   std::vector<float> v(len), d((size_t)P * len), acc(len);
   std::vector<uint8_t> q(len);
@@ -383,7 +395,7 @@ int oracle_group_position_mode(int P, int o, int len, int bits, int mode, const 
     if (m1) m1[p] = (uint32_t)sb | ((uint32_t)zb << 16);
     if (nq) for (int i = 0; i < len; ++i) nq[(size_t)p * len + i] += 1;
     // The push reveals this rank's stage-1 error; the rank keeps it.
-    if (ep) for (int i = 0; i < len; ++i) ep[i] = v[i] - dp[i];
+    if (ep) for (int i = 0; i < len; ++i) ep[i] = keep_error(v[i] - dp[i], bf16_state, decay);
   }
 
   // The owner's own copy is not quantized; its entry pass adds its held error.
@@ -415,9 +427,17 @@ int oracle_group_position_mode(int P, int o, int len, int bits, int mode, const 
   // The owner keeps the stage-2 error, measured against what ranks receive.
   if (e) {
     float* eo = e + (size_t)o * len;
-    for (int i = 0; i < len; ++i) eo[i] = acc[i] - oracle_bf16_to_f32(y[i]);
+    for (int i = 0; i < len; ++i) eo[i] = keep_error(acc[i] - oracle_bf16_to_f32(y[i]), bf16_state, decay);
   }
   return bad;
+}
+
+int oracle_group_position_mode(int P, int o, int len, int bits, int mode, const uint16_t* x,
+                               float* e, uint16_t* y, uint8_t* q1, uint32_t* m1,
+                               uint8_t* q2, uint32_t* m2, float* acc_out,
+                               uint8_t* nq, int64_t* ties) {
+  return oracle_group_position_ex(P, o, len, bits, mode, 0, 1.0f, x, e, y, q1, m1, q2, m2,
+                                  acc_out, nq, ties);
 }
 
 int oracle_group_position(int P, int o, int len, int bits, const uint16_t* x,
@@ -433,22 +453,31 @@ int oracle_group_position(int P, int o, int len, int bits, const uint16_t* x,
 //   owners [npos]; x [npos][P][len]; e [npos][P][len] or NULL; y [npos][len];
 //   q1 [npos][P][len], m1 [npos][P], q2 [npos][len], m2 [npos] (each or NULL).
 // Returns the number of flagged quantizations, or -1 for invalid arguments.
-int64_t oracle_group_positions_mode(int P, int64_t npos, const int* owners, int len,
-                                    int bits, int mode, const uint16_t* x, float* e, uint16_t* y,
-                                    uint8_t* q1, uint32_t* m1, uint8_t* q2,
-                                    uint32_t* m2, int64_t* ties) {
+int64_t oracle_group_positions_ex(int P, int64_t npos, const int* owners, int len,
+                                  int bits, int mode, int bf16_state, float decay,
+                                  const uint16_t* x, float* e, uint16_t* y,
+                                  uint8_t* q1, uint32_t* m1, uint8_t* q2,
+                                  uint32_t* m2, int64_t* ties) {
   if (P < 1 || npos < 0 || len < 1 || (bits != 4 && bits != 8) || mode < 0 || mode > 2) return -1;
   const size_t blk = (size_t)P * len;
   int64_t bad = 0;
   for (int64_t k = 0; k < npos; ++k) {
     if (owners[k] < 0 || owners[k] >= P) return -1;
-    bad += oracle_group_position_mode(P, owners[k], len, bits, mode, x + k * blk,
+    bad += oracle_group_position_ex(P, owners[k], len, bits, mode, bf16_state, decay, x + k * blk,
                                       e ? e + k * blk : nullptr, y + k * len,
                                       q1 ? q1 + k * blk : nullptr, m1 ? m1 + k * P : nullptr,
                                       q2 ? q2 + k * len : nullptr, m2 ? m2 + k : nullptr,
                                       nullptr, nullptr, ties);
   }
   return bad;
+}
+
+int64_t oracle_group_positions_mode(int P, int64_t npos, const int* owners, int len,
+                                    int bits, int mode, const uint16_t* x, float* e, uint16_t* y,
+                                    uint8_t* q1, uint32_t* m1, uint8_t* q2,
+                                    uint32_t* m2, int64_t* ties) {
+  return oracle_group_positions_ex(P, npos, owners, len, bits, mode, 0, 1.0f, x, e, y, q1, m1,
+                                   q2, m2, ties);
 }
 
 int64_t oracle_group_positions(int P, int64_t npos, const int* owners, int len,
@@ -475,10 +504,11 @@ int64_t oracle_group_positions(int P, int64_t npos, const int* owners, int len,
 //   ties               exact-tie counter, or NULL
 // Returns the number of flagged quantizations, or -1 for invalid arguments.
 // ---------------------------------------------------------------------------
-int64_t oracle_allreduce_mode(int P, int64_t n, int g, int bits, int mode, const uint16_t* x,
-                              uint16_t* out, float* e, uint8_t* q1, uint32_t* m1,
-                              uint8_t* q2, uint32_t* m2, float* acc, uint8_t* nq,
-                              int64_t* ties) {
+int64_t oracle_allreduce_ex(int P, int64_t n, int g, int bits, int mode, int bf16_state,
+                            float decay, const uint16_t* x,
+                            uint16_t* out, float* e, uint8_t* q1, uint32_t* m1,
+                            uint8_t* q2, uint32_t* m2, float* acc, uint8_t* nq,
+                            int64_t* ties) {
   if (P < 1 || n < 0 || g < 1 || (bits != 4 && bits != 8) || n % P != 0) return -1;
   if (mode < 0 || mode > 2) return -1;
   const int64_t m = n / P;
@@ -503,9 +533,9 @@ int64_t oracle_allreduce_mode(int P, int64_t n, int g, int bits, int mode, const
         }
       }
       uint32_t m2g = 0;
-      bad += oracle_group_position_mode(P, o, len, bits, mode, xg.data(), e ? eg.data() : nullptr,
-                                        yg.data(), q1g.data(), m1g.data(), q2g.data(), &m2g,
-                                        accg.data(), nqg.data(), ties);
+      bad += oracle_group_position_ex(P, o, len, bits, mode, bf16_state, decay, xg.data(),
+                                      e ? eg.data() : nullptr, yg.data(), q1g.data(), m1g.data(),
+                                      q2g.data(), &m2g, accg.data(), nqg.data(), ties);
       for (int p = 0; p < P; ++p) {
         for (int i = 0; i < len; ++i) {
           out[p * n + start + i] = yg[i];
@@ -523,6 +553,14 @@ int64_t oracle_allreduce_mode(int P, int64_t n, int g, int bits, int mode, const
     }
   }
   return bad;
+}
+
+int64_t oracle_allreduce_mode(int P, int64_t n, int g, int bits, int mode, const uint16_t* x,
+                              uint16_t* out, float* e, uint8_t* q1, uint32_t* m1,
+                              uint8_t* q2, uint32_t* m2, float* acc, uint8_t* nq,
+                              int64_t* ties) {
+  return oracle_allreduce_ex(P, n, g, bits, mode, 0, 1.0f, x, out, e, q1, m1, q2, m2, acc, nq,
+                             ties);
 }
 
 int64_t oracle_allreduce(int P, int64_t n, int g, int bits, const uint16_t* x,
