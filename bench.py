@@ -51,19 +51,21 @@ def code_bytes_per_elem(bits: int) -> float:
     return bits / 8 + 4 / G
 
 
-def kernel_bytes(P: int, n: int, bits: int, compensated: bool, fused: bool) -> dict:
+def kernel_bytes(P: int, n: int, bits: int, compensated: bool, fused: bool,
+                 state_bytes: int = 4) -> dict:
     """Algorithmic bytes each kernel must move per call (one call = P ranks x n).
 
-    push:   reads the non-owned bf16 input, reads+writes its fp32 state, writes
-            codes + meta:                  (P-1) n (2 + 8 + c)
+    push:   reads the non-owned bf16 input, reads+writes its state, writes
+            codes + meta:                  (P-1) n (2 + 2e + c)
     reduce: reads P-1 code tiles + meta, the owner's bf16 input and state
             (read+write), writes gather codes + meta:
-                                           (P-1) n c + n (2 + 8 + c)
+                                           (P-1) n c + n (2 + 2e + c)
             (+ 2 P n when it also writes the P outputs)
     gather: reads gather codes + meta, writes P bf16 outputs:  n c + 2 P n
-    The state terms (8 B per element) drop out when uncompensated."""
+    e is the state's bytes per element (4 fp32, 2 bf16); the state terms drop
+    out when uncompensated."""
     c = code_bytes_per_elem(bits)
-    st = 8 if compensated else 0
+    st = 2 * state_bytes if compensated else 0
     d = {"push": (P - 1) * n * (2 + st + c),
          "reduce": (P - 1) * n * c + n * (2 + st + c) + (2 * P * n if fused else 0)}
     if not fused:
@@ -73,8 +75,8 @@ def kernel_bytes(P: int, n: int, bits: int, compensated: bool, fused: bool) -> d
     return d
 
 
-def call_model_bytes(P, n, bits, compensated, fused):
-    return sum(kernel_bytes(P, n, bits, compensated, fused).values())
+def call_model_bytes(P, n, bits, compensated, fused, state_bytes=4):
+    return sum(kernel_bytes(P, n, bits, compensated, fused, state_bytes).values())
 
 
 # ---------------------------------------------------------------- helpers ----
@@ -206,6 +208,13 @@ def whole_job_gbs(bytes_per_rank_per_step: float, steps: int, world: int, max_ms
 
 # ------------------------------------------------------------- our arm -------
 
+def set_state(echo, plan, args):
+    """Applies --state/--decay to a plan; returns the state's bytes per element."""
+    bf16 = args.state == "bf16"
+    echo.echo_set_state(plan, echo.ECHO_STATE_BF16 if bf16 else echo.ECHO_STATE_F32, args.decay)
+    return 2 if bf16 else 4
+
+
 def build_inputs(number, seq, distinct, device):
     import torch
     from bit_error_compensated_gb300.workloads import WORKLOADS, rank_inputs
@@ -236,8 +245,10 @@ def run_ours(args, rank, local, world):
     plan = echo.echo_plan(P, n, G, bits)
     echo.echo_set_fused(plan, fused)
     echo.echo_set_quantizer(plan, args.quantizer)
+    sb = set_state(echo, plan, args)
+    sdt = torch.bfloat16 if sb == 2 else torch.float32
     states = {"fwd": echo.COMP_DEFAULT,
-              "bwd": torch.zeros((P, n), dtype=torch.float32, device=dev) if any(
+              "bwd": torch.zeros((P, n), dtype=sdt, device=dev) if any(
                   c.state == "bwd" for c in seq) else None,
               "none": None}
     out_rows = list(out)
@@ -274,7 +285,7 @@ def run_ours(args, rank, local, world):
     value = whole_job_gbs(bytes_in_per_call * calls, args.steps, world, max_ms)
     per_call_s = max_ms / 1e3 / (args.steps * calls)
     compensated_calls = sum(1 for c in seq if c.state != "none")
-    model = (compensated_calls * call_model_bytes(P, n, bits, True, fused) +
+    model = (compensated_calls * call_model_bytes(P, n, bits, True, fused, sb) +
              (calls - compensated_calls) * call_model_bytes(P, n, bits, False, fused)) / calls
     hbm, hbm_src = load_peaks()
 
@@ -298,7 +309,7 @@ def run_ours(args, rank, local, world):
         per_kernel_ms["reduce"] += evs[1].elapsed_time(evs[2])
         per_kernel_ms["gather"] += evs[2].elapsed_time(evs[3])
     nlaunch = len(ev_sets)
-    kb_comp = kernel_bytes(P, n, bits, True, fused)
+    kb_comp = kernel_bytes(P, n, bits, True, fused, sb)
     kb_unc = kernel_bytes(P, n, bits, False, fused)
     ran = [k for k in ("push", "reduce", "gather") if k in kb_comp and (k != "push" or P > 1)]
     avg_us = {k: per_kernel_ms[k] / nlaunch * 1e3 for k in ran}
@@ -320,10 +331,11 @@ def run_ours(args, rank, local, world):
         "config": {"workload": w.name, "P": P, "n_per_rank": n, "bits": bits, "g": G,
                    "calls_per_step": calls, "compensated": compensated_calls == calls,
                    "fused_gather": bool(fused), "quantizer": QUANTIZERS[args.quantizer],
+                   "state": {"format": "bf16" if sb == 2 else "fp32", "decay": args.decay},
                    "io": "bf16 in/out, fp32 arithmetic, "
-                   f"{bits}-bit codes, fp32 state",
+                   f"{bits}-bit codes, {'bf16' if sb == 2 else 'fp32'} state",
                    "l2": f"inputs distinct per call ({calls} x {P * n * 2 >> 20} MiB resident); "
-                         f"per-call working set {(P * n * (2 + 2 + 8)) >> 20} MiB > L2",
+                         f"per-call working set {(P * n * (2 + 2 + 2 * sb)) >> 20} MiB > L2",
                    "parallelism": f"replicas x{world}" if world > 1 else "1 GPU, P ranks emulated"},
         "hbm_roofline_frac": round(model / per_call_s / 1e9 / hbm, 4),
         "hbm_roofline_frac_spec": round(model / per_call_s / 1e9 / SPEC_HBM_GBS, 4),
@@ -340,7 +352,7 @@ def run_ours(args, rank, local, world):
     if args.also:
         result["also"] = {}
         for num in [int(v) for v in args.also.split(",") if v]:
-            result["also"][WORKLOADS[num].name] = time_other(echo, num, bits, fused, dev)
+            result["also"][WORKLOADS[num].name] = time_other(echo, num, bits, fused, dev, args)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline_oracle(number, bits, budget_s=args.cpu_budget)
     del plan
@@ -404,7 +416,7 @@ def run_e2e(args, echo, plan, xs, seq, states, dev, world):
             "host_inputs": f"{distinct} distinct pinned input sets cycled over the {calls} calls"}
 
 
-def time_other(echo, number, bits, fused, dev, reps=3):
+def time_other(echo, number, bits, fused, dev, args, reps=3):
     """Time another workload's call sequence (8 distinct inputs cycled): GB/s
     and the pipeline's fraction of the HBM roofline.  No parity here: the
     GPU tests check these workloads against the oracle."""
@@ -417,7 +429,9 @@ def time_other(echo, number, bits, fused, dev, reps=3):
     out = torch.empty((w.P, w.n), dtype=torch.bfloat16, device=dev)
     plan = echo.echo_plan(w.P, w.n, G, bits)
     echo.echo_set_fused(plan, fused)
-    bwd = torch.zeros((w.P, w.n), dtype=torch.float32, device=dev)
+    echo.echo_set_quantizer(plan, args.quantizer)
+    sb = set_state(echo, plan, args)
+    bwd = torch.zeros((w.P, w.n), dtype=torch.bfloat16 if sb == 2 else torch.float32, device=dev)
     comps = [{"fwd": echo.COMP_DEFAULT, "bwd": bwd, "none": None}[c.state] for c in seq]
     rows = [list(xs[k]) for k in range(distinct)]
     out_rows = list(out)
@@ -438,7 +452,7 @@ def time_other(echo, number, bits, fused, dev, reps=3):
     per_call_s = a.elapsed_time(b) / 1e3 / (reps * len(seq))
     hbm, _ = load_peaks()
     comp_calls = sum(1 for c in seq if c.state != "none")
-    model = (comp_calls * call_model_bytes(w.P, w.n, bits, True, fused) +
+    model = (comp_calls * call_model_bytes(w.P, w.n, bits, True, fused, sb) +
              (len(seq) - comp_calls) * call_model_bytes(w.P, w.n, bits, False, fused)) / len(seq)
     del plan, xs
     torch.cuda.empty_cache()
@@ -548,31 +562,39 @@ def run_accuracy(args):
     x = torch.empty((P, n), dtype=torch.bfloat16, device=dev)
     out = torch.empty_like(x)
     rows = {}
-    for qz in (0, 1, 2):
-        for compensated in (True, False):
-            plan = echo.echo_plan(P, n, G, bits)
-            echo.echo_set_quantizer(plan, qz)
-            states = {}
-            drift = torch.zeros(n, dtype=torch.float64, device=dev)
-            rel, scale = [], None
-            for c in seq:
-                rank_inputs(number, c, dev, out=x)
-                comp = None
-                if compensated and c.state != "none":
-                    comp = states.setdefault(c.state, torch.zeros((P, n), device=dev))
-                echo.echo_allreduce(plan, list(x), list(out), comp)
-                exact = x.double().sum(0)
-                err = out[0].double() - exact
-                drift += err
-                ex_rms = float(exact.square().mean().sqrt())
-                scale = scale or ex_rms
-                rel.append(float(err.square().mean().sqrt()) / ex_rms)
-            if echo.echo_get_status(plan) != 0:
-                raise RuntimeError("status word set")
-            rows[f"{QUANTIZERS[qz]}, {'compensated' if compensated else 'uncompensated'}"] = {
-                "per_call_rel_rms": round(sum(rel) / len(rel), 6),
-                "drift_rel_rms": round(float(drift.square().mean().sqrt()) / scale, 6)}
-            del plan
+    # (quantizer, compensated, bf16 state, decay)
+    variants = [(qz, comp, False, 1.0) for qz in (0, 1, 2) for comp in (True, False)]
+    variants += [(0, True, True, 1.0), (0, True, False, 0.9), (0, True, True, 0.9)]
+    for qz, compensated, bf16_state, decay in variants:
+        plan = echo.echo_plan(P, n, G, bits)
+        echo.echo_set_quantizer(plan, qz)
+        echo.echo_set_state(plan, echo.ECHO_STATE_BF16 if bf16_state else echo.ECHO_STATE_F32,
+                            decay)
+        sdt = torch.bfloat16 if bf16_state else torch.float32
+        states = {}
+        drift = torch.zeros(n, dtype=torch.float64, device=dev)
+        rel, scale = [], None
+        for c in seq:
+            rank_inputs(number, c, dev, out=x)
+            comp = None
+            if compensated and c.state != "none":
+                comp = states.setdefault(c.state, torch.zeros((P, n), dtype=sdt, device=dev))
+            echo.echo_allreduce(plan, list(x), list(out), comp)
+            exact = x.double().sum(0)
+            err = out[0].double() - exact
+            drift += err
+            ex_rms = float(exact.square().mean().sqrt())
+            scale = scale or ex_rms
+            rel.append(float(err.square().mean().sqrt()) / ex_rms)
+        if echo.echo_get_status(plan) != 0:
+            raise RuntimeError("status word set")
+        label = f"{QUANTIZERS[qz]}, {'compensated' if compensated else 'uncompensated'}"
+        if bf16_state or decay != 1.0:
+            label += f" ({'bf16' if bf16_state else 'fp32'} state, decay {decay})"
+        rows[label] = {
+            "per_call_rel_rms": round(sum(rel) / len(rel), 6),
+            "drift_rel_rms": round(float(drift.square().mean().sqrt()) / scale, 6)}
+        del plan
     return {"workload": w.name, "bits": bits, "calls": len(seq), "results": rows}
 
 
@@ -589,6 +611,10 @@ def main(argv=None):
     ap.add_argument("--fused", action="store_true", help="reduce kernel writes the outputs itself")
     ap.add_argument("--quantizer", type=int, default=0, choices=[0, 1, 2],
                     help="0 zero-aware (the method), 1 naive zero-point, 2 symmetric grid")
+    ap.add_argument("--state", choices=["f32", "bf16"], default="f32",
+                    help="compensator state storage (bf16 halves its traffic)")
+    ap.add_argument("--decay", type=float, default=1.0,
+                    help="kept error = decay x revealed error (1 = plain error feedback)")
     ap.add_argument("--also", default="4", help="other workloads to time, comma-separated ('' for none)")
     ap.add_argument("--calls", type=int, default=0,
                     help="time only the first N calls of the sequence (profiling runs)")

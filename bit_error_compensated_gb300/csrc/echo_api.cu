@@ -23,6 +23,8 @@ struct echo_plan_s {
   cudaStream_t last_stream = nullptr;
   int fused = 0;
   int mode = ECHO_QUANT_ZERO_AWARE;
+  int state_bf16 = 0;               // ECHO_STATE_BF16 selected
+  float decay = 1.0f;
   cudaEvent_t ev[4] = {nullptr, nullptr, nullptr, nullptr};
   int timing = 0;
 };
@@ -173,6 +175,8 @@ int echo_allreduce(echo_plan_t plan, const void* const* in, void* const* out,
   a.Gs_pad = plan->Gs_pad;
   a.P = P;
   a.mode = plan->mode;
+  a.state_bf16 = plan->state_bf16;
+  a.decay = plan->decay;
 
   // Programmatic dependent launch lets each kernel's blocks be scheduled while
   // the previous kernel drains; every kernel waits (griddepcontrol.wait) before
@@ -253,6 +257,25 @@ int echo_set_fused(echo_plan_t plan, int fused) {
 int echo_set_quantizer(echo_plan_t plan, int mode) {
   if (plan == nullptr || mode < ECHO_QUANT_ZERO_AWARE || mode > ECHO_QUANT_SYMMETRIC) return ECHO_ERR_ARG;
   plan->mode = mode;
+  return ECHO_OK;
+}
+
+int echo_set_state(echo_plan_t plan, int format, float decay) {
+  if (plan == nullptr || (format != ECHO_STATE_F32 && format != ECHO_STATE_BF16)) return ECHO_ERR_ARG;
+  if (!(decay > 0.0f && decay <= 1.0f)) return ECHO_ERR_ARG;      // also rejects NaN
+  const int bf16 = format == ECHO_STATE_BF16;
+  if (bf16 != plan->state_bf16) {
+    int rc = check_device(plan);
+    if (rc != ECHO_OK) return rc;
+    // The held values mean nothing in the other format: start from zero.  The
+    // allocation (fp32-sized) serves both.
+    if (plan->comp != nullptr && plan->comp_bytes > 0)
+      ECHO_CUDA(cudaMemsetAsync(plan->comp, 0, (size_t)plan->P * plan->n * sizeof(float),
+                                plan->last_stream));
+    plan->state_bf16 = bf16;
+    plan->comp_bytes = (size_t)plan->P * plan->n * (bf16 ? 2 : 4);
+  }
+  plan->decay = decay;
   return ECHO_OK;
 }
 

@@ -115,6 +115,8 @@ extern "C" int echo_allreduce_noalloc(int P, int64_t n, int bits, const void* co
   a.Gs = Gs;
   a.Gs_pad = Gs_pad;
   a.P = P;
+  a.state_bf16 = 0;            // fp32 state, plain error feedback
+  a.decay = 1.0f;
 
   // The kernels only OR flags into the status word; it is the one part of the
   // array that must start at zero.  The receive slots are fully rewritten by

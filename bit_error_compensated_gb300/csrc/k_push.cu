@@ -36,23 +36,24 @@ namespace {
 #endif
 constexpr int kPushStages = ECHO_PUSH_STAGES;      // quads in flight per warp
 constexpr int kQuadX = 4 * kGroup * 2;      // bf16 bytes of a quad
-constexpr int kQuadE = 4 * kGroup * 4;      // fp32 state bytes of a quad
 
-template <bool COMP>
-constexpr int push_stage_bytes() { return kQuadX + (COMP ? kQuadE : 0); }
+template <int SF>
+constexpr int push_stage_bytes() { return kQuadX + 4 * kGroup * state_bytes<SF>(); }
 
-template <bool COMP>
+template <int SF>
 constexpr size_t push_smem_bytes() {
-  return (size_t)(kThreads / 32) * kPushStages * push_stage_bytes<COMP>();
+  return (size_t)(kThreads / 32) * kPushStages * push_stage_bytes<SF>();
 }
 
-template <int BITS, bool COMP, int MODE>
+template <int BITS, int SF, int MODE>
 __global__ void __launch_bounds__(kThreads)
 push_kernel(const CallArgs a) {
   constexpr float L = (float)((1 << BITS) - 1);
   constexpr int CB = 16 * BITS;                     // code bytes per group
   constexpr int S = kPushStages;
-  constexpr int SB = push_stage_bytes<COMP>();
+  constexpr int SB = push_stage_bytes<SF>();
+  constexpr bool COMP = SF != kNoState;
+  constexpr int EB = state_bytes<SF>();             // state bytes per element
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(8) uint64_t bars[kThreads / 32][S];
 
@@ -63,7 +64,8 @@ push_kernel(const CallArgs a) {
   const int slot = o * (P - 1) + (p < o ? p : p - 1);
   const int64_t Gs = a.Gs;
   const __nv_bfloat16* xs = a.in[p] + (int64_t)o * Gs * kGroup;
-  float* es = COMP ? a.comp + (int64_t)p * a.n + (int64_t)o * Gs * kGroup : nullptr;
+  uint8_t* es = COMP ? reinterpret_cast<uint8_t*>(a.comp) +
+                           ((int64_t)p * a.n + (int64_t)o * Gs * kGroup) * EB : nullptr;
   uint8_t* cs = a.codes1 + (int64_t)slot * Gs * CB;
   uint32_t* ms = a.meta1 + (int64_t)slot * a.Gs_pad;
 
@@ -95,9 +97,9 @@ push_kernel(const CallArgs a) {
     const int64_t g0 = 4 * qd;
     const uint32_t ng = (uint32_t)((Gs - g0) < 4 ? (Gs - g0) : 4);
     const uint32_t bar = bar0 + 8 * st;
-    mbar_expect_tx(bar, ng * (COMP ? 768u : 256u));
+    mbar_expect_tx(bar, ng * (256u + 128u * EB));
     bulk_g2s(smem_addr(wbuf + st * SB), xs + g0 * kGroup, ng * 256u, bar, pol);
-    if (COMP) bulk_g2s(smem_addr(wbuf + st * SB + kQuadX), es + g0 * kGroup, ng * 512u, bar, pol);
+    if (COMP) bulk_g2s(smem_addr(wbuf + st * SB + kQuadX), es + g0 * kGroup * EB, ng * 128u * EB, bar, pol);
   };
   if (lane == 0) {
 #pragma unroll
@@ -125,15 +127,14 @@ push_kernel(const CallArgs a) {
       const uint2* sx = reinterpret_cast<const uint2*>(wbuf + st * SB) + quarter * 32;
 #pragma unroll
       for (int c = 0; c < 4; ++c) bf16x4_to_f32(sx[8 * c + q], v + 4 * c);
-      if (COMP) {
-        const float4* se = reinterpret_cast<const float4*>(wbuf + st * SB + kQuadX) + quarter * 32;
+      if constexpr (COMP) {
+        const uint8_t* se = wbuf + st * SB + kQuadX;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-          const float4 e = se[8 * c + q];
-          v[4 * c + 0] = __fadd_rn(v[4 * c + 0], e.x);
-          v[4 * c + 1] = __fadd_rn(v[4 * c + 1], e.y);
-          v[4 * c + 2] = __fadd_rn(v[4 * c + 2], e.z);
-          v[4 * c + 3] = __fadd_rn(v[4 * c + 3], e.w);
+          float e[4];
+          state_load4<SF>(se, quarter * kGroup + chunk_at(c, q), e);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) v[4 * c + k] = __fadd_rn(v[4 * c + k], e[k]);
         }
       }
     } else {
@@ -161,15 +162,13 @@ push_kernel(const CallArgs a) {
           st_hint_u32(cg + 64 * hh + 4 * q, pack4<8>(c), codes_pol);
           st_hint_u32(cg + 64 * hh + 32 + 4 * q, pack4<8>(c + 4), codes_pol);
         }
-        if (COMP) {
-          float* eg = es + j * kGroup;
+        if constexpr (COMP) {
           const float* vv = v + 8 * hh;
-          *reinterpret_cast<float4*>(eg + chunk_at(2 * hh, q)) =
-              make_float4(__fsub_rn(vv[0], d[0]), __fsub_rn(vv[1], d[1]),
-                          __fsub_rn(vv[2], d[2]), __fsub_rn(vv[3], d[3]));
-          *reinterpret_cast<float4*>(eg + chunk_at(2 * hh + 1, q)) =
-              make_float4(__fsub_rn(vv[4], d[4]), __fsub_rn(vv[5], d[5]),
-                          __fsub_rn(vv[6], d[6]), __fsub_rn(vv[7], d[7]));
+          float r[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) r[k] = __fsub_rn(vv[k], d[k]);
+          state_store4<SF>(es, j * kGroup + chunk_at(2 * hh, q), r, a.decay);
+          state_store4<SF>(es, j * kGroup + chunk_at(2 * hh + 1, q), r + 4, a.decay);
         }
       }
     }
@@ -181,7 +180,7 @@ push_kernel(const CallArgs a) {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-template <int BITS, bool COMP, int MODE>
+template <int BITS, int SF, int MODE>
 cudaError_t launch_t(const CallArgs& a, cudaStream_t s, bool pdl) {
   static int resident_cache[64] = {0};
   int dev = 0;
@@ -190,10 +189,10 @@ cudaError_t launch_t(const CallArgs& a, cudaStream_t s, bool pdl) {
   if (resident == 0) {
     int sms = 0, per_sm = 0;
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    cudaFuncSetAttribute(push_kernel<BITS, COMP, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         (int)push_smem_bytes<COMP>());
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, push_kernel<BITS, COMP, MODE>, kThreads,
-                                                  push_smem_bytes<COMP>());
+    cudaFuncSetAttribute(push_kernel<BITS, SF, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         (int)push_smem_bytes<SF>());
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, push_kernel<BITS, SF, MODE>, kThreads,
+                                                  push_smem_bytes<SF>());
     resident = sms * (per_sm > 0 ? per_sm : 1);
   }
   const int pairs = a.P * (a.P - 1);
@@ -208,27 +207,35 @@ cudaError_t launch_t(const CallArgs& a, cudaStream_t s, bool pdl) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)bx, (unsigned)pairs);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = push_smem_bytes<COMP>();
+  cfg.dynamicSmemBytes = push_smem_bytes<SF>();
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, push_kernel<BITS, COMP, MODE>, a);
+  return cudaLaunchKernelEx(&cfg, push_kernel<BITS, SF, MODE>, a);
+}
+
+template <int MODE>
+cudaError_t launch_mode(const CallArgs& a, int bits, cudaStream_t s, bool pdl) {
+  const int sf = a.comp == nullptr ? kNoState : (a.state_bf16 ? kStateBF16 : kStateF32);
+  if (bits == 4) {
+    if (sf == kStateF32) return launch_t<4, kStateF32, MODE>(a, s, pdl);
+    if (sf == kStateBF16) return launch_t<4, kStateBF16, MODE>(a, s, pdl);
+    return launch_t<4, kNoState, MODE>(a, s, pdl);
+  }
+  if (sf == kStateF32) return launch_t<8, kStateF32, MODE>(a, s, pdl);
+  if (sf == kStateBF16) return launch_t<8, kStateBF16, MODE>(a, s, pdl);
+  return launch_t<8, kNoState, MODE>(a, s, pdl);
 }
 
 }  // namespace
 
 cudaError_t launch_push(const CallArgs& a, int bits, cudaStream_t s, bool pdl) {
-  const bool comp = a.comp != nullptr;
-#define ECHO_PUSH_MODE(M)                                                         \
-  if (bits == 4) return comp ? launch_t<4, true, M>(a, s, pdl) : launch_t<4, false, M>(a, s, pdl); \
-  return comp ? launch_t<8, true, M>(a, s, pdl) : launch_t<8, false, M>(a, s, pdl);
-  if (a.mode == kNaiveZeroPoint) { ECHO_PUSH_MODE(kNaiveZeroPoint) }
-  if (a.mode == kSymmetric) { ECHO_PUSH_MODE(kSymmetric) }
-  ECHO_PUSH_MODE(kZeroAware)
-#undef ECHO_PUSH_MODE
+  if (a.mode == kNaiveZeroPoint) return launch_mode<kNaiveZeroPoint>(a, bits, s, pdl);
+  if (a.mode == kSymmetric) return launch_mode<kSymmetric>(a, bits, s, pdl);
+  return launch_mode<kZeroAware>(a, bits, s, pdl);
 }
 
 }  // namespace echo

@@ -29,6 +29,12 @@
 #ifndef ECHO_REDUCE_RING
 #define ECHO_REDUCE_RING 2
 #endif
+// Blocks per SM the register allocation must allow.  The shared-memory ring
+// already caps residency near this (about 62 KB a block at 4 ranks), so a
+// lower figure buys registers without costing occupancy.
+#ifndef ECHO_REDUCE_MIN_BLOCKS
+#define ECHO_REDUCE_MIN_BLOCKS 3
+#endif
 
 namespace echo {
 namespace {
@@ -37,26 +43,28 @@ constexpr int kReduceRing = ECHO_REDUCE_RING;   // tiles in flight per block
 
 // Shared-memory stage of one tile: [P-1][T][CB] received codes, [P-1][T] meta
 // words, [T] x 256 B owner bf16 input, [T] x 512 B owner state (compensated).
-template <int BITS, bool COMP>
+template <int BITS, int SF>
 __host__ __device__ inline uint32_t stage_bytes(int P) {
   return (uint32_t)((P - 1) * kReduceTile * (16 * BITS + 4) + kReduceTile * 256 +
-                    (COMP ? kReduceTile * 512 : 0));
+                    kReduceTile * 128 * state_bytes<SF>());
 }
 
 // Computes one owner tile (t groups from j0 of segment o) held in a stage,
 // writing the gather codes, meta, new owner state and (FUSED) all P outputs
 // to global memory.  Every thread of the block takes part.
-template <int BITS, bool COMP, bool FUSED, int MODE>
+template <int BITS, int SF, bool FUSED, int MODE>
 __device__ __forceinline__ void reduce_tile(const CallArgs& a, const uint8_t* stage, int o,
                                             int64_t j0, int t) {
   constexpr float L = (float)((1 << BITS) - 1);
+  constexpr bool COMP = SF != kNoState;
+  constexpr int EB = state_bytes<SF>();
   constexpr int CB = 16 * BITS;
   constexpr int T = kReduceTile;
   const int P = a.P;
   const uint8_t* s_codes = stage;
   const uint32_t* s_meta = reinterpret_cast<const uint32_t*>(stage + (P - 1) * T * CB);
   const uint2* s_x = reinterpret_cast<const uint2*>(stage + (P - 1) * T * (CB + 4));
-  const float4* s_e = reinterpret_cast<const float4*>(stage + (P - 1) * T * (CB + 4) + T * 256);
+  const uint8_t* s_e = stage + (P - 1) * T * (CB + 4) + T * 256;           // [T] group states
   // The gather kernel reads these codes next: keep them in L2.
   const uint64_t codes_pol = kCodesPolicyLast ? policy_evict_last() : policy_evict_normal();
   const int warp = threadIdx.x >> 5;
@@ -86,12 +94,11 @@ __device__ __forceinline__ void reduce_tile(const CallArgs& a, const uint8_t* st
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         bf16x4_to_f32(s_x[gs * 32 + 8 * c + q], term + 4 * c);
-        if (COMP) {
-          const float4 e = s_e[gs * 32 + 8 * c + q];
-          term[4 * c + 0] = __fadd_rn(term[4 * c + 0], e.x);
-          term[4 * c + 1] = __fadd_rn(term[4 * c + 1], e.y);
-          term[4 * c + 2] = __fadd_rn(term[4 * c + 2], e.z);
-          term[4 * c + 3] = __fadd_rn(term[4 * c + 3], e.w);
+        if constexpr (COMP) {
+          float e[4];
+          state_load4<SF>(s_e, gs * kGroup + chunk_at(c, q), e);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) term[4 * c + k] = __fadd_rn(term[4 * c + k], e[k]);
         }
       }
     };
@@ -138,15 +145,14 @@ __device__ __forceinline__ void reduce_tile(const CallArgs& a, const uint8_t* st
       const uint2 yv = f32x4_to_bf16(deq + 4, yb + 4);
       const int64_t ea = grp * kGroup + chunk_at(2 * hh, q);
       const int64_t eb = grp * kGroup + chunk_at(2 * hh + 1, q);
-      if (COMP) {
-        float* eo = a.comp + (int64_t)o * a.n;
+      if constexpr (COMP) {
+        uint8_t* eo = reinterpret_cast<uint8_t*>(a.comp) + (int64_t)o * a.n * EB;
         const float* aa = acc + 8 * hh;
-        *reinterpret_cast<float4*>(eo + ea) =
-            make_float4(__fsub_rn(aa[0], yb[0]), __fsub_rn(aa[1], yb[1]),
-                        __fsub_rn(aa[2], yb[2]), __fsub_rn(aa[3], yb[3]));
-        *reinterpret_cast<float4*>(eo + eb) =
-            make_float4(__fsub_rn(aa[4], yb[4]), __fsub_rn(aa[5], yb[5]),
-                        __fsub_rn(aa[6], yb[6]), __fsub_rn(aa[7], yb[7]));
+        float r[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) r[k] = __fsub_rn(aa[k], yb[k]);
+        state_store4<SF>(eo, ea, r, a.decay);
+        state_store4<SF>(eo, eb, r + 4, a.decay);
       }
       if (FUSED) {
         for (int r = 0; r < P; ++r) {
@@ -162,17 +168,19 @@ __device__ __forceinline__ void reduce_tile(const CallArgs& a, const uint8_t* st
   }
 }
 
-template <int BITS, bool COMP, bool FUSED, int MODE>
-__global__ void __launch_bounds__(kThreads)
+template <int BITS, int SF, bool FUSED, int MODE>
+__global__ void __launch_bounds__(kThreads, ECHO_REDUCE_MIN_BLOCKS)
 reduce_kernel(const CallArgs a, int64_t tiles_per_seg, int64_t ntiles) {
   constexpr int CB = 16 * BITS;            // code bytes per group
+  constexpr bool COMP = SF != kNoState;
+  constexpr int EB = state_bytes<SF>();    // state bytes per element
   constexpr int T = kReduceTile;
   constexpr int R = kReduceRing;
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(8) uint64_t full[R];
 
   const int P = a.P;
-  const uint32_t sbytes = stage_bytes<BITS, COMP>(P);
+  const uint32_t sbytes = stage_bytes<BITS, SF>(P);
   const uint32_t full0 = smem_addr(&full[0]);
   if (threadIdx.x == 0) {
     for (int st = 0; st < R; ++st) mbar_init(full0 + 8 * st, 1);
@@ -198,11 +206,12 @@ reduce_kernel(const CallArgs a, int64_t tiles_per_seg, int64_t ntiles) {
     const uint32_t bar = full0 + 8 * st;
     uint8_t* stage = smem + (size_t)st * sbytes;
     const int64_t g0 = (int64_t)o * a.Gs + j0;
-    mbar_expect_tx(bar, (uint32_t)((P - 1) * (t * CB + meta_bytes) + t * 256 + (COMP ? t * 512 : 0)));
+    mbar_expect_tx(bar, (uint32_t)((P - 1) * (t * CB + meta_bytes) + t * 256 + t * 128 * EB));
     bulk_g2s(smem_addr(stage + (P - 1) * T * (CB + 4)), a.in[o] + g0 * kGroup, (uint32_t)(t * 256),
              bar, pol);
     if (COMP) bulk_g2s(smem_addr(stage + (P - 1) * T * (CB + 4) + T * 256),
-                       a.comp + (int64_t)o * a.n + g0 * kGroup, (uint32_t)(t * 512), bar, pol);
+                       reinterpret_cast<const uint8_t*>(a.comp) + ((int64_t)o * a.n + g0 * kGroup) * EB,
+                       (uint32_t)(t * 128 * EB), bar, pol);
   };
   auto issue_codes = [&](int64_t k, int st) {
     int o, t;
@@ -248,7 +257,7 @@ reduce_kernel(const CallArgs a, int64_t tiles_per_seg, int64_t ntiles) {
     int o, t;
     int64_t j0;
     tile_of(k, o, j0, t);
-    reduce_tile<BITS, COMP, FUSED, MODE>(a, smem + (size_t)st * sbytes, o, j0, t);
+    reduce_tile<BITS, SF, FUSED, MODE>(a, smem + (size_t)st * sbytes, o, j0, t);
     if (exists(k + R)) {                           // block-uniform
       fence_proxy_async();                         // this thread's reads before the refill
       __syncthreads();
@@ -261,22 +270,22 @@ reduce_kernel(const CallArgs a, int64_t tiles_per_seg, int64_t ntiles) {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-template <int BITS, bool COMP, bool FUSED>
+template <int BITS, int SF, bool FUSED>
 size_t smem_bytes(int P) {
-  return (size_t)kReduceRing * stage_bytes<BITS, COMP>(P);
+  return (size_t)kReduceRing * stage_bytes<BITS, SF>(P);
 }
 
-template <int BITS, bool COMP, bool FUSED, int MODE>
+template <int BITS, int SF, bool FUSED, int MODE>
 cudaError_t launch_t(const CallArgs& a, cudaStream_t s, bool pdl) {
   static int resident_cache[64][ECHO_MAX_RANKS + 1] = {{0}};
   int dev = 0;
   cudaGetDevice(&dev);
-  const size_t smem = smem_bytes<BITS, COMP, FUSED>(a.P);
+  const size_t smem = smem_bytes<BITS, SF, FUSED>(a.P);
   int& resident = resident_cache[dev & 63][a.P];
   if (resident == 0) {
     int sms = 0, per_sm = 0;
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, reduce_kernel<BITS, COMP, FUSED, MODE>,
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, reduce_kernel<BITS, SF, FUSED, MODE>,
                                                   kThreads, smem);
     resident = sms * (per_sm > 0 ? per_sm : 1);
   }
@@ -294,38 +303,41 @@ cudaError_t launch_t(const CallArgs& a, cudaStream_t s, bool pdl) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, reduce_kernel<BITS, COMP, FUSED, MODE>, a, tiles_per_seg, ntiles);
+  return cudaLaunchKernelEx(&cfg, reduce_kernel<BITS, SF, FUSED, MODE>, a, tiles_per_seg, ntiles);
 }
 
-template <int BITS, bool COMP, bool FUSED, int MODE>
+template <int BITS, int SF, bool FUSED, int MODE>
 cudaError_t set_attr() {
-  return cudaFuncSetAttribute(reduce_kernel<BITS, COMP, FUSED, MODE>,
+  return cudaFuncSetAttribute(reduce_kernel<BITS, SF, FUSED, MODE>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)smem_bytes<BITS, COMP, FUSED>(ECHO_MAX_RANKS));
+                              (int)smem_bytes<BITS, SF, FUSED>(ECHO_MAX_RANKS));
 }
 
 template <int MODE>
 cudaError_t launch_mode(const CallArgs& a, int bits, bool fused, cudaStream_t s, bool pdl) {
-  const bool comp = a.comp != nullptr;
+  const int sf = a.comp == nullptr ? kNoState : (a.state_bf16 ? kStateBF16 : kStateF32);
+#define ECHO_REDUCE_SF(B, SFV)                                                            \
+  return fused ? launch_t<B, SFV, true, MODE>(a, s, pdl) : launch_t<B, SFV, false, MODE>(a, s, pdl);
   if (bits == 4) {
-    if (comp) return fused ? launch_t<4, true, true, MODE>(a, s, pdl) : launch_t<4, true, false, MODE>(a, s, pdl);
-    return fused ? launch_t<4, false, true, MODE>(a, s, pdl) : launch_t<4, false, false, MODE>(a, s, pdl);
+    if (sf == kStateF32) { ECHO_REDUCE_SF(4, kStateF32) }
+    if (sf == kStateBF16) { ECHO_REDUCE_SF(4, kStateBF16) }
+    ECHO_REDUCE_SF(4, kNoState)
   }
-  if (comp) return fused ? launch_t<8, true, true, MODE>(a, s, pdl) : launch_t<8, true, false, MODE>(a, s, pdl);
-  return fused ? launch_t<8, false, true, MODE>(a, s, pdl) : launch_t<8, false, false, MODE>(a, s, pdl);
+  if (sf == kStateF32) { ECHO_REDUCE_SF(8, kStateF32) }
+  if (sf == kStateBF16) { ECHO_REDUCE_SF(8, kStateBF16) }
+  ECHO_REDUCE_SF(8, kNoState)
+#undef ECHO_REDUCE_SF
 }
 
 template <int MODE>
 cudaError_t prepare_mode() {
   cudaError_t e = cudaSuccess, r;
-  if ((r = set_attr<4, true, true, MODE>()) != cudaSuccess) e = r;
-  if ((r = set_attr<4, true, false, MODE>()) != cudaSuccess) e = r;
-  if ((r = set_attr<4, false, true, MODE>()) != cudaSuccess) e = r;
-  if ((r = set_attr<4, false, false, MODE>()) != cudaSuccess) e = r;
-  if ((r = set_attr<8, true, true, MODE>()) != cudaSuccess) e = r;
-  if ((r = set_attr<8, true, false, MODE>()) != cudaSuccess) e = r;
-  if ((r = set_attr<8, false, true, MODE>()) != cudaSuccess) e = r;
-  if ((r = set_attr<8, false, false, MODE>()) != cudaSuccess) e = r;
+#define ECHO_PREP(B, SFV)                                                                 \
+  if ((r = set_attr<B, SFV, true, MODE>()) != cudaSuccess) e = r;                         \
+  if ((r = set_attr<B, SFV, false, MODE>()) != cudaSuccess) e = r;
+  ECHO_PREP(4, kNoState) ECHO_PREP(4, kStateF32) ECHO_PREP(4, kStateBF16)
+  ECHO_PREP(8, kNoState) ECHO_PREP(8, kStateF32) ECHO_PREP(8, kStateBF16)
+#undef ECHO_PREP
   return e;
 }
 

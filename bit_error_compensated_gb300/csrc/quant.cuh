@@ -316,6 +316,42 @@ __device__ __forceinline__ uint2 f32x4_to_bf16(const float f[4], float back[4]) 
   return r;
 }
 
+// Storage of the compensator state: none (uncompensated), fp32, or bf16
+// (rounded to nearest even).  Element i of rank p lives at p*n + i either way.
+enum StateFmt : int { kNoState = 0, kStateF32 = 1, kStateBF16 = 2 };
+
+template <int SF>
+constexpr int state_bytes() { return SF == kStateBF16 ? 2 : (SF == kStateF32 ? 4 : 0); }
+
+// The 4 state values of a chunk at element index i of `base` (global or
+// shared memory), as fp32 (exact for both formats).
+template <int SF>
+__device__ __forceinline__ void state_load4(const uint8_t* base, int64_t i, float e[4]) {
+  if constexpr (SF == kStateF32) {
+    const float4 v = *reinterpret_cast<const float4*>(base + 4 * i);
+    e[0] = v.x; e[1] = v.y; e[2] = v.z; e[3] = v.w;
+  } else {
+    bf16x4_to_f32(*reinterpret_cast<const uint2*>(base + 2 * i), e);
+  }
+}
+
+// Keeps the revealed errors r of a chunk: decay * r, stored as fp32 or
+// rounded to bf16.  With decay 1 the product is r itself (exact for every
+// non-NaN value), so plain error feedback takes the same code.
+template <int SF>
+__device__ __forceinline__ void state_store4(uint8_t* base, int64_t i, const float r[4],
+                                             float decay) {
+  float t[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) t[k] = __fmul_rn(decay, r[k]);
+  if constexpr (SF == kStateF32) {
+    *reinterpret_cast<float4*>(base + 4 * i) = make_float4(t[0], t[1], t[2], t[3]);
+  } else {
+    float back[4];
+    *reinterpret_cast<uint2*>(base + 2 * i) = f32x4_to_bf16(t, back);
+  }
+}
+
 // Element offset, within a group, of chunk c (0..3) of quarter lane q (0..7).
 __device__ __forceinline__ int chunk_at(int c, int q) { return 32 * c + 4 * q; }
 

@@ -31,6 +31,8 @@ ECHO_MAX_RANKS = 16
 ECHO_QUANT_ZERO_AWARE = 0
 ECHO_QUANT_NAIVE_ZERO_POINT = 1
 ECHO_QUANT_SYMMETRIC = 2
+ECHO_STATE_F32 = 0
+ECHO_STATE_BF16 = 1
 COMP_DEFAULT = ctypes.c_void_p(-1 & (2 ** 64 - 1))   # ECHO_COMP_DEFAULT
 
 _vp, _i32, _i64, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
@@ -47,6 +49,7 @@ _SIGS = {
     "echo_set_fused": (_i32, [_vp, _i32]),
     "echo_set_timing": (_i32, [_vp, ctypes.POINTER(_vp), _i32]),
     "echo_set_quantizer": (_i32, [_vp, _i32]),
+    "echo_set_state": (_i32, [_vp, _i32, ctypes.c_float]),
     "echo_allreduce_noalloc": (_i32, [_i32, _i64, _i32, ctypes.POINTER(_vp), ctypes.POINTER(_vp),
                                       _vp, _vp]),
     "echo_plan_destroy": (None, [_vp]),
@@ -170,6 +173,10 @@ def echo_set_fused(plan: Plan, fused: bool) -> None:
 
 def echo_set_quantizer(plan: Plan, mode: int) -> None:
     _check(_lib.echo_set_quantizer(plan, mode), "echo_set_quantizer")
+
+
+def echo_set_state(plan: Plan, fmt: int = ECHO_STATE_F32, decay: float = 1.0) -> None:
+    _check(_lib.echo_set_state(plan, fmt, decay), "echo_set_state")
 
 
 def echo_set_timing(plan: Plan, events) -> None:

@@ -77,7 +77,7 @@ typedef struct echo_plan_s* echo_plan_t;
  * echo_plan -- build the layout for P emulated ranks of n bf16 elements each,
  * groups of g elements and b-bit codes, and allocate (cudaMalloc, on the
  * current device) the plan's receive slots and its own compensator state
- * (P*n fp32, zeroed).  Synchronizes the device once.
+ * (P*n fp32, zeroed; room enough for either format of echo_set_state).  Synchronizes the device once.
  *   P     1..ECHO_MAX_RANKS
  *   n     elements per rank, a multiple of P*g (n = 0 gives an empty plan)
  *   g     group size; 128 on the GPU
@@ -99,8 +99,9 @@ int echo_plan(int P, int64_t n, int g, int bits, echo_plan_t* out);
  *   comp_state  NULL: uncompensated call (no state read or written);
  *               ECHO_COMP_DEFAULT: the plan's own state;
  *               otherwise a caller device buffer of echo_comp_bytes(plan) bytes,
- *               16-byte aligned, fp32 laid out [P][n] (rank p's error for its
- *               element i at p*n + i), zero before the first call of a sequence;
+ *               16-byte aligned, laid out [P][n] (rank p's error for its
+ *               element i at p*n + i) in fp32, or bf16 after echo_set_state,
+ *               zero before the first call of a sequence;
  *               read and updated in place.
  *   stream      cudaStream_t as void*.
  * Enqueues three kernels (push, reduce, gather; or two when the fused gather is
@@ -124,7 +125,8 @@ int echo_reset_comp(echo_plan_t plan);
  */
 int echo_reset_comp_async(echo_plan_t plan, void* comp_state, void* stream);
 
-/* Bytes of one compensator state: P * n * 4.  0 for a NULL plan. */
+/* Bytes of one compensator state: P * n * 4 (fp32 state, the default) or
+ * P * n * 2 (bf16 state, see echo_set_state).  0 for a NULL plan. */
 size_t echo_comp_bytes(echo_plan_t plan);
 
 /* Bytes of the plan's receive-slot workspace (what echo_debug_wire copies). */
@@ -240,6 +242,28 @@ int echo_allreduce_noalloc(int P, int64_t n, int bits, const void* const* in,
 #define ECHO_QUANT_NAIVE_ZERO_POINT 1
 #define ECHO_QUANT_SYMMETRIC        2
 int echo_set_quantizer(echo_plan_t plan, int mode);
+
+/*
+ * echo_set_state -- choose how a plan's calls keep the compensator state (the
+ * reduced-precision and decayed variants of the error feedback; the pages name
+ * a "two-timescale" compensator of the paper's Sec. 3 but print neither its
+ * equations nor a decay constant, so both options are readings):
+ *   format  ECHO_STATE_F32 (default): each kept error is an fp32 value;
+ *           ECHO_STATE_BF16: each kept error is rounded to bf16 (nearest
+ *           even) when stored, halving the state's size and traffic.
+ *   decay   the kept error is fl32(decay * r) for each revealed error r (then
+ *           rounded to bf16 under ECHO_STATE_BF16); 1 (default) is plain
+ *           error feedback, below 1 a leaky one.  Must be finite, in (0, 1].
+ * The state layout stays [P][n] (element i of rank p at p*n + i) in the chosen
+ * type; echo_comp_bytes(plan) becomes P*n*4 or P*n*2 accordingly, and a caller
+ * state passed to echo_allreduce must hold that many bytes in that type.
+ * Changing the format zeroes the plan's own state (ordered as
+ * echo_reset_comp); changing only the decay keeps it.  Invalid values return
+ * ECHO_ERR_ARG and leave the plan unchanged.
+ */
+#define ECHO_STATE_F32  0
+#define ECHO_STATE_BF16 1
+int echo_set_state(echo_plan_t plan, int format, float decay);
 
 /* Free everything the plan allocated.  NULL is accepted. */
 void echo_plan_destroy(echo_plan_t plan);

@@ -94,9 +94,9 @@ class SampledOracle:
     so this is exactly the oracle's whole call restricted to them)."""
 
     def __init__(self, P: int, Gs: int, groups: np.ndarray, bits_: int, g: int = 128,
-                 mode: int = 0):
+                 mode: int = 0, bf16_state: bool = False, decay: float = 1.0):
         self.P, self.Gs, self.groups, self.bits, self.g = P, Gs, groups, bits_, g
-        self.mode = mode
+        self.mode, self.bf16_state, self.decay = mode, bf16_state, decay
         self.owners = (groups // Gs).astype(np.int32)
         self.idx = group_element_index(groups, g)
         self.idx_t = None
@@ -116,7 +116,7 @@ class SampledOracle:
         if state is not None:
             e = self.states.setdefault(state, np.zeros((npos, self.P, self.g), np.float32))
         r = oracle.group_positions(self.P, self.owners, self.bits, x, e, want_wire=want_wire,
-                                   mode=self.mode)
+                                   mode=self.mode, bf16_state=self.bf16_state, decay=self.decay)
         r["y_rows"] = r["y"].reshape(-1)          # [npos*g], same for every rank
         return r
 

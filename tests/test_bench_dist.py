@@ -65,3 +65,7 @@ def test_byte_model_matches_the_per_element_totals():
     assert bench.call_model_bytes(P, n, 8, True, False) == pytest.approx(P * n * (12 + 2 * 1.03125))
     # the fused gather skips one read of the gather codes
     assert bench.call_model_bytes(P, n, 4, True, True) == pytest.approx(P * n * (12 + 2 * c) - n * c)
+    # a bf16 state moves 4 B per element instead of 8 (13.06 -> 9.06 B at 4-bit)
+    assert bench.call_model_bytes(P, n, 4, True, False, 2) == pytest.approx(P * n * (8 + 2 * c))
+    assert (bench.call_model_bytes(P, n, 4, True, False) -
+            bench.call_model_bytes(P, n, 4, True, False, 2)) == pytest.approx(4 * P * n)

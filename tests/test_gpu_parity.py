@@ -34,13 +34,17 @@ def _inputs(P, n, seed, scale=1.0):
     return (x * spread).to(torch.bfloat16)
 
 
-def _run_sequence(echo, P, Gs, bits_, mode, fused, calls=3, seed=0, inplace=False, quant=0):
+def _run_sequence(echo, P, Gs, bits_, mode, fused, calls=3, seed=0, inplace=False, quant=0,
+                  bf16_state=False, decay=1.0):
     n = P * G * Gs
     plan = echo.echo_plan(P, n, G, bits_)
     echo.echo_set_fused(plan, fused)
     echo.echo_set_quantizer(plan, quant)
+    echo.echo_set_state(plan, echo.ECHO_STATE_BF16 if bf16_state else echo.ECHO_STATE_F32, decay)
+    assert echo.echo_comp_bytes(plan) == P * n * (2 if bf16_state else 4)
     lay = echo.echo_wire_layout(plan)
-    comp_t = torch.zeros((P, n), dtype=torch.float32, device="cuda") if mode == "caller" else None
+    sdt = torch.bfloat16 if bf16_state else torch.float32
+    comp_t = torch.zeros((P, n), dtype=sdt, device="cuda") if mode == "caller" else None
     comp_arg = {"none": None, "default": echo.COMP_DEFAULT, "caller": comp_t}[mode]
     e_ref = None if mode == "none" else np.zeros((P, n), np.float32)
     for k in range(calls):
@@ -50,13 +54,15 @@ def _run_sequence(echo, P, Gs, bits_, mode, fused, calls=3, seed=0, inplace=Fals
         echo.echo_allreduce(plan, list(x), list(out), comp_arg)
         torch.cuda.synchronize()
         assert echo.echo_get_status(plan) == 0
-        ref = oracle.allreduce(xb, G, bits_, e=e_ref, want_wire=True, mode=quant)
+        ref = oracle.allreduce(xb, G, bits_, e=e_ref, want_wire=True, mode=quant,
+                               bf16_state=bf16_state, decay=decay)
         got = bits(out)
         assert np.array_equal(got, ref["out"]), f"outputs differ at call {k}"
         wire = wire_to_canonical(echo.echo_debug_wire(plan), lay, P, n, bits_)
         assert_wire_equal(wire, ref, P)
         if mode == "caller":
-            assert_state_close(comp_t.cpu().numpy(), e_ref, f"state after call {k}")
+            # a bf16 state widens to fp32 exactly
+            assert_state_close(comp_t.float().cpu().numpy(), e_ref, f"state after call {k}")
     return plan
 
 
@@ -77,6 +83,47 @@ def test_ablation_quantizers_match_oracle(echo, P, bits_, mode, fused, quant):
     """The two quantizers of the paper's Table 8 ablation ("naive zero-point",
     "symmetric grid"), selected with echo_set_quantizer."""
     _run_sequence(echo, P, 37, bits_, mode, fused, seed=500 + 10 * P + bits_, quant=quant)
+
+
+@pytest.mark.parametrize("fused", [0, 1])
+@pytest.mark.parametrize("state", [(True, 1.0), (False, 0.75), (True, 0.5)])
+@pytest.mark.parametrize("bits_", [4, 8])
+@pytest.mark.parametrize("P", [1, 2, 4, 8, 16])
+def test_state_options_match_oracle(echo, P, bits_, state, fused):
+    """The compensator state kept in bf16 and/or decayed (echo_set_state)."""
+    bf16_state, decay = state
+    _run_sequence(echo, P, 37, bits_, "caller", fused, calls=4, seed=700 + 10 * P + bits_,
+                  bf16_state=bf16_state, decay=decay)
+
+
+@pytest.mark.parametrize("quant", [1, 2])
+def test_state_options_with_ablation_quantizers(echo, quant):
+    _run_sequence(echo, 4, 37, 4, "caller", 0, seed=800 + quant, quant=quant,
+                  bf16_state=True, decay=0.9)
+
+
+def test_state_format_switch(echo):
+    """Changing the format zeroes the plan's own state; changing only the decay
+    keeps it.  Checked through the outputs, which depend on the held state."""
+    P, Gs = 4, 37
+    n = P * G * Gs
+    plan = echo.echo_plan(P, n, G, 4)
+    e = np.zeros((P, n), np.float32)
+    steps = [(False, 1.0), (False, 1.0), (True, 1.0), (True, 1.0), (True, 0.5), (True, 0.5),
+             (False, 0.5), (False, 1.0)]
+    prev = steps[0]
+    for k, (bf16_state, decay) in enumerate(steps):
+        echo.echo_set_state(plan, echo.ECHO_STATE_BF16 if bf16_state else echo.ECHO_STATE_F32,
+                            decay)
+        if bf16_state != prev[0]:
+            e[:] = 0
+        prev = (bf16_state, decay)
+        x = _inputs(P, n, 900 + k)
+        out = torch.empty_like(x)
+        echo.echo_allreduce(plan, list(x), list(out), echo.COMP_DEFAULT)
+        torch.cuda.synchronize()
+        ref = oracle.allreduce(bits(x), G, 4, e=e, bf16_state=bf16_state, decay=decay)
+        assert np.array_equal(bits(out), ref["out"]), f"call {k}"
 
 
 @pytest.mark.parametrize("Gs", [1, 4, 31, 32, 33, 64, 129])
@@ -225,6 +272,12 @@ def test_argument_errors(echo):
     with pytest.raises(echo.EchoError) as ei:
         echo.echo_set_quantizer(plan, 3)
     assert ei.value.status == echo.ECHO_ERR_ARG
+    for fmt, decay in [(2, 1.0), (-1, 1.0), (0, 0.0), (0, -0.5), (1, 1.5), (0, float("nan")),
+                       (0, float("inf"))]:
+        with pytest.raises(echo.EchoError) as ei:
+            echo.echo_set_state(plan, fmt, decay)
+        assert ei.value.status == echo.ECHO_ERR_ARG
+    assert echo.echo_comp_bytes(plan) == plan.P * plan.n * 4       # unchanged
 
 
 @pytest.mark.parametrize("bits_", [4, 8])

@@ -46,15 +46,18 @@ def test_p2_n4096_full(echo):
     print(f"p2_n4096: exact rounding ties in the oracle: {ties}; code mismatches: 0")
 
 
-def _sampled_sequence(echo, number, bits_, sample, calls=None, wire_calls=(0,), quant=0):
+def _sampled_sequence(echo, number, bits_, sample, calls=None, wire_calls=(0,), quant=0,
+                      bf16_state=False, decay=1.0):
     w = WORKLOADS[number]
     P, n = w.P, w.n
     plan = echo.echo_plan(P, n, G, bits_)
     echo.echo_set_quantizer(plan, quant)
+    echo.echo_set_state(plan, echo.ECHO_STATE_BF16 if bf16_state else echo.ECHO_STATE_F32, decay)
+    sdt = torch.bfloat16 if bf16_state else torch.float32
     lay = echo.echo_wire_layout(plan)
     Gs = lay["Gs"]
     groups = sample_groups(P, Gs, sample, seed=number)
-    so = SampledOracle(P, Gs, groups, bits_, mode=quant)
+    so = SampledOracle(P, Gs, groups, bits_, mode=quant, bf16_state=bf16_state, decay=decay)
     states = {}
     x = torch.empty((P, n), dtype=torch.bfloat16, device="cuda")
     out = torch.empty_like(x)
@@ -66,7 +69,7 @@ def _sampled_sequence(echo, number, bits_, sample, calls=None, wire_calls=(0,), 
         rank_inputs(number, c, "cuda", out=x)
         comp = None
         if c.state != "none":
-            comp = states.setdefault(c.state, torch.zeros((P, n), device="cuda"))
+            comp = states.setdefault(c.state, torch.zeros((P, n), dtype=sdt, device="cuda"))
         echo.echo_allreduce(plan, list(x), list(out), comp)
         xs = bits(so.gather(x))
         check_wire = k in wire_calls or k == len(seq) - 1
@@ -76,7 +79,8 @@ def _sampled_sequence(echo, number, bits_, sample, calls=None, wire_calls=(0,), 
         for p in range(P):
             assert np.array_equal(got[p], ref["y_rows"]), f"call {k} rank {p}"
         if comp is not None:
-            assert_state_close(so.gather(comp).numpy(), so.state_rows(c.state), f"state call {k}")
+            assert_state_close(so.gather(comp).float().numpy(), so.state_rows(c.state),
+                               f"state call {k}")
         if check_wire:
             wire = sampled_wire(echo.echo_debug_wire(plan), lay, P, groups, bits_)
             for p in range(P):
@@ -111,3 +115,14 @@ def test_p4_2048x4096_ablation_quantizers_sampled(echo, quant):
     """The Table 8 ablation quantizers over the first 16 calls of the 64-call
     workload, at full size."""
     _sampled_sequence(echo, 2, 4, sample=512, calls=16, quant=quant)
+
+
+@pytest.mark.parametrize("state", [(True, 1.0), (False, 0.9), (True, 0.9)])
+def test_p4_2048x4096_state_options_sampled(echo, state):
+    """The compensator state in bf16 and/or decayed, over the first 16 calls of
+    the 64-call workload, at full size."""
+    _sampled_sequence(echo, 2, 4, sample=512, calls=16, bf16_state=state[0], decay=state[1])
+
+
+def test_p8_1gib_bf16_state_sampled(echo):
+    _sampled_sequence(echo, 3, 4, sample=2048, calls=4, bf16_state=True)
