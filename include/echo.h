@@ -245,9 +245,10 @@ int echo_set_quantizer(echo_plan_t plan, int mode);
 
 /*
  * echo_set_state -- choose how a plan's calls keep the compensator state (the
- * reduced-precision and decayed variants of the error feedback; the pages name
- * a "two-timescale" compensator of the paper's Sec. 3 but print neither its
- * equations nor a decay constant, so both options are readings):
+ * reduced-precision and decayed variants of the error feedback; the article's
+ * section "The cancellation rule" names a two-timescale compensator but no
+ * page prints its equations, its precision or a decay constant, so both
+ * options are readings):
  *   format  ECHO_STATE_F32 (default): each kept error is an fp32 value;
  *           ECHO_STATE_BF16: each kept error is rounded to bf16 (nearest
  *           even) when stored, halving the state's size and traffic.
