@@ -46,13 +46,13 @@ L2_BYTES = 126 * 2 ** 20
 
 # ------------------------------------------------------------- byte model ----
 
-def code_bytes_per_elem(bits: int) -> float:
-    """Codes plus the 4-byte meta word of each 128-element group."""
-    return bits / 8 + 4 / G
+def code_bytes_per_elem(bits: int, g: int = G) -> float:
+    """Codes plus the 4-byte meta word of each g-element group."""
+    return bits / 8 + 4 / g
 
 
 def kernel_bytes(P: int, n: int, bits: int, compensated: bool, fused: bool,
-                 state_bytes: int = 4) -> dict:
+                 state_bytes: int = 4, g: int = G) -> dict:
     """Algorithmic bytes each kernel must move per call (one call = P ranks x n).
 
     push:   reads the non-owned bf16 input, reads+writes its state, writes
@@ -64,7 +64,7 @@ def kernel_bytes(P: int, n: int, bits: int, compensated: bool, fused: bool,
     gather: reads gather codes + meta, writes P bf16 outputs:  n c + 2 P n
     e is the state's bytes per element (4 fp32, 2 bf16); the state terms drop
     out when uncompensated."""
-    c = code_bytes_per_elem(bits)
+    c = code_bytes_per_elem(bits, g)
     st = 2 * state_bytes if compensated else 0
     d = {"push": (P - 1) * n * (2 + st + c),
          "reduce": (P - 1) * n * c + n * (2 + st + c) + (2 * P * n if fused else 0)}
@@ -75,8 +75,8 @@ def kernel_bytes(P: int, n: int, bits: int, compensated: bool, fused: bool,
     return d
 
 
-def call_model_bytes(P, n, bits, compensated, fused, state_bytes=4):
-    return sum(kernel_bytes(P, n, bits, compensated, fused, state_bytes).values())
+def call_model_bytes(P, n, bits, compensated, fused, state_bytes=4, g=G):
+    return sum(kernel_bytes(P, n, bits, compensated, fused, state_bytes, g).values())
 
 
 # ---------------------------------------------------------------- helpers ----
@@ -242,7 +242,8 @@ def run_ours(args, rank, local, world):
     calls = len(seq)
     xs = build_inputs(number, seq, calls, dev)
     out = torch.empty((P, n), dtype=torch.bfloat16, device=dev)
-    plan = echo.echo_plan(P, n, G, bits)
+    g = args.g
+    plan = echo.echo_plan(P, n, g, bits)
     echo.echo_set_fused(plan, fused)
     echo.echo_set_quantizer(plan, args.quantizer)
     sb = set_state(echo, plan, args)
@@ -285,8 +286,8 @@ def run_ours(args, rank, local, world):
     value = whole_job_gbs(bytes_in_per_call * calls, args.steps, world, max_ms)
     per_call_s = max_ms / 1e3 / (args.steps * calls)
     compensated_calls = sum(1 for c in seq if c.state != "none")
-    model = (compensated_calls * call_model_bytes(P, n, bits, True, fused, sb) +
-             (calls - compensated_calls) * call_model_bytes(P, n, bits, False, fused)) / calls
+    model = (compensated_calls * call_model_bytes(P, n, bits, True, fused, sb, g) +
+             (calls - compensated_calls) * call_model_bytes(P, n, bits, False, fused, g=g)) / calls
     hbm, hbm_src = load_peaks()
 
     # Per-kernel durations: the same K steps again, with events around each
@@ -309,8 +310,8 @@ def run_ours(args, rank, local, world):
         per_kernel_ms["reduce"] += evs[1].elapsed_time(evs[2])
         per_kernel_ms["gather"] += evs[2].elapsed_time(evs[3])
     nlaunch = len(ev_sets)
-    kb_comp = kernel_bytes(P, n, bits, True, fused, sb)
-    kb_unc = kernel_bytes(P, n, bits, False, fused)
+    kb_comp = kernel_bytes(P, n, bits, True, fused, sb, g)
+    kb_unc = kernel_bytes(P, n, bits, False, fused, g=g)
     ran = [k for k in ("push", "reduce", "gather") if k in kb_comp and (k != "push" or P > 1)]
     avg_us = {k: per_kernel_ms[k] / nlaunch * 1e3 for k in ran}
     dominant = max(avg_us, key=lambda k: avg_us[k])
@@ -328,7 +329,7 @@ def run_ours(args, rank, local, world):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(max_ms / args.steps, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded; shapes and distributions of the workload, no dataset)",
-        "config": {"workload": w.name, "P": P, "n_per_rank": n, "bits": bits, "g": G,
+        "config": {"workload": w.name, "P": P, "n_per_rank": n, "bits": bits, "g": g,
                    "calls_per_step": calls, "compensated": compensated_calls == calls,
                    "fused_gather": bool(fused), "quantizer": QUANTIZERS[args.quantizer],
                    "state": {"format": "bf16" if sb == 2 else "fp32", "decay": args.decay},
@@ -354,7 +355,7 @@ def run_ours(args, rank, local, world):
         for num in [int(v) for v in args.also.split(",") if v]:
             result["also"][WORKLOADS[num].name] = time_other(echo, num, bits, fused, dev, args)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        result["cpu_baseline"] = cpu_baseline_oracle(number, bits, budget_s=args.cpu_budget)
+        result["cpu_baseline"] = cpu_baseline_oracle(args, budget_s=args.cpu_budget)
     del plan
     return result
 
@@ -427,7 +428,7 @@ def time_other(echo, number, bits, fused, dev, args, reps=3):
     distinct = min(8, len(seq))
     xs = build_inputs(number, seq, distinct, dev)
     out = torch.empty((w.P, w.n), dtype=torch.bfloat16, device=dev)
-    plan = echo.echo_plan(w.P, w.n, G, bits)
+    plan = echo.echo_plan(w.P, w.n, args.g, bits)
     echo.echo_set_fused(plan, fused)
     echo.echo_set_quantizer(plan, args.quantizer)
     sb = set_state(echo, plan, args)
@@ -452,8 +453,8 @@ def time_other(echo, number, bits, fused, dev, args, reps=3):
     per_call_s = a.elapsed_time(b) / 1e3 / (reps * len(seq))
     hbm, _ = load_peaks()
     comp_calls = sum(1 for c in seq if c.state != "none")
-    model = (comp_calls * call_model_bytes(w.P, w.n, bits, True, fused, sb) +
-             (len(seq) - comp_calls) * call_model_bytes(w.P, w.n, bits, False, fused)) / len(seq)
+    model = (comp_calls * call_model_bytes(w.P, w.n, bits, True, fused, sb, args.g) +
+             (len(seq) - comp_calls) * call_model_bytes(w.P, w.n, bits, False, fused, g=args.g)) / len(seq)
     del plan, xs
     torch.cuda.empty_cache()
     return {"gbs": round(w.P * w.n * 2 / per_call_s / 1e9, 2), "us_per_call": round(per_call_s * 1e6, 2),
@@ -469,24 +470,25 @@ class OracleSample:
     positions -- exactly the oracle's work on them, since positions are
     independent -- with 4 distinct inputs cycled and the state carried."""
 
-    def __init__(self, number, bits):
+    def __init__(self, number, bits, g=G, mode=0, bf16_state=False, decay=1.0):
         import numpy as np
         import torch
         from bit_error_compensated_gb300.workloads import WORKLOADS, call_sequence, rank_inputs
         w = WORKLOADS[number]
         self.w, self.bits, self.P = w, bits, w.P
+        self.opts = dict(mode=mode, bf16_state=bf16_state, decay=decay)
         seq = call_sequence(number, steps=1)
-        Gs = w.n // w.P // G
+        Gs = w.n // w.P // g
         rng = np.random.default_rng(number)
         pos = np.sort(rng.choice(w.P * Gs, size=max(1, w.P * Gs // 8), replace=False))
         self.owners = (pos // Gs).astype(np.int32)
-        idx = (pos[:, None] * G + np.arange(G)[None, :]).ravel()
-        self.e = np.zeros((pos.size, w.P, G), np.float32)
+        idx = (pos[:, None] * g + np.arange(g)[None, :]).ravel()
+        self.e = np.zeros((pos.size, w.P, g), np.float32)
         self.inputs = []
         for k in range(min(len(seq), 4)):
             x = rank_inputs(number, seq[k], "cpu").view(torch.int16).numpy().view(np.uint16)
-            self.inputs.append(np.ascontiguousarray(x[:, idx].reshape(w.P, pos.size, G).transpose(1, 0, 2)))
-        self.bytes_per_step = pos.size * w.P * G * 2
+            self.inputs.append(np.ascontiguousarray(x[:, idx].reshape(w.P, pos.size, g).transpose(1, 0, 2)))
+        self.bytes_per_step = pos.size * w.P * g * 2
         self.sample = (f"each step: one call of {w.name} on a fixed 1/8 sample of its group "
                        f"positions ({pos.size} of {w.P * Gs}), 4 distinct inputs cycled, state carried; "
                        f"single-threaded")
@@ -494,14 +496,21 @@ class OracleSample:
 
     def step(self):
         import oracle
-        oracle.group_positions(self.P, self.owners, self.bits, self.inputs[self.i % len(self.inputs)], self.e)
+        oracle.group_positions(self.P, self.owners, self.bits, self.inputs[self.i % len(self.inputs)], self.e,
+                               **self.opts)
         self.i += 1
 
 
-def cpu_baseline_oracle(number, bits, budget_s=12.0):
+def oracle_sample(args):
+    """OracleSample of the workload and options the GPU arm runs."""
+    return OracleSample(args.workload, args.bits, args.g, args.quantizer, args.state == "bf16",
+                        args.decay)
+
+
+def cpu_baseline_oracle(args, budget_s=12.0):
     """The oracle as it stands, single-threaded on one host core, for about
     `budget_s` seconds of steps of OracleSample."""
-    s = OracleSample(number, bits)
+    s = oracle_sample(args)
     s.step()
     steps, t = 0, time.perf_counter()
     while time.perf_counter() - t < budget_s:
@@ -515,7 +524,7 @@ def cpu_baseline_oracle(number, bits, budget_s=12.0):
 def run_reference(args, rank, world):
     """`--impl reference`: the oracle on the host cores, K timed steps of
     OracleSample after W warm-up steps."""
-    s = OracleSample(args.workload, args.bits)
+    s = oracle_sample(args)
     for _ in range(args.warmup):
         s.step()
     t = time.perf_counter()
@@ -529,8 +538,10 @@ def run_reference(args, rank, world):
             "ms_per_step": round(sec / args.steps * 1e3, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic (seeded; shapes and distributions of the workload, no dataset)",
-            "config": {"workload": w.name, "P": w.P, "n_per_rank": w.n, "bits": args.bits, "g": G,
-                       "compensated": True},
+            "config": {"workload": w.name, "P": w.P, "n_per_rank": w.n, "bits": args.bits, "g": args.g,
+                       "compensated": True, "quantizer": QUANTIZERS[args.quantizer],
+                       "state": {"format": "bf16" if args.state == "bf16" else "fp32",
+                                 "decay": args.decay}},
             "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
                              "sample": s.sample},
             "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
@@ -566,7 +577,7 @@ def run_accuracy(args):
     variants = [(qz, comp, False, 1.0) for qz in (0, 1, 2) for comp in (True, False)]
     variants += [(0, True, True, 1.0), (0, True, False, 0.9), (0, True, True, 0.9)]
     for qz, compensated, bf16_state, decay in variants:
-        plan = echo.echo_plan(P, n, G, bits)
+        plan = echo.echo_plan(P, n, args.g, bits)
         echo.echo_set_quantizer(plan, qz)
         echo.echo_set_state(plan, echo.ECHO_STATE_BF16 if bf16_state else echo.ECHO_STATE_F32,
                             decay)
@@ -608,6 +619,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", type=int, default=2, help="1..5 (default 2: P=4, 2048x4096, 64 calls)")
     ap.add_argument("--bits", type=int, default=4, choices=[4, 8])
+    ap.add_argument("--g", type=int, default=G, choices=[64, 128, 256], help="elements per group")
     ap.add_argument("--fused", action="store_true", help="reduce kernel writes the outputs itself")
     ap.add_argument("--quantizer", type=int, default=0, choices=[0, 1, 2],
                     help="0 zero-aware (the method), 1 naive zero-point, 2 symmetric grid")

@@ -19,7 +19,11 @@ ROOT = PKG.parent
 CSRC = PKG / "csrc"
 LIBDIR = PKG / "lib"
 LIB = LIBDIR / "libecho.so"
-SOURCES = ["echo_api.cu", "k_push.cu", "k_reduce.cu", "k_gather.cu", "echo_noalloc.cu"]
+# (source, group size it is compiled for, or None).  Every kernel source is
+# compiled once per supported group size; the objects compile in parallel.
+GROUPS = (64, 128, 256)
+SOURCES = [("echo_api.cu", None), ("echo_noalloc.cu", None)] + [
+    (src, g) for src in ("k_push.cu", "k_reduce.cu", "k_gather.cu") for g in GROUPS]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -44,7 +48,7 @@ def _stale() -> bool:
     if not LIB.exists():
         return True
     t = LIB.stat().st_mtime
-    deps = [CSRC / s for s in SOURCES] + list(CSRC.glob("*.h")) + list(CSRC.glob("*.cuh"))
+    deps = [CSRC / s for s, _ in SOURCES] + list(CSRC.glob("*.h")) + list(CSRC.glob("*.cuh"))
     deps.append(ROOT / "include" / "echo.h")
     return any(d.stat().st_mtime > t for d in deps)
 
@@ -57,10 +61,12 @@ def build_library(force: bool = False, ptxas_verbose: bool = False) -> Path:
     objdir.mkdir(parents=True, exist_ok=True)
     LIBDIR.mkdir(exist_ok=True)
     procs = []
-    for src in SOURCES:
-        obj = objdir / (Path(src).stem + ".o")
-        cmd = [cc, *_flags(ptxas_verbose), "-c", str(CSRC / src), "-o", str(obj)]
-        procs.append((src, obj, subprocess.Popen(cmd, stdout=subprocess.PIPE,
+    for src, g in SOURCES:
+        stem = Path(src).stem + ("" if g is None else f"_g{g}")
+        obj = objdir / (stem + ".o")
+        defs = [] if g is None else [f"-DECHO_G={g}"]
+        cmd = [cc, *_flags(ptxas_verbose), *defs, "-c", str(CSRC / src), "-o", str(obj)]
+        procs.append((stem, obj, subprocess.Popen(cmd, stdout=subprocess.PIPE,
                                                  stderr=subprocess.STDOUT, text=True)))
     failed = []
     for src, obj, pr in procs:

@@ -64,6 +64,27 @@ bool g_kernels_prepared[64] = {false};
 
 namespace echo {
 int note_cuda_error(cudaError_t e) { return cuda_fail(e); }
+
+#define ECHO_BY_GROUP(g, call) ((g) == 64 ? call<64> : (g) == 256 ? call<256> : call<128>)
+
+cudaError_t launch_push(const CallArgs& a, int g, int bits, cudaStream_t s, bool pdl) {
+  return ECHO_BY_GROUP(g, launch_push_g)(a, bits, s, pdl);
+}
+cudaError_t launch_reduce(const CallArgs& a, int g, int bits, bool fused, cudaStream_t s, bool pdl) {
+  return ECHO_BY_GROUP(g, launch_reduce_g)(a, bits, fused, s, pdl);
+}
+cudaError_t launch_gather(const CallArgs& a, int g, int bits, cudaStream_t s, bool pdl) {
+  return ECHO_BY_GROUP(g, launch_gather_g)(a, bits, s, pdl);
+}
+#undef ECHO_BY_GROUP
+
+cudaError_t prepare_kernels() {
+  cudaError_t e = cudaSuccess, r;
+  if ((r = prepare_reduce_g<64>()) != cudaSuccess) e = r;
+  if ((r = prepare_reduce_g<128>()) != cudaSuccess) e = r;
+  if ((r = prepare_reduce_g<256>()) != cudaSuccess) e = r;
+  return e;
+}
 }  // namespace echo
 
 extern "C" {
@@ -73,7 +94,7 @@ int echo_plan(int P, int64_t n, int g, int bits, echo_plan_t* out) {
   *out = nullptr;
   if (P < 1 || P > ECHO_MAX_RANKS || g < 1) return ECHO_ERR_ARG;
   if (bits != 4 && bits != 8) return ECHO_ERR_UNSUPPORTED;
-  if (g != echo::kGroup) return ECHO_ERR_UNSUPPORTED;
+  if (!echo::group_supported(g)) return ECHO_ERR_UNSUPPORTED;
   if (n < 0 || n % ((int64_t)P * g) != 0) return ECHO_ERR_SHAPE;
   if (n > ((int64_t)1 << 40)) return ECHO_ERR_SHAPE;
 
@@ -184,11 +205,11 @@ int echo_allreduce(echo_plan_t plan, const void* const* in, void* const* out,
   // launch an ordinary stream-ordered one.
   const bool pdl = plan->timing == 0;
   if (plan->timing) ECHO_CUDA(cudaEventRecord(plan->ev[0], s));
-  if (P > 1) ECHO_CUDA(echo::launch_push(a, plan->bits, s, pdl));
+  if (P > 1) ECHO_CUDA(echo::launch_push(a, plan->g, plan->bits, s, pdl));
   if (plan->timing) ECHO_CUDA(cudaEventRecord(plan->ev[1], s));
-  ECHO_CUDA(echo::launch_reduce(a, plan->bits, plan->fused != 0, s, pdl));
+  ECHO_CUDA(echo::launch_reduce(a, plan->g, plan->bits, plan->fused != 0, s, pdl));
   if (plan->timing) ECHO_CUDA(cudaEventRecord(plan->ev[2], s));
-  if (!plan->fused) ECHO_CUDA(echo::launch_gather(a, plan->bits, s, pdl));
+  if (!plan->fused) ECHO_CUDA(echo::launch_gather(a, plan->g, plan->bits, s, pdl));
   if (plan->timing) ECHO_CUDA(cudaEventRecord(plan->ev[3], s));
   return ECHO_OK;
 }

@@ -10,15 +10,19 @@
 
 namespace echo {
 
-// Elements per quantization group on the GPU.
+// Elements per quantization group the GPU supports: 64, 128 (the method's
+// default) and 256.  Each kernel source is compiled once per group size, with
+// ECHO_G set to it.
 constexpr int kGroup = 128;
-// Groups per reduce tile (one thread block of the reduce kernel); a multiple
-// of 4 so that every tile's meta words form a 16-byte-aligned bulk copy.
+constexpr bool group_supported(int g) { return g == 64 || g == 128 || g == 256; }
+// Elements per reduce tile (one thread block of the reduce kernel works on one
+// tile at a time): kReduceTileElems / g groups, a multiple of 4 for every
+// supported g, so that every tile's meta words form a 16-byte-aligned copy.
 #ifndef ECHO_REDUCE_TILE
-#define ECHO_REDUCE_TILE 32
+#define ECHO_REDUCE_TILE 32   // in groups of 128
 #endif
-constexpr int kReduceTile = ECHO_REDUCE_TILE;
-static_assert(kReduceTile % 4 == 0 && kReduceTile >= 4, "reduce tile: multiple of 4 groups");
+constexpr int kReduceTileElems = ECHO_REDUCE_TILE * 128;
+static_assert(kReduceTileElems % (4 * 256) == 0, "reduce tile: a multiple of 4 groups of 256");
 // Threads per block of every kernel.
 constexpr int kThreads = 256;
 
@@ -37,7 +41,7 @@ struct CallArgs {
   uint32_t* meta2;     // gather meta  [P owners][Gs_pad]
   int* status;         // device status word
   int64_t n;           // elements per rank
-  int64_t Gs;          // groups per owner segment (m / 128)
+  int64_t Gs;          // groups per owner segment (m / g)
   int64_t Gs_pad;      // Gs rounded up to a multiple of 4
   int P;
   int mode;            // quantizer: 0 zero-aware (the method), 1 naive zero point, 2 symmetric
@@ -45,11 +49,22 @@ struct CallArgs {
   float decay;         // the kept error is decay * (revealed error); 1 = plain feedback
 };
 
-// Launchers (one translation unit each).  They return the launch error.
-cudaError_t launch_push(const CallArgs& a, int bits, cudaStream_t s, bool pdl);
-cudaError_t launch_reduce(const CallArgs& a, int bits, bool fused, cudaStream_t s, bool pdl);
-cudaError_t launch_gather(const CallArgs& a, int bits, cudaStream_t s, bool pdl);
-// One-time per-device set-up of kernel attributes (dynamic shared memory).
+// Launchers for group size G, defined in the translation unit compiled with
+// ECHO_G = G.  They return the launch error.
+template <int G> cudaError_t launch_push_g(const CallArgs& a, int bits, cudaStream_t s, bool pdl);
+template <int G>
+cudaError_t launch_reduce_g(const CallArgs& a, int bits, bool fused, cudaStream_t s, bool pdl);
+template <int G> cudaError_t launch_gather_g(const CallArgs& a, int bits, cudaStream_t s, bool pdl);
+// One-time per-device set-up of the reduce kernels' attributes (dynamic
+// shared memory) for group size G.
+template <int G> cudaError_t prepare_reduce_g();
+
+// Dispatch on the group size g (defined in echo_api.cu, which sees only the
+// declarations above, so each kernel source instantiates its own g alone).
+cudaError_t launch_push(const CallArgs& a, int g, int bits, cudaStream_t s, bool pdl);
+cudaError_t launch_reduce(const CallArgs& a, int g, int bits, bool fused, cudaStream_t s, bool pdl);
+cudaError_t launch_gather(const CallArgs& a, int g, int bits, cudaStream_t s, bool pdl);
+// Attributes of every reduce kernel, all group sizes.
 cudaError_t prepare_kernels();
 // Records `e` as the error echo_strerror(ECHO_ERR_CUDA) reports in this thread
 // and returns ECHO_ERR_CUDA.

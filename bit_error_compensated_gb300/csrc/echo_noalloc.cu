@@ -122,9 +122,9 @@ extern "C" int echo_allreduce_noalloc(int P, int64_t n, int bits, const void* co
   // array that must start at zero.  The receive slots are fully rewritten by
   // every call before they are read.
   cudaError_t e = cudaMemsetAsync(a.status, 0, sizeof(int), s);
-  if (e == cudaSuccess && P > 1) e = echo::launch_push(a, bits, s, true);
-  if (e == cudaSuccess) e = echo::launch_reduce(a, bits, false, s, true);
-  if (e == cudaSuccess) e = echo::launch_gather(a, bits, s, true);
+  if (e == cudaSuccess && P > 1) e = echo::launch_push(a, echo::kGroup, bits, s, true);
+  if (e == cudaSuccess) e = echo::launch_reduce(a, echo::kGroup, bits, false, s, true);
+  if (e == cudaSuccess) e = echo::launch_gather(a, echo::kGroup, bits, s, true);
   if (e != cudaSuccess) return echo::note_cuda_error(e);
   return ECHO_OK;
 }

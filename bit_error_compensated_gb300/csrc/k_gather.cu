@@ -5,25 +5,27 @@
 // all-gather is one read of each segment's codes and P writes of the decoded
 // bf16 values.
 //
-// Half a warp per group, 8 consecutive elements per lane: a warp reads the
-// codes and meta words of two adjacent groups and writes, per rank, one
-// 16-byte streaming store per lane (2 x 256 B per warp).  U group pairs per warp are read before any is
-// written, to keep several code reads in flight.  Write-bound: P * 2 bytes out
-// per element.
+// g/8 lanes per group of g elements, 8 consecutive elements per lane: a warp
+// reads the codes and meta words of 256/g adjacent groups (256 elements) and
+// writes, per rank, one 16-byte streaming store per lane (512 B per warp).
+// U such runs per warp are read before any is written, to keep several code
+// reads in flight.  Write-bound: P * 2 bytes out per element.
 #include "echo_internal.h"
 #include "quant.cuh"
 
 namespace echo {
 namespace {
 
-template <int BITS, int U, int MODE>
+template <int BITS, int U, int MODE, int G>
 __global__ void __launch_bounds__(kThreads)
 gather_kernel(const CallArgs a) {
-  constexpr int CB = 16 * BITS;
+  constexpr int CB = G * BITS / 8;
+  constexpr int LG = G / 8;         // lanes per group
+  constexpr int GW = 32 / LG;       // groups per warp run
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int lane = threadIdx.x & 31;
-  const int half = lane >> 4;
-  const int h = lane & 15;          // lane h of a half decodes elements [8h, 8h+8)
+  const int sub = lane / LG;
+  const int h = lane % LG;          // lane h of a group decodes elements [8h, 8h+8)
   const int64_t wg = (int64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
   const int64_t nw = (int64_t)gridDim.x * (kThreads / 32);
   const int P = a.P;
@@ -32,14 +34,14 @@ gather_kernel(const CallArgs a) {
   const uint8_t* cs = a.codes2 + (int64_t)o * Gs * CB;
   const uint32_t* ms = a.meta2 + (int64_t)o * a.Gs_pad;
 
-  // Two adjacent groups per warp (half a warp each), U pairs in flight.
-  for (int64_t pair0 = wg; 2 * pair0 < Gs; pair0 += nw * U) {
+  // GW adjacent groups per warp run, U runs in flight.
+  for (int64_t run0 = wg; GW * run0 < Gs; run0 += nw * U) {
     uint2 word[U];
     uint32_t meta[U];
     int64_t w[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      w[u] = 2 * (pair0 + (int64_t)u * nw) + half;
+      w[u] = GW * (run0 + (int64_t)u * nw) + sub;
       if (w[u] < Gs) {
         meta[u] = ms[w[u]];
         const uint8_t* cg = cs + w[u] * CB;
@@ -67,7 +69,7 @@ gather_kernel(const CallArgs a) {
       const uint2 ya = f32x4_to_bf16(deq, yb);
       const uint2 yv = f32x4_to_bf16(deq + 4, yb + 4);
       const uint4 y = make_uint4(ya.x, ya.y, yv.x, yv.y);
-      const int64_t e0 = ((int64_t)o * Gs + w[u]) * kGroup + 8 * h;
+      const int64_t e0 = ((int64_t)o * Gs + w[u]) * G + 8 * h;
       for (int r = 0; r < P; ++r) __stcs(reinterpret_cast<uint4*>(a.out[r] + e0), y);
     }
   }
@@ -77,9 +79,9 @@ gather_kernel(const CallArgs a) {
 #ifndef ECHO_GATHER_UNROLL
 #define ECHO_GATHER_UNROLL 4
 #endif
-constexpr int kGatherUnroll = ECHO_GATHER_UNROLL;  // group pairs in flight per warp
+constexpr int kGatherUnroll = ECHO_GATHER_UNROLL;  // warp runs in flight per warp
 
-template <int BITS, int MODE>
+template <int BITS, int MODE, int G>
 cudaError_t launch_t(const CallArgs& a, cudaStream_t s, bool pdl) {
   static int grid_cache[64] = {0};
   int dev = 0;
@@ -88,13 +90,13 @@ cudaError_t launch_t(const CallArgs& a, cudaStream_t s, bool pdl) {
   if (grid == 0) {
     int sms = 0, per_sm = 0;
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gather_kernel<BITS, kGatherUnroll, MODE>,
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gather_kernel<BITS, kGatherUnroll, MODE, G>,
                                                   kThreads, 0);
     grid = sms * (per_sm > 0 ? per_sm : 1);
   }
   // Blocks per owner segment: enough to fill the GPU once across the P
-  // segments, but no more than the segment has group pairs for.
-  const int64_t per_block = (int64_t)(kThreads / 32) * kGatherUnroll * 2;
+  // segments, but no more than the segment has warp runs for.
+  const int64_t per_block = (int64_t)(kThreads / 32) * kGatherUnroll * (256 / G);
   const int64_t need = (a.Gs + per_block - 1) / per_block;
   int64_t bx = (grid + a.P - 1) / a.P;
   if (bx > need) bx = need;
@@ -109,17 +111,27 @@ cudaError_t launch_t(const CallArgs& a, cudaStream_t s, bool pdl) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, gather_kernel<BITS, kGatherUnroll, MODE>, a);
+  return cudaLaunchKernelEx(&cfg, gather_kernel<BITS, kGatherUnroll, MODE, G>, a);
+}
+
+template <int MODE, int G>
+cudaError_t launch_mode(const CallArgs& a, int bits, cudaStream_t s, bool pdl) {
+  return bits == 4 ? launch_t<4, MODE, G>(a, s, pdl) : launch_t<8, MODE, G>(a, s, pdl);
 }
 
 }  // namespace
 
-cudaError_t launch_gather(const CallArgs& a, int bits, cudaStream_t s, bool pdl) {
-  if (a.mode == kNaiveZeroPoint)
-    return bits == 4 ? launch_t<4, kNaiveZeroPoint>(a, s, pdl) : launch_t<8, kNaiveZeroPoint>(a, s, pdl);
-  if (a.mode == kSymmetric)
-    return bits == 4 ? launch_t<4, kSymmetric>(a, s, pdl) : launch_t<8, kSymmetric>(a, s, pdl);
-  return bits == 4 ? launch_t<4, kZeroAware>(a, s, pdl) : launch_t<8, kZeroAware>(a, s, pdl);
+template <int G>
+cudaError_t launch_gather_g(const CallArgs& a, int bits, cudaStream_t s, bool pdl) {
+  if (a.mode == kNaiveZeroPoint) return launch_mode<kNaiveZeroPoint, G>(a, bits, s, pdl);
+  if (a.mode == kSymmetric) return launch_mode<kSymmetric, G>(a, bits, s, pdl);
+  return launch_mode<kZeroAware, G>(a, bits, s, pdl);
 }
+
+#ifndef ECHO_G
+#define ECHO_G 128
+#endif
+static_assert(group_supported(ECHO_G), "ECHO_G: 64, 128 or 256");
+template cudaError_t launch_gather_g<ECHO_G>(const CallArgs&, int, cudaStream_t, bool);
 
 }  // namespace echo

@@ -9,21 +9,21 @@
 // v - deq(q), replaces it (the update changes nothing this call computes).
 //
 // Grid: blockIdx.y is a (sender p, owner o) segment pair, blockIdx.x strides
-// over the segment's groups, so no division is needed per group.  A quarter
-// warp per 128-element group (quant.cuh); a warp works on four adjacent
-// groups at a time (a "quad": 1 KB of bf16 input and 2 KB of fp32 state,
-// contiguous).
+// over the segment's groups, so no division is needed per group.  g/16 lanes
+// per group of g elements (quant.cuh); a warp works on 512 adjacent elements
+// at a time (a "unit": 512/g groups, 1 KB of bf16 input and 2 KB of fp32 or
+// 1 KB of bf16 state, contiguous).
 //
 // Each warp runs its own kPushStages-deep pipeline: lane 0 issues 1-D bulk
-// copies (cp.async.bulk, the TMA engine) of the next quads' input and state
+// copies (cp.async.bulk, the TMA engine) of the next units' input and state
 // into the warp's shared-memory stages, each stage completing on its own
-// mbarrier, while the warp quantizes the current quad from shared memory and
+// mbarrier, while the warp quantizes the current unit from shared memory and
 // stores codes, meta and the new state straight to global memory.  Loads stay
 // in flight during compute without holding registers.  The waits are bounded
 // and their outcome is the same for the whole warp: on timeout the warp
 // records ECHO_ERR_TIMEOUT, waits once more (bounded) for each copy it still
-// has in flight, and returns.  HBM-bound: per group 256 B + 512 B read,
-// 512 B + codes + 4 B of meta written.
+// has in flight, and returns.  HBM-bound: per element 2 B of input and the
+// state read, the state and b/8 B of codes written, plus 4 B of meta a group.
 #include "echo_internal.h"
 #include "quant.cuh"
 #include "tma.cuh"
@@ -34,22 +34,25 @@ namespace {
 #ifndef ECHO_PUSH_STAGES
 #define ECHO_PUSH_STAGES 2
 #endif
-constexpr int kPushStages = ECHO_PUSH_STAGES;      // quads in flight per warp
-constexpr int kQuadX = 4 * kGroup * 2;      // bf16 bytes of a quad
+constexpr int kPushStages = ECHO_PUSH_STAGES;      // units in flight per warp
+constexpr int kUnit = 512;                         // elements of a unit (32 lanes x 16)
+constexpr int kUnitX = kUnit * 2;                  // bf16 bytes of a unit
 
 template <int SF>
-constexpr int push_stage_bytes() { return kQuadX + 4 * kGroup * state_bytes<SF>(); }
+constexpr int push_stage_bytes() { return kUnitX + kUnit * state_bytes<SF>(); }
 
 template <int SF>
 constexpr size_t push_smem_bytes() {
   return (size_t)(kThreads / 32) * kPushStages * push_stage_bytes<SF>();
 }
 
-template <int BITS, int SF, int MODE>
+template <int BITS, int SF, int MODE, int G>
 __global__ void __launch_bounds__(kThreads)
 push_kernel(const CallArgs a) {
   constexpr float L = (float)((1 << BITS) - 1);
-  constexpr int CB = 16 * BITS;                     // code bytes per group
+  constexpr int NL = G / 16;                        // lanes per group
+  constexpr int GPW = 32 / NL;                      // groups per unit
+  constexpr int CB = G * BITS / 8;                  // code bytes per group
   constexpr int S = kPushStages;
   constexpr int SB = push_stage_bytes<SF>();
   constexpr bool COMP = SF != kNoState;
@@ -63,19 +66,19 @@ push_kernel(const CallArgs a) {
   const int o = oi + (oi >= p ? 1 : 0);             // owner of the segment
   const int slot = o * (P - 1) + (p < o ? p : p - 1);
   const int64_t Gs = a.Gs;
-  const __nv_bfloat16* xs = a.in[p] + (int64_t)o * Gs * kGroup;
+  const __nv_bfloat16* xs = a.in[p] + (int64_t)o * Gs * G;
   uint8_t* es = COMP ? reinterpret_cast<uint8_t*>(a.comp) +
-                           ((int64_t)p * a.n + (int64_t)o * Gs * kGroup) * EB : nullptr;
+                           ((int64_t)p * a.n + (int64_t)o * Gs * G) * EB : nullptr;
   uint8_t* cs = a.codes1 + (int64_t)slot * Gs * CB;
   uint32_t* ms = a.meta1 + (int64_t)slot * a.Gs_pad;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int quarter = lane >> 3;                    // group within the quad
-  const int q = lane & 7;
+  const int sub = lane / NL;                        // group within the unit
+  const int q = lane % NL;                          // lane within the group
   const int64_t wg = (int64_t)blockIdx.x * (kThreads / 32) + warp;
   const int64_t nw = (int64_t)gridDim.x * (kThreads / 32);
-  const int64_t nquads = (Gs + 3) / 4;
+  const int64_t nunits = (Gs + GPW - 1) / GPW;
   uint8_t* wbuf = smem + (size_t)warp * S * SB;
   const uint32_t bar0 = smem_addr(&bars[warp][0]);
 
@@ -92,21 +95,21 @@ push_kernel(const CallArgs a) {
   const uint64_t codes_pol = kCodesPolicyLast ? policy_evict_last() : policy_evict_normal();
   // Lane 0: start the copies of iteration i into stage st.
   auto issue = [&](int64_t i, int st) {
-    const int64_t qd = wg + i * nw;
-    if (qd >= nquads) return;
-    const int64_t g0 = 4 * qd;
-    const uint32_t ng = (uint32_t)((Gs - g0) < 4 ? (Gs - g0) : 4);
+    const int64_t ud = wg + i * nw;
+    if (ud >= nunits) return;
+    const int64_t g0 = GPW * ud;
+    const uint32_t ng = (uint32_t)((Gs - g0) < GPW ? (Gs - g0) : GPW);
     const uint32_t bar = bar0 + 8 * st;
-    mbar_expect_tx(bar, ng * (256u + 128u * EB));
-    bulk_g2s(smem_addr(wbuf + st * SB), xs + g0 * kGroup, ng * 256u, bar, pol);
-    if (COMP) bulk_g2s(smem_addr(wbuf + st * SB + kQuadX), es + g0 * kGroup * EB, ng * 128u * EB, bar, pol);
+    mbar_expect_tx(bar, ng * G * (2u + EB));
+    bulk_g2s(smem_addr(wbuf + st * SB), xs + g0 * G, ng * G * 2u, bar, pol);
+    if (COMP) bulk_g2s(smem_addr(wbuf + st * SB + kUnitX), es + g0 * G * EB, ng * G * EB, bar, pol);
   };
   if (lane == 0) {
 #pragma unroll
     for (int st = 0; st < S; ++st) issue(st, st);
   }
 
-  for (int64_t i = 0; wg + i * nw < nquads; ++i) {
+  for (int64_t i = 0; wg + i * nw < nunits; ++i) {
     const int st = (int)(i % S);
     const uint32_t parity = (uint32_t)((i / S) & 1);
     if (!mbar_wait_warp(bar0 + 8 * st, parity)) {        // same outcome for every lane
@@ -114,32 +117,32 @@ push_kernel(const CallArgs a) {
         atomicOr(a.status, kStatusTimeout);
         for (int k = 0; k < S; ++k) {             // copies still in flight
           const int64_t ii = i + k;
-          if (wg + ii * nw < nquads)
+          if (wg + ii * nw < nunits)
             mbar_wait_bounded(bar0 + 8 * (int)(ii % S), (uint32_t)((ii / S) & 1));
         }
       }
       return;
     }
-    const int64_t j = 4 * (wg + i * nw) + quarter;   // this quarter's group
+    const int64_t j = GPW * (wg + i * nw) + sub;     // this lane's group
     const bool valid = j < Gs;
     float v[16];
     if (valid) {
-      const uint2* sx = reinterpret_cast<const uint2*>(wbuf + st * SB) + quarter * 32;
+      const uint2* sx = reinterpret_cast<const uint2*>(wbuf + st * SB) + sub * (G / 4);
 #pragma unroll
-      for (int c = 0; c < 4; ++c) bf16x4_to_f32(sx[8 * c + q], v + 4 * c);
+      for (int c = 0; c < 4; ++c) bf16x4_to_f32(sx[chunk_at<NL>(c, q) / 4], v + 4 * c);
       if constexpr (COMP) {
-        const uint8_t* se = wbuf + st * SB + kQuadX;
+        const uint8_t* se = wbuf + st * SB + kUnitX;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           float e[4];
-          state_load4<SF>(se, quarter * kGroup + chunk_at(c, q), e);
+          state_load4<SF>(se, sub * G + chunk_at<NL>(c, q), e);
 #pragma unroll
           for (int k = 0; k < 4; ++k) v[4 * c + k] = __fadd_rn(v[4 * c + k], e[k]);
         }
       }
     } else {
 #pragma unroll
-      for (int k = 0; k < 16; ++k) v[k] = 0.0f;      // idle quarter of a short quad
+      for (int k = 0; k < 16; ++k) v[k] = 0.0f;      // idle lanes of a short unit
     }
     // The stage has been read into registers: hand it back to the copy engine.
     __syncwarp();
@@ -148,7 +151,7 @@ push_kernel(const CallArgs a) {
       issue(i + S, st);
     }
 
-    const GroupGrid gg = group_grid<MODE>(v, L);
+    const GroupGrid gg = group_grid<MODE, NL>(v, L);
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {                 // chunks 2hh and 2hh+1
       float c[8], d[8];
@@ -156,19 +159,19 @@ push_kernel(const CallArgs a) {
       if (valid) {
         uint8_t* cg = cs + j * CB;
         if (BITS == 4) {
-          st_hint_u16(cg + 32 * hh + 2 * q, pack4<4>(c), codes_pol);
-          st_hint_u16(cg + 32 * hh + 16 + 2 * q, pack4<4>(c + 4), codes_pol);
+          st_hint_u16(cg + chunk_code_byte<4, NL>(2 * hh, q), pack4<4>(c), codes_pol);
+          st_hint_u16(cg + chunk_code_byte<4, NL>(2 * hh + 1, q), pack4<4>(c + 4), codes_pol);
         } else {
-          st_hint_u32(cg + 64 * hh + 4 * q, pack4<8>(c), codes_pol);
-          st_hint_u32(cg + 64 * hh + 32 + 4 * q, pack4<8>(c + 4), codes_pol);
+          st_hint_u32(cg + chunk_code_byte<8, NL>(2 * hh, q), pack4<8>(c), codes_pol);
+          st_hint_u32(cg + chunk_code_byte<8, NL>(2 * hh + 1, q), pack4<8>(c + 4), codes_pol);
         }
         if constexpr (COMP) {
           const float* vv = v + 8 * hh;
           float r[8];
 #pragma unroll
           for (int k = 0; k < 8; ++k) r[k] = __fsub_rn(vv[k], d[k]);
-          state_store4<SF>(es, j * kGroup + chunk_at(2 * hh, q), r, a.decay);
-          state_store4<SF>(es, j * kGroup + chunk_at(2 * hh + 1, q), r + 4, a.decay);
+          state_store4<SF>(es, j * G + chunk_at<NL>(2 * hh, q), r, a.decay);
+          state_store4<SF>(es, j * G + chunk_at<NL>(2 * hh + 1, q), r + 4, a.decay);
         }
       }
     }
@@ -180,7 +183,7 @@ push_kernel(const CallArgs a) {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-template <int BITS, int SF, int MODE>
+template <int BITS, int SF, int MODE, int G>
 cudaError_t launch_t(const CallArgs& a, cudaStream_t s, bool pdl) {
   static int resident_cache[64] = {0};
   int dev = 0;
@@ -189,16 +192,16 @@ cudaError_t launch_t(const CallArgs& a, cudaStream_t s, bool pdl) {
   if (resident == 0) {
     int sms = 0, per_sm = 0;
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    cudaFuncSetAttribute(push_kernel<BITS, SF, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaFuncSetAttribute(push_kernel<BITS, SF, MODE, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          (int)push_smem_bytes<SF>());
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, push_kernel<BITS, SF, MODE>, kThreads,
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, push_kernel<BITS, SF, MODE, G>, kThreads,
                                                   push_smem_bytes<SF>());
     resident = sms * (per_sm > 0 ? per_sm : 1);
   }
   const int pairs = a.P * (a.P - 1);
   // Blocks per segment: enough to fill the GPU once across all segments, but
-  // no more than the segment has quads for (8 warps x 1 quad each).
-  const int64_t per_block = (int64_t)(kThreads / 32) * 4;
+  // no more than the segment has units for (8 warps x 1 unit each).
+  const int64_t per_block = (int64_t)(kThreads / 32) * (32 / (G / 16));
   const int64_t need = (a.Gs + per_block - 1) / per_block;
   int64_t bx = (resident + pairs - 1) / pairs;
   if (bx > need) bx = need;
@@ -214,28 +217,35 @@ cudaError_t launch_t(const CallArgs& a, cudaStream_t s, bool pdl) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, push_kernel<BITS, SF, MODE>, a);
+  return cudaLaunchKernelEx(&cfg, push_kernel<BITS, SF, MODE, G>, a);
 }
 
-template <int MODE>
+template <int MODE, int G>
 cudaError_t launch_mode(const CallArgs& a, int bits, cudaStream_t s, bool pdl) {
   const int sf = a.comp == nullptr ? kNoState : (a.state_bf16 ? kStateBF16 : kStateF32);
   if (bits == 4) {
-    if (sf == kStateF32) return launch_t<4, kStateF32, MODE>(a, s, pdl);
-    if (sf == kStateBF16) return launch_t<4, kStateBF16, MODE>(a, s, pdl);
-    return launch_t<4, kNoState, MODE>(a, s, pdl);
+    if (sf == kStateF32) return launch_t<4, kStateF32, MODE, G>(a, s, pdl);
+    if (sf == kStateBF16) return launch_t<4, kStateBF16, MODE, G>(a, s, pdl);
+    return launch_t<4, kNoState, MODE, G>(a, s, pdl);
   }
-  if (sf == kStateF32) return launch_t<8, kStateF32, MODE>(a, s, pdl);
-  if (sf == kStateBF16) return launch_t<8, kStateBF16, MODE>(a, s, pdl);
-  return launch_t<8, kNoState, MODE>(a, s, pdl);
+  if (sf == kStateF32) return launch_t<8, kStateF32, MODE, G>(a, s, pdl);
+  if (sf == kStateBF16) return launch_t<8, kStateBF16, MODE, G>(a, s, pdl);
+  return launch_t<8, kNoState, MODE, G>(a, s, pdl);
 }
 
 }  // namespace
 
-cudaError_t launch_push(const CallArgs& a, int bits, cudaStream_t s, bool pdl) {
-  if (a.mode == kNaiveZeroPoint) return launch_mode<kNaiveZeroPoint>(a, bits, s, pdl);
-  if (a.mode == kSymmetric) return launch_mode<kSymmetric>(a, bits, s, pdl);
-  return launch_mode<kZeroAware>(a, bits, s, pdl);
+template <int G>
+cudaError_t launch_push_g(const CallArgs& a, int bits, cudaStream_t s, bool pdl) {
+  if (a.mode == kNaiveZeroPoint) return launch_mode<kNaiveZeroPoint, G>(a, bits, s, pdl);
+  if (a.mode == kSymmetric) return launch_mode<kSymmetric, G>(a, bits, s, pdl);
+  return launch_mode<kZeroAware, G>(a, bits, s, pdl);
 }
+
+#ifndef ECHO_G
+#define ECHO_G 128
+#endif
+static_assert(group_supported(ECHO_G), "ECHO_G: 64, 128 or 256");
+template cudaError_t launch_push_g<ECHO_G>(const CallArgs&, int, cudaStream_t, bool);
 
 }  // namespace echo

@@ -10,10 +10,11 @@
 // decoded value s * (q - z).  Each step is one IEEE fp32 operation with
 // explicit round-to-nearest intrinsics, so no multiply-add is ever fused.
 //
-// Thread mapping: a quarter warp (8 lanes) per group of 128 values; lane q of
-// the quarter holds 16 values in four chunks of 4 consecutive elements,
-// chunk c being elements [32c + 4q, 32c + 4q + 4), so that every warp-wide
-// load or store of a chunk covers four contiguous runs, one per group.
+// Thread mapping: NL = g/16 lanes per group of g values (4 lanes for g = 64,
+// a quarter warp for 128, half a warp for 256); lane q of the group holds 16
+// values in four chunks of 4 consecutive elements, chunk c being elements
+// [4 NL c + 4q, 4 NL c + 4q + 4), so that every warp-wide load or store of a
+// chunk covers 32/NL contiguous runs, one per group.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -38,22 +39,32 @@ __device__ __forceinline__ float max_nan(float a, float b) {
   return r;
 }
 
-// Zero-aware range of a group over the 8 lanes of a quarter warp (all 32
-// lanes must call it; each quarter reduces its own group).
-__device__ __forceinline__ void quarter_range(const float v[16], float& lo, float& hi) {
+// Butterfly over the NL lanes of a group (aligned lane blocks of NL).
+template <int NL>
+__device__ __forceinline__ float group_min(float x) {
+#pragma unroll
+  for (int off = NL / 2; off > 0; off >>= 1) x = min_nan(x, __shfl_xor_sync(kFull, x, off));
+  return x;
+}
+template <int NL>
+__device__ __forceinline__ float group_max(float x) {
+#pragma unroll
+  for (int off = NL / 2; off > 0; off >>= 1) x = max_nan(x, __shfl_xor_sync(kFull, x, off));
+  return x;
+}
+
+// Zero-aware range of a group over its NL lanes (all 32 lanes must call it;
+// each block of NL lanes reduces its own group).
+template <int NL>
+__device__ __forceinline__ void group_range(const float v[16], float& lo, float& hi) {
   float a[4], b[4];
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
     a[k] = min_nan(min_nan(v[4 * k], v[4 * k + 1]), min_nan(v[4 * k + 2], v[4 * k + 3]));
     b[k] = max_nan(max_nan(v[4 * k], v[4 * k + 1]), max_nan(v[4 * k + 2], v[4 * k + 3]));
   }
-  lo = min_nan(min_nan(min_nan(a[0], a[1]), min_nan(a[2], a[3])), 0.0f);
-  hi = max_nan(max_nan(max_nan(b[0], b[1]), max_nan(b[2], b[3])), 0.0f);
-#pragma unroll
-  for (int off = 4; off > 0; off >>= 1) {
-    lo = min_nan(lo, __shfl_xor_sync(kFull, lo, off));
-    hi = max_nan(hi, __shfl_xor_sync(kFull, hi, off));
-  }
+  lo = group_min<NL>(min_nan(min_nan(min_nan(a[0], a[1]), min_nan(a[2], a[3])), 0.0f));
+  hi = group_max<NL>(max_nan(max_nan(max_nan(b[0], b[1]), max_nan(b[2], b[3])), 0.0f));
 }
 
 struct GroupGrid {
@@ -144,20 +155,19 @@ __device__ __forceinline__ void quantize8(const float v[8], const GroupGrid& gg,
 //                    2^(b-1); q = clamp(rint(v / s), +-(2^(b-1) - 1)) + 2^(b-1).
 enum QuantMode : int { kZeroAware = 0, kNaiveZeroPoint = 1, kSymmetric = 2 };
 
-// The grid of one group held by a quarter warp (16 values per lane); every
-// lane of the warp must call it.  For kNaiveZeroPoint, zf holds the offset m.
-template <int MODE>
+// The grid of one group held by NL lanes (16 values per lane); every lane of
+// the warp must call it.  For kNaiveZeroPoint, zf holds the offset m.
+template <int MODE, int NL>
 __device__ __forceinline__ GroupGrid group_grid(const float v[16], float L) {
   if constexpr (MODE == kZeroAware) {
     float lo, hi;
-    quarter_range(v, lo, hi);
+    group_range<NL>(v, lo, hi);
     return make_grid(lo, hi, L);
   } else if constexpr (MODE == kSymmetric) {
     float a = 0.0f;
 #pragma unroll
     for (int k = 0; k < 16; ++k) a = max_nan(a, fabsf(v[k]));
-#pragma unroll
-    for (int off = 4; off > 0; off >>= 1) a = max_nan(a, __shfl_xor_sync(kFull, a, off));
+    a = group_max<NL>(a);
     const float zf = __fadd_rn(__fmul_rn(L, 0.5f), 0.5f);   // 2^(b-1), exact
     __half sh = __float2half_ru(__fdiv_rn(a, __fsub_rn(zf, 1.0f)));
     float s = __half2float(sh);
@@ -179,11 +189,8 @@ __device__ __forceinline__ GroupGrid group_grid(const float v[16], float L) {
       lo = min_nan(lo, v[k]);
       hi = max_nan(hi, v[k]);
     }
-#pragma unroll
-    for (int off = 4; off > 0; off >>= 1) {
-      lo = min_nan(lo, __shfl_xor_sync(kFull, lo, off));
-      hi = max_nan(hi, __shfl_xor_sync(kFull, hi, off));
-    }
+    lo = group_min<NL>(lo);
+    hi = group_max<NL>(hi);
     const __half mh = __float2half_rd(lo);
     const float m = __half2float(mh);
     __half sh = __float2half_ru(__fdiv_rn(__fsub_rn(hi, m), L));
@@ -352,7 +359,14 @@ __device__ __forceinline__ void state_store4(uint8_t* base, int64_t i, const flo
   }
 }
 
-// Element offset, within a group, of chunk c (0..3) of quarter lane q (0..7).
-__device__ __forceinline__ int chunk_at(int c, int q) { return 32 * c + 4 * q; }
+// Element offset, within a group, of chunk c (0..3) of lane q (0..NL-1) of
+// the group's NL lanes.
+template <int NL>
+__device__ __forceinline__ int chunk_at(int c, int q) { return 4 * NL * c + 4 * q; }
+
+// Byte offset, within a group's packed codes, of chunk c of lane q: 4 codes
+// of BITS bits each, stored contiguously.
+template <int BITS, int NL>
+__device__ __forceinline__ int chunk_code_byte(int c, int q) { return chunk_at<NL>(c, q) * BITS / 8; }
 
 }  // namespace echo

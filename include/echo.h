@@ -59,7 +59,7 @@ extern "C" {
 #define ECHO_ERR_ARG         1  /* NULL pointer, P outside 1..ECHO_MAX_RANKS, g < 1,
                                    aliasing other than out[p] == in[p], wrong device */
 #define ECHO_ERR_SHAPE       2  /* n < 0, or n not a multiple of P*g */
-#define ECHO_ERR_UNSUPPORTED 3  /* bits not 4 or 8, or g other than 128 */
+#define ECHO_ERR_UNSUPPORTED 3  /* bits not 4 or 8, or g not 64, 128 or 256 */
 #define ECHO_ERR_ALIGN       4  /* a device pointer not 16-byte aligned */
 #define ECHO_ERR_CUDA        5  /* a CUDA runtime call failed */
 #define ECHO_ERR_OVERFLOW    6  /* (status word) a non-finite input or an fp16 step overflow */
@@ -80,7 +80,9 @@ typedef struct echo_plan_s* echo_plan_t;
  * (P*n fp32, zeroed; room enough for either format of echo_set_state).  Synchronizes the device once.
  *   P     1..ECHO_MAX_RANKS
  *   n     elements per rank, a multiple of P*g (n = 0 gives an empty plan)
- *   g     group size; 128 on the GPU
+ *   g     elements per group: 128 (the method's), or 64 or 256 (the group-size
+ *         rows of the paper's Table 8 ablation); wire codes take g*b/8 bytes
+ *         and one 4-byte meta word per group
  *   bits  4 or 8
  *   out   receives the plan handle; the caller frees it with echo_plan_destroy.
  * Segments are contiguous: rank o owns elements [o*m, (o+1)*m), m = n/P

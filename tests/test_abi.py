@@ -52,7 +52,8 @@ def test_host_argument_checks_without_gpu(lib):
     assert lib.echo_plan(17, 17 * 128, 128, 4, ctypes.byref(h)) == echo.ECHO_ERR_ARG
     assert lib.echo_plan(2, 256, 0, 4, ctypes.byref(h)) == echo.ECHO_ERR_ARG
     assert lib.echo_plan(2, 256, 128, 5, ctypes.byref(h)) == echo.ECHO_ERR_UNSUPPORTED
-    assert lib.echo_plan(2, 256, 64, 4, ctypes.byref(h)) == echo.ECHO_ERR_UNSUPPORTED
+    assert lib.echo_plan(2, 256, 32, 4, ctypes.byref(h)) == echo.ECHO_ERR_UNSUPPORTED
+    assert lib.echo_plan(2, 1024, 512, 4, ctypes.byref(h)) == echo.ECHO_ERR_UNSUPPORTED
     assert lib.echo_plan(2, 300, 128, 4, ctypes.byref(h)) == echo.ECHO_ERR_SHAPE
     assert lib.echo_plan(2, -256, 128, 4, ctypes.byref(h)) == echo.ECHO_ERR_SHAPE
     assert lib.echo_plan(2, 256, 128, 4, None) == echo.ECHO_ERR_ARG

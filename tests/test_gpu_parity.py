@@ -35,9 +35,9 @@ def _inputs(P, n, seed, scale=1.0):
 
 
 def _run_sequence(echo, P, Gs, bits_, mode, fused, calls=3, seed=0, inplace=False, quant=0,
-                  bf16_state=False, decay=1.0):
-    n = P * G * Gs
-    plan = echo.echo_plan(P, n, G, bits_)
+                  bf16_state=False, decay=1.0, g=G):
+    n = P * g * Gs
+    plan = echo.echo_plan(P, n, g, bits_)
     echo.echo_set_fused(plan, fused)
     echo.echo_set_quantizer(plan, quant)
     echo.echo_set_state(plan, echo.ECHO_STATE_BF16 if bf16_state else echo.ECHO_STATE_F32, decay)
@@ -54,7 +54,7 @@ def _run_sequence(echo, P, Gs, bits_, mode, fused, calls=3, seed=0, inplace=Fals
         echo.echo_allreduce(plan, list(x), list(out), comp_arg)
         torch.cuda.synchronize()
         assert echo.echo_get_status(plan) == 0
-        ref = oracle.allreduce(xb, G, bits_, e=e_ref, want_wire=True, mode=quant,
+        ref = oracle.allreduce(xb, g, bits_, e=e_ref, want_wire=True, mode=quant,
                                bf16_state=bf16_state, decay=decay)
         got = bits(out)
         assert np.array_equal(got, ref["out"]), f"outputs differ at call {k}"
@@ -124,6 +124,37 @@ def test_state_format_switch(echo):
         torch.cuda.synchronize()
         ref = oracle.allreduce(bits(x), G, 4, e=e, bf16_state=bf16_state, decay=decay)
         assert np.array_equal(bits(out), ref["out"]), f"call {k}"
+
+
+# Groups per owner segment that leave a ragged last reduce tile (64 groups of
+# 64, 16 groups of 256), a ragged last push unit (8 groups of 64; 2 of 256)
+# and, for 64, a ragged last gather run (4 groups).
+GS_RAGGED = {64: 75, 256: 37}
+
+
+@pytest.mark.parametrize("fused", [0, 1])
+@pytest.mark.parametrize("mode", ["none", "caller"])
+@pytest.mark.parametrize("bits_", [4, 8])
+@pytest.mark.parametrize("P", [1, 2, 3, 4, 8, 16])
+@pytest.mark.parametrize("g", [64, 256])
+def test_group_sizes_match_oracle(echo, g, P, bits_, mode, fused):
+    """Groups of 64 and 256 elements (the group-size rows of the paper's
+    Table 8 ablation)."""
+    _run_sequence(echo, P, GS_RAGGED[g], bits_, mode, fused, seed=1000 + g + 10 * P + bits_, g=g)
+
+
+@pytest.mark.parametrize("opts", [dict(quant=1), dict(quant=2), dict(bf16_state=True),
+                                  dict(bf16_state=True, decay=0.5, quant=2)])
+@pytest.mark.parametrize("g", [64, 256])
+def test_group_sizes_with_options(echo, g, opts):
+    _run_sequence(echo, 4, GS_RAGGED[g], 4, "caller", 0, seed=1100 + g, g=g, **opts)
+
+
+@pytest.mark.parametrize("g,Gs", [(64, 1), (64, 7), (64, 8), (64, 63), (64, 64), (64, 65),
+                                  (64, 129), (256, 1), (256, 2), (256, 3), (256, 15), (256, 16),
+                                  (256, 17), (256, 33)])
+def test_group_size_tile_boundaries(echo, g, Gs):
+    _run_sequence(echo, 4, Gs, 4, "caller", 0, calls=2, seed=Gs, g=g)
 
 
 @pytest.mark.parametrize("Gs", [1, 4, 31, 32, 33, 64, 129])
@@ -269,6 +300,10 @@ def test_argument_errors(echo):
     with pytest.raises(echo.EchoError) as ei:
         echo.echo_plan(2, 2 * G, G, 6)
     assert ei.value.status == echo.ECHO_ERR_UNSUPPORTED
+    for g in (32, 96, 512):                             # group sizes the GPU does not take
+        with pytest.raises(echo.EchoError) as ei:
+            echo.echo_plan(2, 2 * 512 * 3, g, 4)
+        assert ei.value.status == echo.ECHO_ERR_UNSUPPORTED
     with pytest.raises(echo.EchoError) as ei:
         echo.echo_set_quantizer(plan, 3)
     assert ei.value.status == echo.ECHO_ERR_ARG

@@ -47,17 +47,17 @@ def test_p2_n4096_full(echo):
 
 
 def _sampled_sequence(echo, number, bits_, sample, calls=None, wire_calls=(0,), quant=0,
-                      bf16_state=False, decay=1.0):
+                      bf16_state=False, decay=1.0, g=G):
     w = WORKLOADS[number]
     P, n = w.P, w.n
-    plan = echo.echo_plan(P, n, G, bits_)
+    plan = echo.echo_plan(P, n, g, bits_)
     echo.echo_set_quantizer(plan, quant)
     echo.echo_set_state(plan, echo.ECHO_STATE_BF16 if bf16_state else echo.ECHO_STATE_F32, decay)
     sdt = torch.bfloat16 if bf16_state else torch.float32
     lay = echo.echo_wire_layout(plan)
     Gs = lay["Gs"]
     groups = sample_groups(P, Gs, sample, seed=number)
-    so = SampledOracle(P, Gs, groups, bits_, mode=quant, bf16_state=bf16_state, decay=decay)
+    so = SampledOracle(P, Gs, groups, bits_, g=g, mode=quant, bf16_state=bf16_state, decay=decay)
     states = {}
     x = torch.empty((P, n), dtype=torch.bfloat16, device="cuda")
     out = torch.empty_like(x)
@@ -126,3 +126,9 @@ def test_p4_2048x4096_state_options_sampled(echo, state):
 
 def test_p8_1gib_bf16_state_sampled(echo):
     _sampled_sequence(echo, 3, 4, sample=2048, calls=4, bf16_state=True)
+
+
+@pytest.mark.parametrize("g", [64, 256])
+def test_p4_2048x4096_group_sizes_sampled(echo, g):
+    """Groups of 64 and 256 over the first 16 calls of the 64-call workload."""
+    _sampled_sequence(echo, 2, 4, sample=512 * 128 // g, calls=16, g=g)

@@ -70,11 +70,11 @@ def test_worked_example_by_hand():
     assert np.array_equal(y[0] - exact, -e.astype(np.float64).sum(axis=0))
 
 
+@pytest.mark.parametrize("g", [64, 128, 256])
 @pytest.mark.parametrize("P", [1, 2, 3, 4, 5, 8])
 @pytest.mark.parametrize("bits", [4, 8])
-def test_identical_outputs_and_at_most_twice(P, bits):
-    rng = np.random.default_rng(100 * P + bits)
-    g = 128
+def test_identical_outputs_and_at_most_twice(P, bits, g):
+    rng = np.random.default_rng(100 * P + bits + g)
     n = P * g * 3
     x = random_x(rng, P, n)
     e = (rng.standard_normal((P, n)) * 0.01).astype(np.float32)
@@ -92,11 +92,12 @@ def test_identical_outputs_and_at_most_twice(P, bits):
     assert r["nq"].max() <= 2
 
 
+@pytest.mark.parametrize("g", [64, 128, 256])
 @pytest.mark.parametrize("bits", [4, 8])
-def test_single_rank_is_one_group_quantization(bits):
+def test_single_rank_is_one_group_quantization(bits, g):
     """P=1: nothing is pushed, and the call quantizes x + e once per group."""
     rng = np.random.default_rng(7)
-    g, n = 128, 128 * 5
+    n = g * 5
     x = random_x(rng, 1, n)
     e = (rng.standard_normal((1, n)) * 0.05).astype(np.float32)
     e0 = e.copy()
@@ -179,11 +180,12 @@ def _run_sequence(P, n, g, bits, calls, compensated, seed, scale=1.0):
     return D, D1, e
 
 
-def test_telescoping_identity_of_error_feedback():
+@pytest.mark.parametrize("g", [64, 128, 256])
+def test_telescoping_identity_of_error_feedback(g):
     """With error feedback, y_k = sum_p x_pk + E_{k-1} - E_k up to fp32 rounding of
     the adds, so the accumulated error D_N equals -E_N (E_0 = 0): it is set by
     the state alone and does not grow with N."""
-    P, n, g, bits, N = 4, 4 * 256, 128, 4, 200
+    P, n, bits, N = 4, 4 * 512, 4, 200
     D, _, e = _run_sequence(P, n, g, bits, N, True, seed=5)
     E = e.astype(np.float64).sum(axis=0)
     slack = N * P * 2.0 ** -22 * 8.0            # |x| <~ 5, rounding of adds per call

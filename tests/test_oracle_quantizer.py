@@ -51,14 +51,15 @@ def _groups(rng, bits, count=300, g=128):
     return out
 
 
+@pytest.mark.parametrize("g", [64, 128, 256])
 @pytest.mark.parametrize("bits", [4, 8])
-def test_codes_are_brute_force_optimal(bits):
+def test_codes_are_brute_force_optimal(bits, g):
     """Each code minimises |v - s(q - z)| over all 2^b codes for the chosen (s, z),
     up to the rounding of the fp32 quotient v/s; exact ties go to the even q - z."""
     L = (1 << bits) - 1
-    rng = np.random.default_rng(10 + bits)
+    rng = np.random.default_rng(10 + bits + g)
     ties_seen = 0
-    for v in _groups(rng, bits):
+    for v in _groups(rng, bits, g=g):
         q, sb, zb, bad, _ = oracle.quantize_group(v, bits)
         assert bad == 0
         s = float(oracle.f16_to_f32([sb])[0])
@@ -79,13 +80,14 @@ def test_codes_are_brute_force_optimal(bits):
         assert ties_seen > 0  # the on-grid groups do produce exact ties
 
 
+@pytest.mark.parametrize("g", [64, 128, 256])
 @pytest.mark.parametrize("bits", [4, 8])
-def test_step_is_least_fp16_above_range_over_levels(bits):
+def test_step_is_least_fp16_above_range_over_levels(bits, g):
     """s is the smallest fp16 value >= fl32((hi - lo) / (2^b - 1)), with the range
     widened to contain 0; an all-zero group gets s = 1."""
     L = (1 << bits) - 1
-    rng = np.random.default_rng(20 + bits)
-    for v in _groups(rng, bits):
+    rng = np.random.default_rng(20 + bits + g)
+    for v in _groups(rng, bits, g=g):
         _, sb, _, _, _ = oracle.quantize_group(v, bits)
         s = np.array([sb], np.uint16).view(np.float16)[0]
         lo = np.float32(min(0.0, float(v.min())))
