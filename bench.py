@@ -246,6 +246,7 @@ def run_ours(args, rank, local, world):
     plan = echo.echo_plan(P, n, g, bits)
     echo.echo_set_fused(plan, fused)
     echo.echo_set_quantizer(plan, args.quantizer)
+    echo.echo_set_persistent(plan, args.persistent)
     sb = set_state(echo, plan, args)
     sdt = torch.bfloat16 if sb == 2 else torch.float32
     states = {"fwd": echo.COMP_DEFAULT,
@@ -259,7 +260,7 @@ def run_ours(args, rank, local, world):
         for ins, comp in call_args:
             echo.echo_allreduce(plan, ins, out_rows, comp, stream)
 
-    launches_per_call = (2 if fused else 3) - (1 if P == 1 else 0)
+    launches_per_call = 1 if args.persistent else (2 if fused else 3) - (1 if P == 1 else 0)
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize(dev)
@@ -312,12 +313,20 @@ def run_ours(args, rank, local, world):
     nlaunch = len(ev_sets)
     kb_comp = kernel_bytes(P, n, bits, True, fused, sb, g)
     kb_unc = kernel_bytes(P, n, bits, False, fused, g=g)
-    ran = [k for k in ("push", "reduce", "gather") if k in kb_comp and (k != "push" or P > 1)]
+    if args.persistent:
+        # one kernel does the whole call: its events span push, reduce and gather
+        kb_comp = {"call": sum(kb_comp.values())}
+        kb_unc = {"call": sum(kb_unc.values())}
+        per_kernel_ms = {"call": per_kernel_ms["push"]}
+        ran = ["call"]
+    else:
+        ran = [k for k in ("push", "reduce", "gather") if k in kb_comp and (k != "push" or P > 1)]
     avg_us = {k: per_kernel_ms[k] / nlaunch * 1e3 for k in ran}
     dominant = max(avg_us, key=lambda k: avg_us[k])
     kbytes = (compensated_calls * kb_comp[dominant] + (calls - compensated_calls) * kb_unc[dominant]) / calls
     achieved = kbytes / (avg_us[dominant] / 1e6) / 1e9
-    kname = {"push": "push_kernel", "reduce": "reduce_kernel", "gather": "gather_kernel"}[dominant]
+    kname = {"push": "push_kernel", "reduce": "reduce_kernel", "gather": "gather_kernel",
+             "call": "call_kernel"}[dominant]
     traffic = profiled_traffic(kname, w.name)
     roofline = {"bound": "hbm", "kernel": kname, "achieved": round(achieved, 1), "peak": hbm,
                 "unit": "GB/s", "frac": round(achieved / hbm, 4), "traffic": traffic,
@@ -332,6 +341,7 @@ def run_ours(args, rank, local, world):
         "config": {"workload": w.name, "P": P, "n_per_rank": n, "bits": bits, "g": g,
                    "calls_per_step": calls, "compensated": compensated_calls == calls,
                    "fused_gather": bool(fused), "quantizer": QUANTIZERS[args.quantizer],
+                   "schedule": "one persistent kernel" if args.persistent else "three kernels",
                    "state": {"format": "bf16" if sb == 2 else "fp32", "decay": args.decay},
                    "io": "bf16 in/out, fp32 arithmetic, "
                    f"{bits}-bit codes, {'bf16' if sb == 2 else 'fp32'} state",
@@ -431,6 +441,7 @@ def time_other(echo, number, bits, fused, dev, args, reps=3):
     plan = echo.echo_plan(w.P, w.n, args.g, bits)
     echo.echo_set_fused(plan, fused)
     echo.echo_set_quantizer(plan, args.quantizer)
+    echo.echo_set_persistent(plan, args.persistent)
     sb = set_state(echo, plan, args)
     bwd = torch.zeros((w.P, w.n), dtype=torch.bfloat16 if sb == 2 else torch.float32, device=dev)
     comps = [{"fwd": echo.COMP_DEFAULT, "bwd": bwd, "none": None}[c.state] for c in seq]
@@ -621,6 +632,8 @@ def main(argv=None):
     ap.add_argument("--bits", type=int, default=4, choices=[4, 8])
     ap.add_argument("--g", type=int, default=G, choices=[64, 128, 256], help="elements per group")
     ap.add_argument("--fused", action="store_true", help="reduce kernel writes the outputs itself")
+    ap.add_argument("--persistent", action="store_true",
+                    help="one persistent kernel per call instead of three")
     ap.add_argument("--quantizer", type=int, default=0, choices=[0, 1, 2],
                     help="0 zero-aware (the method), 1 naive zero-point, 2 symmetric grid")
     ap.add_argument("--state", choices=["f32", "bf16"], default="f32",

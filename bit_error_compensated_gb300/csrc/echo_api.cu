@@ -25,6 +25,10 @@ struct echo_plan_s {
   int mode = ECHO_QUANT_ZERO_AWARE;
   int state_bf16 = 0;               // ECHO_STATE_BF16 selected
   float decay = 1.0f;
+  int persistent = 0;               // one persistent kernel per call (k_call.cu)
+  uint32_t* sched = nullptr;        // its schedule words, zero between calls
+  int64_t tiles = 0;                // reduce tiles per segment
+  int64_t hold = -1;                // test hook, see echo_debug_hold_push
   cudaEvent_t ev[4] = {nullptr, nullptr, nullptr, nullptr};
   int timing = 0;
 };
@@ -76,6 +80,10 @@ cudaError_t launch_reduce(const CallArgs& a, int g, int bits, bool fused, cudaSt
 cudaError_t launch_gather(const CallArgs& a, int g, int bits, cudaStream_t s, bool pdl) {
   return ECHO_BY_GROUP(g, launch_gather_g)(a, bits, s, pdl);
 }
+cudaError_t launch_call(const CallArgs& a, const CallSched& sch, int g, int bits, bool fused,
+                        cudaStream_t s) {
+  return ECHO_BY_GROUP(g, launch_call_g)(a, sch, bits, fused, s);
+}
 #undef ECHO_BY_GROUP
 
 cudaError_t prepare_kernels() {
@@ -119,6 +127,9 @@ int echo_plan(int P, int64_t n, int g, int bits, echo_plan_t* out) {
   p->off[3] = (int64_t)align_up(p->off[2] + codes2, 256);
   p->wire_bytes = align_up(p->off[3] + meta2, 256);
   p->comp_bytes = (size_t)P * n * sizeof(float);
+  const int64_t T = echo::kReduceTileElems / g;
+  p->tiles = (p->Gs + T - 1) / T;
+  const size_t sched_bytes = (size_t)echo::sched_words(P, p->tiles) * sizeof(uint32_t);
 
   cudaError_t e = cudaGetDevice(&p->device);
   if (e == cudaSuccess && p->device >= 0 && p->device < 64 && !g_kernels_prepared[p->device]) {
@@ -128,6 +139,8 @@ int echo_plan(int P, int64_t n, int g, int bits, echo_plan_t* out) {
   if (e == cudaSuccess && p->wire_bytes > 0) e = cudaMalloc((void**)&p->wire, p->wire_bytes);
   if (e == cudaSuccess && p->comp_bytes > 0) e = cudaMalloc((void**)&p->comp, p->comp_bytes);
   if (e == cudaSuccess) e = cudaMalloc((void**)&p->status, sizeof(int));
+  if (e == cudaSuccess) e = cudaMalloc((void**)&p->sched, sched_bytes);
+  if (e == cudaSuccess) e = cudaMemset(p->sched, 0, sched_bytes);
   if (e == cudaSuccess && p->wire_bytes > 0) e = cudaMemset(p->wire, 0, p->wire_bytes);
   if (e == cudaSuccess && p->comp_bytes > 0) e = cudaMemset(p->comp, 0, p->comp_bytes);
   if (e == cudaSuccess) e = cudaMemset(p->status, 0, sizeof(int));
@@ -203,6 +216,21 @@ int echo_allreduce(echo_plan_t plan, const void* const* in, void* const* out,
   // the previous kernel drains; every kernel waits (griddepcontrol.wait) before
   // touching data the previous one wrote.  Timing events in between make each
   // launch an ordinary stream-ordered one.
+  if (plan->persistent) {
+    echo::CallSched sch;
+    sch.tiles = plan->tiles;
+    sch.round = sch.lag = sch.total = 0;       // set by the launcher
+    sch.hold = plan->hold;
+    sch.push_done = plan->sched;
+    sch.reduce_done = plan->sched + (int64_t)P * plan->tiles;
+    sch.ctrl = plan->sched + 2 * (int64_t)P * plan->tiles;
+    if (plan->timing) ECHO_CUDA(cudaEventRecord(plan->ev[0], s));
+    ECHO_CUDA(echo::launch_call(a, sch, plan->g, plan->bits, plan->fused != 0, s));
+    if (plan->timing) {
+      for (int k = 1; k < 4; ++k) ECHO_CUDA(cudaEventRecord(plan->ev[k], s));
+    }
+    return ECHO_OK;
+  }
   const bool pdl = plan->timing == 0;
   if (plan->timing) ECHO_CUDA(cudaEventRecord(plan->ev[0], s));
   if (P > 1) ECHO_CUDA(echo::launch_push(a, plan->g, plan->bits, s, pdl));
@@ -254,6 +282,13 @@ int echo_get_status(echo_plan_t plan, void* stream, int* status) {
   ECHO_CUDA(cudaStreamSynchronize(s));
   *status = (word & echo::kStatusTimeout) ? ECHO_ERR_TIMEOUT
             : (word & echo::kStatusOverflow) ? ECHO_ERR_OVERFLOW : ECHO_OK;
+  if (word & echo::kStatusTimeout) {
+    // A persistent call that gave up leaves its schedule words part-way:
+    // clear them so that the next call starts clean.
+    ECHO_CUDA(cudaMemsetAsync(plan->sched, 0,
+                              (size_t)echo::sched_words(plan->P, plan->tiles) * sizeof(uint32_t), s));
+    ECHO_CUDA(cudaStreamSynchronize(s));
+  }
   return ECHO_OK;
 }
 
@@ -272,6 +307,22 @@ int echo_debug_wire(echo_plan_t plan, void* host_dst, size_t bytes, void* stream
 int echo_set_fused(echo_plan_t plan, int fused) {
   if (plan == nullptr || (fused != 0 && fused != 1)) return ECHO_ERR_ARG;
   plan->fused = fused;
+  return ECHO_OK;
+}
+
+int echo_set_persistent(echo_plan_t plan, int on) {
+  if (plan == nullptr || (on != 0 && on != 1)) return ECHO_ERR_ARG;
+  // Tickets are 32-bit: at most 3 tiles rounds of P (P+1) tickets (plus the
+  // claims that find none).
+  if (on && 3 * (int64_t)plan->P * (plan->P + 1) * plan->tiles > ((int64_t)1 << 31))
+    return ECHO_ERR_UNSUPPORTED;
+  plan->persistent = on;
+  return ECHO_OK;
+}
+
+int echo_debug_hold_push(echo_plan_t plan, int64_t item) {
+  if (plan == nullptr || item < -1) return ECHO_ERR_ARG;
+  plan->hold = item;
   return ECHO_OK;
 }
 
@@ -320,6 +371,7 @@ void echo_plan_destroy(echo_plan_t plan) {
   if (plan->wire) cudaFree(plan->wire);
   if (plan->comp) cudaFree(plan->comp);
   if (plan->status) cudaFree(plan->status);
+  if (plan->sched) cudaFree(plan->sched);
   delete plan;
 }
 

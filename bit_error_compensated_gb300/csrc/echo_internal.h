@@ -25,6 +25,13 @@ constexpr int kReduceTileElems = ECHO_REDUCE_TILE * 128;
 static_assert(kReduceTileElems % (4 * 256) == 0, "reduce tile: a multiple of 4 groups of 256");
 // Threads per block of every kernel.
 constexpr int kThreads = 256;
+// Blocks per SM the register allocation of the reduce and persistent kernels
+// must allow.  Their shared-memory stages already cap residency near this
+// (about 62 KB a block at 4 ranks), so a lower figure buys registers without
+// costing occupancy.
+#ifndef ECHO_REDUCE_MIN_BLOCKS
+#define ECHO_REDUCE_MIN_BLOCKS 3
+#endif
 
 // Status-word bits written by the kernels (read by echo_get_status).
 constexpr int kStatusOverflow = 1;
@@ -49,6 +56,20 @@ struct CallArgs {
   float decay;         // the kept error is decay * (revealed error); 1 = plain feedback
 };
 
+// The schedule of the single persistent kernel of a call (k_call.cu).
+struct CallSched {
+  int64_t tiles;          // reduce tiles per owner segment
+  int64_t round;          // tickets per round (set by the launcher)
+  int64_t lag;            // D: round r reduces tile r - D, gathers tile r - 2D (launcher)
+  int64_t total;          // tickets of the call (launcher)
+  int64_t hold;           // test hook: this push ticket never reports completion; -1 none
+  uint32_t* push_done;    // [P][tiles] pushes of the tile finished in this call
+  uint32_t* reduce_done;  // [P][tiles] the tile's reduce finished in this call
+  uint32_t* ctrl;         // [0] ticket counter, [1] blocks finished, [2] abort
+};
+// 32-bit words of a plan's schedule area.
+inline int64_t sched_words(int P, int64_t tiles) { return 2 * (int64_t)P * tiles + 4; }
+
 // Launchers for group size G, defined in the translation unit compiled with
 // ECHO_G = G.  They return the launch error.
 template <int G> cudaError_t launch_push_g(const CallArgs& a, int bits, cudaStream_t s, bool pdl);
@@ -59,11 +80,17 @@ template <int G> cudaError_t launch_gather_g(const CallArgs& a, int bits, cudaSt
 // shared memory) for group size G.
 template <int G> cudaError_t prepare_reduce_g();
 
+template <int G>
+cudaError_t launch_call_g(const CallArgs& a, const CallSched& sch, int bits, bool fused,
+                          cudaStream_t s);
+
 // Dispatch on the group size g (defined in echo_api.cu, which sees only the
 // declarations above, so each kernel source instantiates its own g alone).
 cudaError_t launch_push(const CallArgs& a, int g, int bits, cudaStream_t s, bool pdl);
 cudaError_t launch_reduce(const CallArgs& a, int g, int bits, bool fused, cudaStream_t s, bool pdl);
 cudaError_t launch_gather(const CallArgs& a, int g, int bits, cudaStream_t s, bool pdl);
+cudaError_t launch_call(const CallArgs& a, const CallSched& sch, int g, int bits, bool fused,
+                        cudaStream_t s);
 // Attributes of every reduce kernel, all group sizes.
 cudaError_t prepare_kernels();
 // Records `e` as the error echo_strerror(ECHO_ERR_CUDA) reports in this thread

@@ -1,0 +1,389 @@
+// k_call.cu -- one whole all-reduce call ("Echo: Error-Compensated 4-Bit
+// Tensor-Parallel Communication", Fig. 2) in a single persistent kernel, the
+// one-GPU counterpart of the paper's staggered push / reduce / gather tiles
+// (Fig. 2(b)): a reduce tile starts as soon as its P-1 pushes are done and a
+// gather tile as soon as its reduce is, with no kernel boundary in between.
+//
+// Work items, in ticket order, come in rounds: round r holds the push of
+// tile r from every sender to every owner, the reduce of tile r - D of every
+// owner and (unless the reduce writes the outputs itself) the gather of tile
+// r - 2D, where the lag D is about two waves of items in flight, so a reduce
+// tile is claimed when its pushes are most likely done and pushes, reduces
+// and gathers, which load memory and ALU differently, share the GPU.  Slots
+// whose tile is out of range are skipped.  A tile is kReduceTileElems elements
+// of a segment.  Blocks claim items from one atomic ticket counter.  A reduce item waits for a per-tile counter of
+// finished pushes, a gather item for a per-tile reduce flag; each consumer
+// resets what it consumed, and the last block to finish resets the ticket
+// counter, so the words are zero again for the next call.  An item only ever
+// waits on items with smaller tickets; the launch is cooperative, so all
+// blocks are co-resident.
+//
+// Each block pipelines two items: while it computes one, thread 0 has
+// already claimed the next and, if that item's inputs are final, started its
+// bulk copies (cp.async.bulk) into the other shared-memory stage.  If they
+// are not, the block first finishes and signals the current item and only
+// then waits, so a block never waits while holding an item it has not
+// signalled: the waiting item with the smallest ticket always has all its
+// inputs on their way, and every wait ends.
+//
+// Every wait is bounded (kWaitLimitNs) and also gives up when another block
+// has set the abort word; a block that gives up records ECHO_ERR_TIMEOUT in
+// the status word, sets the abort word, lets its copies in flight land
+// (bounded) and stops.  echo_get_status clears the schedule words after a
+// timeout.
+#include "stages.cuh"
+
+namespace echo {
+namespace {
+
+constexpr int kPushItem = 0, kReduceItem = 1, kGatherItem = 2, kEmptyItem = 3;
+// A push item is one 512-element unit per warp, a gather item two or more
+// 256-element runs per warp.
+static_assert(kReduceTileElems == kUnit * (kThreads / 32), "tile: one push unit per warp");
+static_assert(kReduceTileElems % (kRun * (kThreads / 32)) == 0, "tile: whole gather runs per warp");
+
+#ifndef ECHO_CALL_LAG_WAVES
+#define ECHO_CALL_LAG_WAVES 1
+#endif
+constexpr int kCallLagWaves = ECHO_CALL_LAG_WAVES;
+
+struct Item {
+  int kind, p, o;
+  int64_t k;
+};
+
+__device__ __forceinline__ Item item_of(const CallArgs& a, const CallSched& sch, int64_t t) {
+  const int P = a.P;
+  const int pairs = P * (P - 1);
+  const int64_t r = t / sch.round;
+  const int slot = (int)(t - r * sch.round);
+  Item it;
+  if (slot < pairs) {
+    it.kind = kPushItem;
+    it.k = r;
+    it.p = slot / (P - 1);
+    const int oi = slot - it.p * (P - 1);
+    it.o = oi + (oi >= it.p ? 1 : 0);
+  } else if (slot < pairs + P) {
+    it.kind = kReduceItem;
+    it.k = r - sch.lag;
+    it.o = it.p = slot - pairs;
+  } else {
+    it.kind = kGatherItem;
+    it.k = r - 2 * sch.lag;
+    it.o = it.p = slot - pairs - P;
+  }
+  if (it.k < 0 || it.k >= sch.tiles) it.kind = kEmptyItem;
+  return it;
+}
+
+// Release forms of the completion signals: the block's results (ordered
+// before thread 0 by the barrier) become visible before the counter or flag.
+__device__ __forceinline__ void add_release(uint32_t* p, uint32_t v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ void st_release(uint32_t* p, uint32_t v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ uint32_t ld_relaxed(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Orders this thread's earlier generic-proxy view of global memory (the
+// acquire of a flag) before its later bulk copies reading that memory.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// Thread 0: waits until *w == want, or gives up (bounded, or when the abort
+// word is set).  Returns false on giving up.
+__device__ __forceinline__ bool wait_word(const uint32_t* w, uint32_t want, const uint32_t* abort) {
+  if (ld_acquire(w) == want) return true;
+  const uint64_t t0 = global_ns();
+  for (;;) {
+    if (ld_acquire(w) == want) return true;
+    if (ld_relaxed(abort) != 0 || global_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+
+template <int BITS, int SF, int MODE, int G, bool FUSED>
+__global__ void __launch_bounds__(kThreads, ECHO_REDUCE_MIN_BLOCKS)
+call_kernel(const CallArgs a, const CallSched sch) {
+  constexpr int T = tile_groups<G>();
+  constexpr int NL = G / 16;
+  constexpr int GPW = 32 / NL;
+  constexpr int EB = state_bytes<SF>();
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ __align__(8) uint64_t full[2];
+  __shared__ int64_t s_item[2];                  // the item of each stage
+  __shared__ int s_pending[2];                   // its inputs still to be waited for
+
+  const int P = a.P;
+  const int64_t Gs = a.Gs;
+  const uint32_t sbytes = reduce_stage_bytes<BITS, SF, G>(P);
+  const uint32_t full0 = smem_addr(&full[0]);
+  uint32_t* const ticket = sch.ctrl;
+  uint32_t* const finished = sch.ctrl + 1;
+  uint32_t* const abort = sch.ctrl + 2;
+  const int64_t runs_total = (Gs * G + kRun - 1) / kRun;
+
+  uint64_t pol = 0;
+  // Thread 0: is the input of item `it` final?  1 yes (and consumed: the
+  // counter or flag is reset for the next call), 0 not yet (only when not
+  // `blocking`), -1 gave up (the abort word is then set).
+  auto inputs_ready = [&](const Item& it, bool blocking) -> int {
+    if (it.kind == kPushItem || (it.kind == kReduceItem && P == 1)) return 1;
+    const int64_t tile = (int64_t)it.o * sch.tiles + it.k;
+    uint32_t* w = it.kind == kReduceItem ? sch.push_done + tile : sch.reduce_done + tile;
+    const uint32_t want = it.kind == kReduceItem ? (uint32_t)(P - 1) : 1u;
+    if (blocking) {
+      if (!wait_word(w, want, abort)) {
+        atomicOr(a.status, kStatusTimeout);
+        atomicExch(abort, 1u);
+        return -1;
+      }
+    } else if (ld_acquire(w) != want) {
+      return 0;
+    }
+    *w = 0;                                      // consumed; zero for the next call
+    fence_proxy_async_global();                  // before bulk copies of what it guards
+    return 1;
+  };
+  // Thread 0: starts the copies of item `it` into stage st.
+  auto issue = [&](const Item& it, int st) {
+    const int64_t j0 = it.k * T;
+    const int tg = (int)((Gs - j0) < T ? (Gs - j0) : T);     // groups in the tile
+    uint8_t* stage = smem + (size_t)st * sbytes;
+    const uint32_t bar = full0 + 8 * st;
+    if (it.kind == kPushItem) {
+      const PushPlace pl = push_place<BITS, SF, G>(a, it.p, it.o);
+      mbar_expect_tx(bar, (uint32_t)tg * G * (2u + EB));
+      bulk_g2s(smem_addr(stage), pl.xs + j0 * G, (uint32_t)tg * G * 2u, bar, pol);
+      if (SF != kNoState)
+        bulk_g2s(smem_addr(stage + T * G * 2), pl.es + j0 * G * EB, (uint32_t)tg * G * EB, bar, pol);
+    } else if (it.kind == kReduceItem) {
+      reduce_issue_own<BITS, SF, G>(a, stage, bar, it.o, j0, tg, pol);
+      reduce_issue_codes<BITS, SF, G>(a, stage, bar, it.o, j0, tg, pol);
+    }
+  };
+  // Thread 0: the next non-empty ticket, or sch.total when there is none.
+  // The ticket after it is fetched right away and used next time, so the
+  // atomic's latency passes while the block computes.
+  int64_t pre = 0;
+  auto take = [&]() -> int64_t {
+    int64_t t = pre;
+    for (;;) {
+      if (t >= sch.total) {                      // (the abort word is read only by waits)
+        pre = sch.total;
+        return sch.total;
+      }
+      if (item_of(a, sch, t).kind != kEmptyItem) break;
+      t = (int64_t)atomicAdd(ticket, 1u);
+    }
+    pre = (int64_t)atomicAdd(ticket, 1u);
+    return t;
+  };
+
+  if (threadIdx.x == 0) {
+    mbar_init(full0, 1);
+    mbar_init(full0 + 8, 1);
+    fence_barrier_init();
+    pol = policy_evict_first();                  // inputs and state are read once per call
+    if (ld_relaxed(abort) != 0) atomicOr(a.status, kStatusTimeout);   // an earlier call gave up
+    // The block holds no item yet, so it may wait.
+    pre = (int64_t)atomicAdd(ticket, 1u);
+    int64_t t = take();
+    if (t < sch.total) {
+      const Item it = item_of(a, sch, t);
+      if (inputs_ready(it, true) < 0) t = sch.total;
+      else issue(it, 0);
+    }
+    s_item[0] = t;
+  }
+  __syncthreads();
+
+  const uint64_t codes_pol = kCodesPolicyLast ? policy_evict_last() : policy_evict_normal();
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  uint32_t phase0 = 0u, phase1 = 0u;             // mbarrier phase of each stage
+  for (int i = 0;; ++i) {
+    const int st = i & 1;
+    const int64_t t = s_item[st];
+    if (t >= sch.total) break;                   // block-uniform
+    const Item it = item_of(a, sch, t);
+    const int64_t j0 = it.k * T;
+    const int tg = (int)((Gs - j0) < T ? (Gs - j0) : T);
+    uint8_t* stage = smem + (size_t)st * sbytes;
+    if (it.kind != kGatherItem) {
+      const uint32_t ph = st ? phase1 : phase0;
+      if (!mbar_wait_block(full0 + 8 * st, ph)) {                  // same outcome for all
+        if (threadIdx.x == 0) {
+          atomicOr(a.status, kStatusTimeout);
+          atomicExch(abort, 1u);
+          mbar_wait_bounded(full0 + 8 * st, ph);                   // let the copies land
+        }
+        break;
+      }
+      if (st) phase1 ^= 1u; else phase0 ^= 1u;
+    }
+    // Thread 0 takes the next item now and, if its inputs are final, starts
+    // its copies into the other stage (free: its last item was finished
+    // before the barrier that ended the previous iteration).  If they are
+    // not, it waits only after this item is done and signalled: a block never
+    // waits while it holds an item it has not signalled.
+    if (threadIdx.x == 0) {
+      const int64_t t1 = take();
+      int pend = 0;
+      if (t1 < sch.total) {
+        const Item it1 = item_of(a, sch, t1);
+        if (inputs_ready(it1, false) == 1) issue(it1, st ^ 1);
+        else pend = 1;
+      }
+      s_item[st ^ 1] = t1;
+      s_pending[st ^ 1] = pend;
+    }
+
+    if (it.kind == kPushItem) {
+      // One 512-element unit per warp: groups [j0 + warp*GPW, +GPW) of the tile.
+      const PushPlace pl = push_place<BITS, SF, G>(a, it.p, it.o);
+      const int sub = lane / NL;
+      const int q = lane % NL;
+      const int gl = warp * GPW + sub;           // group within the tile
+      const bool valid = gl < tg;
+      float v[16];
+      if (valid) {
+        push_load<SF, G>(stage + warp * kUnitX, stage + T * G * 2 + warp * kUnit * EB, sub, q, v);
+      } else {
+#pragma unroll
+        for (int k = 0; k < 16; ++k) v[k] = 0.0f;
+      }
+      push_finish<BITS, SF, MODE, G>(a, v, valid, j0 + gl, q, pl.es, pl.cs, pl.ms, codes_pol);
+    } else if (it.kind == kReduceItem) {
+      reduce_tile<BITS, SF, FUSED, MODE, G>(a, stage, it.o, j0, tg);
+    } else {
+      const int64_t r0 = it.k * (T * G / kRun);
+      const int64_t r1 = r0 + T * G / kRun < runs_total ? r0 + T * G / kRun : runs_total;
+      gather_runs<BITS, (T * G / kRun) / (kThreads / 32), MODE, G>(a, it.o, r0 + warp,
+                                                                   kThreads / 32, r1);
+    }
+
+    fence_proxy_async();                         // this thread's stage reads before a refill
+    __syncthreads();                             // the item is done; s_item, s_pending set
+    const bool pend = s_pending[st ^ 1] != 0;    // block-uniform
+    if (threadIdx.x == 0) {
+      if (it.kind != kGatherItem && t != sch.hold) {
+        const int64_t tile = (int64_t)it.o * sch.tiles + it.k;
+        if (it.kind == kPushItem)
+          add_release(sch.push_done + tile, 1u);
+        else if (!FUSED)
+          st_release(sch.reduce_done + tile, 1u);
+      }
+      if (pend) {                                // now the block holds nothing unsignalled
+        const int64_t t1 = s_item[st ^ 1];
+        const Item it1 = item_of(a, sch, t1);
+        if (inputs_ready(it1, true) < 0) s_item[st ^ 1] = sch.total;
+        else issue(it1, st ^ 1);
+      }
+    }
+    if (pend) __syncthreads();                   // s_item[st ^ 1] final
+  }
+
+  // The last block to stop claiming resets the ticket counter for the next call.
+  if (threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(finished, 1u) == gridDim.x - 1) {
+      atomicExch(ticket, 0u);
+      atomicExch(finished, 0u);
+    }
+  }
+}
+
+template <int BITS, int SF, int MODE, int G, bool FUSED>
+cudaError_t launch_t(const CallArgs& a, const CallSched& sch, cudaStream_t s) {
+  static int resident_cache[64][ECHO_MAX_RANKS + 1] = {{0}};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const size_t smem = 2 * (size_t)reduce_stage_bytes<BITS, SF, G>(a.P);
+  int& resident = resident_cache[dev & 63][a.P];
+  if (resident == 0) {
+    int sms = 0, per_sm = 0;
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    cudaError_t e = cudaFuncSetAttribute(call_kernel<BITS, SF, MODE, G, FUSED>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)(2 * reduce_stage_bytes<BITS, SF, G>(ECHO_MAX_RANKS)));
+    if (e != cudaSuccess) return e;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, call_kernel<BITS, SF, MODE, G, FUSED>,
+                                                      kThreads, smem);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) return cudaErrorInvalidConfiguration;
+    resident = sms * per_sm;
+  }
+  // Rounds of P(P-1) pushes, P reduces and (unfused) P gathers; the lag is
+  // about kCallLagWaves waves of items in flight (two per block).
+  CallSched sc = sch;
+  const int P = a.P;
+  sc.round = (int64_t)P * (P - 1) + P + (FUSED ? 0 : P);
+  int64_t lag = (kCallLagWaves * 2 * (int64_t)resident + sc.round - 1) / sc.round;
+  if (P == 1) lag = 0;                           // nothing to wait for
+  sc.lag = lag < sc.tiles ? lag : sc.tiles;
+  sc.total = sc.round * (sc.tiles + (FUSED ? 1 : 2) * sc.lag);
+  // Every block resident at once (a cooperative launch checks it), and no
+  // more blocks than items.
+  const int64_t items = (FUSED ? 1 : 2) * (int64_t)P * sc.tiles + (int64_t)P * (P - 1) * sc.tiles;
+  const int64_t blocks = items < resident ? items : resident;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)blocks);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, call_kernel<BITS, SF, MODE, G, FUSED>, a, sc);
+}
+
+template <int MODE, int G>
+cudaError_t launch_mode(const CallArgs& a, const CallSched& sch, int bits, bool fused,
+                        cudaStream_t s) {
+  const int sf = a.comp == nullptr ? kNoState : (a.state_bf16 ? kStateBF16 : kStateF32);
+#define ECHO_CALL_SF(B, SFV)                                                                 \
+  return fused ? launch_t<B, SFV, MODE, G, true>(a, sch, s) : launch_t<B, SFV, MODE, G, false>(a, sch, s);
+  if (bits == 4) {
+    if (sf == kStateF32) { ECHO_CALL_SF(4, kStateF32) }
+    if (sf == kStateBF16) { ECHO_CALL_SF(4, kStateBF16) }
+    ECHO_CALL_SF(4, kNoState)
+  }
+  if (sf == kStateF32) { ECHO_CALL_SF(8, kStateF32) }
+  if (sf == kStateBF16) { ECHO_CALL_SF(8, kStateBF16) }
+  ECHO_CALL_SF(8, kNoState)
+#undef ECHO_CALL_SF
+}
+
+}  // namespace
+
+template <int G>
+cudaError_t launch_call_g(const CallArgs& a, const CallSched& sch, int bits, bool fused,
+                          cudaStream_t s) {
+  if (a.mode == kNaiveZeroPoint) return launch_mode<kNaiveZeroPoint, G>(a, sch, bits, fused, s);
+  if (a.mode == kSymmetric) return launch_mode<kSymmetric, G>(a, sch, bits, fused, s);
+  return launch_mode<kZeroAware, G>(a, sch, bits, fused, s);
+}
+
+#ifndef ECHO_G
+#define ECHO_G 128
+#endif
+static_assert(group_supported(ECHO_G), "ECHO_G: 64, 128 or 256");
+template cudaError_t launch_call_g<ECHO_G>(const CallArgs&, const CallSched&, int, bool, cudaStream_t);
+
+}  // namespace echo

@@ -10,8 +10,7 @@
 // writes, per rank, one 16-byte streaming store per lane (512 B per warp).
 // U such runs per warp are read before any is written, to keep several code
 // reads in flight.  Write-bound: P * 2 bytes out per element.
-#include "echo_internal.h"
-#include "quant.cuh"
+#include "stages.cuh"
 
 namespace echo {
 namespace {
@@ -19,60 +18,11 @@ namespace {
 template <int BITS, int U, int MODE, int G>
 __global__ void __launch_bounds__(kThreads)
 gather_kernel(const CallArgs a) {
-  constexpr int CB = G * BITS / 8;
-  constexpr int LG = G / 8;         // lanes per group
-  constexpr int GW = 32 / LG;       // groups per warp run
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int lane = threadIdx.x & 31;
-  const int sub = lane / LG;
-  const int h = lane % LG;          // lane h of a group decodes elements [8h, 8h+8)
   const int64_t wg = (int64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
   const int64_t nw = (int64_t)gridDim.x * (kThreads / 32);
-  const int P = a.P;
-  const int o = blockIdx.y;                       // owner segment
-  const int64_t Gs = a.Gs;
-  const uint8_t* cs = a.codes2 + (int64_t)o * Gs * CB;
-  const uint32_t* ms = a.meta2 + (int64_t)o * a.Gs_pad;
-
-  // GW adjacent groups per warp run, U runs in flight.
-  for (int64_t run0 = wg; GW * run0 < Gs; run0 += nw * U) {
-    uint2 word[U];
-    uint32_t meta[U];
-    int64_t w[U];
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      w[u] = GW * (run0 + (int64_t)u * nw) + sub;
-      if (w[u] < Gs) {
-        meta[u] = ms[w[u]];
-        const uint8_t* cg = cs + w[u] * CB;
-        if (BITS == 4) {
-          word[u].x = reinterpret_cast<const uint32_t*>(cg)[h];
-          word[u].y = 0;
-        } else {
-          word[u] = reinterpret_cast<const uint2*>(cg)[h];
-        }
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      if (w[u] >= Gs) continue;
-      float s, zf;
-      unpack_meta(meta[u], s, zf);
-      float deq[8], yb[8];
-      if (BITS == 4) {
-        decode4_mode<4, MODE>(word[u].x, s, zf, deq);
-        decode4_mode<4, MODE>(word[u].x >> 16, s, zf, deq + 4);
-      } else {
-        decode4_mode<8, MODE>(word[u].x, s, zf, deq);
-        decode4_mode<8, MODE>(word[u].y, s, zf, deq + 4);
-      }
-      const uint2 ya = f32x4_to_bf16(deq, yb);
-      const uint2 yv = f32x4_to_bf16(deq + 4, yb + 4);
-      const uint4 y = make_uint4(ya.x, ya.y, yv.x, yv.y);
-      const int64_t e0 = ((int64_t)o * Gs + w[u]) * G + 8 * h;
-      for (int r = 0; r < P; ++r) __stcs(reinterpret_cast<uint4*>(a.out[r] + e0), y);
-    }
-  }
+  const int64_t runs = (a.Gs * G + kRun - 1) / kRun;
+  gather_runs<BITS, U, MODE, G>(a, (int)blockIdx.y, wg, nw, runs);   // blockIdx.y: owner segment
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 

@@ -24,9 +24,7 @@
 // records ECHO_ERR_TIMEOUT, waits once more (bounded) for each copy it still
 // has in flight, and returns.  HBM-bound: per element 2 B of input and the
 // state read, the state and b/8 B of codes written, plus 4 B of meta a group.
-#include "echo_internal.h"
-#include "quant.cuh"
-#include "tma.cuh"
+#include "stages.cuh"
 
 namespace echo {
 namespace {
@@ -35,28 +33,19 @@ namespace {
 #define ECHO_PUSH_STAGES 2
 #endif
 constexpr int kPushStages = ECHO_PUSH_STAGES;      // units in flight per warp
-constexpr int kUnit = 512;                         // elements of a unit (32 lanes x 16)
-constexpr int kUnitX = kUnit * 2;                  // bf16 bytes of a unit
-
-template <int SF>
-constexpr int push_stage_bytes() { return kUnitX + kUnit * state_bytes<SF>(); }
 
 template <int SF>
 constexpr size_t push_smem_bytes() {
-  return (size_t)(kThreads / 32) * kPushStages * push_stage_bytes<SF>();
+  return (size_t)(kThreads / 32) * kPushStages * push_unit_bytes<SF>();
 }
 
 template <int BITS, int SF, int MODE, int G>
 __global__ void __launch_bounds__(kThreads)
 push_kernel(const CallArgs a) {
-  constexpr float L = (float)((1 << BITS) - 1);
   constexpr int NL = G / 16;                        // lanes per group
   constexpr int GPW = 32 / NL;                      // groups per unit
-  constexpr int CB = G * BITS / 8;                  // code bytes per group
   constexpr int S = kPushStages;
-  constexpr int SB = push_stage_bytes<SF>();
-  constexpr bool COMP = SF != kNoState;
-  constexpr int EB = state_bytes<SF>();             // state bytes per element
+  constexpr int SB = push_unit_bytes<SF>();
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(8) uint64_t bars[kThreads / 32][S];
 
@@ -64,13 +53,8 @@ push_kernel(const CallArgs a) {
   const int p = (int)blockIdx.y / (P - 1);          // sender
   const int oi = (int)blockIdx.y - p * (P - 1);
   const int o = oi + (oi >= p ? 1 : 0);             // owner of the segment
-  const int slot = o * (P - 1) + (p < o ? p : p - 1);
+  const PushPlace pl = push_place<BITS, SF, G>(a, p, o);
   const int64_t Gs = a.Gs;
-  const __nv_bfloat16* xs = a.in[p] + (int64_t)o * Gs * G;
-  uint8_t* es = COMP ? reinterpret_cast<uint8_t*>(a.comp) +
-                           ((int64_t)p * a.n + (int64_t)o * Gs * G) * EB : nullptr;
-  uint8_t* cs = a.codes1 + (int64_t)slot * Gs * CB;
-  uint32_t* ms = a.meta1 + (int64_t)slot * a.Gs_pad;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -99,10 +83,7 @@ push_kernel(const CallArgs a) {
     if (ud >= nunits) return;
     const int64_t g0 = GPW * ud;
     const uint32_t ng = (uint32_t)((Gs - g0) < GPW ? (Gs - g0) : GPW);
-    const uint32_t bar = bar0 + 8 * st;
-    mbar_expect_tx(bar, ng * G * (2u + EB));
-    bulk_g2s(smem_addr(wbuf + st * SB), xs + g0 * G, ng * G * 2u, bar, pol);
-    if (COMP) bulk_g2s(smem_addr(wbuf + st * SB + kUnitX), es + g0 * G * EB, ng * G * EB, bar, pol);
+    push_issue<SF, G>(pl, g0, ng, wbuf + st * SB, bar0 + 8 * st, pol);
   };
   if (lane == 0) {
 #pragma unroll
@@ -127,19 +108,7 @@ push_kernel(const CallArgs a) {
     const bool valid = j < Gs;
     float v[16];
     if (valid) {
-      const uint2* sx = reinterpret_cast<const uint2*>(wbuf + st * SB) + sub * (G / 4);
-#pragma unroll
-      for (int c = 0; c < 4; ++c) bf16x4_to_f32(sx[chunk_at<NL>(c, q) / 4], v + 4 * c);
-      if constexpr (COMP) {
-        const uint8_t* se = wbuf + st * SB + kUnitX;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          float e[4];
-          state_load4<SF>(se, sub * G + chunk_at<NL>(c, q), e);
-#pragma unroll
-          for (int k = 0; k < 4; ++k) v[4 * c + k] = __fadd_rn(v[4 * c + k], e[k]);
-        }
-      }
+      push_load<SF, G>(wbuf + st * SB, wbuf + st * SB + kUnitX, sub, q, v);
     } else {
 #pragma unroll
       for (int k = 0; k < 16; ++k) v[k] = 0.0f;      // idle lanes of a short unit
@@ -150,35 +119,7 @@ push_kernel(const CallArgs a) {
       fence_proxy_async();
       issue(i + S, st);
     }
-
-    const GroupGrid gg = group_grid<MODE, NL>(v, L);
-#pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {                 // chunks 2hh and 2hh+1
-      float c[8], d[8];
-      quantize8_mode<MODE>(v + 8 * hh, gg, L, c, d);
-      if (valid) {
-        uint8_t* cg = cs + j * CB;
-        if (BITS == 4) {
-          st_hint_u16(cg + chunk_code_byte<4, NL>(2 * hh, q), pack4<4>(c), codes_pol);
-          st_hint_u16(cg + chunk_code_byte<4, NL>(2 * hh + 1, q), pack4<4>(c + 4), codes_pol);
-        } else {
-          st_hint_u32(cg + chunk_code_byte<8, NL>(2 * hh, q), pack4<8>(c), codes_pol);
-          st_hint_u32(cg + chunk_code_byte<8, NL>(2 * hh + 1, q), pack4<8>(c + 4), codes_pol);
-        }
-        if constexpr (COMP) {
-          const float* vv = v + 8 * hh;
-          float r[8];
-#pragma unroll
-          for (int k = 0; k < 8; ++k) r[k] = __fsub_rn(vv[k], d[k]);
-          state_store4<SF>(es, j * G + chunk_at<NL>(2 * hh, q), r, a.decay);
-          state_store4<SF>(es, j * G + chunk_at<NL>(2 * hh + 1, q), r + 4, a.decay);
-        }
-      }
-    }
-    if (valid && q == 0) {
-      st_hint_u32(ms + j, gg.meta, codes_pol);
-      if (!gg.finite) atomicOr(a.status, kStatusOverflow);
-    }
+    push_finish<BITS, SF, MODE, G>(a, v, valid, j, q, pl.es, pl.cs, pl.ms, codes_pol);
   }
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }

@@ -75,6 +75,68 @@ struct GroupGrid {
   bool finite;    // false: non-finite input or step overflow; results unspecified
 };
 
+// ------------------------------------------------------------- pairs ----
+// Elementwise fp32 add / sub / mul / fma on pairs of values.  Each half is
+// rounded to nearest exactly as by __fadd_rn / __fsub_rn / __fmul_rn /
+// __fmaf_rn (IEEE, subnormals kept); the sm_100 family issues one packed
+// f32x2 instruction per pair, half the instructions of the scalar form.
+#ifndef ECHO_F32X2
+#define ECHO_F32X2 1
+#endif
+
+#if ECHO_F32X2
+#define ECHO_PAIR_OP(NAME, OP)                                                              \
+  __device__ __forceinline__ void NAME(float& r0, float& r1, float a0, float a1, float b0,  \
+                                       float b1) {                                          \
+    asm("{\n\t.reg .b64 pa, pb, pr;\n\t"                                                   \
+        "mov.b64 pa, {%2, %3};\n\tmov.b64 pb, {%4, %5};\n\t" OP                             \
+        " pr, pa, pb;\n\tmov.b64 {%0, %1}, pr;\n\t}"                                        \
+        : "=f"(r0), "=f"(r1) : "f"(a0), "f"(a1), "f"(b0), "f"(b1));                        \
+  }
+ECHO_PAIR_OP(add2, "add.rn.f32x2")
+ECHO_PAIR_OP(sub2, "sub.rn.f32x2")
+ECHO_PAIR_OP(mul2, "mul.rn.f32x2")
+#undef ECHO_PAIR_OP
+__device__ __forceinline__ void fma2(float& r0, float& r1, float a0, float a1, float b0, float b1,
+                                     float c0, float c1) {
+  asm("{\n\t.reg .b64 pa, pb, pc, pr;\n\t"
+      "mov.b64 pa, {%2, %3};\n\tmov.b64 pb, {%4, %5};\n\tmov.b64 pc, {%6, %7};\n\t"
+      "fma.rn.f32x2 pr, pa, pb, pc;\n\tmov.b64 {%0, %1}, pr;\n\t}"
+      : "=f"(r0), "=f"(r1) : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+#else
+__device__ __forceinline__ void add2(float& r0, float& r1, float a0, float a1, float b0, float b1) {
+  r0 = __fadd_rn(a0, b0); r1 = __fadd_rn(a1, b1);
+}
+__device__ __forceinline__ void sub2(float& r0, float& r1, float a0, float a1, float b0, float b1) {
+  r0 = __fsub_rn(a0, b0); r1 = __fsub_rn(a1, b1);
+}
+__device__ __forceinline__ void mul2(float& r0, float& r1, float a0, float a1, float b0, float b1) {
+  r0 = __fmul_rn(a0, b0); r1 = __fmul_rn(a1, b1);
+}
+__device__ __forceinline__ void fma2(float& r0, float& r1, float a0, float a1, float b0, float b1,
+                                     float c0, float c1) {
+  r0 = __fmaf_rn(a0, b0, c0); r1 = __fmaf_rn(a1, b1, c1);
+}
+#endif
+
+// Arrays of N (even) values: r = a + b, r = a - b, r = a * b, r = a * s.
+template <int N>
+__device__ __forceinline__ void add_n(float* r, const float* a, const float* b) {
+#pragma unroll
+  for (int k = 0; k < N; k += 2) add2(r[k], r[k + 1], a[k], a[k + 1], b[k], b[k + 1]);
+}
+template <int N>
+__device__ __forceinline__ void sub_n(float* r, const float* a, const float* b) {
+#pragma unroll
+  for (int k = 0; k < N; k += 2) sub2(r[k], r[k + 1], a[k], a[k + 1], b[k], b[k + 1]);
+}
+template <int N>
+__device__ __forceinline__ void mul_ns(float* r, const float* a, float s) {
+#pragma unroll
+  for (int k = 0; k < N; k += 2) mul2(r[k], r[k + 1], a[k], a[k + 1], s, s);
+}
+
 // rint(t) for |t| < 2^22 with two fp32 adds: at 1.5 * 2^23 the fp32 spacing
 // is 1, so the first add rounds t to an integer (to nearest, ties to even)
 // and the second removes the offset exactly.  Runs on the FMA pipe.
@@ -124,25 +186,36 @@ __device__ __forceinline__ GroupGrid make_grid(float lo, float hi, float L) {
 // so rint(fl(v / s)) >= rint(fl(lo / s)) = -z (division and rint are monotonic
 // and odd-symmetric), and c >= 0 already.  (For a non-finite group the codes
 // are unspecified; pack4 still confines each packed word to its own bytes.)
+//
+// Since r and z are small integers, clamp(r + z, L) - z = min(r, L - z)
+// exactly: the clamped offset cm = q - z gives both c = cm + z and d = cm * s.
 __device__ __forceinline__ void quantize8(const float v[8], const GroupGrid& gg, float L,
                                           float c[8], float d[8]) {
-  float r[8];
+  constexpr float M = 12582912.0f;                 // 1.5 * 2^23, see rint_small
+  float t[8], r[8], e[8];
+  mul_ns<8>(t, v, gg.inv);
+#pragma unroll
+  for (int k = 0; k < 8; k += 2) {
+    add2(r[k], r[k + 1], t[k], t[k + 1], M, M);
+    sub2(r[k], r[k + 1], r[k], r[k + 1], M, M);
+  }
+  sub_n<8>(e, t, r);
   float dev = 0.0f;
 #pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    const float t = __fmul_rn(v[k], gg.inv);
-    r[k] = rint_small(t);
-    dev = fmaxf(dev, fabsf(__fsub_rn(t, r[k])));
-  }
+  for (int k = 0; k < 8; ++k) dev = fmaxf(dev, fabsf(e[k]));
   if (dev >= kFastRintLimit) {
+    // (+ 0 turns a -0 from rintf into +0, as the fast path gives, so that
+    // cm * s below is +0 where (q - z) * s is.)
 #pragma unroll
-    for (int k = 0; k < 8; ++k) r[k] = rintf(__fdiv_rn(v[k], gg.s));
+    for (int k = 0; k < 8; ++k) r[k] = __fadd_rn(rintf(__fdiv_rn(v[k], gg.s)), 0.0f);
   }
+  const float lz = __fsub_rn(L, gg.zf);            // exact
+  float cm[8];
 #pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    c[k] = fminf(__fadd_rn(r[k], gg.zf), L);
-    d[k] = __fmul_rn(__fsub_rn(c[k], gg.zf), gg.s);   // (q - z) exact, times s
-  }
+  for (int k = 0; k < 8; ++k) cm[k] = fminf(r[k], lz);
+#pragma unroll
+  for (int k = 0; k < 8; k += 2) add2(c[k], c[k + 1], cm[k], cm[k + 1], gg.zf, gg.zf);
+  mul_ns<8>(d, cm, gg.s);
 }
 
 // Quantizer variants: the method's zero-aware asymmetric quantizer and the two
@@ -260,6 +333,29 @@ __device__ __forceinline__ uint32_t small_int_bits(float w) {
   return __float_as_uint(__fadd_rn(w, 8388608.0f)) & 0xFFFFu;
 }
 
+// Two chunks (c[0..3] and c[4..7]) at once, on pairs.
+template <int BITS>
+__device__ __forceinline__ void pack8(const float c[8], uint32_t& w0, uint32_t& w1) {
+  constexpr float B = 8388608.0f;                  // 2^23
+  float a0, a1;
+  if (BITS == 4) {
+    fma2(a0, a1, c[1], c[5], 16.0f, 16.0f, c[0], c[4]);
+    fma2(a0, a1, c[2], c[6], 256.0f, 256.0f, a0, a1);
+    fma2(a0, a1, c[3], c[7], 4096.0f, 4096.0f, a0, a1);
+    add2(a0, a1, a0, a1, B, B);
+    w0 = __float_as_uint(a0) & 0xFFFFu;
+    w1 = __float_as_uint(a1) & 0xFFFFu;
+  } else {
+    float b0, b1;
+    fma2(a0, a1, c[1], c[5], 256.0f, 256.0f, c[0], c[4]);   // bytes 0, 1
+    fma2(b0, b1, c[3], c[7], 256.0f, 256.0f, c[2], c[6]);   // bytes 2, 3
+    add2(a0, a1, a0, a1, B, B);
+    add2(b0, b1, b0, b1, B, B);
+    w0 = __byte_perm(__float_as_uint(a0), __float_as_uint(b0), 0x5410);
+    w1 = __byte_perm(__float_as_uint(a1), __float_as_uint(b1), 0x5410);
+  }
+}
+
 template <int BITS>
 __device__ __forceinline__ uint32_t pack4(const float c[4]) {
   if (BITS == 4) {
@@ -277,10 +373,13 @@ template <int BITS>
 __device__ __forceinline__ void decode4(uint32_t w, float s, float zf, float d[4]) {
   constexpr uint32_t MASK = (1u << BITS) - 1;
   const float bias = __fadd_rn(8388608.0f, zf);   // 2^23 + z, exact
+  float q23[4];
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const float q23 = __uint_as_float(0x4B000000u | ((w >> (BITS * k)) & MASK));  // 2^23 + q
-    d[k] = __fmul_rn(__fsub_rn(q23, bias), s);    // q - z exact
+  for (int k = 0; k < 4; ++k) q23[k] = __uint_as_float(0x4B000000u | ((w >> (BITS * k)) & MASK));
+#pragma unroll
+  for (int k = 0; k < 4; k += 2) {
+    sub2(d[k], d[k + 1], q23[k], q23[k + 1], bias, bias);   // q - z exact
+    mul2(d[k], d[k + 1], d[k], d[k + 1], s, s);
   }
 }
 
@@ -349,8 +448,7 @@ template <int SF>
 __device__ __forceinline__ void state_store4(uint8_t* base, int64_t i, const float r[4],
                                              float decay) {
   float t[4];
-#pragma unroll
-  for (int k = 0; k < 4; ++k) t[k] = __fmul_rn(decay, r[k]);
+  mul_ns<4>(t, r, decay);
   if constexpr (SF == kStateF32) {
     *reinterpret_cast<float4*>(base + 4 * i) = make_float4(t[0], t[1], t[2], t[3]);
   } else {

@@ -50,6 +50,8 @@ _SIGS = {
     "echo_set_timing": (_i32, [_vp, ctypes.POINTER(_vp), _i32]),
     "echo_set_quantizer": (_i32, [_vp, _i32]),
     "echo_set_state": (_i32, [_vp, _i32, ctypes.c_float]),
+    "echo_set_persistent": (_i32, [_vp, _i32]),
+    "echo_debug_hold_push": (_i32, [_vp, _i64]),
     "echo_allreduce_noalloc": (_i32, [_i32, _i64, _i32, ctypes.POINTER(_vp), ctypes.POINTER(_vp),
                                       _vp, _vp]),
     "echo_plan_destroy": (None, [_vp]),
@@ -177,6 +179,14 @@ def echo_set_quantizer(plan: Plan, mode: int) -> None:
 
 def echo_set_state(plan: Plan, fmt: int = ECHO_STATE_F32, decay: float = 1.0) -> None:
     _check(_lib.echo_set_state(plan, fmt, decay), "echo_set_state")
+
+
+def echo_set_persistent(plan: Plan, on: bool) -> None:
+    _check(_lib.echo_set_persistent(plan, 1 if on else 0), "echo_set_persistent")
+
+
+def echo_debug_hold_push(plan: Plan, item: int) -> None:
+    _check(_lib.echo_debug_hold_push(plan, item), "echo_debug_hold_push")
 
 
 def echo_set_timing(plan: Plan, events) -> None:

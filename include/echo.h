@@ -224,6 +224,34 @@ int echo_allreduce_noalloc(int P, int64_t n, int bits, const void* const* in,
                            void* const* out, void* comp_state, void* stream);
 
 /*
+ * echo_set_persistent -- run each later echo_allreduce of the plan as one
+ * persistent kernel instead of three kernels (on = 1), or back (on = 0).
+ * The paper overlaps the push, reduce and gather of different tiles
+ * (Fig. 2(b)); here every (sender, owner, tile) push, every reduce tile and
+ * every gather tile is a work item that blocks claim in order from an atomic
+ * ticket counter, and a reduce tile starts as soon as its P-1 pushes are done
+ * (a gather tile as soon as its reduce is), with per-tile counters in the
+ * plan.  Results are bit-identical to the three-kernel path, with or without
+ * the fused gather.  The launch is cooperative (every block resident).  Every
+ * device-side wait is bounded (1 s); a call that gives up sets the status word
+ * to ECHO_ERR_TIMEOUT and leaves its results unspecified, and the following
+ * echo_get_status clears the plan's schedule words so that the next call
+ * starts clean.  Returns ECHO_ERR_UNSUPPORTED for a problem with 2^31 or more
+ * work items, ECHO_ERR_ARG for on not 0 or 1.
+ */
+int echo_set_persistent(echo_plan_t plan, int on);
+
+/*
+ * echo_debug_hold_push -- test hook for the bounded waits of the persistent
+ * kernel: in every later persistent call, the push work item with ticket
+ * `item` (0-based; items are ordered tile by tile, then by sender and owner)
+ * does its work but never reports it, so the reduce of its tile waits until
+ * its bound and the call ends with ECHO_ERR_TIMEOUT.  -1 (the default) turns
+ * the hook off.  ECHO_ERR_ARG for item < -1.
+ */
+int echo_debug_hold_push(echo_plan_t plan, int64_t item);
+
+/*
  * echo_set_quantizer -- choose the group quantizer of a plan's calls.
  *   ECHO_QUANT_ZERO_AWARE (default): the method's zero-aware asymmetric
  *     quantizer (the "full" row of the paper's Table 8), as described at the

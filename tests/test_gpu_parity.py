@@ -35,10 +35,11 @@ def _inputs(P, n, seed, scale=1.0):
 
 
 def _run_sequence(echo, P, Gs, bits_, mode, fused, calls=3, seed=0, inplace=False, quant=0,
-                  bf16_state=False, decay=1.0, g=G):
+                  bf16_state=False, decay=1.0, g=G, persistent=False):
     n = P * g * Gs
     plan = echo.echo_plan(P, n, g, bits_)
     echo.echo_set_fused(plan, fused)
+    echo.echo_set_persistent(plan, persistent)
     echo.echo_set_quantizer(plan, quant)
     echo.echo_set_state(plan, echo.ECHO_STATE_BF16 if bf16_state else echo.ECHO_STATE_F32, decay)
     assert echo.echo_comp_bytes(plan) == P * n * (2 if bf16_state else 4)
@@ -155,6 +156,83 @@ def test_group_sizes_with_options(echo, g, opts):
                                   (256, 17), (256, 33)])
 def test_group_size_tile_boundaries(echo, g, Gs):
     _run_sequence(echo, 4, Gs, 4, "caller", 0, calls=2, seed=Gs, g=g)
+
+
+@pytest.mark.parametrize("fused", [0, 1])
+@pytest.mark.parametrize("mode", ["none", "default", "caller"])
+@pytest.mark.parametrize("bits_", [4, 8])
+@pytest.mark.parametrize("P", [1, 2, 3, 4, 8, 16])
+def test_persistent_matches_oracle(echo, P, bits_, mode, fused):
+    """The whole call as one persistent kernel (echo_set_persistent)."""
+    _run_sequence(echo, P, 37, bits_, mode, fused, seed=2000 + P * 10 + bits_, persistent=True)
+
+
+@pytest.mark.parametrize("opts", [dict(g=64), dict(g=256), dict(quant=1), dict(quant=2),
+                                  dict(bf16_state=True, decay=0.5), dict(g=64, quant=2, fused=1),
+                                  dict(g=256, bf16_state=True, fused=1), dict(inplace=True),
+                                  dict(inplace=True, fused=1)])
+def test_persistent_with_options(echo, opts):
+    opts = dict(opts)
+    g = opts.pop("g", G)
+    fused = opts.pop("fused", 0)
+    _run_sequence(echo, 4, {64: 75, 128: 37, 256: 37}[g], 4, "caller", fused, seed=2100, g=g,
+                  persistent=True, **opts)
+
+
+@pytest.mark.parametrize("Gs", [1, 2, 31, 32, 33, 64, 129, 300])
+def test_persistent_tile_boundaries(echo, Gs):
+    _run_sequence(echo, 3, Gs, 4, "caller", 0, calls=2, seed=Gs, persistent=True)
+
+
+def test_persistent_same_bits_as_three_kernels(echo):
+    """Outputs, state and every wire byte of a call sequence agree between the
+    two schedules."""
+    P, Gs = 4, 70
+    n = P * G * Gs
+    res = []
+    for persistent in (False, True):
+        plan = echo.echo_plan(P, n, G, 4)
+        echo.echo_set_persistent(plan, persistent)
+        comp = torch.zeros((P, n), device="cuda")
+        outs = []
+        for k in range(4):
+            x = _inputs(P, n, 3000 + k)
+            out = torch.empty_like(x)
+            echo.echo_allreduce(plan, list(x), list(out), comp)
+            outs.append(bits(out))
+        torch.cuda.synchronize()
+        res.append((outs, comp.cpu().numpy().view(np.uint32), echo.echo_debug_wire(plan)))
+    assert all(np.array_equal(a, b) for a, b in zip(res[0][0], res[1][0]))
+    assert np.array_equal(res[0][1], res[1][1])
+    assert res[0][2] == res[1][2]
+
+
+def test_persistent_bounded_wait_reports_timeout(echo):
+    """A push that never reports completion (the hold hook) makes the reduce
+    of its tile wait until its 1 s bound: the call ends with ECHO_ERR_TIMEOUT
+    instead of hanging, echo_get_status clears the schedule, and the next call
+    is correct again."""
+    import time
+    P, Gs = 4, 37
+    n = P * G * Gs
+    plan = echo.echo_plan(P, n, G, 4)
+    echo.echo_set_persistent(plan, True)
+    x = _inputs(P, n, 77)
+    out = torch.empty_like(x)
+    echo.echo_debug_hold_push(plan, 5)
+    t0 = time.monotonic()
+    echo.echo_allreduce(plan, list(x), list(out), None)
+    torch.cuda.synchronize()
+    waited = time.monotonic() - t0
+    assert echo.echo_get_status(plan) == echo.ECHO_ERR_TIMEOUT
+    assert 0.5 < waited < 10.0
+    echo.echo_debug_hold_push(plan, -1)
+    for k in range(2):
+        xk = _inputs(P, n, 78 + k)
+        echo.echo_allreduce(plan, list(xk), list(out), None)
+        torch.cuda.synchronize()
+        assert echo.echo_get_status(plan) == 0
+        assert np.array_equal(bits(out), oracle.allreduce(bits(xk), G, 4)["out"])
 
 
 @pytest.mark.parametrize("Gs", [1, 4, 31, 32, 33, 64, 129])
@@ -313,6 +391,11 @@ def test_argument_errors(echo):
             echo.echo_set_state(plan, fmt, decay)
         assert ei.value.status == echo.ECHO_ERR_ARG
     assert echo.echo_comp_bytes(plan) == plan.P * plan.n * 4       # unchanged
+    for bad in (2, -1):                                 # the C call takes 0 or 1 only
+        assert echo._lib.echo_set_persistent(plan, bad) == echo.ECHO_ERR_ARG
+    with pytest.raises(echo.EchoError) as ei:
+        echo.echo_debug_hold_push(plan, -2)
+    assert ei.value.status == echo.ECHO_ERR_ARG
 
 
 @pytest.mark.parametrize("bits_", [4, 8])

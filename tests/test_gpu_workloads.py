@@ -47,10 +47,12 @@ def test_p2_n4096_full(echo):
 
 
 def _sampled_sequence(echo, number, bits_, sample, calls=None, wire_calls=(0,), quant=0,
-                      bf16_state=False, decay=1.0, g=G):
+                      bf16_state=False, decay=1.0, g=G, persistent=False, fused=False):
     w = WORKLOADS[number]
     P, n = w.P, w.n
     plan = echo.echo_plan(P, n, g, bits_)
+    echo.echo_set_persistent(plan, persistent)
+    echo.echo_set_fused(plan, fused)
     echo.echo_set_quantizer(plan, quant)
     echo.echo_set_state(plan, echo.ECHO_STATE_BF16 if bf16_state else echo.ECHO_STATE_F32, decay)
     sdt = torch.bfloat16 if bf16_state else torch.float32
@@ -132,3 +134,18 @@ def test_p8_1gib_bf16_state_sampled(echo):
 def test_p4_2048x4096_group_sizes_sampled(echo, g):
     """Groups of 64 and 256 over the first 16 calls of the 64-call workload."""
     _sampled_sequence(echo, 2, 4, sample=512 * 128 // g, calls=16, g=g)
+
+
+@pytest.mark.parametrize("fused", [False, True])
+def test_p4_2048x4096_persistent_sampled(echo, fused):
+    """The persistent kernel over the first 16 calls of the 64-call workload."""
+    _sampled_sequence(echo, 2, 4, sample=512, calls=16, persistent=True, fused=fused)
+
+
+def test_p8_1gib_persistent_sampled(echo):
+    _sampled_sequence(echo, 3, 4, sample=2048, calls=1, persistent=True)
+
+
+def test_p4_32768x1024_persistent_sampled(echo):
+    """Two states (forward and backward sites) through the persistent kernel."""
+    _sampled_sequence(echo, 5, 4, sample=256, calls=24, persistent=True)
