@@ -364,6 +364,10 @@ def run_ours(args, rank, local, world):
         result["also"] = {}
         for num in [int(v) for v in args.also.split(",") if v]:
             result["also"][WORKLOADS[num].name] = time_other(echo, num, bits, fused, dev, args)
+        if not args.persistent:
+            # the same workload with the other gather variant, for comparison
+            other = "separate gather kernel" if fused else "gather fused into reduce"
+            result["also"][f"{w.name} ({other})"] = time_other(echo, number, bits, not fused, dev, args)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline_oracle(args, budget_s=args.cpu_budget)
     del plan
@@ -631,7 +635,10 @@ def main(argv=None):
     ap.add_argument("--workload", type=int, default=2, help="1..5 (default 2: P=4, 2048x4096, 64 calls)")
     ap.add_argument("--bits", type=int, default=4, choices=[4, 8])
     ap.add_argument("--g", type=int, default=G, choices=[64, 128, 256], help="elements per group")
-    ap.add_argument("--fused", action="store_true", help="reduce kernel writes the outputs itself")
+    ap.add_argument("--unfused", action="store_true",
+                    help="separate gather kernel (three kernels per call); by default the reduce "
+                         "kernel writes the outputs itself")
+    ap.add_argument("--fused", action="store_true", help=argparse.SUPPRESS)   # the default
     ap.add_argument("--persistent", action="store_true",
                     help="one persistent kernel per call instead of three")
     ap.add_argument("--quantizer", type=int, default=0, choices=[0, 1, 2],
@@ -649,6 +656,7 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     args = ap.parse_args(argv)
+    args.fused = not args.unfused
     if args.warmup < 3 and args.impl == "ours":
         ap.error("--warmup must be at least 3")
 

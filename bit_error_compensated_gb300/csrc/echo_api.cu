@@ -21,7 +21,7 @@ struct echo_plan_s {
   size_t comp_bytes = 0;
   int* status = nullptr;            // device status word
   cudaStream_t last_stream = nullptr;
-  int fused = 0;
+  int fused = 1;                    // the reduce kernel writes the outputs (no gather kernel)
   int mode = ECHO_QUANT_ZERO_AWARE;
   int state_bf16 = 0;               // ECHO_STATE_BF16 selected
   float decay = 1.0f;
@@ -127,7 +127,7 @@ int echo_plan(int P, int64_t n, int g, int bits, echo_plan_t* out) {
   p->off[3] = (int64_t)align_up(p->off[2] + codes2, 256);
   p->wire_bytes = align_up(p->off[3] + meta2, 256);
   p->comp_bytes = (size_t)P * n * sizeof(float);
-  const int64_t T = echo::kReduceTileElems / g;
+  const int64_t T = echo::kCallTileElems / g;       // tiles of the persistent schedule
   p->tiles = (p->Gs + T - 1) / T;
   const size_t sched_bytes = (size_t)echo::sched_words(P, p->tiles) * sizeof(uint32_t);
 

@@ -10,7 +10,7 @@
 // r - 2D, where the lag D is about two waves of items in flight, so a reduce
 // tile is claimed when its pushes are most likely done and pushes, reduces
 // and gathers, which load memory and ALU differently, share the GPU.  Slots
-// whose tile is out of range are skipped.  A tile is kReduceTileElems elements
+// whose tile is out of range are skipped.  A tile is kCallTileElems elements
 // of a segment.  Blocks claim items from one atomic ticket counter.  A reduce item waits for a per-tile counter of
 // finished pushes, a gather item for a per-tile reduce flag; each consumer
 // resets what it consumed, and the last block to finish resets the ticket
@@ -39,8 +39,8 @@ namespace {
 constexpr int kPushItem = 0, kReduceItem = 1, kGatherItem = 2, kEmptyItem = 3;
 // A push item is one 512-element unit per warp, a gather item two or more
 // 256-element runs per warp.
-static_assert(kReduceTileElems == kUnit * (kThreads / 32), "tile: one push unit per warp");
-static_assert(kReduceTileElems % (kRun * (kThreads / 32)) == 0, "tile: whole gather runs per warp");
+static_assert(kCallTileElems == kUnit * (kThreads / 32), "tile: one push unit per warp");
+static_assert(kCallTileElems % (kRun * (kThreads / 32)) == 0, "tile: whole gather runs per warp");
 
 #ifndef ECHO_CALL_LAG_WAVES
 #define ECHO_CALL_LAG_WAVES 1
@@ -118,7 +118,7 @@ __device__ __forceinline__ bool wait_word(const uint32_t* w, uint32_t want, cons
 template <int BITS, int SF, int MODE, int G, bool FUSED>
 __global__ void __launch_bounds__(kThreads, ECHO_REDUCE_MIN_BLOCKS)
 call_kernel(const CallArgs a, const CallSched sch) {
-  constexpr int T = tile_groups<G>();
+  constexpr int T = tile_groups<G, kCallTileElems>();
   constexpr int NL = G / 16;
   constexpr int GPW = 32 / NL;
   constexpr int EB = state_bytes<SF>();
@@ -129,7 +129,7 @@ call_kernel(const CallArgs a, const CallSched sch) {
 
   const int P = a.P;
   const int64_t Gs = a.Gs;
-  const uint32_t sbytes = reduce_stage_bytes<BITS, SF, G>(P);
+  const uint32_t sbytes = reduce_stage_bytes<BITS, SF, G, kCallTileElems>(P);
   const uint32_t full0 = smem_addr(&full[0]);
   uint32_t* const ticket = sch.ctrl;
   uint32_t* const finished = sch.ctrl + 1;
@@ -171,8 +171,8 @@ call_kernel(const CallArgs a, const CallSched sch) {
       if (SF != kNoState)
         bulk_g2s(smem_addr(stage + T * G * 2), pl.es + j0 * G * EB, (uint32_t)tg * G * EB, bar, pol);
     } else if (it.kind == kReduceItem) {
-      reduce_issue_own<BITS, SF, G>(a, stage, bar, it.o, j0, tg, pol);
-      reduce_issue_codes<BITS, SF, G>(a, stage, bar, it.o, j0, tg, pol);
+      reduce_issue_own<BITS, SF, G, kCallTileElems>(a, stage, bar, it.o, j0, tg, pol);
+      reduce_issue_codes<BITS, SF, G, kCallTileElems>(a, stage, bar, it.o, j0, tg, pol);
     }
   };
   // Thread 0: the next non-empty ticket, or sch.total when there is none.
@@ -268,7 +268,7 @@ call_kernel(const CallArgs a, const CallSched sch) {
       }
       push_finish<BITS, SF, MODE, G>(a, v, valid, j0 + gl, q, pl.es, pl.cs, pl.ms, codes_pol);
     } else if (it.kind == kReduceItem) {
-      reduce_tile<BITS, SF, FUSED, MODE, G>(a, stage, it.o, j0, tg);
+      reduce_tile<BITS, SF, FUSED, MODE, G, kCallTileElems, kThreads / 32>(a, stage, it.o, j0, tg);
     } else {
       const int64_t r0 = it.k * (T * G / kRun);
       const int64_t r1 = r0 + T * G / kRun < runs_total ? r0 + T * G / kRun : runs_total;
@@ -312,14 +312,14 @@ cudaError_t launch_t(const CallArgs& a, const CallSched& sch, cudaStream_t s) {
   static int resident_cache[64][ECHO_MAX_RANKS + 1] = {{0}};
   int dev = 0;
   cudaGetDevice(&dev);
-  const size_t smem = 2 * (size_t)reduce_stage_bytes<BITS, SF, G>(a.P);
+  const size_t smem = 2 * (size_t)reduce_stage_bytes<BITS, SF, G, kCallTileElems>(a.P);
   int& resident = resident_cache[dev & 63][a.P];
   if (resident == 0) {
     int sms = 0, per_sm = 0;
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     cudaError_t e = cudaFuncSetAttribute(call_kernel<BITS, SF, MODE, G, FUSED>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)(2 * reduce_stage_bytes<BITS, SF, G>(ECHO_MAX_RANKS)));
+                                         (int)(2 * reduce_stage_bytes<BITS, SF, G, kCallTileElems>(ECHO_MAX_RANKS)));
     if (e != cudaSuccess) return e;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, call_kernel<BITS, SF, MODE, G, FUSED>,
                                                       kThreads, smem);

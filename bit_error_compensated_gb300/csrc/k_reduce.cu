@@ -34,16 +34,19 @@ namespace {
 
 constexpr int kReduceRing = ECHO_REDUCE_RING;   // tiles in flight per block
 
+constexpr int kTE = kReduceTileElems;
+constexpr int kRThreads = 32 * kReduceWarps;
+
 template <int BITS, int SF, bool FUSED, int MODE, int G>
-__global__ void __launch_bounds__(kThreads, ECHO_REDUCE_MIN_BLOCKS)
+__global__ void __launch_bounds__(kRThreads, ECHO_REDUCE_MIN_BLOCKS * kThreads / kRThreads)
 reduce_kernel(const CallArgs a, int64_t tiles_per_seg, int64_t ntiles) {
-  constexpr int T = tile_groups<G>();
+  constexpr int T = tile_groups<G, kTE>();
   constexpr int R = kReduceRing;
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(8) uint64_t full[R];
 
   const int P = a.P;
-  const uint32_t sbytes = reduce_stage_bytes<BITS, SF, G>(P);
+  const uint32_t sbytes = reduce_stage_bytes<BITS, SF, G, kTE>(P);
   const uint32_t full0 = smem_addr(&full[0]);
   if (threadIdx.x == 0) {
     for (int st = 0; st < R; ++st) mbar_init(full0 + 8 * st, 1);
@@ -65,13 +68,13 @@ reduce_kernel(const CallArgs a, int64_t tiles_per_seg, int64_t ntiles) {
     int o, t;
     int64_t j0;
     tile_of(k, o, j0, t);
-    reduce_issue_own<BITS, SF, G>(a, smem + (size_t)st * sbytes, full0 + 8 * st, o, j0, t, pol);
+    reduce_issue_own<BITS, SF, G, kTE>(a, smem + (size_t)st * sbytes, full0 + 8 * st, o, j0, t, pol);
   };
   auto issue_codes = [&](int64_t k, int st) {
     int o, t;
     int64_t j0;
     tile_of(k, o, j0, t);
-    reduce_issue_codes<BITS, SF, G>(a, smem + (size_t)st * sbytes, full0 + 8 * st, o, j0, t, pol);
+    reduce_issue_codes<BITS, SF, G, kTE>(a, smem + (size_t)st * sbytes, full0 + 8 * st, o, j0, t, pol);
   };
 
   if (threadIdx.x == 0) {
@@ -102,7 +105,7 @@ reduce_kernel(const CallArgs a, int64_t tiles_per_seg, int64_t ntiles) {
     int o, t;
     int64_t j0;
     tile_of(k, o, j0, t);
-    reduce_tile<BITS, SF, FUSED, MODE, G>(a, smem + (size_t)st * sbytes, o, j0, t);
+    reduce_tile<BITS, SF, FUSED, MODE, G, kTE, kReduceWarps>(a, smem + (size_t)st * sbytes, o, j0, t);
     if (exists(k + R)) {                           // block-uniform
       fence_proxy_async();                         // this thread's reads before the refill
       __syncthreads();
@@ -117,7 +120,7 @@ reduce_kernel(const CallArgs a, int64_t tiles_per_seg, int64_t ntiles) {
 
 template <int BITS, int SF, int G>
 size_t smem_bytes(int P) {
-  return (size_t)kReduceRing * reduce_stage_bytes<BITS, SF, G>(P);
+  return (size_t)kReduceRing * reduce_stage_bytes<BITS, SF, G, kTE>(P);
 }
 
 template <int BITS, int SF, bool FUSED, int MODE, int G>
@@ -131,17 +134,17 @@ cudaError_t launch_t(const CallArgs& a, cudaStream_t s, bool pdl) {
     int sms = 0, per_sm = 0;
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, reduce_kernel<BITS, SF, FUSED, MODE, G>,
-                                                  kThreads, smem);
+                                                  kRThreads, smem);
     resident = sms * (per_sm > 0 ? per_sm : 1);
   }
-  constexpr int T = tile_groups<G>();
+  constexpr int T = tile_groups<G, kTE>();
   const int64_t tiles_per_seg = (a.Gs + T - 1) / T;
   const int64_t ntiles = tiles_per_seg * a.P;
   // A ring of 1 is one tile per block; otherwise one resident wave of blocks.
   const int64_t blocks = (kReduceRing == 1 || ntiles < resident) ? ntiles : resident;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)blocks);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(kRThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];

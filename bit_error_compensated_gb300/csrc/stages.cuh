@@ -126,27 +126,27 @@ __device__ __forceinline__ void push_issue(const PushPlace& pl, int64_t g0, uint
 
 // ---------------------------------------------------------------- reduce ----
 
-// Groups per reduce tile.
-template <int G>
-constexpr int tile_groups() { return kReduceTileElems / G; }
+// Groups per reduce tile of TE elements.
+template <int G, int TE>
+constexpr int tile_groups() { return TE / G; }
 
 // Shared-memory stage of one reduce tile of T groups: [P-1][T][CB] received
 // codes, [P-1][T] meta words, [T][G] owner bf16 input, [T][G] owner state
 // (when compensated).  Every region starts on a 16-byte boundary.
-template <int BITS, int SF, int G>
+template <int BITS, int SF, int G, int TE>
 __host__ __device__ inline uint32_t reduce_stage_bytes(int P) {
-  constexpr int T = tile_groups<G>();
+  constexpr int T = tile_groups<G, TE>();
   return (uint32_t)((P - 1) * T * (G * BITS / 8 + 4) + T * G * 2 + T * G * state_bytes<SF>());
 }
 
 // Thread 0: arms `bar` for the whole tile (t groups from j0 of segment o) and
 // copies the owner's own input and state tile into the stage.
-template <int BITS, int SF, int G>
+template <int BITS, int SF, int G, int TE>
 __device__ __forceinline__ void reduce_issue_own(const CallArgs& a, uint8_t* stage, uint32_t bar,
                                                  int o, int64_t j0, int t, uint64_t pol) {
   constexpr int CB = G * BITS / 8;
   constexpr int EB = state_bytes<SF>();
-  constexpr int T = tile_groups<G>();
+  constexpr int T = tile_groups<G, TE>();
   const int P = a.P;
   const uint32_t meta_bytes = (uint32_t)(((t + 3) & ~3) * 4);
   const int64_t g0 = (int64_t)o * a.Gs + j0;
@@ -161,11 +161,11 @@ __device__ __forceinline__ void reduce_issue_own(const CallArgs& a, uint8_t* sta
 
 // Thread 0: copies the tile's P-1 received code tiles and meta words.  The
 // meta copy is rounded up to 4 words (the slot rows are padded to Gs_pad).
-template <int BITS, int SF, int G>
+template <int BITS, int SF, int G, int TE>
 __device__ __forceinline__ void reduce_issue_codes(const CallArgs& a, uint8_t* stage, uint32_t bar,
                                                    int o, int64_t j0, int t, uint64_t pol) {
   constexpr int CB = G * BITS / 8;
-  constexpr int T = tile_groups<G>();
+  constexpr int T = tile_groups<G, TE>();
   const int P = a.P;
   const uint32_t meta_bytes = (uint32_t)(((t + 3) & ~3) * 4);
   for (int js = 0; js < P - 1; ++js) {
@@ -179,8 +179,8 @@ __device__ __forceinline__ void reduce_issue_codes(const CallArgs& a, uint8_t* s
 
 // Computes one owner tile (t groups from j0 of segment o) held in a stage,
 // writing the gather codes, meta, new owner state and (FUSED) all P outputs
-// to global memory.  Every thread of the block takes part; no block barrier.
-template <int BITS, int SF, bool FUSED, int MODE, int G>
+// to global memory.  The NW warps of the block take part; no block barrier.
+template <int BITS, int SF, bool FUSED, int MODE, int G, int TE, int NW>
 __device__ __forceinline__ void reduce_tile(const CallArgs& a, const uint8_t* stage, int o,
                                             int64_t j0, int t) {
   constexpr float L = (float)((1 << BITS) - 1);
@@ -189,7 +189,7 @@ __device__ __forceinline__ void reduce_tile(const CallArgs& a, const uint8_t* st
   constexpr int NL = G / 16;                 // lanes per group
   constexpr int GPW = 32 / NL;               // groups per warp per pass
   constexpr int CB = G * BITS / 8;
-  constexpr int T = tile_groups<G>();
+  constexpr int T = tile_groups<G, TE>();
   const int P = a.P;
   const uint8_t* s_codes = stage;
   const uint32_t* s_meta = reinterpret_cast<const uint32_t*>(stage + (P - 1) * T * CB);
@@ -202,7 +202,7 @@ __device__ __forceinline__ void reduce_tile(const CallArgs& a, const uint8_t* st
   const int sub = lane / NL;
   const int q = lane % NL;
   // GPW groups per warp per pass (NL lanes each, see quant.cuh).
-  for (int gq = GPW * warp; gq < t; gq += GPW * (kThreads / 32)) {
+  for (int gq = GPW * warp; gq < t; gq += GPW * NW) {
     const int gl = gq + sub;                       // group within the tile
     const bool valid = gl < t;
     const int gs = valid ? gl : gq;                // idle lanes read a valid group

@@ -106,8 +106,9 @@ int echo_plan(int P, int64_t n, int g, int bits, echo_plan_t* out);
  *               zero before the first call of a sequence;
  *               read and updated in place.
  *   stream      cudaStream_t as void*.
- * Enqueues three kernels (push, reduce, gather; or two when the fused gather is
- * selected with echo_set_fused) and returns.  Inputs must stay valid and
+ * Enqueues two kernels (push, then reduce, which also writes the outputs;
+ * three with a separate gather kernel, see echo_set_fused; one with
+ * echo_set_persistent) and returns.  Inputs must stay valid and
  * unmodified until the work completes.  Non-finite inputs or an fp16 step
  * overflow do not fail the call: they set the plan's status word (see
  * echo_get_status) and leave the affected groups' results unspecified.
@@ -167,11 +168,13 @@ int echo_get_status(echo_plan_t plan, void* stream, int* status);
 int echo_debug_wire(echo_plan_t plan, void* host_dst, size_t bytes, void* stream);
 
 /*
- * echo_set_fused -- 0 (default): the gather is its own kernel, which reads the
- * gather codes back and writes all P outputs.  1: the reduce kernel writes the
- * P outputs itself from the values it just encoded (the gather codes are
- * still written); this skips one kernel and one read of the gather codes.
- * Both give bit-identical outputs, state and codes.
+ * echo_set_fused -- 1 (default): the reduce kernel writes the P outputs
+ * itself from the values it has just encoded (the gather codes are still
+ * written); with every rank's output in this GPU's memory, that is the
+ * all-gather's decode without a second read of the codes or a third kernel.
+ * 0: the gather is its own kernel, which reads the gather codes back and
+ * writes all P outputs, as each receiving rank would.  Both give
+ * bit-identical outputs, state and codes.
  */
 int echo_set_fused(echo_plan_t plan, int fused);
 
