@@ -125,8 +125,11 @@ def test_every_schedule_finishes():
         assert _run(P, tiles, fused, D, nblocks, seed), (P, tiles, fused, D, nblocks, seed)
 
 
-@pytest.mark.parametrize("P,fused", [(2, True), (4, False)])
-def test_waiting_before_signalling_deadlocks(P, fused):
-    """The control: one block that waits for its next item's inputs before
-    signalling its current item blocks on itself."""
-    assert not _run(P, 1, fused, 0, 1, 0, wait_before_signal=True)
+@pytest.mark.parametrize("fused", [True, False])
+def test_waiting_before_signalling_deadlocks(fused):
+    """The control: with two ranks the last push of a tile (rank 1 to owner 0)
+    is an input of the first reduce, which comes next; one block that waited
+    for that reduce's inputs before signalling the push would block on
+    itself."""
+    assert not _run(2, 1, fused, 0, 1, 0, wait_before_signal=True)
+    assert _run(2, 1, fused, 0, 1, 0)
