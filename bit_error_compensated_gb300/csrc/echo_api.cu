@@ -166,7 +166,7 @@ int echo_allreduce(echo_plan_t plan, const void* const* in, void* const* out,
   if (comp_state == ECHO_COMP_DEFAULT) {
     comp = plan->comp;
   } else if (comp_state != nullptr) {
-    if (!aligned16(comp_state)) return ECHO_ERR_ALIGN;
+    if (((uintptr_t)comp_state & 31u) != 0) return ECHO_ERR_ALIGN;   // 32-byte state stores
     comp = static_cast<float*>(comp_state);
   }
   // Aliasing: out[p] may be in[p]; otherwise outputs overlap nothing, and the
@@ -381,7 +381,7 @@ const char* echo_strerror(int status) {
     case ECHO_ERR_ARG: return "invalid argument";
     case ECHO_ERR_SHAPE: return "n must be a non-negative multiple of P*g";
     case ECHO_ERR_UNSUPPORTED: return "unsupported configuration (bits must be 4 or 8, g must be 128)";
-    case ECHO_ERR_ALIGN: return "device pointer not 16-byte aligned";
+    case ECHO_ERR_ALIGN: return "device pointer not 16-byte aligned (32 for a compensator state)";
     case ECHO_ERR_CUDA: return cudaGetErrorString(g_last_cuda);
     case ECHO_ERR_OVERFLOW: return "non-finite input or fp16 step overflow in some group";
     case ECHO_ERR_TIMEOUT: return "a device-side wait gave up";

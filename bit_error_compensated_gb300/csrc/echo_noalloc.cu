@@ -77,7 +77,7 @@ extern "C" int echo_allreduce_noalloc(int P, int64_t n, int bits, const void* co
     if (in[p] == nullptr || out[p] == nullptr) return ECHO_ERR_ARG;
     if (!aligned16(in[p]) || !aligned16(out[p])) return ECHO_ERR_ALIGN;
   }
-  if (comp_state != nullptr && !aligned16(comp_state)) return ECHO_ERR_ALIGN;
+  if (comp_state != nullptr && ((uintptr_t)comp_state & 31u) != 0) return ECHO_ERR_ALIGN;
   for (int p = 0; p < P; ++p) {            // same aliasing rules as echo_allreduce
     const uintptr_t op = (uintptr_t)out[p];
     for (int q = 0; q < P; ++q) {

@@ -12,9 +12,10 @@
 //
 // Thread mapping: NL = g/16 lanes per group of g values (4 lanes for g = 64,
 // a quarter warp for 128, half a warp for 256); lane q of the group holds 16
-// values in four chunks of 4 consecutive elements, chunk c being elements
-// [4 NL c + 4q, 4 NL c + 4q + 4), so that every warp-wide load or store of a
-// chunk covers 32/NL contiguous runs, one per group.
+// values in two halves of 8 consecutive elements, half h being elements
+// [8 NL h + 8q, 8 NL h + 8q + 8), so that every warp-wide access to a half
+// covers 32/NL contiguous runs, one per group, with 16- or 32-byte accesses
+// per lane.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -399,6 +400,14 @@ __device__ __forceinline__ void decode4_mode(uint32_t w, float s, float zf, floa
   }
 }
 
+// bf16 <-> f32 for 8 values held in 16 bytes.
+__device__ __forceinline__ void bf16x8_to_f32(uint4 r, float f[8]) {
+  f[0] = __uint_as_float(r.x << 16); f[1] = __uint_as_float(r.x & 0xFFFF0000u);
+  f[2] = __uint_as_float(r.y << 16); f[3] = __uint_as_float(r.y & 0xFFFF0000u);
+  f[4] = __uint_as_float(r.z << 16); f[5] = __uint_as_float(r.z & 0xFFFF0000u);
+  f[6] = __uint_as_float(r.w << 16); f[7] = __uint_as_float(r.w & 0xFFFF0000u);
+}
+
 // bf16 <-> f32 for a chunk of 4 values held in 8 bytes.
 __device__ __forceinline__ void bf16x4_to_f32(uint2 r, float f[4]) {
   f[0] = __uint_as_float(r.x << 16);
@@ -429,42 +438,50 @@ enum StateFmt : int { kNoState = 0, kStateF32 = 1, kStateBF16 = 2 };
 template <int SF>
 constexpr int state_bytes() { return SF == kStateBF16 ? 2 : (SF == kStateF32 ? 4 : 0); }
 
-// The 4 state values of a chunk at element index i of `base` (global or
-// shared memory), as fp32 (exact for both formats).
+// The 8 state values of a half at element index i (a multiple of 8) of a
+// stage in shared memory, as fp32 (exact for both formats).
 template <int SF>
-__device__ __forceinline__ void state_load4(const uint8_t* base, int64_t i, float e[4]) {
+__device__ __forceinline__ void state_load8(const uint8_t* base, int i, float e[8]) {
   if constexpr (SF == kStateF32) {
-    const float4 v = *reinterpret_cast<const float4*>(base + 4 * i);
-    e[0] = v.x; e[1] = v.y; e[2] = v.z; e[3] = v.w;
+    const float4 a = *reinterpret_cast<const float4*>(base + 4 * i);
+    const float4 b = *reinterpret_cast<const float4*>(base + 4 * i + 16);
+    e[0] = a.x; e[1] = a.y; e[2] = a.z; e[3] = a.w;
+    e[4] = b.x; e[5] = b.y; e[6] = b.z; e[7] = b.w;
   } else {
-    bf16x4_to_f32(*reinterpret_cast<const uint2*>(base + 2 * i), e);
+    bf16x8_to_f32(*reinterpret_cast<const uint4*>(base + 2 * i), e);
   }
 }
 
-// Keeps the revealed errors r of a chunk: decay * r, stored as fp32 or
-// rounded to bf16.  With decay 1 the product is r itself (exact for every
-// non-NaN value), so plain error feedback takes the same code.
+// Keeps the revealed errors r of a half in global memory at element index i
+// (a multiple of 8; the state buffer is 32-byte aligned): decay * r, stored
+// as fp32 (one 32-byte store) or rounded to bf16 (one 16-byte store).  With
+// decay 1 the product is r itself (exact for every non-NaN value), so plain
+// error feedback takes the same code.
 template <int SF>
-__device__ __forceinline__ void state_store4(uint8_t* base, int64_t i, const float r[4],
+__device__ __forceinline__ void state_store8(uint8_t* base, int64_t i, const float r[8],
                                              float decay) {
-  float t[4];
-  mul_ns<4>(t, r, decay);
+  float t[8];
+  mul_ns<8>(t, r, decay);
   if constexpr (SF == kStateF32) {
-    *reinterpret_cast<float4*>(base + 4 * i) = make_float4(t[0], t[1], t[2], t[3]);
+    asm volatile("st.global.v8.f32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
+                 :: "l"(base + 4 * i), "f"(t[0]), "f"(t[1]), "f"(t[2]), "f"(t[3]), "f"(t[4]),
+                    "f"(t[5]), "f"(t[6]), "f"(t[7]) : "memory");
   } else {
     float back[4];
-    *reinterpret_cast<uint2*>(base + 2 * i) = f32x4_to_bf16(t, back);
+    const uint2 lo = f32x4_to_bf16(t, back);
+    const uint2 hi = f32x4_to_bf16(t + 4, back);
+    *reinterpret_cast<uint4*>(base + 2 * i) = make_uint4(lo.x, lo.y, hi.x, hi.y);
   }
 }
 
-// Element offset, within a group, of chunk c (0..3) of lane q (0..NL-1) of
-// the group's NL lanes.
+// Element offset, within a group, of half h (0, 1) of lane q (0..NL-1) of the
+// group's NL lanes.
 template <int NL>
-__device__ __forceinline__ int chunk_at(int c, int q) { return 4 * NL * c + 4 * q; }
+__device__ __forceinline__ int half_at(int h, int q) { return 8 * NL * h + 8 * q; }
 
-// Byte offset, within a group's packed codes, of chunk c of lane q: 4 codes
-// of BITS bits each, stored contiguously.
+// Byte offset, within a group's packed codes, of half h of lane q: 8 codes of
+// BITS bits each, stored contiguously (4 or 8 bytes).
 template <int BITS, int NL>
-__device__ __forceinline__ int chunk_code_byte(int c, int q) { return chunk_at<NL>(c, q) * BITS / 8; }
+__device__ __forceinline__ int half_code_byte(int h, int q) { return half_at<NL>(h, q) * BITS / 8; }
 
 }  // namespace echo

@@ -37,17 +37,27 @@ template <int SF, int G>
 __device__ __forceinline__ void push_load(const uint8_t* sx, const uint8_t* se, int sub, int q,
                                           float v[16]) {
   constexpr int NL = G / 16;
-  const uint2* x2 = reinterpret_cast<const uint2*>(sx) + sub * (G / 4);
+  const uint4* x8 = reinterpret_cast<const uint4*>(sx);
 #pragma unroll
-  for (int c = 0; c < 4; ++c) bf16x4_to_f32(x2[chunk_at<NL>(c, q) / 4], v + 4 * c);
-  if constexpr (SF != kNoState) {
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      float e[4];
-      state_load4<SF>(se, sub * G + chunk_at<NL>(c, q), e);
-      add_n<4>(v + 4 * c, v + 4 * c, e);
+  for (int h = 0; h < 2; ++h) {
+    const int i = sub * G + half_at<NL>(h, q);
+    bf16x8_to_f32(x8[i / 8], v + 8 * h);
+    if constexpr (SF != kNoState) {
+      float e[8];
+      state_load8<SF>(se, i, e);
+      add_n<8>(v + 8 * h, v + 8 * h, e);
     }
   }
+}
+
+// The 8 codes of a half (integer-valued floats) packed into one word and
+// stored with an L2 policy: 32 bits for 4-bit codes, 64 for 8-bit.
+template <int BITS>
+__device__ __forceinline__ void store_codes8(uint8_t* p, const float c[8], uint64_t pol) {
+  uint32_t w0, w1;
+  pack8<BITS>(c, w0, w1);
+  if (BITS == 4) st_hint_u32(p, w0 | (w1 << 16), pol);
+  else st_hint_u64(p, (uint64_t)w0 | ((uint64_t)w1 << 32), pol);
 }
 
 // Quantizes group j of a sender's segment (all 32 lanes call it; lanes whose
@@ -62,25 +72,15 @@ __device__ __forceinline__ void push_finish(const CallArgs& a, const float v[16]
   constexpr int CB = G * BITS / 8;
   const GroupGrid gg = group_grid<MODE, NL>(v, L);
 #pragma unroll
-  for (int hh = 0; hh < 2; ++hh) {                 // chunks 2hh and 2hh+1
+  for (int hh = 0; hh < 2; ++hh) {                 // the lane's two halves
     float c[8], d[8];
     quantize8_mode<MODE>(v + 8 * hh, gg, L, c, d);
     if (valid) {
-      uint8_t* cg = cs + j * CB;
-      uint32_t w0, w1;
-      pack8<BITS>(c, w0, w1);
-      if (BITS == 4) {
-        st_hint_u16(cg + chunk_code_byte<4, NL>(2 * hh, q), w0, codes_pol);
-        st_hint_u16(cg + chunk_code_byte<4, NL>(2 * hh + 1, q), w1, codes_pol);
-      } else {
-        st_hint_u32(cg + chunk_code_byte<8, NL>(2 * hh, q), w0, codes_pol);
-        st_hint_u32(cg + chunk_code_byte<8, NL>(2 * hh + 1, q), w1, codes_pol);
-      }
+      store_codes8<BITS>(cs + j * CB + half_code_byte<BITS, NL>(hh, q), c, codes_pol);
       if constexpr (SF != kNoState) {
         float r[8];
         sub_n<8>(r, v + 8 * hh, d);
-        state_store4<SF>(es, j * G + chunk_at<NL>(2 * hh, q), r, a.decay);
-        state_store4<SF>(es, j * G + chunk_at<NL>(2 * hh + 1, q), r + 4, a.decay);
+        state_store8<SF>(es, j * G + half_at<NL>(hh, q), r, a.decay);
       }
     }
   }
@@ -193,7 +193,7 @@ __device__ __forceinline__ void reduce_tile(const CallArgs& a, const uint8_t* st
   const int P = a.P;
   const uint8_t* s_codes = stage;
   const uint32_t* s_meta = reinterpret_cast<const uint32_t*>(stage + (P - 1) * T * CB);
-  const uint2* s_x = reinterpret_cast<const uint2*>(stage + (P - 1) * T * (CB + 4));
+  const uint4* s_x = reinterpret_cast<const uint4*>(stage + (P - 1) * T * (CB + 4));
   const uint8_t* s_e = stage + (P - 1) * T * (CB + 4) + T * G * 2;         // [T] group states
   // The gather reads these codes next: keep them in L2.
   const uint64_t codes_pol = kCodesPolicyLast ? policy_evict_last() : policy_evict_normal();
@@ -213,22 +213,29 @@ __device__ __forceinline__ void reduce_tile(const CallArgs& a, const uint8_t* st
       unpack_meta(s_meta[js * T + gs], s, zf);
       const uint8_t* cg = s_codes + (js * T + gs) * CB;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const uint8_t* cw = cg + chunk_code_byte<BITS, NL>(c, q);
-        const uint32_t w = BITS == 4 ? (uint32_t)*reinterpret_cast<const uint16_t*>(cw)
-                                     : *reinterpret_cast<const uint32_t*>(cw);
-        decode4_mode<BITS, MODE>(w, s, zf, term + 4 * c);
+      for (int h = 0; h < 2; ++h) {
+        const uint8_t* cw = cg + half_code_byte<BITS, NL>(h, q);
+        if (BITS == 4) {
+          const uint32_t w = *reinterpret_cast<const uint32_t*>(cw);
+          decode4_mode<4, MODE>(w, s, zf, term + 8 * h);
+          decode4_mode<4, MODE>(w >> 16, s, zf, term + 8 * h + 4);
+        } else {
+          const uint2 w = *reinterpret_cast<const uint2*>(cw);
+          decode4_mode<8, MODE>(w.x, s, zf, term + 8 * h);
+          decode4_mode<8, MODE>(w.y, s, zf, term + 8 * h + 4);
+        }
       }
     };
     // The owner's own term: its bf16 input plus (compensated) its held error.
     auto own_term = [&](float term[16]) {
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        bf16x4_to_f32(s_x[(gs * G + chunk_at<NL>(c, q)) / 4], term + 4 * c);
+      for (int h = 0; h < 2; ++h) {
+        const int i = gs * G + half_at<NL>(h, q);
+        bf16x8_to_f32(s_x[i / 8], term + 8 * h);
         if constexpr (COMP) {
-          float e[4];
-          state_load4<SF>(s_e, gs * G + chunk_at<NL>(c, q), e);
-          add_n<4>(term + 4 * c, term + 4 * c, e);
+          float e[8];
+          state_load8<SF>(s_e, i, e);
+          add_n<8>(term + 8 * h, term + 8 * h, e);
         }
       }
     };
@@ -255,37 +262,24 @@ __device__ __forceinline__ void reduce_tile(const CallArgs& a, const uint8_t* st
     const GroupGrid gg = group_grid<MODE, NL>(acc, L);
     const int64_t grp = (int64_t)o * a.Gs + j0 + gl;           // group index in the rank tensor
 #pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {               // chunks 2hh and 2hh+1
+    for (int hh = 0; hh < 2; ++hh) {               // the lane's two halves
       float c[8], deq[8];
       quantize8_mode<MODE>(acc + 8 * hh, gg, L, c, deq);
       if (!valid) continue;
-      uint8_t* cg = a.codes2 + grp * CB;
-      uint32_t w0, w1;
-      pack8<BITS>(c, w0, w1);
-      if (BITS == 4) {
-        st_hint_u16(cg + chunk_code_byte<4, NL>(2 * hh, q), w0, codes_pol);
-        st_hint_u16(cg + chunk_code_byte<4, NL>(2 * hh + 1, q), w1, codes_pol);
-      } else {
-        st_hint_u32(cg + chunk_code_byte<8, NL>(2 * hh, q), w0, codes_pol);
-        st_hint_u32(cg + chunk_code_byte<8, NL>(2 * hh + 1, q), w1, codes_pol);
-      }
+      store_codes8<BITS>(a.codes2 + grp * CB + half_code_byte<BITS, NL>(hh, q), c, codes_pol);
       float yb[8];
       const uint2 ya = f32x4_to_bf16(deq, yb);
       const uint2 yv = f32x4_to_bf16(deq + 4, yb + 4);
-      const int64_t ea = grp * G + chunk_at<NL>(2 * hh, q);
-      const int64_t eb = grp * G + chunk_at<NL>(2 * hh + 1, q);
+      const int64_t e = grp * G + half_at<NL>(hh, q);
       if constexpr (COMP) {
         uint8_t* eo = reinterpret_cast<uint8_t*>(a.comp) + (int64_t)o * a.n * EB;
         float r[8];
         sub_n<8>(r, acc + 8 * hh, yb);
-        state_store4<SF>(eo, ea, r, a.decay);
-        state_store4<SF>(eo, eb, r + 4, a.decay);
+        state_store8<SF>(eo, e, r, a.decay);
       }
       if (FUSED) {
-        for (int r = 0; r < P; ++r) {
-          __stcs(reinterpret_cast<uint2*>(a.out[r] + ea), ya);
-          __stcs(reinterpret_cast<uint2*>(a.out[r] + eb), yv);
-        }
+        const uint4 y = make_uint4(ya.x, ya.y, yv.x, yv.y);
+        for (int r = 0; r < P; ++r) __stcs(reinterpret_cast<uint4*>(a.out[r] + e), y);
       }
     }
     if (valid && q == 0) {

@@ -113,12 +113,11 @@ __device__ __forceinline__ bool mbar_wait_block(uint32_t bar, uint32_t parity) {
 
 // Global stores with an L2 cache policy (createpolicy): the codes written by
 // one kernel and read by the next are kept in L2 with evict_last.
-__device__ __forceinline__ void st_hint_u16(void* p, uint32_t v, uint64_t pol) {
-  asm volatile("st.global.L2::cache_hint.b16 [%0], %1, %2;"
-               :: "l"(p), "h"((unsigned short)v), "l"(pol) : "memory");
-}
 __device__ __forceinline__ void st_hint_u32(void* p, uint32_t v, uint64_t pol) {
   asm volatile("st.global.L2::cache_hint.b32 [%0], %1, %2;" :: "l"(p), "r"(v), "l"(pol) : "memory");
+}
+__device__ __forceinline__ void st_hint_u64(void* p, uint64_t v, uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.b64 [%0], %1, %2;" :: "l"(p), "l"(v), "l"(pol) : "memory");
 }
 
 }  // namespace echo

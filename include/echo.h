@@ -60,7 +60,8 @@ extern "C" {
                                    aliasing other than out[p] == in[p], wrong device */
 #define ECHO_ERR_SHAPE       2  /* n < 0, or n not a multiple of P*g */
 #define ECHO_ERR_UNSUPPORTED 3  /* bits not 4 or 8, or g not 64, 128 or 256 */
-#define ECHO_ERR_ALIGN       4  /* a device pointer not 16-byte aligned */
+#define ECHO_ERR_ALIGN       4  /* an input or output not 16-byte aligned, or a
+                                   compensator state not 32-byte aligned */
 #define ECHO_ERR_CUDA        5  /* a CUDA runtime call failed */
 #define ECHO_ERR_OVERFLOW    6  /* (status word) a non-finite input or an fp16 step overflow */
 #define ECHO_ERR_TIMEOUT     7  /* (status word) a device-side wait gave up */
@@ -101,7 +102,7 @@ int echo_plan(int P, int64_t n, int g, int bits, echo_plan_t* out);
  *   comp_state  NULL: uncompensated call (no state read or written);
  *               ECHO_COMP_DEFAULT: the plan's own state;
  *               otherwise a caller device buffer of echo_comp_bytes(plan) bytes,
- *               16-byte aligned, laid out [P][n] (rank p's error for its
+ *               32-byte aligned, laid out [P][n] (rank p's error for its
  *               element i at p*n + i) in fp32, or bf16 after echo_set_state,
  *               zero before the first call of a sequence;
  *               read and updated in place.
@@ -215,6 +216,7 @@ int echo_set_timing(echo_plan_t plan, void* const* events, int count);
  *               4-bit codes fits up to 2048 x 4096 elements per rank.
  *   in, out     as for echo_allreduce (same alignment and aliasing rules).
  *   comp_state  NULL (uncompensated) or a caller device buffer of P*n*4 bytes,
+ *               32-byte aligned,
  *               fp32 [P][n], as for echo_allreduce; ECHO_COMP_DEFAULT is
  *               rejected (ECHO_ERR_ARG) since there is no plan.
  *   stream      cudaStream_t as void*.
