@@ -55,7 +55,7 @@ def _load():
         lib.oracle_f32_to_bf16_rn.argtypes = [ctypes.c_float]
         lib.oracle_f32_to_bf16_rn.restype = ctypes.c_uint16
         for fn in ("oracle_f32_to_f16_ru_n", "oracle_f16_to_f32_n", "oracle_f32_to_bf16_rn_n",
-                   "oracle_f32_to_f16_rd_n"):
+                   "oracle_f32_to_f16_rd_n", "oracle_f32_to_f16_rn_n"):
             getattr(lib, fn).argtypes = [P, i64, P]
             getattr(lib, fn).restype = None
         lib.oracle_quantize_group.argtypes = [P, i32, i32, P, P, P, P]
@@ -102,6 +102,14 @@ def f32_to_f16_ru(x: np.ndarray) -> np.ndarray:
     return out
 
 
+def f32_to_f16_rn(x: np.ndarray) -> np.ndarray:
+    """float32 -> binary16 bits, round to nearest, ties to even."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    out = np.empty(x.shape, np.uint16)
+    _load().oracle_f32_to_f16_rn_n(_ptr(x), x.size, _ptr(out))
+    return out
+
+
 def f32_to_f16_rd(x: np.ndarray) -> np.ndarray:
     """binary32 -> binary16 bits, rounding toward -infinity (element-wise)."""
     x = np.ascontiguousarray(x, dtype=np.float32).ravel()
@@ -137,6 +145,8 @@ def bf16_to_f32(b: np.ndarray) -> np.ndarray:
 # Quantizer variants: the method's zero-aware asymmetric quantizer and the two
 # ablations of Table 8 ("naive zero-point", "symmetric grid").
 ZERO_AWARE, NAIVE_ZERO_POINT, SYMMETRIC = 0, 1, 2
+# Compensator state storage (the value kept for each revealed error).
+STATE_F32, STATE_BF16, STATE_F16 = 0, 1, 2
 
 def quantize_group(v: np.ndarray, bits: int, mode: int = ZERO_AWARE):
     """Q_b on one group.  Returns (codes uint8, s_bits, z_bits, flagged, ties);
@@ -197,9 +207,16 @@ def group_position(P: int, owner: int, bits: int, x: np.ndarray, e: np.ndarray |
     return r
 
 
+def _state_fmt(bf16_state: bool, state_fmt: int | None) -> int:
+    fmt = (STATE_BF16 if bf16_state else STATE_F32) if state_fmt is None else state_fmt
+    if fmt not in (STATE_F32, STATE_BF16, STATE_F16):
+        raise ValueError(f"state format {fmt}")
+    return fmt
+
+
 def group_positions(P: int, owners: np.ndarray, bits: int, x: np.ndarray,
                     e: np.ndarray | None, want_wire: bool = False, mode: int = ZERO_AWARE,
-                    bf16_state: bool = False, decay: float = 1.0):
+                    bf16_state: bool = False, decay: float = 1.0, state_fmt: int | None = None):
     """Many independent group positions at once.
 
     owners [npos] int; x [npos, P, len] bf16 bits; e [npos, P, len] float32
@@ -218,7 +235,8 @@ def group_positions(P: int, owners: np.ndarray, bits: int, x: np.ndarray,
         r.update(q1=np.zeros((npos, P, ln), np.uint8), m1=np.zeros((npos, P), np.uint32),
                  q2=np.zeros((npos, ln), np.uint8), m2=np.zeros(npos, np.uint32))
     ties = ctypes.c_int64(0)
-    bad = lib.oracle_group_positions_ex(P, npos, _ptr(owners), ln, bits, mode, int(bf16_state),
+    bad = lib.oracle_group_positions_ex(P, npos, _ptr(owners), ln, bits, mode,
+                                        _state_fmt(bf16_state, state_fmt),
                                         decay, _ptr(x), _ptr(e), _ptr(r["y"]), _ptr(r.get("q1")),
                                         _ptr(r.get("m1")), _ptr(r.get("q2")), _ptr(r.get("m2")),
                                         ctypes.byref(ties))
@@ -231,13 +249,15 @@ def group_positions(P: int, owners: np.ndarray, bits: int, x: np.ndarray,
 
 def allreduce(x: np.ndarray, g: int, bits: int, e: np.ndarray | None = None,
               want_wire: bool = False, want_acc: bool = False, want_nq: bool = False,
-              mode: int = ZERO_AWARE, bf16_state: bool = False, decay: float = 1.0):
+              mode: int = ZERO_AWARE, bf16_state: bool = False, decay: float = 1.0,
+              state_fmt: int | None = None):
     """One emulated all-reduce call.
 
     x: [P, n] uint16 bf16 bits.  e: [P, n] float32 compensator state, updated IN
-    PLACE, or None for an uncompensated call.  With bf16_state the state keeps
-    bf16-rounded values (still in the float32 array); decay scales each revealed
-    error before it is kept.  Returns a dict with ``out``
+    PLACE, or None for an uncompensated call.  state_fmt (STATE_F32, STATE_BF16,
+    STATE_F16; bf16_state=True is STATE_BF16) makes the state keep values
+    rounded to that type (still in the float32 array); decay scales each
+    revealed error before it is kept.  Returns a dict with ``out``
     ([P, n] bf16 bits), ``flagged``, ``ties`` and, on request, the wire codes in
     the oracle's canonical layout (q1 [P, n], m1 [P, P, Gs], q2 [n], m2 [P, Gs]),
     the owner sums ``acc`` [n] and the quantization counts ``nq`` [P, n].
@@ -258,7 +278,7 @@ def allreduce(x: np.ndarray, g: int, bits: int, e: np.ndarray | None = None,
     if want_nq:
         r["nq"] = np.zeros((P, n), np.uint8)
     ties = ctypes.c_int64(0)
-    bad = lib.oracle_allreduce_ex(P, n, g, bits, mode, int(bf16_state), decay, _ptr(x),
+    bad = lib.oracle_allreduce_ex(P, n, g, bits, mode, _state_fmt(bf16_state, state_fmt), decay, _ptr(x),
                                   _ptr(r["out"]), _ptr(e),
                                     _ptr(r.get("q1")), _ptr(r.get("m1")), _ptr(r.get("q2")),
                                     _ptr(r.get("m2")), _ptr(r.get("acc")), _ptr(r.get("nq")),

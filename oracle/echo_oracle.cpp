@@ -176,6 +176,30 @@ void oracle_f32_to_f16_rd_n(const float* x, int64_t count, uint16_t* out) {
   for (int64_t i = 0; i < count; ++i) out[i] = oracle_f32_to_f16_rd(x[i]);
 }
 
+// binary32 -> binary16, round to nearest, ties to even: whichever of the two
+// directed roundings lies nearer to x (distances compared exactly in double,
+// where every binary16 and binary32 value and their differences here are
+// exact); on a tie, the one whose last significand bit is 0.  Beyond the
+// largest finite value the next step up is taken to be 2^16 (as IEEE rounding
+// does), so x >= 65520 rounds to infinity.  NaN stays NaN.
+uint16_t oracle_f32_to_f16_rn(float x) {
+  const uint16_t up = oracle_f32_to_f16_ru(x);
+  if (x != x) return up;
+  const uint16_t dn = oracle_f32_to_f16_rd(x);
+  if (up == dn) return up;
+  const double xd = (double)x;
+  const double vu = up == 0x7C00 ? 65536.0 : (double)oracle_f16_to_f32(up);
+  const double vd = dn == 0xFC00 ? -65536.0 : (double)oracle_f16_to_f32(dn);
+  const double du = vu - xd, dd = xd - vd;
+  if (du < dd) return up;
+  if (dd < du) return dn;
+  return (up & 1) == 0 ? up : dn;
+}
+
+void oracle_f32_to_f16_rn_n(const float* x, int64_t count, uint16_t* out) {
+  for (int64_t i = 0; i < count; ++i) out[i] = oracle_f32_to_f16_rn(x[i]);
+}
+
 // Quantizer variants (a mode argument where the functions take one).
 enum { kZeroAware = 0, kNaiveZeroPoint = 1, kSymmetric = 2 };
 
@@ -362,14 +386,17 @@ void oracle_pack_codes(const uint8_t* q, int64_t count, int bits, uint8_t* out) 
 // Returns the number of quantizations flagged non-finite (0 when all is fine).
 // ---------------------------------------------------------------------------
 // The value the state keeps for a revealed error r: decay * r (one fp32
-// multiply), rounded to bf16 when the state is stored in bf16.  The state
-// array itself stays fp32 (holding bf16 values in that case).
-static float keep_error(float r, int bf16_state, float decay) {
+// multiply), rounded to nearest-even bf16 or fp16 when the state is stored in
+// that type (state_fmt 1 or 2; 0 is fp32).  The state array itself stays fp32
+// (holding bf16 or fp16 values in those cases).
+static float keep_error(float r, int state_fmt, float decay) {
   const float t = decay * r;
-  return bf16_state ? oracle_bf16_to_f32(oracle_f32_to_bf16_rn(t)) : t;
+  if (state_fmt == 1) return oracle_bf16_to_f32(oracle_f32_to_bf16_rn(t));
+  if (state_fmt == 2) return oracle_f16_to_f32(oracle_f32_to_f16_rn(t));
+  return t;
 }
 
-int oracle_group_position_ex(int P, int o, int len, int bits, int mode, int bf16_state,
+int oracle_group_position_ex(int P, int o, int len, int bits, int mode, int state_fmt,
                              float decay, const uint16_t* x, float* e, uint16_t* y,
                              uint8_t* q1, uint32_t* m1, uint8_t* q2, uint32_t* m2,
                              float* acc_out, uint8_t* nq, int64_t* ties) {
@@ -395,7 +422,7 @@ int oracle_group_position_ex(int P, int o, int len, int bits, int mode, int bf16
     if (m1) m1[p] = (uint32_t)sb | ((uint32_t)zb << 16);
     if (nq) for (int i = 0; i < len; ++i) nq[(size_t)p * len + i] += 1;
     // The push reveals this rank's stage-1 error; the rank keeps it.
-    if (ep) for (int i = 0; i < len; ++i) ep[i] = keep_error(v[i] - dp[i], bf16_state, decay);
+    if (ep) for (int i = 0; i < len; ++i) ep[i] = keep_error(v[i] - dp[i], state_fmt, decay);
   }
 
   // The owner's own copy is not quantized; its entry pass adds its held error.
@@ -427,7 +454,7 @@ int oracle_group_position_ex(int P, int o, int len, int bits, int mode, int bf16
   // The owner keeps the stage-2 error, measured against what ranks receive.
   if (e) {
     float* eo = e + (size_t)o * len;
-    for (int i = 0; i < len; ++i) eo[i] = keep_error(acc[i] - oracle_bf16_to_f32(y[i]), bf16_state, decay);
+    for (int i = 0; i < len; ++i) eo[i] = keep_error(acc[i] - oracle_bf16_to_f32(y[i]), state_fmt, decay);
   }
   return bad;
 }
@@ -454,7 +481,7 @@ int oracle_group_position(int P, int o, int len, int bits, const uint16_t* x,
 //   q1 [npos][P][len], m1 [npos][P], q2 [npos][len], m2 [npos] (each or NULL).
 // Returns the number of flagged quantizations, or -1 for invalid arguments.
 int64_t oracle_group_positions_ex(int P, int64_t npos, const int* owners, int len,
-                                  int bits, int mode, int bf16_state, float decay,
+                                  int bits, int mode, int state_fmt, float decay,
                                   const uint16_t* x, float* e, uint16_t* y,
                                   uint8_t* q1, uint32_t* m1, uint8_t* q2,
                                   uint32_t* m2, int64_t* ties) {
@@ -463,7 +490,7 @@ int64_t oracle_group_positions_ex(int P, int64_t npos, const int* owners, int le
   int64_t bad = 0;
   for (int64_t k = 0; k < npos; ++k) {
     if (owners[k] < 0 || owners[k] >= P) return -1;
-    bad += oracle_group_position_ex(P, owners[k], len, bits, mode, bf16_state, decay, x + k * blk,
+    bad += oracle_group_position_ex(P, owners[k], len, bits, mode, state_fmt, decay, x + k * blk,
                                       e ? e + k * blk : nullptr, y + k * len,
                                       q1 ? q1 + k * blk : nullptr, m1 ? m1 + k * P : nullptr,
                                       q2 ? q2 + k * len : nullptr, m2 ? m2 + k : nullptr,
@@ -504,7 +531,7 @@ int64_t oracle_group_positions(int P, int64_t npos, const int* owners, int len,
 //   ties               exact-tie counter, or NULL
 // Returns the number of flagged quantizations, or -1 for invalid arguments.
 // ---------------------------------------------------------------------------
-int64_t oracle_allreduce_ex(int P, int64_t n, int g, int bits, int mode, int bf16_state,
+int64_t oracle_allreduce_ex(int P, int64_t n, int g, int bits, int mode, int state_fmt,
                             float decay, const uint16_t* x,
                             uint16_t* out, float* e, uint8_t* q1, uint32_t* m1,
                             uint8_t* q2, uint32_t* m2, float* acc, uint8_t* nq,
@@ -533,7 +560,7 @@ int64_t oracle_allreduce_ex(int P, int64_t n, int g, int bits, int mode, int bf1
         }
       }
       uint32_t m2g = 0;
-      bad += oracle_group_position_ex(P, o, len, bits, mode, bf16_state, decay, xg.data(),
+      bad += oracle_group_position_ex(P, o, len, bits, mode, state_fmt, decay, xg.data(),
                                       e ? eg.data() : nullptr, yg.data(), q1g.data(), m1g.data(),
                                       q2g.data(), &m2g, accg.data(), nqg.data(), ties);
       for (int p = 0; p < P; ++p) {

@@ -30,6 +30,22 @@ def _sweep_f32(stride=4099, seed=0):
     return np.concatenate([allpos, allpos | np.uint32(0x80000000)]).view(np.float32)
 
 
+def test_f16_round_nearest_even_matches_numpy():
+    """Round to nearest, ties to even (the compensator's fp16 state), against
+    numpy's float16 cast; the sweep adds every exact midpoint between
+    consecutive binary16 values (the ties) and the overflow threshold 65520."""
+    h = np.arange(0, 0x7C00, dtype=np.uint16).view(np.float16).astype(np.float64)
+    mids = ((h[:-1] + h[1:]) / 2).astype(np.float32)
+    assert np.array_equal(mids.astype(np.float64), (h[:-1] + h[1:]) / 2)      # exact in fp32
+    x = np.concatenate([_sweep_f32(), mids, -mids,
+                        np.array([65520.0, -65520.0, 65519.996, np.inf, -np.inf], np.float32)])
+    with np.errstate(over="ignore"):
+        want = x.astype(np.float16).view(np.uint16)
+    got = oracle.f32_to_f16_rn(x)
+    assert np.array_equal(got, want)
+    assert np.isnan(oracle.f32_to_f16_rn(np.array([np.nan], np.float32)).view(np.float16)[0])
+
+
 def test_f16_round_up_is_least_upper_bound():
     x = _sweep_f32()
     r = oracle.f32_to_f16_ru(x).view(np.float16)
