@@ -208,11 +208,19 @@ def whole_job_gbs(bytes_per_rank_per_step: float, steps: int, world: int, max_ms
 
 # ------------------------------------------------------------- our arm -------
 
+STATE_FMT = {"f32": 0, "bf16": 1, "f16": 2}            # ECHO_STATE_* codes
+STATE_NAME = {"f32": "fp32", "bf16": "bf16", "f16": "fp16"}
+
+
+def state_dtype(args):
+    import torch
+    return {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}[args.state]
+
+
 def set_state(echo, plan, args):
     """Applies --state/--decay to a plan; returns the state's bytes per element."""
-    bf16 = args.state == "bf16"
-    echo.echo_set_state(plan, echo.ECHO_STATE_BF16 if bf16 else echo.ECHO_STATE_F32, args.decay)
-    return 2 if bf16 else 4
+    echo.echo_set_state(plan, STATE_FMT[args.state], args.decay)
+    return 4 if args.state == "f32" else 2
 
 
 def build_inputs(number, seq, distinct, device):
@@ -248,7 +256,7 @@ def run_ours(args, rank, local, world):
     echo.echo_set_quantizer(plan, args.quantizer)
     echo.echo_set_persistent(plan, args.persistent)
     sb = set_state(echo, plan, args)
-    sdt = torch.bfloat16 if sb == 2 else torch.float32
+    sdt = state_dtype(args)
     states = {"fwd": echo.COMP_DEFAULT,
               "bwd": torch.zeros((P, n), dtype=sdt, device=dev) if any(
                   c.state == "bwd" for c in seq) else None,
@@ -342,9 +350,9 @@ def run_ours(args, rank, local, world):
                    "calls_per_step": calls, "compensated": compensated_calls == calls,
                    "fused_gather": bool(fused), "quantizer": QUANTIZERS[args.quantizer],
                    "schedule": "one persistent kernel" if args.persistent else "three kernels",
-                   "state": {"format": "bf16" if sb == 2 else "fp32", "decay": args.decay},
+                   "state": {"format": STATE_NAME[args.state], "decay": args.decay},
                    "io": "bf16 in/out, fp32 arithmetic, "
-                   f"{bits}-bit codes, {'bf16' if sb == 2 else 'fp32'} state",
+                   f"{bits}-bit codes, {STATE_NAME[args.state]} state",
                    "l2": f"inputs distinct per call ({calls} x {P * n * 2 >> 20} MiB resident); "
                          f"per-call working set {(P * n * (2 + 2 + 2 * sb)) >> 20} MiB > L2",
                    "parallelism": f"replicas x{world}" if world > 1 else "1 GPU, P ranks emulated"},
@@ -447,7 +455,7 @@ def time_other(echo, number, bits, fused, dev, args, reps=3):
     echo.echo_set_quantizer(plan, args.quantizer)
     echo.echo_set_persistent(plan, args.persistent)
     sb = set_state(echo, plan, args)
-    bwd = torch.zeros((w.P, w.n), dtype=torch.bfloat16 if sb == 2 else torch.float32, device=dev)
+    bwd = torch.zeros((w.P, w.n), dtype=state_dtype(args), device=dev)
     comps = [{"fwd": echo.COMP_DEFAULT, "bwd": bwd, "none": None}[c.state] for c in seq]
     rows = [list(xs[k]) for k in range(distinct)]
     out_rows = list(out)
@@ -485,13 +493,13 @@ class OracleSample:
     positions -- exactly the oracle's work on them, since positions are
     independent -- with 4 distinct inputs cycled and the state carried."""
 
-    def __init__(self, number, bits, g=G, mode=0, bf16_state=False, decay=1.0):
+    def __init__(self, number, bits, g=G, mode=0, state_fmt=0, decay=1.0):
         import numpy as np
         import torch
         from bit_error_compensated_gb300.workloads import WORKLOADS, call_sequence, rank_inputs
         w = WORKLOADS[number]
         self.w, self.bits, self.P = w, bits, w.P
-        self.opts = dict(mode=mode, bf16_state=bf16_state, decay=decay)
+        self.opts = dict(mode=mode, state_fmt=state_fmt, decay=decay)
         seq = call_sequence(number, steps=1)
         Gs = w.n // w.P // g
         rng = np.random.default_rng(number)
@@ -518,7 +526,7 @@ class OracleSample:
 
 def oracle_sample(args):
     """OracleSample of the workload and options the GPU arm runs."""
-    return OracleSample(args.workload, args.bits, args.g, args.quantizer, args.state == "bf16",
+    return OracleSample(args.workload, args.bits, args.g, args.quantizer, STATE_FMT[args.state],
                         args.decay)
 
 
@@ -555,7 +563,7 @@ def run_reference(args, rank, world):
             "data": "synthetic (seeded; shapes and distributions of the workload, no dataset)",
             "config": {"workload": w.name, "P": w.P, "n_per_rank": w.n, "bits": args.bits, "g": args.g,
                        "compensated": True, "quantizer": QUANTIZERS[args.quantizer],
-                       "state": {"format": "bf16" if args.state == "bf16" else "fp32",
+                       "state": {"format": STATE_NAME[args.state],
                                  "decay": args.decay}},
             "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
                              "sample": s.sample},
@@ -588,15 +596,15 @@ def run_accuracy(args):
     x = torch.empty((P, n), dtype=torch.bfloat16, device=dev)
     out = torch.empty_like(x)
     rows = {}
-    # (quantizer, compensated, bf16 state, decay)
-    variants = [(qz, comp, False, 1.0) for qz in (0, 1, 2) for comp in (True, False)]
-    variants += [(0, True, True, 1.0), (0, True, False, 0.9), (0, True, True, 0.9)]
-    for qz, compensated, bf16_state, decay in variants:
+    # (quantizer, compensated, state format, decay)
+    variants = [(qz, comp, "f32", 1.0) for qz in (0, 1, 2) for comp in (True, False)]
+    variants += [(0, True, "bf16", 1.0), (0, True, "f16", 1.0), (0, True, "f32", 0.9),
+                 (0, True, "bf16", 0.9)]
+    for qz, compensated, fmt, decay in variants:
         plan = echo.echo_plan(P, n, args.g, bits)
         echo.echo_set_quantizer(plan, qz)
-        echo.echo_set_state(plan, echo.ECHO_STATE_BF16 if bf16_state else echo.ECHO_STATE_F32,
-                            decay)
-        sdt = torch.bfloat16 if bf16_state else torch.float32
+        echo.echo_set_state(plan, STATE_FMT[fmt], decay)
+        sdt = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}[fmt]
         states = {}
         drift = torch.zeros(n, dtype=torch.float64, device=dev)
         rel, scale = [], None
@@ -615,8 +623,8 @@ def run_accuracy(args):
         if echo.echo_get_status(plan) != 0:
             raise RuntimeError("status word set")
         label = f"{QUANTIZERS[qz]}, {'compensated' if compensated else 'uncompensated'}"
-        if bf16_state or decay != 1.0:
-            label += f" ({'bf16' if bf16_state else 'fp32'} state, decay {decay})"
+        if fmt != "f32" or decay != 1.0:
+            label += f" ({STATE_NAME[fmt]} state, decay {decay})"
         rows[label] = {
             "per_call_rel_rms": round(sum(rel) / len(rel), 6),
             "drift_rel_rms": round(float(drift.square().mean().sqrt()) / scale, 6)}
@@ -643,8 +651,8 @@ def main(argv=None):
                     help="one persistent kernel per call instead of three")
     ap.add_argument("--quantizer", type=int, default=0, choices=[0, 1, 2],
                     help="0 zero-aware (the method), 1 naive zero-point, 2 symmetric grid")
-    ap.add_argument("--state", choices=["f32", "bf16"], default="f32",
-                    help="compensator state storage (bf16 halves its traffic)")
+    ap.add_argument("--state", choices=["f32", "bf16", "f16"], default="f32",
+                    help="compensator state storage (bf16 or fp16 halve its traffic)")
     ap.add_argument("--decay", type=float, default=1.0,
                     help="kept error = decay x revealed error (1 = plain error feedback)")
     ap.add_argument("--also", default="4", help="other workloads to time, comma-separated ('' for none)")

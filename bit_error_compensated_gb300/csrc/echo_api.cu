@@ -23,7 +23,7 @@ struct echo_plan_s {
   cudaStream_t last_stream = nullptr;
   int fused = 1;                    // the reduce kernel writes the outputs (no gather kernel)
   int mode = ECHO_QUANT_ZERO_AWARE;
-  int state_bf16 = 0;               // ECHO_STATE_BF16 selected
+  int state_fmt = ECHO_STATE_F32;   // ECHO_STATE_*
   float decay = 1.0f;
   int persistent = 0;               // one persistent kernel per call (k_call.cu)
   uint32_t* sched = nullptr;        // its schedule words, zero between calls
@@ -209,7 +209,7 @@ int echo_allreduce(echo_plan_t plan, const void* const* in, void* const* out,
   a.Gs_pad = plan->Gs_pad;
   a.P = P;
   a.mode = plan->mode;
-  a.state_bf16 = plan->state_bf16;
+  a.state_fmt = plan->state_fmt;
   a.decay = plan->decay;
 
   // Programmatic dependent launch lets each kernel's blocks be scheduled while
@@ -333,19 +333,20 @@ int echo_set_quantizer(echo_plan_t plan, int mode) {
 }
 
 int echo_set_state(echo_plan_t plan, int format, float decay) {
-  if (plan == nullptr || (format != ECHO_STATE_F32 && format != ECHO_STATE_BF16)) return ECHO_ERR_ARG;
+  if (plan == nullptr || (format != ECHO_STATE_F32 && format != ECHO_STATE_BF16 &&
+                          format != ECHO_STATE_F16))
+    return ECHO_ERR_ARG;
   if (!(decay > 0.0f && decay <= 1.0f)) return ECHO_ERR_ARG;      // also rejects NaN
-  const int bf16 = format == ECHO_STATE_BF16;
-  if (bf16 != plan->state_bf16) {
+  if (format != plan->state_fmt) {
     int rc = check_device(plan);
     if (rc != ECHO_OK) return rc;
-    // The held values mean nothing in the other format: start from zero.  The
-    // allocation (fp32-sized) serves both.
+    // The held values mean nothing in another format: start from zero.  The
+    // allocation (fp32-sized) serves every format.
     if (plan->comp != nullptr && plan->comp_bytes > 0)
       ECHO_CUDA(cudaMemsetAsync(plan->comp, 0, (size_t)plan->P * plan->n * sizeof(float),
                                 plan->last_stream));
-    plan->state_bf16 = bf16;
-    plan->comp_bytes = (size_t)plan->P * plan->n * (bf16 ? 2 : 4);
+    plan->state_fmt = format;
+    plan->comp_bytes = (size_t)plan->P * plan->n * (format == ECHO_STATE_F32 ? 4 : 2);
   }
   plan->decay = decay;
   return ECHO_OK;

@@ -60,7 +60,7 @@ struct CallArgs {
   int64_t Gs_pad;      // Gs rounded up to a multiple of 4
   int P;
   int mode;            // quantizer: 0 zero-aware (the method), 1 naive zero point, 2 symmetric
-  int state_bf16;      // the state at comp is bf16 (else fp32)
+  int state_fmt;       // format of the state at comp: 0 fp32, 1 bf16, 2 fp16
   float decay;         // the kept error is decay * (revealed error); 1 = plain feedback
 };
 

@@ -115,7 +115,7 @@ extern "C" int echo_allreduce_noalloc(int P, int64_t n, int bits, const void* co
   a.Gs = Gs;
   a.Gs_pad = Gs_pad;
   a.P = P;
-  a.state_bf16 = 0;            // fp32 state, plain error feedback
+  a.state_fmt = 0;             // fp32 state, plain error feedback
   a.decay = 1.0f;
 
   // The kernels only OR flags into the status word; it is the one part of the

@@ -356,16 +356,18 @@ cudaError_t launch_t(const CallArgs& a, const CallSched& sch, cudaStream_t s) {
 template <int MODE, int G>
 cudaError_t launch_mode(const CallArgs& a, const CallSched& sch, int bits, bool fused,
                         cudaStream_t s) {
-  const int sf = a.comp == nullptr ? kNoState : (a.state_bf16 ? kStateBF16 : kStateF32);
+  const int sf = state_fmt_of(a.comp, a.state_fmt);
 #define ECHO_CALL_SF(B, SFV)                                                                 \
   return fused ? launch_t<B, SFV, MODE, G, true>(a, sch, s) : launch_t<B, SFV, MODE, G, false>(a, sch, s);
   if (bits == 4) {
     if (sf == kStateF32) { ECHO_CALL_SF(4, kStateF32) }
     if (sf == kStateBF16) { ECHO_CALL_SF(4, kStateBF16) }
+    if (sf == kStateF16) { ECHO_CALL_SF(4, kStateF16) }
     ECHO_CALL_SF(4, kNoState)
   }
   if (sf == kStateF32) { ECHO_CALL_SF(8, kStateF32) }
   if (sf == kStateBF16) { ECHO_CALL_SF(8, kStateBF16) }
+  if (sf == kStateF16) { ECHO_CALL_SF(8, kStateF16) }
   ECHO_CALL_SF(8, kNoState)
 #undef ECHO_CALL_SF
 }

@@ -163,14 +163,16 @@ cudaError_t launch_t(const CallArgs& a, cudaStream_t s, bool pdl) {
 
 template <int MODE, int G>
 cudaError_t launch_mode(const CallArgs& a, int bits, cudaStream_t s, bool pdl) {
-  const int sf = a.comp == nullptr ? kNoState : (a.state_bf16 ? kStateBF16 : kStateF32);
+  const int sf = state_fmt_of(a.comp, a.state_fmt);
   if (bits == 4) {
     if (sf == kStateF32) return launch_t<4, kStateF32, MODE, G>(a, s, pdl);
     if (sf == kStateBF16) return launch_t<4, kStateBF16, MODE, G>(a, s, pdl);
+    if (sf == kStateF16) return launch_t<4, kStateF16, MODE, G>(a, s, pdl);
     return launch_t<4, kNoState, MODE, G>(a, s, pdl);
   }
   if (sf == kStateF32) return launch_t<8, kStateF32, MODE, G>(a, s, pdl);
   if (sf == kStateBF16) return launch_t<8, kStateBF16, MODE, G>(a, s, pdl);
+  if (sf == kStateF16) return launch_t<8, kStateF16, MODE, G>(a, s, pdl);
   return launch_t<8, kNoState, MODE, G>(a, s, pdl);
 }
 

@@ -164,17 +164,19 @@ cudaError_t set_attr() {
 
 template <int MODE, int G>
 cudaError_t launch_mode(const CallArgs& a, int bits, bool fused, cudaStream_t s, bool pdl) {
-  const int sf = a.comp == nullptr ? kNoState : (a.state_bf16 ? kStateBF16 : kStateF32);
+  const int sf = state_fmt_of(a.comp, a.state_fmt);
 #define ECHO_REDUCE_SF(B, SFV)                                                            \
   return fused ? launch_t<B, SFV, true, MODE, G>(a, s, pdl)                               \
                : launch_t<B, SFV, false, MODE, G>(a, s, pdl);
   if (bits == 4) {
     if (sf == kStateF32) { ECHO_REDUCE_SF(4, kStateF32) }
     if (sf == kStateBF16) { ECHO_REDUCE_SF(4, kStateBF16) }
+    if (sf == kStateF16) { ECHO_REDUCE_SF(4, kStateF16) }
     ECHO_REDUCE_SF(4, kNoState)
   }
   if (sf == kStateF32) { ECHO_REDUCE_SF(8, kStateF32) }
   if (sf == kStateBF16) { ECHO_REDUCE_SF(8, kStateBF16) }
+  if (sf == kStateF16) { ECHO_REDUCE_SF(8, kStateF16) }
   ECHO_REDUCE_SF(8, kNoState)
 #undef ECHO_REDUCE_SF
 }
@@ -185,8 +187,8 @@ cudaError_t prepare_mode() {
 #define ECHO_PREP(B, SFV)                                                                 \
   if ((r = set_attr<B, SFV, true, MODE, G>()) != cudaSuccess) e = r;                      \
   if ((r = set_attr<B, SFV, false, MODE, G>()) != cudaSuccess) e = r;
-  ECHO_PREP(4, kNoState) ECHO_PREP(4, kStateF32) ECHO_PREP(4, kStateBF16)
-  ECHO_PREP(8, kNoState) ECHO_PREP(8, kStateF32) ECHO_PREP(8, kStateBF16)
+  ECHO_PREP(4, kNoState) ECHO_PREP(4, kStateF32) ECHO_PREP(4, kStateBF16) ECHO_PREP(4, kStateF16)
+  ECHO_PREP(8, kNoState) ECHO_PREP(8, kStateF32) ECHO_PREP(8, kStateBF16) ECHO_PREP(8, kStateF16)
 #undef ECHO_PREP
   return e;
 }

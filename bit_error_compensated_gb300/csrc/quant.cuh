@@ -431,12 +431,19 @@ __device__ __forceinline__ uint2 f32x4_to_bf16(const float f[4], float back[4]) 
   return r;
 }
 
-// Storage of the compensator state: none (uncompensated), fp32, or bf16
-// (rounded to nearest even).  Element i of rank p lives at p*n + i either way.
-enum StateFmt : int { kNoState = 0, kStateF32 = 1, kStateBF16 = 2 };
+// Storage of the compensator state: none (uncompensated), fp32, or bf16 or
+// fp16 (each rounded to nearest even).  Element i of rank p lives at p*n + i
+// in every format.
+enum StateFmt : int { kNoState = 0, kStateF32 = 1, kStateBF16 = 2, kStateF16 = 3 };
+
+// The state format of a call: its comp pointer and the plan's format code
+// (0 fp32, 1 bf16, 2 fp16).
+__host__ __device__ inline int state_fmt_of(const void* comp, int code) {
+  return comp == nullptr ? kNoState : code == 1 ? kStateBF16 : code == 2 ? kStateF16 : kStateF32;
+}
 
 template <int SF>
-constexpr int state_bytes() { return SF == kStateBF16 ? 2 : (SF == kStateF32 ? 4 : 0); }
+constexpr int state_bytes() { return SF == kStateF32 ? 4 : (SF == kNoState ? 0 : 2); }
 
 // The 8 state values of a half at element index i (a multiple of 8) of a
 // stage in shared memory, as fp32 (exact for both formats).
@@ -447,8 +454,17 @@ __device__ __forceinline__ void state_load8(const uint8_t* base, int i, float e[
     const float4 b = *reinterpret_cast<const float4*>(base + 4 * i + 16);
     e[0] = a.x; e[1] = a.y; e[2] = a.z; e[3] = a.w;
     e[4] = b.x; e[5] = b.y; e[6] = b.z; e[7] = b.w;
-  } else {
+  } else if constexpr (SF == kStateBF16) {
     bf16x8_to_f32(*reinterpret_cast<const uint4*>(base + 2 * i), e);
+  } else {
+    const uint4 w = *reinterpret_cast<const uint4*>(base + 2 * i);
+    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&u[k]));
+      e[2 * k] = f.x;
+      e[2 * k + 1] = f.y;
+    }
   }
 }
 
@@ -466,11 +482,19 @@ __device__ __forceinline__ void state_store8(uint8_t* base, int64_t i, const flo
     asm volatile("st.global.v8.f32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
                  :: "l"(base + 4 * i), "f"(t[0]), "f"(t[1]), "f"(t[2]), "f"(t[3]), "f"(t[4]),
                     "f"(t[5]), "f"(t[6]), "f"(t[7]) : "memory");
-  } else {
+  } else if constexpr (SF == kStateBF16) {
     float back[4];
     const uint2 lo = f32x4_to_bf16(t, back);
     const uint2 hi = f32x4_to_bf16(t + 4, back);
     *reinterpret_cast<uint4*>(base + 2 * i) = make_uint4(lo.x, lo.y, hi.x, hi.y);
+  } else {
+    uint32_t u[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const __half2 h = __floats2half2_rn(t[2 * k], t[2 * k + 1]);
+      u[k] = *reinterpret_cast<const uint32_t*>(&h);
+    }
+    *reinterpret_cast<uint4*>(base + 2 * i) = make_uint4(u[0], u[1], u[2], u[3]);
   }
 }
 

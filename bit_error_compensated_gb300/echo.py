@@ -33,6 +33,7 @@ ECHO_QUANT_NAIVE_ZERO_POINT = 1
 ECHO_QUANT_SYMMETRIC = 2
 ECHO_STATE_F32 = 0
 ECHO_STATE_BF16 = 1
+ECHO_STATE_F16 = 2
 COMP_DEFAULT = ctypes.c_void_p(-1 & (2 ** 64 - 1))   # ECHO_COMP_DEFAULT
 
 _vp, _i32, _i64, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t

@@ -103,7 +103,8 @@ int echo_plan(int P, int64_t n, int g, int bits, echo_plan_t* out);
  *               ECHO_COMP_DEFAULT: the plan's own state;
  *               otherwise a caller device buffer of echo_comp_bytes(plan) bytes,
  *               32-byte aligned, laid out [P][n] (rank p's error for its
- *               element i at p*n + i) in fp32, or bf16 after echo_set_state,
+ *               element i at p*n + i) in fp32, or bf16 or fp16 after
+ *               echo_set_state,
  *               zero before the first call of a sequence;
  *               read and updated in place.
  *   stream      cudaStream_t as void*.
@@ -130,7 +131,7 @@ int echo_reset_comp(echo_plan_t plan);
 int echo_reset_comp_async(echo_plan_t plan, void* comp_state, void* stream);
 
 /* Bytes of one compensator state: P * n * 4 (fp32 state, the default) or
- * P * n * 2 (bf16 state, see echo_set_state).  0 for a NULL plan. */
+ * P * n * 2 (bf16 or fp16 state, see echo_set_state).  0 for a NULL plan. */
 size_t echo_comp_bytes(echo_plan_t plan);
 
 /* Bytes of the plan's receive-slot workspace (what echo_debug_wire copies). */
@@ -286,7 +287,10 @@ int echo_set_quantizer(echo_plan_t plan, int mode);
  * options are readings):
  *   format  ECHO_STATE_F32 (default): each kept error is an fp32 value;
  *           ECHO_STATE_BF16: each kept error is rounded to bf16 (nearest
- *           even) when stored, halving the state's size and traffic.
+ *           even) when stored, halving the state's size and traffic;
+ *           ECHO_STATE_F16: the same with fp16 (nearest even): 3 more
+ *           significand bits than bf16 but a range that ends at 65504 and
+ *           turns subnormal below 6.1e-5, where small errors lose precision.
  *   decay   the kept error is fl32(decay * r) for each revealed error r (then
  *           rounded to bf16 under ECHO_STATE_BF16); 1 (default) is plain
  *           error feedback, below 1 a leaky one.  Must be finite, in (0, 1].
@@ -299,6 +303,7 @@ int echo_set_quantizer(echo_plan_t plan, int mode);
  */
 #define ECHO_STATE_F32  0
 #define ECHO_STATE_BF16 1
+#define ECHO_STATE_F16  2
 int echo_set_state(echo_plan_t plan, int format, float decay);
 
 /* Free everything the plan allocated.  NULL is accepted. */

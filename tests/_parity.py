@@ -12,6 +12,10 @@ import oracle
 STATE_RTOL = 1e-6
 
 
+# torch dtype of a compensator state in each format (0 fp32, 1 bf16, 2 fp16)
+STATE_DTYPES = {0: torch.float32, 1: torch.bfloat16, 2: torch.float16}
+
+
 def bits(t: torch.Tensor) -> np.ndarray:
     """bf16 tensor -> numpy uint16 bit patterns (host copy)."""
     return t.detach().contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
@@ -94,9 +98,9 @@ class SampledOracle:
     so this is exactly the oracle's whole call restricted to them)."""
 
     def __init__(self, P: int, Gs: int, groups: np.ndarray, bits_: int, g: int = 128,
-                 mode: int = 0, bf16_state: bool = False, decay: float = 1.0):
+                 mode: int = 0, state_fmt: int = 0, decay: float = 1.0):
         self.P, self.Gs, self.groups, self.bits, self.g = P, Gs, groups, bits_, g
-        self.mode, self.bf16_state, self.decay = mode, bf16_state, decay
+        self.mode, self.state_fmt, self.decay = mode, state_fmt, decay
         self.owners = (groups // Gs).astype(np.int32)
         self.idx = group_element_index(groups, g)
         self.idx_t = None
@@ -116,7 +120,7 @@ class SampledOracle:
         if state is not None:
             e = self.states.setdefault(state, np.zeros((npos, self.P, self.g), np.float32))
         r = oracle.group_positions(self.P, self.owners, self.bits, x, e, want_wire=want_wire,
-                                   mode=self.mode, bf16_state=self.bf16_state, decay=self.decay)
+                                   mode=self.mode, state_fmt=self.state_fmt, decay=self.decay)
         r["y_rows"] = r["y"].reshape(-1)          # [npos*g], same for every rank
         return r
 

@@ -76,6 +76,6 @@ def test_comp_default_sentinel_matches_header():
                  "ECHO_ERR_ALIGN", "ECHO_ERR_CUDA", "ECHO_ERR_OVERFLOW", "ECHO_ERR_TIMEOUT",
                  "ECHO_ERR_TOO_LARGE", "ECHO_MAX_RANKS", "ECHO_QUANT_ZERO_AWARE",
                  "ECHO_QUANT_NAIVE_ZERO_POINT", "ECHO_QUANT_SYMMETRIC", "ECHO_STATE_F32",
-                 "ECHO_STATE_BF16"):
+                 "ECHO_STATE_BF16", "ECHO_STATE_F16"):
         m = re.search(rf"#define {name}\s+(\d+)", text)
         assert m and int(m.group(1)) == getattr(echo, name), name

@@ -11,7 +11,7 @@ import pytest
 import torch
 
 import oracle
-from _parity import assert_state_close, assert_wire_equal, bits, wire_to_canonical
+from _parity import STATE_DTYPES, assert_state_close, assert_wire_equal, bits, wire_to_canonical
 
 pytestmark = pytest.mark.gpu
 
@@ -35,16 +35,16 @@ def _inputs(P, n, seed, scale=1.0):
 
 
 def _run_sequence(echo, P, Gs, bits_, mode, fused, calls=3, seed=0, inplace=False, quant=0,
-                  bf16_state=False, decay=1.0, g=G, persistent=False):
+                  fmt=0, decay=1.0, g=G, persistent=False):
     n = P * g * Gs
     plan = echo.echo_plan(P, n, g, bits_)
     echo.echo_set_fused(plan, fused)
     echo.echo_set_persistent(plan, persistent)
     echo.echo_set_quantizer(plan, quant)
-    echo.echo_set_state(plan, echo.ECHO_STATE_BF16 if bf16_state else echo.ECHO_STATE_F32, decay)
-    assert echo.echo_comp_bytes(plan) == P * n * (2 if bf16_state else 4)
+    echo.echo_set_state(plan, fmt, decay)
+    assert echo.echo_comp_bytes(plan) == P * n * (4 if fmt == 0 else 2)
     lay = echo.echo_wire_layout(plan)
-    sdt = torch.bfloat16 if bf16_state else torch.float32
+    sdt = STATE_DTYPES[fmt]
     comp_t = torch.zeros((P, n), dtype=sdt, device="cuda") if mode == "caller" else None
     comp_arg = {"none": None, "default": echo.COMP_DEFAULT, "caller": comp_t}[mode]
     e_ref = None if mode == "none" else np.zeros((P, n), np.float32)
@@ -56,13 +56,13 @@ def _run_sequence(echo, P, Gs, bits_, mode, fused, calls=3, seed=0, inplace=Fals
         torch.cuda.synchronize()
         assert echo.echo_get_status(plan) == 0
         ref = oracle.allreduce(xb, g, bits_, e=e_ref, want_wire=True, mode=quant,
-                               bf16_state=bf16_state, decay=decay)
+                               state_fmt=fmt, decay=decay)
         got = bits(out)
         assert np.array_equal(got, ref["out"]), f"outputs differ at call {k}"
         wire = wire_to_canonical(echo.echo_debug_wire(plan), lay, P, n, bits_)
         assert_wire_equal(wire, ref, P)
         if mode == "caller":
-            # a bf16 state widens to fp32 exactly
+            # a bf16 or fp16 state widens to fp32 exactly
             assert_state_close(comp_t.float().cpu().numpy(), e_ref, f"state after call {k}")
     return plan
 
@@ -87,20 +87,20 @@ def test_ablation_quantizers_match_oracle(echo, P, bits_, mode, fused, quant):
 
 
 @pytest.mark.parametrize("fused", [0, 1])
-@pytest.mark.parametrize("state", [(True, 1.0), (False, 0.75), (True, 0.5)])
+@pytest.mark.parametrize("state", [(1, 1.0), (0, 0.75), (1, 0.5), (2, 1.0), (2, 0.5)])
 @pytest.mark.parametrize("bits_", [4, 8])
 @pytest.mark.parametrize("P", [1, 2, 4, 8, 16])
 def test_state_options_match_oracle(echo, P, bits_, state, fused):
-    """The compensator state kept in bf16 and/or decayed (echo_set_state)."""
-    bf16_state, decay = state
+    """The compensator state kept in bf16 or fp16 and/or decayed (echo_set_state)."""
+    fmt, decay = state
     _run_sequence(echo, P, 37, bits_, "caller", fused, calls=4, seed=700 + 10 * P + bits_,
-                  bf16_state=bf16_state, decay=decay)
+                  fmt=fmt, decay=decay)
 
 
 @pytest.mark.parametrize("quant", [1, 2])
 def test_state_options_with_ablation_quantizers(echo, quant):
     _run_sequence(echo, 4, 37, 4, "caller", 0, seed=800 + quant, quant=quant,
-                  bf16_state=True, decay=0.9)
+                  fmt=quant, decay=0.9)   # bf16 state with the naive quantizer, fp16 with the symmetric
 
 
 def test_state_format_switch(echo):
@@ -110,20 +110,19 @@ def test_state_format_switch(echo):
     n = P * G * Gs
     plan = echo.echo_plan(P, n, G, 4)
     e = np.zeros((P, n), np.float32)
-    steps = [(False, 1.0), (False, 1.0), (True, 1.0), (True, 1.0), (True, 0.5), (True, 0.5),
-             (False, 0.5), (False, 1.0)]
+    steps = [(0, 1.0), (0, 1.0), (1, 1.0), (1, 1.0), (1, 0.5), (2, 0.5), (2, 1.0),
+             (0, 0.5), (0, 1.0)]
     prev = steps[0]
-    for k, (bf16_state, decay) in enumerate(steps):
-        echo.echo_set_state(plan, echo.ECHO_STATE_BF16 if bf16_state else echo.ECHO_STATE_F32,
-                            decay)
-        if bf16_state != prev[0]:
+    for k, (fmt, decay) in enumerate(steps):
+        echo.echo_set_state(plan, fmt, decay)
+        if fmt != prev[0]:
             e[:] = 0
-        prev = (bf16_state, decay)
+        prev = (fmt, decay)
         x = _inputs(P, n, 900 + k)
         out = torch.empty_like(x)
         echo.echo_allreduce(plan, list(x), list(out), echo.COMP_DEFAULT)
         torch.cuda.synchronize()
-        ref = oracle.allreduce(bits(x), G, 4, e=e, bf16_state=bf16_state, decay=decay)
+        ref = oracle.allreduce(bits(x), G, 4, e=e, state_fmt=fmt, decay=decay)
         assert np.array_equal(bits(out), ref["out"]), f"call {k}"
 
 
@@ -144,8 +143,8 @@ def test_group_sizes_match_oracle(echo, g, P, bits_, mode, fused):
     _run_sequence(echo, P, GS_RAGGED[g], bits_, mode, fused, seed=1000 + g + 10 * P + bits_, g=g)
 
 
-@pytest.mark.parametrize("opts", [dict(quant=1), dict(quant=2), dict(bf16_state=True),
-                                  dict(bf16_state=True, decay=0.5, quant=2)])
+@pytest.mark.parametrize("opts", [dict(quant=1), dict(quant=2), dict(fmt=1), dict(fmt=2),
+                                  dict(fmt=1, decay=0.5, quant=2), dict(fmt=2, decay=0.5, quant=1)])
 @pytest.mark.parametrize("g", [64, 256])
 def test_group_sizes_with_options(echo, g, opts):
     _run_sequence(echo, 4, GS_RAGGED[g], 4, "caller", 0, seed=1100 + g, g=g, **opts)
@@ -168,8 +167,8 @@ def test_persistent_matches_oracle(echo, P, bits_, mode, fused):
 
 
 @pytest.mark.parametrize("opts", [dict(g=64), dict(g=256), dict(quant=1), dict(quant=2),
-                                  dict(bf16_state=True, decay=0.5), dict(g=64, quant=2, fused=1),
-                                  dict(g=256, bf16_state=True, fused=1), dict(inplace=True),
+                                  dict(fmt=1, decay=0.5), dict(g=64, quant=2, fused=1),
+                                  dict(g=256, fmt=1, fused=1), dict(fmt=2), dict(inplace=True),
                                   dict(inplace=True, fused=1)])
 def test_persistent_with_options(echo, opts):
     opts = dict(opts)
@@ -385,7 +384,7 @@ def test_argument_errors(echo):
     with pytest.raises(echo.EchoError) as ei:
         echo.echo_set_quantizer(plan, 3)
     assert ei.value.status == echo.ECHO_ERR_ARG
-    for fmt, decay in [(2, 1.0), (-1, 1.0), (0, 0.0), (0, -0.5), (1, 1.5), (0, float("nan")),
+    for fmt, decay in [(3, 1.0), (-1, 1.0), (0, 0.0), (0, -0.5), (1, 1.5), (0, float("nan")),
                        (0, float("inf"))]:
         with pytest.raises(echo.EchoError) as ei:
             echo.echo_set_state(plan, fmt, decay)

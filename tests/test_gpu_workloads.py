@@ -12,7 +12,7 @@ import pytest
 import torch
 
 import oracle
-from _parity import (SampledOracle, assert_state_close, assert_wire_equal, bits,
+from _parity import (STATE_DTYPES, SampledOracle, assert_state_close, assert_wire_equal, bits,
                      sample_groups, sampled_wire, wire_to_canonical)
 from bit_error_compensated_gb300.workloads import WORKLOADS, call_sequence, rank_inputs
 
@@ -47,19 +47,19 @@ def test_p2_n4096_full(echo):
 
 
 def _sampled_sequence(echo, number, bits_, sample, calls=None, wire_calls=(0,), quant=0,
-                      bf16_state=False, decay=1.0, g=G, persistent=False, fused=False):
+                      fmt=0, decay=1.0, g=G, persistent=False, fused=False):
     w = WORKLOADS[number]
     P, n = w.P, w.n
     plan = echo.echo_plan(P, n, g, bits_)
     echo.echo_set_persistent(plan, persistent)
     echo.echo_set_fused(plan, fused)
     echo.echo_set_quantizer(plan, quant)
-    echo.echo_set_state(plan, echo.ECHO_STATE_BF16 if bf16_state else echo.ECHO_STATE_F32, decay)
-    sdt = torch.bfloat16 if bf16_state else torch.float32
+    echo.echo_set_state(plan, fmt, decay)
+    sdt = STATE_DTYPES[fmt]
     lay = echo.echo_wire_layout(plan)
     Gs = lay["Gs"]
     groups = sample_groups(P, Gs, sample, seed=number)
-    so = SampledOracle(P, Gs, groups, bits_, g=g, mode=quant, bf16_state=bf16_state, decay=decay)
+    so = SampledOracle(P, Gs, groups, bits_, g=g, mode=quant, state_fmt=fmt, decay=decay)
     states = {}
     x = torch.empty((P, n), dtype=torch.bfloat16, device="cuda")
     out = torch.empty_like(x)
@@ -119,15 +119,15 @@ def test_p4_2048x4096_ablation_quantizers_sampled(echo, quant):
     _sampled_sequence(echo, 2, 4, sample=512, calls=16, quant=quant)
 
 
-@pytest.mark.parametrize("state", [(True, 1.0), (False, 0.9), (True, 0.9)])
+@pytest.mark.parametrize("state", [(1, 1.0), (0, 0.9), (1, 0.9), (2, 1.0)])
 def test_p4_2048x4096_state_options_sampled(echo, state):
-    """The compensator state in bf16 and/or decayed, over the first 16 calls of
-    the 64-call workload, at full size."""
-    _sampled_sequence(echo, 2, 4, sample=512, calls=16, bf16_state=state[0], decay=state[1])
+    """The compensator state in bf16 or fp16 and/or decayed, over the first 16
+    calls of the 64-call workload, at full size."""
+    _sampled_sequence(echo, 2, 4, sample=512, calls=16, fmt=state[0], decay=state[1])
 
 
 def test_p8_1gib_bf16_state_sampled(echo):
-    _sampled_sequence(echo, 3, 4, sample=2048, calls=4, bf16_state=True)
+    _sampled_sequence(echo, 3, 4, sample=2048, calls=4, fmt=1)
 
 
 @pytest.mark.parametrize("g", [64, 256])
