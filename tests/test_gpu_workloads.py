@@ -1,11 +1,13 @@
 """The five workloads at their full sizes, in the launch configuration the bench
-times, checked against the oracle on a fixed sample of group positions carried
-through every call of the sequence (positions are independent, so the oracle on
-a sample is exactly the oracle's whole call restricted to it).  The two-rank
-workload is small enough to compare in full, wire codes included.
+times, checked against the oracle over their whole call sequences.
 
-Sample sizes keep each test within tens of seconds of oracle time; every sample
-includes the first and last group of every owner segment.
+p2_n4096, p4_2048x4096 and p4_8192x4096 are compared in full: every output of
+every rank, the whole compensator state and the wire codes.  p8_1gib and
+p4_32768x1024 are compared on a fixed 1/64 sample of group positions carried
+through every call (positions are independent, so the oracle on a sample is
+exactly the oracle's whole call restricted to it); every sample includes the
+first and last group of every owner segment.  Shorter runs check the options
+(quantizers, state formats, group sizes, the persistent kernel) at full size.
 """
 import numpy as np
 import pytest
@@ -44,6 +46,36 @@ def test_p2_n4096_full(echo):
         assert_wire_equal(wire_to_canonical(echo.echo_debug_wire(plan), lay, w.P, w.n, 4), ref, w.P)
         assert_state_close(comp.cpu().numpy(), e_ref)
     print(f"p2_n4096: exact rounding ties in the oracle: {ties}; code mismatches: 0")
+
+
+def _full_sequence(echo, number, bits_, wire_every=1):
+    """Every call of workload `number` compared in full with the oracle."""
+    w = WORKLOADS[number]
+    P, n = w.P, w.n
+    plan = echo.echo_plan(P, n, G, bits_)
+    lay = echo.echo_wire_layout(plan)
+    states, refs = {}, {}
+    x = torch.empty((P, n), dtype=torch.bfloat16, device="cuda")
+    out = torch.empty_like(x)
+    seq = call_sequence(number)
+    ties = 0
+    for k, c in enumerate(seq):
+        rank_inputs(number, c, "cuda", out=x)
+        comp = None
+        if c.state != "none":
+            comp = states.setdefault(c.state, torch.zeros((P, n), device="cuda"))
+            refs.setdefault(c.state, np.zeros((P, n), np.float32))
+        echo.echo_allreduce(plan, list(x), list(out), comp)
+        check_wire = k % wire_every == 0 or k == len(seq) - 1
+        ref = oracle.allreduce(bits(x), G, bits_, e=refs.get(c.state), want_wire=check_wire)
+        ties += ref["ties"]
+        assert np.array_equal(bits(out), ref["out"]), f"outputs, call {k}"
+        if comp is not None:
+            assert_state_close(comp.cpu().numpy(), refs[c.state], f"state, call {k}")
+        if check_wire:
+            assert_wire_equal(wire_to_canonical(echo.echo_debug_wire(plan), lay, P, n, bits_), ref, P)
+    print(f"{w.name} ({bits_}-bit): {len(seq)} calls compared in full; exact rounding ties in "
+          f"the oracle: {ties}; mismatches: 0")
 
 
 def _sampled_sequence(echo, number, bits_, sample, calls=None, wire_calls=(0,), quant=0,
@@ -95,21 +127,25 @@ def _sampled_sequence(echo, number, bits_, sample, calls=None, wire_calls=(0,), 
           f"exact rounding ties in the oracle: {ties}; code mismatches: 0")
 
 
-def test_p4_2048x4096_sampled(echo):
-    _sampled_sequence(echo, 2, 4, sample=1024)
+def test_p4_2048x4096_full(echo):
+    _full_sequence(echo, 2, 4)
 
 
 @pytest.mark.parametrize("bits_", [4, 8])
 def test_p8_1gib_sampled(echo, bits_):
-    _sampled_sequence(echo, 3, bits_, sample=4096)
+    w = WORKLOADS[3]
+    _sampled_sequence(echo, 3, bits_, sample=w.n // G // 64)          # 1/64 of the positions
 
 
-def test_p4_8192x4096_sampled(echo):
-    _sampled_sequence(echo, 4, 4, sample=1024)
+def test_p4_8192x4096_full(echo):
+    _full_sequence(echo, 4, 4, wire_every=8)
 
 
 def test_p4_32768x1024_sampled(echo):
-    _sampled_sequence(echo, 5, 4, sample=384)
+    """All 1 120 calls (10 steps of 56 forward and 56 backward sites, two
+    states) on 1/64 of the positions."""
+    w = WORKLOADS[5]
+    _sampled_sequence(echo, 5, 4, sample=w.n // G // 64)
 
 
 @pytest.mark.parametrize("quant", [1, 2])
