@@ -40,6 +40,18 @@ __device__ __forceinline__ float max_nan(float a, float b) {
   return r;
 }
 
+// Three-input forms (one instruction on the sm_100 family).
+__device__ __forceinline__ float min3_nan(float a, float b, float c) {
+  float r;
+  asm("min.NaN.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+__device__ __forceinline__ float max3_nan(float a, float b, float c) {
+  float r;
+  asm("max.NaN.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
 // Butterfly over the NL lanes of a group (aligned lane blocks of NL).
 template <int NL>
 __device__ __forceinline__ float group_min(float x) {
@@ -56,16 +68,31 @@ __device__ __forceinline__ float group_max(float x) {
 
 // Zero-aware range of a group over its NL lanes (all 32 lanes must call it;
 // each block of NL lanes reduces its own group).
+#ifndef ECHO_RANGE3
+#define ECHO_RANGE3 1
+#endif
 template <int NL>
 __device__ __forceinline__ void group_range(const float v[16], float& lo, float& hi) {
-  float a[4], b[4];
+#if !ECHO_RANGE3
+  float a2[4], b2[4];
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
-    a[k] = min_nan(min_nan(v[4 * k], v[4 * k + 1]), min_nan(v[4 * k + 2], v[4 * k + 3]));
-    b[k] = max_nan(max_nan(v[4 * k], v[4 * k + 1]), max_nan(v[4 * k + 2], v[4 * k + 3]));
+    a2[k] = min_nan(min_nan(v[4 * k], v[4 * k + 1]), min_nan(v[4 * k + 2], v[4 * k + 3]));
+    b2[k] = max_nan(max_nan(v[4 * k], v[4 * k + 1]), max_nan(v[4 * k + 2], v[4 * k + 3]));
   }
-  lo = group_min<NL>(min_nan(min_nan(min_nan(a[0], a[1]), min_nan(a[2], a[3])), 0.0f));
-  hi = group_max<NL>(max_nan(max_nan(max_nan(b[0], b[1]), max_nan(b[2], b[3])), 0.0f));
+  lo = group_min<NL>(min_nan(min_nan(min_nan(a2[0], a2[1]), min_nan(a2[2], a2[3])), 0.0f));
+  hi = group_max<NL>(max_nan(max_nan(max_nan(b2[0], b2[1]), max_nan(b2[2], b2[3])), 0.0f));
+  return;
+#endif
+  // 16 values and 0 in 8 three-input steps each (two independent chains).
+  float a = min3_nan(v[0], v[1], 0.0f), c = min3_nan(v[2], v[3], v[4]);
+  float b = max3_nan(v[0], v[1], 0.0f), d = max3_nan(v[2], v[3], v[4]);
+  a = min3_nan(a, v[5], v[6]);   c = min3_nan(c, v[7], v[8]);
+  b = max3_nan(b, v[5], v[6]);   d = max3_nan(d, v[7], v[8]);
+  a = min3_nan(a, v[9], v[10]);  c = min3_nan(c, v[11], v[12]);
+  b = max3_nan(b, v[9], v[10]);  d = max3_nan(d, v[11], v[12]);
+  lo = group_min<NL>(min3_nan(a, c, min_nan(v[13], min_nan(v[14], v[15]))));
+  hi = group_max<NL>(max3_nan(b, d, max_nan(v[13], max_nan(v[14], v[15]))));
 }
 
 struct GroupGrid {
@@ -416,19 +443,20 @@ __device__ __forceinline__ void bf16x4_to_f32(uint2 r, float f[4]) {
   f[3] = __uint_as_float(r.y & 0xFFFF0000u);
 }
 
-__device__ __forceinline__ uint2 f32x4_to_bf16(const float f[4], float back[4]) {
-  const __nv_bfloat16 b0 = __float2bfloat16_rn(f[0]);
-  const __nv_bfloat16 b1 = __float2bfloat16_rn(f[1]);
-  const __nv_bfloat16 b2 = __float2bfloat16_rn(f[2]);
-  const __nv_bfloat16 b3 = __float2bfloat16_rn(f[3]);
-  back[0] = __bfloat162float(b0);
-  back[1] = __bfloat162float(b1);
-  back[2] = __bfloat162float(b2);
-  back[3] = __bfloat162float(b3);
-  uint2 r;
-  r.x = (uint32_t)__bfloat16_as_ushort(b0) | ((uint32_t)__bfloat16_as_ushort(b1) << 16);
-  r.y = (uint32_t)__bfloat16_as_ushort(b2) | ((uint32_t)__bfloat16_as_ushort(b3) << 16);
-  return r;
+
+// 8 values rounded to bf16 (nearest even) two at a time, packed into 16 bytes
+// (element 2k in the low half of word k), with the rounded values widened
+// back to fp32 exactly in `back`.
+__device__ __forceinline__ uint4 f32x8_to_bf16(const float f[8], float back[8]) {
+  uint32_t w[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(f[2 * k], f[2 * k + 1]);
+    w[k] = *reinterpret_cast<const uint32_t*>(&h);
+    back[2 * k] = __uint_as_float(w[k] << 16);
+    back[2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
 // Storage of the compensator state: none (uncompensated), fp32, or bf16 or
@@ -483,10 +511,8 @@ __device__ __forceinline__ void state_store8(uint8_t* base, int64_t i, const flo
                  :: "l"(base + 4 * i), "f"(t[0]), "f"(t[1]), "f"(t[2]), "f"(t[3]), "f"(t[4]),
                     "f"(t[5]), "f"(t[6]), "f"(t[7]) : "memory");
   } else if constexpr (SF == kStateBF16) {
-    float back[4];
-    const uint2 lo = f32x4_to_bf16(t, back);
-    const uint2 hi = f32x4_to_bf16(t + 4, back);
-    *reinterpret_cast<uint4*>(base + 2 * i) = make_uint4(lo.x, lo.y, hi.x, hi.y);
+    float back[8];
+    *reinterpret_cast<uint4*>(base + 2 * i) = f32x8_to_bf16(t, back);
   } else {
     uint32_t u[4];
 #pragma unroll

@@ -268,8 +268,7 @@ __device__ __forceinline__ void reduce_tile(const CallArgs& a, const uint8_t* st
       if (!valid) continue;
       store_codes8<BITS>(a.codes2 + grp * CB + half_code_byte<BITS, NL>(hh, q), c, codes_pol);
       float yb[8];
-      const uint2 ya = f32x4_to_bf16(deq, yb);
-      const uint2 yv = f32x4_to_bf16(deq + 4, yb + 4);
+      const uint4 y = f32x8_to_bf16(deq, yb);
       const int64_t e = grp * G + half_at<NL>(hh, q);
       if constexpr (COMP) {
         uint8_t* eo = reinterpret_cast<uint8_t*>(a.comp) + (int64_t)o * a.n * EB;
@@ -278,7 +277,6 @@ __device__ __forceinline__ void reduce_tile(const CallArgs& a, const uint8_t* st
         state_store8<SF>(eo, e, r, a.decay);
       }
       if (FUSED) {
-        const uint4 y = make_uint4(ya.x, ya.y, yv.x, yv.y);
         for (int r = 0; r < P; ++r) __stcs(reinterpret_cast<uint4*>(a.out[r] + e), y);
       }
     }
@@ -345,9 +343,7 @@ __device__ __forceinline__ void gather_runs(const CallArgs& a, int o, int64_t ru
         decode4_mode<8, MODE>(word[u].x, s, zf, deq);
         decode4_mode<8, MODE>(word[u].y, s, zf, deq + 4);
       }
-      const uint2 ya = f32x4_to_bf16(deq, yb);
-      const uint2 yv = f32x4_to_bf16(deq + 4, yb + 4);
-      const uint4 y = make_uint4(ya.x, ya.y, yv.x, yv.y);
+      const uint4 y = f32x8_to_bf16(deq, yb);
       const int64_t e0 = ((int64_t)o * Gs + w[u]) * G + 8 * h;
       for (int r = 0; r < P; ++r) __stcs(reinterpret_cast<uint4*>(a.out[r] + e0), y);
     }
