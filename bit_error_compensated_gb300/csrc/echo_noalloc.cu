@@ -1,8 +1,8 @@
 // echo_noalloc.cu -- echo_allreduce_noalloc: the emulated all-reduce for
 // callers that must not allocate device memory (contract in include/echo.h).
 //
-// The receive slots that the push kernel writes and the reduce and gather
-// kernels read live in a file-scope __device__ array instead of a plan's
+// The receive slots that the push kernel writes and the reduce kernel reads
+// (and writes its gather codes to) live in a file-scope __device__ array instead of a plan's
 // cudaMalloc'd workspace.  Host code never passes the array's name to a kernel
 // (on the host it is only a stand-in symbol): the device address is looked up
 // once per device with cudaGetSymbolAddress and passed as a plain pointer.
@@ -123,8 +123,8 @@ extern "C" int echo_allreduce_noalloc(int P, int64_t n, int bits, const void* co
   // every call before they are read.
   cudaError_t e = cudaMemsetAsync(a.status, 0, sizeof(int), s);
   if (e == cudaSuccess && P > 1) e = echo::launch_push(a, echo::kGroup, bits, s, true);
-  if (e == cudaSuccess) e = echo::launch_reduce(a, echo::kGroup, bits, false, s, true);
-  if (e == cudaSuccess) e = echo::launch_gather(a, echo::kGroup, bits, s, true);
+  // The reduce kernel writes the P outputs itself (the fused gather).
+  if (e == cudaSuccess) e = echo::launch_reduce(a, echo::kGroup, bits, true, s, true);
   if (e != cudaSuccess) return echo::note_cuda_error(e);
   return ECHO_OK;
 }

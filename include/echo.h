@@ -221,9 +221,9 @@ int echo_set_timing(echo_plan_t plan, void* const* events, int count);
  *               fp32 [P][n], as for echo_allreduce; ECHO_COMP_DEFAULT is
  *               rejected (ECHO_ERR_ARG) since there is no plan.
  *   stream      cudaStream_t as void*.
- * Outputs, state and codes are bit-identical to echo_allreduce's (unfused
- * gather).  Non-finite inputs are not reported: there is no status word to
- * read back.
+ * Two kernels (push, then reduce writing the outputs).  Outputs, state and
+ * codes are bit-identical to echo_allreduce's.  Non-finite inputs are not
+ * reported: there is no status word to read back.
  */
 #define ECHO_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
 int echo_allreduce_noalloc(int P, int64_t n, int bits, const void* const* in,
@@ -231,7 +231,8 @@ int echo_allreduce_noalloc(int P, int64_t n, int bits, const void* const* in,
 
 /*
  * echo_set_persistent -- run each later echo_allreduce of the plan as one
- * persistent kernel instead of three kernels (on = 1), or back (on = 0).
+ * persistent kernel instead of two or three kernels (on = 1), or back
+ * (on = 0).
  * The paper overlaps the push, reduce and gather of different tiles
  * (Fig. 2(b)); here every (sender, owner, tile) push, every reduce tile and
  * every gather tile is a work item that blocks claim in order from an atomic

@@ -365,6 +365,13 @@ def test_argument_errors(echo):
     with pytest.raises(echo.EchoError) as ei:          # misaligned by 2 bytes
         echo.echo_allreduce(plan, [x[0, 1:], x[1]], [out[0], out[1]], None)
     assert ei.value.status == echo.ECHO_ERR_ALIGN
+    # a compensator state must be 32-byte aligned: 16 bytes off is rejected
+    state = torch.zeros(P * n + 8, dtype=torch.float32, device="cuda")
+    with pytest.raises(echo.EchoError) as ei:
+        echo.echo_allreduce(plan, [x[0, :n], x[1, :n]], [out[0, :n], out[1, :n]], state[4:])
+    assert ei.value.status == echo.ECHO_ERR_ALIGN
+    echo.echo_allreduce(plan, [x[0, :n], x[1, :n]], [out[0, :n], out[1, :n]], state[8:])
+    torch.cuda.synchronize()
     with pytest.raises(echo.EchoError) as ei:          # out[0] overlaps in[1]
         echo.echo_allreduce(plan, [x[0], x[1]], [x[1], out[1]], None)
     assert ei.value.status == echo.ECHO_ERR_ARG
