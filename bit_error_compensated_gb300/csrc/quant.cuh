@@ -213,7 +213,7 @@ __device__ __forceinline__ GroupGrid make_grid(float lo, float hi, float L) {
 // IEEE division.  Only the upper clamp is applied: for a finite group v >= lo,
 // so rint(fl(v / s)) >= rint(fl(lo / s)) = -z (division and rint are monotonic
 // and odd-symmetric), and c >= 0 already.  (For a non-finite group the codes
-// are unspecified; pack4 still confines each packed word to its own bytes.)
+// are unspecified; pack8 still confines each packed word to its own bytes.)
 //
 // Since r and z are small integers, clamp(r + z, L) - z = min(r, L - z)
 // exactly: the clamped offset cm = q - z gives both c = cm + z and d = cm * s.
@@ -352,16 +352,12 @@ __device__ __forceinline__ void unpack_meta(uint32_t meta, float& s, float& zf) 
   zf = __half2float(__ushort_as_half((unsigned short)(meta >> 16)));
 }
 
-// Packing of 4 consecutive codes of a chunk.  4-bit: element 2i in the low
-// nibble of byte i, so 4 codes form one little-endian 16-bit word; 8-bit: one
-// byte each, one 32-bit word.  The codes are integer-valued floats, so the
-// word is built with exact fp arithmetic (every intermediate is an integer
-// below 2^16) and read out of the mantissa of 2^23 + word.
-__device__ __forceinline__ uint32_t small_int_bits(float w) {
-  return __float_as_uint(__fadd_rn(w, 8388608.0f)) & 0xFFFFu;
-}
-
-// Two chunks (c[0..3] and c[4..7]) at once, on pairs.
+// Packing of 4 consecutive codes.  4-bit: element 2i in the low nibble of
+// byte i, so 4 codes form one little-endian 16-bit word; 8-bit: one byte
+// each, one 32-bit word.  The codes are integer-valued floats, so the word is
+// built with exact fp arithmetic (every intermediate is an integer below
+// 2^16) and read out of the mantissa of 2^23 + word.  Two runs of 4 (c[0..3]
+// into w0, c[4..7] into w1) at once, on pairs.
 template <int BITS>
 __device__ __forceinline__ void pack8(const float c[8], uint32_t& w0, uint32_t& w1) {
   constexpr float B = 8388608.0f;                  // 2^23
@@ -382,17 +378,6 @@ __device__ __forceinline__ void pack8(const float c[8], uint32_t& w0, uint32_t& 
     w0 = __byte_perm(__float_as_uint(a0), __float_as_uint(b0), 0x5410);
     w1 = __byte_perm(__float_as_uint(a1), __float_as_uint(b1), 0x5410);
   }
-}
-
-template <int BITS>
-__device__ __forceinline__ uint32_t pack4(const float c[4]) {
-  if (BITS == 4) {
-    const float w = __fmaf_rn(c[3], 4096.0f, __fmaf_rn(c[2], 256.0f, __fmaf_rn(c[1], 16.0f, c[0])));
-    return small_int_bits(w);
-  }
-  const uint32_t lo = small_int_bits(__fmaf_rn(c[1], 256.0f, c[0]));
-  const uint32_t hi = small_int_bits(__fmaf_rn(c[3], 256.0f, c[2]));
-  return __byte_perm(lo, hi, 0x5410);
 }
 
 // Decoding of a packed chunk word: (q - z) * s for its 4 codes.  The code is
@@ -434,15 +419,6 @@ __device__ __forceinline__ void bf16x8_to_f32(uint4 r, float f[8]) {
   f[4] = __uint_as_float(r.z << 16); f[5] = __uint_as_float(r.z & 0xFFFF0000u);
   f[6] = __uint_as_float(r.w << 16); f[7] = __uint_as_float(r.w & 0xFFFF0000u);
 }
-
-// bf16 <-> f32 for a chunk of 4 values held in 8 bytes.
-__device__ __forceinline__ void bf16x4_to_f32(uint2 r, float f[4]) {
-  f[0] = __uint_as_float(r.x << 16);
-  f[1] = __uint_as_float(r.x & 0xFFFF0000u);
-  f[2] = __uint_as_float(r.y << 16);
-  f[3] = __uint_as_float(r.y & 0xFFFF0000u);
-}
-
 
 // 8 values rounded to bf16 (nearest even) two at a time, packed into 16 bytes
 // (element 2k in the low half of word k), with the rounded values widened

@@ -25,7 +25,7 @@ def lib():
     return ctypes.CDLL(str(build_library()))
 
 
-def test_headers_declare_the_north_star_calls():
+def test_headers_declare_the_three_named_calls():
     d = _declared()
     assert {"echo_plan", "echo_allreduce", "echo_reset_comp"} <= d
     assert len(d) >= 12
