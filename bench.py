@@ -274,6 +274,20 @@ def run_ours(args, rank, local, world):
     torch.cuda.synchronize(dev)
     if echo.echo_get_status(plan, stream) != 0:
         raise RuntimeError("device status word set during warm-up")
+    if args.graph:
+        # The whole call sequence captured once as a CUDA graph and replayed
+        # as one step: the calls are the same, their launches cost less.
+        graph = torch.cuda.CUDAGraph()
+        gstream = torch.cuda.Stream(dev)
+        gstream.wait_stream(stream)
+        with torch.cuda.graph(graph, stream=gstream):
+            for ins, comp in call_args:
+                echo.echo_allreduce(plan, ins, out_rows, comp, gstream)
+        torch.cuda.synchronize(dev)
+        step = graph.replay
+        for _ in range(args.warmup):
+            step()
+        torch.cuda.synchronize(dev)
 
     # Timed region: K steps, CUDA events on the launching stream.
     clocks = ClockSampler(local)
@@ -349,7 +363,9 @@ def run_ours(args, rank, local, world):
         "config": {"workload": w.name, "P": P, "n_per_rank": n, "bits": bits, "g": g,
                    "calls_per_step": calls, "compensated": compensated_calls == calls,
                    "fused_gather": bool(fused), "quantizer": QUANTIZERS[args.quantizer],
-                   "schedule": "one persistent kernel" if args.persistent else "three kernels",
+                   "schedule": ("one persistent kernel" if args.persistent else
+                                "two kernels" if fused else "three kernels")
+                               + (", CUDA graph of the call sequence" if args.graph else ""),
                    "state": {"format": STATE_NAME[args.state], "decay": args.decay},
                    "io": "bf16 in/out, fp32 arithmetic, "
                    f"{bits}-bit codes, {STATE_NAME[args.state]} state",
@@ -648,7 +664,9 @@ def main(argv=None):
                          "kernel writes the outputs itself")
     ap.add_argument("--fused", action="store_true", help=argparse.SUPPRESS)   # the default
     ap.add_argument("--persistent", action="store_true",
-                    help="one persistent kernel per call instead of three")
+                    help="one persistent kernel per call instead of two or three")
+    ap.add_argument("--graph", action="store_true",
+                    help="time replays of the call sequence captured as a CUDA graph")
     ap.add_argument("--quantizer", type=int, default=0, choices=[0, 1, 2],
                     help="0 zero-aware (the method), 1 naive zero-point, 2 symmetric grid")
     ap.add_argument("--state", choices=["f32", "bf16", "f16"], default="f32",

@@ -234,6 +234,35 @@ def test_persistent_bounded_wait_reports_timeout(echo):
         assert np.array_equal(bits(out), oracle.allreduce(bits(xk), G, 4)["out"])
 
 
+@pytest.mark.parametrize("schedule", ["fused", "unfused", "persistent"])
+def test_calls_captured_in_a_cuda_graph(echo, schedule):
+    """A sequence of calls captured once by stream capture and replayed: every
+    replay continues the state, and outputs match the oracle's calls."""
+    P, Gs = 4, 37
+    n = P * G * Gs
+    plan = echo.echo_plan(P, n, G, 4)
+    echo.echo_set_fused(plan, schedule != "unfused")
+    echo.echo_set_persistent(plan, schedule == "persistent")
+    xs = [_inputs(P, n, 4000 + k) for k in range(3)]
+    outs = [torch.empty_like(x) for x in xs]
+    echo.echo_allreduce(plan, list(xs[0]), list(outs[0]), None)      # first use outside capture
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.graph(graph, stream=side):
+        for x, out in zip(xs, outs):
+            echo.echo_allreduce(plan, list(x), list(out), echo.COMP_DEFAULT, side)
+    e = np.zeros((P, n), np.float32)
+    for _ in range(2):
+        graph.replay()
+        torch.cuda.synchronize()
+        for x, out in zip(xs, outs):
+            ref = oracle.allreduce(bits(x), G, 4, e=e)
+            assert np.array_equal(bits(out), ref["out"])
+    assert echo.echo_get_status(plan) == 0
+
+
 @pytest.mark.parametrize("Gs", [1, 4, 31, 32, 33, 64, 129])
 def test_tile_boundaries(echo, Gs):
     _run_sequence(echo, 4, Gs, 4, "caller", 0, calls=2, seed=Gs)
