@@ -293,16 +293,16 @@ def run_ours(args, rank, local, world):
     clocks = ClockSampler(local)
     barrier(world)
     torch.cuda.synchronize(dev)
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
-    t0.record(stream)
-    for _ in range(args.steps):
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    evs[0].record(stream)
+    for i in range(args.steps):
         step()
-    t1.record(stream)
+        evs[i + 1].record(stream)
     torch.cuda.synchronize(dev)
     barrier(world)
     clk = clocks.stop()
-    ms = t0.elapsed_time(t1)
+    ms = evs[0].elapsed_time(evs[-1])
+    step_ms = sorted(evs[i].elapsed_time(evs[i + 1]) for i in range(args.steps))
     max_ms = max_over_ranks(ms, world)
 
     bytes_in_per_call = P * n * 2
@@ -376,6 +376,8 @@ def run_ours(args, rank, local, world):
         "hbm_roofline_frac_spec": round(model / per_call_s / 1e9 / SPEC_HBM_GBS, 4),
         "model_bytes_per_call": int(model),
         "us_per_call": round(per_call_s * 1e6, 2),
+        "step_ms": {"median": round(step_ms[len(step_ms) // 2], 4), "min": round(step_ms[0], 4),
+                    "max": round(step_ms[-1], 4)},
         "per_kernel_us": {k: round(v, 2) for k, v in avg_us.items()},
         "roofline": roofline,
         "gpu_launches": launches_per_call * calls * args.steps,

@@ -1,6 +1,7 @@
 // echo_api.cu -- host side of libecho.so: plans, argument checks, launches.
 // The operation and every call's contract are described in include/echo.h.
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <cstdint>
 #include <cstdio>
@@ -14,10 +15,12 @@ using echo::CallArgs;
 struct echo_plan_s {
   int P = 0, g = 0, bits = 0, device = 0;
   int64_t n = 0, m = 0, Gs = 0, Gs_pad = 0, CB = 0;
-  uint8_t* wire = nullptr;          // one allocation: push codes/meta, gather codes/meta
+  uint8_t* wire = nullptr;          // push codes/meta, gather codes/meta (inside wire_alloc)
+  uint8_t* wire_alloc = nullptr;    // the allocation: guard band, wire, guard band
   size_t wire_bytes = 0;
   int64_t off[4] = {0, 0, 0, 0};
-  float* comp = nullptr;            // the plan's own compensator state
+  float* comp = nullptr;            // the plan's own compensator state (inside comp_alloc)
+  uint8_t* comp_alloc = nullptr;    // guard band, state (fp32-sized), guard band
   size_t comp_bytes = 0;
   int* status = nullptr;            // device status word
   cudaStream_t last_stream = nullptr;
@@ -29,6 +32,7 @@ struct echo_plan_s {
   uint32_t* sched = nullptr;        // its schedule words, zero between calls
   int64_t tiles = 0;                // reduce tiles per segment
   int64_t hold = -1;                // test hook, see echo_debug_hold_push
+  int grid_cap = 0;                 // debug: see echo_debug_set_grid
   cudaEvent_t ev[4] = {nullptr, nullptr, nullptr, nullptr};
   int timing = 0;
 };
@@ -63,6 +67,29 @@ int check_device(const echo_plan_s* plan) {
 }
 
 bool g_kernels_prepared[64] = {false};
+
+// Guard bands around the plan's receive slots and state: filled with a fixed
+// byte at plan time and checked by echo_debug_check_guards.
+constexpr size_t kGuard = 256;
+constexpr int kGuardByte = 0xA5;
+
+// NVTX ranges (domain "echo") around each call, for timeline tools; without
+// a tool attached they cost a branch.
+nvtxDomainHandle_t nvtx_domain() {
+  static nvtxDomainHandle_t d = nvtxDomainCreateA("echo");
+  return d;
+}
+struct NvtxRange {
+  explicit NvtxRange(const char* name) {
+    nvtxEventAttributes_t attr = {};
+    attr.version = NVTX_VERSION;
+    attr.size = NVTX_EVENT_ATTRIB_STRUCT_SIZE;
+    attr.messageType = NVTX_MESSAGE_TYPE_ASCII;
+    attr.message.ascii = name;
+    nvtxDomainRangePushEx(nvtx_domain(), &attr);
+  }
+  ~NvtxRange() { nvtxDomainRangePop(nvtx_domain()); }
+};
 
 }  // namespace
 
@@ -136,8 +163,18 @@ int echo_plan(int P, int64_t n, int g, int bits, echo_plan_t* out) {
     e = echo::prepare_kernels();
     if (e == cudaSuccess) g_kernels_prepared[p->device] = true;
   }
-  if (e == cudaSuccess && p->wire_bytes > 0) e = cudaMalloc((void**)&p->wire, p->wire_bytes);
-  if (e == cudaSuccess && p->comp_bytes > 0) e = cudaMalloc((void**)&p->comp, p->comp_bytes);
+  if (e == cudaSuccess && p->wire_bytes > 0) {
+    e = cudaMalloc((void**)&p->wire_alloc, p->wire_bytes + 2 * kGuard);
+    p->wire = p->wire_alloc + kGuard;
+    if (e == cudaSuccess) e = cudaMemset(p->wire_alloc, kGuardByte, kGuard);
+    if (e == cudaSuccess) e = cudaMemset(p->wire + p->wire_bytes, kGuardByte, kGuard);
+  }
+  if (e == cudaSuccess && p->comp_bytes > 0) {
+    e = cudaMalloc((void**)&p->comp_alloc, p->comp_bytes + 2 * kGuard);
+    p->comp = reinterpret_cast<float*>(p->comp_alloc + kGuard);
+    if (e == cudaSuccess) e = cudaMemset(p->comp_alloc, kGuardByte, kGuard);
+    if (e == cudaSuccess) e = cudaMemset(p->comp_alloc + kGuard + p->comp_bytes, kGuardByte, kGuard);
+  }
   if (e == cudaSuccess) e = cudaMalloc((void**)&p->status, sizeof(int));
   if (e == cudaSuccess) e = cudaMalloc((void**)&p->sched, sched_bytes);
   if (e == cudaSuccess) e = cudaMemset(p->sched, 0, sched_bytes);
@@ -211,6 +248,9 @@ int echo_allreduce(echo_plan_t plan, const void* const* in, void* const* out,
   a.mode = plan->mode;
   a.state_fmt = plan->state_fmt;
   a.decay = plan->decay;
+  a.grid_cap = plan->grid_cap;
+  NvtxRange range(plan->persistent ? "echo_allreduce (persistent)"
+                  : plan->fused ? "echo_allreduce" : "echo_allreduce (separate gather)");
 
   // Programmatic dependent launch lets each kernel's blocks be scheduled while
   // the previous kernel drains; every kernel waits (griddepcontrol.wait) before
@@ -320,6 +360,31 @@ int echo_set_persistent(echo_plan_t plan, int on) {
   return ECHO_OK;
 }
 
+int echo_debug_set_grid(echo_plan_t plan, int blocks) {
+  if (plan == nullptr || blocks < 0) return ECHO_ERR_ARG;
+  plan->grid_cap = blocks;
+  return ECHO_OK;
+}
+
+int echo_debug_check_guards(echo_plan_t plan, int* intact) {
+  if (plan == nullptr || intact == nullptr) return ECHO_ERR_ARG;
+  *intact = 1;
+  int rc = check_device(plan);
+  if (rc != ECHO_OK) return rc;
+  const size_t state_alloc = (size_t)plan->P * plan->n * sizeof(float);
+  const uint8_t* bands[4] = {
+      plan->wire_alloc, plan->wire_alloc ? plan->wire + plan->wire_bytes : nullptr,
+      plan->comp_alloc, plan->comp_alloc ? plan->comp_alloc + kGuard + state_alloc : nullptr};
+  uint8_t host[kGuard];
+  for (const uint8_t* b : bands) {
+    if (b == nullptr) continue;
+    ECHO_CUDA(cudaMemcpy(host, b, kGuard, cudaMemcpyDeviceToHost));
+    for (size_t i = 0; i < kGuard; ++i)
+      if (host[i] != kGuardByte) *intact = 0;
+  }
+  return ECHO_OK;
+}
+
 int echo_debug_hold_push(echo_plan_t plan, int64_t item) {
   if (plan == nullptr || item < -1) return ECHO_ERR_ARG;
   plan->hold = item;
@@ -369,8 +434,8 @@ int echo_set_timing(echo_plan_t plan, void* const* events, int count) {
 
 void echo_plan_destroy(echo_plan_t plan) {
   if (plan == nullptr) return;
-  if (plan->wire) cudaFree(plan->wire);
-  if (plan->comp) cudaFree(plan->comp);
+  if (plan->wire_alloc) cudaFree(plan->wire_alloc);
+  if (plan->comp_alloc) cudaFree(plan->comp_alloc);
   if (plan->status) cudaFree(plan->status);
   if (plan->sched) cudaFree(plan->sched);
   delete plan;

@@ -62,6 +62,7 @@ struct CallArgs {
   int mode;            // quantizer: 0 zero-aware (the method), 1 naive zero point, 2 symmetric
   int state_fmt;       // format of the state at comp: 0 fp32, 1 bf16, 2 fp16
   float decay;         // the kept error is decay * (revealed error); 1 = plain feedback
+  int grid_cap;        // debug: at most this many blocks along each kernel's grid (0: none)
 };
 
 // The schedule of the single persistent kernel of a call (k_call.cu).

@@ -339,7 +339,8 @@ cudaError_t launch_t(const CallArgs& a, const CallSched& sch, cudaStream_t s) {
   // Every block resident at once (a cooperative launch checks it), and no
   // more blocks than items.
   const int64_t items = (FUSED ? 1 : 2) * (int64_t)P * sc.tiles + (int64_t)P * (P - 1) * sc.tiles;
-  const int64_t blocks = items < resident ? items : resident;
+  int64_t blocks = items < resident ? items : resident;
+  if (a.grid_cap > 0 && blocks > a.grid_cap) blocks = a.grid_cap;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)blocks);
   cfg.blockDim = dim3(kThreads);

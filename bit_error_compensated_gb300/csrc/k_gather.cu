@@ -50,6 +50,7 @@ cudaError_t launch_t(const CallArgs& a, cudaStream_t s, bool pdl) {
   const int64_t need = (a.Gs + per_block - 1) / per_block;
   int64_t bx = (grid + a.P - 1) / a.P;
   if (bx > need) bx = need;
+  if (a.grid_cap > 0 && bx > a.grid_cap) bx = a.grid_cap;
   if (bx < 1) bx = 1;
 
   cudaLaunchConfig_t cfg = {};

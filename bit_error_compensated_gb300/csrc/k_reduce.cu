@@ -141,7 +141,8 @@ cudaError_t launch_t(const CallArgs& a, cudaStream_t s, bool pdl) {
   const int64_t tiles_per_seg = (a.Gs + T - 1) / T;
   const int64_t ntiles = tiles_per_seg * a.P;
   // A ring of 1 is one tile per block; otherwise one resident wave of blocks.
-  const int64_t blocks = (kReduceRing == 1 || ntiles < resident) ? ntiles : resident;
+  int64_t blocks = (kReduceRing == 1 || ntiles < resident) ? ntiles : resident;
+  if (a.grid_cap > 0 && blocks > a.grid_cap) blocks = a.grid_cap;   // blocks stride over tiles
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)blocks);
   cfg.blockDim = dim3(kRThreads);

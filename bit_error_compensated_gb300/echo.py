@@ -53,6 +53,8 @@ _SIGS = {
     "echo_set_state": (_i32, [_vp, _i32, ctypes.c_float]),
     "echo_set_persistent": (_i32, [_vp, _i32]),
     "echo_debug_hold_push": (_i32, [_vp, _i64]),
+    "echo_debug_set_grid": (_i32, [_vp, _i32]),
+    "echo_debug_check_guards": (_i32, [_vp, ctypes.POINTER(_i32)]),
     "echo_allreduce_noalloc": (_i32, [_i32, _i64, _i32, ctypes.POINTER(_vp), ctypes.POINTER(_vp),
                                       _vp, _vp]),
     "echo_plan_destroy": (None, [_vp]),
@@ -188,6 +190,16 @@ def echo_set_persistent(plan: Plan, on: bool) -> None:
 
 def echo_debug_hold_push(plan: Plan, item: int) -> None:
     _check(_lib.echo_debug_hold_push(plan, item), "echo_debug_hold_push")
+
+
+def echo_debug_set_grid(plan: Plan, blocks: int) -> None:
+    _check(_lib.echo_debug_set_grid(plan, blocks), "echo_debug_set_grid")
+
+
+def echo_debug_check_guards(plan: Plan) -> bool:
+    intact = ctypes.c_int(0)
+    _check(_lib.echo_debug_check_guards(plan, ctypes.byref(intact)), "echo_debug_check_guards")
+    return bool(intact.value)
 
 
 def echo_set_timing(plan: Plan, events) -> None:

@@ -307,6 +307,24 @@ int echo_set_quantizer(echo_plan_t plan, int mode);
 #define ECHO_STATE_F16  2
 int echo_set_state(echo_plan_t plan, int format, float decay);
 
+/*
+ * echo_debug_set_grid -- debug: launch every kernel of the plan's later calls
+ * with at most `blocks` blocks along the dimension its blocks stride over
+ * (0, the default: the launchers' own choice).  The kernels stride, so any
+ * grid computes the same bits; tests compare a 1-block grid with the default
+ * one to catch indexing that depends on the grid.  ECHO_ERR_ARG for blocks < 0.
+ */
+int echo_debug_set_grid(echo_plan_t plan, int blocks);
+
+/*
+ * echo_debug_check_guards -- debug: the plan's receive slots and its own
+ * compensator state are allocated with a 256-byte guard band on each side,
+ * filled with a fixed byte at plan time.  Writes 1 to *intact if all four
+ * bands still hold it (no kernel wrote outside its buffers), else 0.
+ * Synchronizes the device.
+ */
+int echo_debug_check_guards(echo_plan_t plan, int* intact);
+
 /* Free everything the plan allocated.  NULL is accepted. */
 void echo_plan_destroy(echo_plan_t plan);
 

@@ -34,6 +34,14 @@ def _inputs(P, n, seed, scale=1.0):
     return (x * spread).to(torch.bfloat16)
 
 
+SCHEDULES = ["fused", "unfused", "persistent"]
+
+
+def _set_schedule(echo, plan, schedule):
+    echo.echo_set_fused(plan, schedule != "unfused")
+    echo.echo_set_persistent(plan, schedule == "persistent")
+
+
 def _run_sequence(echo, P, Gs, bits_, mode, fused, calls=3, seed=0, inplace=False, quant=0,
                   fmt=0, decay=1.0, g=G, persistent=False):
     n = P * g * Gs
@@ -263,6 +271,52 @@ def test_calls_captured_in_a_cuda_graph(echo, schedule):
     assert echo.echo_get_status(plan) == 0
 
 
+@pytest.mark.parametrize("schedule", SCHEDULES)
+def test_any_grid_size_gives_the_same_bits(echo, schedule):
+    """The kernels stride over their work, so a 1-, 3- or 7-block grid must give
+    the same outputs, state and codes as the launchers' own grid."""
+    P, Gs = 4, 70
+    n = P * G * Gs
+    res = []
+    for cap in (0, 1, 3, 7):
+        plan = echo.echo_plan(P, n, G, 4)
+        _set_schedule(echo, plan, schedule)
+        echo.echo_debug_set_grid(plan, cap)
+        comp = torch.zeros((P, n), device="cuda")
+        outs = []
+        for k in range(3):
+            x = _inputs(P, n, 5000 + k)
+            out = torch.empty_like(x)
+            echo.echo_allreduce(plan, list(x), list(out), comp)
+            outs.append(bits(out))
+        torch.cuda.synchronize()
+        res.append((outs, comp.cpu().numpy().view(np.uint32), echo.echo_debug_wire(plan)))
+    for other in res[1:]:
+        assert all(np.array_equal(a, b) for a, b in zip(res[0][0], other[0]))
+        assert np.array_equal(res[0][1], other[1])
+        assert res[0][2] == other[2]
+
+
+@pytest.mark.parametrize("case", [(1, 128, 4, 5), (2, 64, 8, 9), (3, 256, 4, 7), (4, 128, 8, 37),
+                                  (8, 64, 4, 75), (16, 256, 8, 3), (5, 128, 4, 33)])
+@pytest.mark.parametrize("schedule", SCHEDULES)
+def test_guard_bands_stay_intact(echo, case, schedule):
+    """Nothing is written outside the receive slots or the plan's state: the
+    guard bands around both still hold their fill after calls of ragged shapes
+    in every state format."""
+    P, g, bits_, Gs = case
+    n = P * g * Gs
+    plan = echo.echo_plan(P, n, g, bits_)
+    _set_schedule(echo, plan, schedule)
+    for fmt in (0, 1, 2):
+        echo.echo_set_state(plan, fmt, 0.5 if fmt else 1.0)
+        for k in range(2):
+            x = _inputs(P, n, 6000 + k)
+            echo.echo_allreduce(plan, list(x), list(torch.empty_like(x)), echo.COMP_DEFAULT)
+    torch.cuda.synchronize()
+    assert echo.echo_debug_check_guards(plan)
+
+
 @pytest.mark.parametrize("Gs", [1, 4, 31, 32, 33, 64, 129])
 def test_tile_boundaries(echo, Gs):
     _run_sequence(echo, 4, Gs, 4, "caller", 0, calls=2, seed=Gs)
@@ -355,9 +409,11 @@ def test_reset_and_resume(echo):
     assert not comp.any()
 
 
-def test_overflow_flag(echo):
+@pytest.mark.parametrize("schedule", SCHEDULES)
+def test_overflow_flag(echo, schedule):
     P, n = 2, 2 * G * 4
     plan = echo.echo_plan(P, n, G, 4)
+    _set_schedule(echo, plan, schedule)
     x = _inputs(P, n, 1)
     x[1, 300] = float("inf")
     echo.echo_allreduce(plan, list(x), list(torch.empty_like(x)), None)
@@ -370,8 +426,10 @@ def test_overflow_flag(echo):
     assert oracle.allreduce(bits(x), G, 4)["flagged"] > 0
 
 
-def test_empty_and_degenerate(echo):
+@pytest.mark.parametrize("schedule", SCHEDULES)
+def test_empty_and_degenerate(echo, schedule):
     plan = echo.echo_plan(4, 0, G, 4)
+    _set_schedule(echo, plan, schedule)
     e = torch.empty((4, 0), dtype=torch.bfloat16, device="cuda")
     ptrs = [torch.empty(8, dtype=torch.bfloat16, device="cuda") for _ in range(4)]
     echo.echo_allreduce(plan, ptrs, [torch.empty(8, dtype=torch.bfloat16, device="cuda")
@@ -380,6 +438,7 @@ def test_empty_and_degenerate(echo):
     # all-zero input: step 1, zero point 0, outputs exactly zero
     P, n = 4, 4 * G * 3
     plan = echo.echo_plan(P, n, G, 4)
+    _set_schedule(echo, plan, schedule)
     x = torch.zeros((P, n), dtype=torch.bfloat16, device="cuda")
     out = torch.ones_like(x)
     echo.echo_allreduce(plan, list(x), list(out), echo.COMP_DEFAULT)
@@ -431,10 +490,14 @@ def test_argument_errors(echo):
     with pytest.raises(echo.EchoError) as ei:
         echo.echo_debug_hold_push(plan, -2)
     assert ei.value.status == echo.ECHO_ERR_ARG
+    with pytest.raises(echo.EchoError) as ei:
+        echo.echo_debug_set_grid(plan, -1)
+    assert ei.value.status == echo.ECHO_ERR_ARG
 
 
+@pytest.mark.parametrize("schedule", SCHEDULES)
 @pytest.mark.parametrize("bits_", [4, 8])
-def test_exact_and_near_rounding_ties(echo, bits_):
+def test_exact_and_near_rounding_ties(echo, bits_, schedule):
     """Inputs on a half-step grid make v/s land exactly on half-integers (ties
     to even) or, with a tiny held error added, within 2^-10..2^-22 of them --
     the cases where the kernels' reciprocal fast path must defer to the exact
@@ -455,6 +518,7 @@ def test_exact_and_near_rounding_ties(echo, bits_):
     x = x.cuda()
     comp = torch.from_numpy(e0.copy()).cuda()
     plan = echo.echo_plan(P, n, G, bits_)
+    _set_schedule(echo, plan, schedule)
     lay = echo.echo_wire_layout(plan)
     out = torch.empty_like(x)
     echo.echo_allreduce(plan, list(x), list(out), comp)
