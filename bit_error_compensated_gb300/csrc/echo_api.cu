@@ -6,6 +6,7 @@
 #include <cstdint>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 #include <new>
 
 #include "echo_internal.h"
@@ -66,7 +67,8 @@ int check_device(const echo_plan_s* plan) {
   return dev == plan->device ? ECHO_OK : ECHO_ERR_ARG;
 }
 
-bool g_kernels_prepared[64] = {false};
+bool g_kernels_prepared[64] = {false};   // guarded by g_prepare_mutex
+std::mutex g_prepare_mutex;
 
 // Guard bands around the plan's receive slots and state: filled with a fixed
 // byte at plan time and checked by echo_debug_check_guards.
@@ -159,9 +161,12 @@ int echo_plan(int P, int64_t n, int g, int bits, echo_plan_t* out) {
   const size_t sched_bytes = (size_t)echo::sched_words(P, p->tiles) * sizeof(uint32_t);
 
   cudaError_t e = cudaGetDevice(&p->device);
-  if (e == cudaSuccess && p->device >= 0 && p->device < 64 && !g_kernels_prepared[p->device]) {
-    e = echo::prepare_kernels();
-    if (e == cudaSuccess) g_kernels_prepared[p->device] = true;
+  if (e == cudaSuccess && p->device >= 0 && p->device < 64) {
+    std::lock_guard<std::mutex> lock(g_prepare_mutex);
+    if (!g_kernels_prepared[p->device]) {
+      e = echo::prepare_kernels();
+      if (e == cudaSuccess) g_kernels_prepared[p->device] = true;
+    }
   }
   if (e == cudaSuccess && p->wire_bytes > 0) {
     e = cudaMalloc((void**)&p->wire_alloc, p->wire_bytes + 2 * kGuard);

@@ -6,6 +6,8 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "../../include/echo.h"
 
 namespace echo {
@@ -40,6 +42,15 @@ constexpr int kThreads = 256;
 #ifndef ECHO_REDUCE_MIN_BLOCKS
 #define ECHO_REDUCE_MIN_BLOCKS 3
 #endif
+
+// A launch parameter computed once per device (and key) by the first call:
+// threads that race on the first call compute the same value, and the reads
+// and writes are atomic.  0 means not yet computed.
+struct CachedInt {
+  std::atomic<int> v{0};
+  int get() const { return v.load(std::memory_order_relaxed); }
+  void set(int x) { v.store(x, std::memory_order_relaxed); }
+};
 
 // Status-word bits written by the kernels (read by echo_get_status).
 constexpr int kStatusOverflow = 1;

@@ -309,11 +309,12 @@ call_kernel(const CallArgs a, const CallSched sch) {
 
 template <int BITS, int SF, int MODE, int G, bool FUSED>
 cudaError_t launch_t(const CallArgs& a, const CallSched& sch, cudaStream_t s) {
-  static int resident_cache[64][ECHO_MAX_RANKS + 1] = {{0}};
+  static CachedInt resident_cache[64][ECHO_MAX_RANKS + 1];
   int dev = 0;
   cudaGetDevice(&dev);
   const size_t smem = 2 * (size_t)reduce_stage_bytes<BITS, SF, G, kCallTileElems>(a.P);
-  int& resident = resident_cache[dev & 63][a.P];
+  CachedInt& cached = resident_cache[dev & 63][a.P];
+  int resident = cached.get();
   if (resident == 0) {
     int sms = 0, per_sm = 0;
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -326,6 +327,7 @@ cudaError_t launch_t(const CallArgs& a, const CallSched& sch, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     if (per_sm < 1) return cudaErrorInvalidConfiguration;
     resident = sms * per_sm;
+    cached.set(resident);
   }
   // Rounds of P(P-1) pushes, P reduces and (unfused) P gathers; the lag is
   // about kCallLagWaves waves of items in flight (two per block).

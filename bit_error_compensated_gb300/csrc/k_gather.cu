@@ -33,16 +33,18 @@ constexpr int kGatherUnroll = ECHO_GATHER_UNROLL;  // warp runs in flight per wa
 
 template <int BITS, int MODE, int G>
 cudaError_t launch_t(const CallArgs& a, cudaStream_t s, bool pdl) {
-  static int grid_cache[64] = {0};
+  static CachedInt grid_cache[64];
   int dev = 0;
   cudaGetDevice(&dev);
-  int& grid = grid_cache[dev & 63];
+  CachedInt& cached = grid_cache[dev & 63];
+  int grid = cached.get();
   if (grid == 0) {
     int sms = 0, per_sm = 0;
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gather_kernel<BITS, kGatherUnroll, MODE, G>,
                                                   kThreads, 0);
     grid = sms * (per_sm > 0 ? per_sm : 1);
+    cached.set(grid);
   }
   // Blocks per owner segment: enough to fill the GPU once across the P
   // segments, but no more than the segment has warp runs for.

@@ -126,10 +126,11 @@ push_kernel(const CallArgs a) {
 
 template <int BITS, int SF, int MODE, int G>
 cudaError_t launch_t(const CallArgs& a, cudaStream_t s, bool pdl) {
-  static int resident_cache[64] = {0};
+  static CachedInt resident_cache[64];
   int dev = 0;
   cudaGetDevice(&dev);
-  int& resident = resident_cache[dev & 63];
+  CachedInt& cached = resident_cache[dev & 63];
+  int resident = cached.get();
   if (resident == 0) {
     int sms = 0, per_sm = 0;
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -138,6 +139,7 @@ cudaError_t launch_t(const CallArgs& a, cudaStream_t s, bool pdl) {
     cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, push_kernel<BITS, SF, MODE, G>, kThreads,
                                                   push_smem_bytes<SF>());
     resident = sms * (per_sm > 0 ? per_sm : 1);
+    cached.set(resident);
   }
   const int pairs = a.P * (a.P - 1);
   // Blocks per segment: enough to fill the GPU once across all segments, but

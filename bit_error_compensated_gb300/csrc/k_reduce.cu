@@ -125,17 +125,19 @@ size_t smem_bytes(int P) {
 
 template <int BITS, int SF, bool FUSED, int MODE, int G>
 cudaError_t launch_t(const CallArgs& a, cudaStream_t s, bool pdl) {
-  static int resident_cache[64][ECHO_MAX_RANKS + 1] = {{0}};
+  static CachedInt resident_cache[64][ECHO_MAX_RANKS + 1];
   int dev = 0;
   cudaGetDevice(&dev);
   const size_t smem = smem_bytes<BITS, SF, G>(a.P);
-  int& resident = resident_cache[dev & 63][a.P];
+  CachedInt& cached = resident_cache[dev & 63][a.P];
+  int resident = cached.get();
   if (resident == 0) {
     int sms = 0, per_sm = 0;
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, reduce_kernel<BITS, SF, FUSED, MODE, G>,
                                                   kRThreads, smem);
     resident = sms * (per_sm > 0 ? per_sm : 1);
+    cached.set(resident);
   }
   constexpr int T = tile_groups<G, kTE>();
   const int64_t tiles_per_seg = (a.Gs + T - 1) / T;
