@@ -116,15 +116,19 @@ def profiled_traffic(kernel: str, workload: str):
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    """nvidia-smi clocks and throttle reasons sampled every 20 ms; each sample
+    is stamped with the host clock on arrival, and only the samples inside
+    the window marked around the timed region are reported."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, device_index: int):
+    def __init__(self, device_index: int, interval_ms: int = 20):
+        import threading
         self.proc = None
-        self.lines = []
+        self.samples = []             # (host time, line)
+        self.window = None
         try:
             import torch
             uuid = str(torch.cuda.get_device_properties(device_index).uuid)
@@ -134,38 +138,60 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200", *sel], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", str(interval_ms), *sel],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
+            return
+        self.reader = threading.Thread(target=self._read, daemon=True)
+        self.reader.start()
+        time.sleep(0.1)               # let the first samples arrive
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.monotonic(), line))
+
+    def mark(self, t0: float, t1: float):
+        """The timed region's host-clock window (after synchronizing at both ends)."""
+        self.window = (t0, t1)
 
     def stop(self):
         if self.proc is None:
             return None
-        time.sleep(0.25)
+        time.sleep(0.05)
         self.proc.terminate()
         try:
-            out, _ = self.proc.communicate(timeout=5)
+            self.proc.wait(timeout=5)
         except Exception:
             self.proc.kill()
-            out, _ = self.proc.communicate()
-        sm, mx, reasons = [], [], set()
+        self.reader.join(timeout=5)
+        parsed = []
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in out.splitlines():
+        for t, line in self.samples:
             f = [x.strip() for x in line.split(",")]
             if len(f) < 9:
                 continue
             try:
-                sm.append(float(f[1]))
-                mx.append(float(f[2]))
+                parsed.append((t, float(f[1]), float(f[2]),
+                               [n for n, v in zip(names, f[5:9]) if v.lower() == "active"]))
             except ValueError:
                 continue
-            for name, val in zip(names, f[5:9]):
-                if val.lower() == "active":
-                    reasons.add(name)
-        if not sm:
+        if not parsed:
             return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
-                "reasons": sorted(reasons)}
+        inside = parsed
+        where = "all samples"
+        if self.window is not None:
+            t0, t1 = self.window
+            inside = [p for p in parsed if t0 <= p[0] <= t1]
+            where = "inside the timed region"
+            if not inside:          # a region shorter than the interval: the next sample
+                after = [p for p in parsed if p[0] >= t0]
+                inside = after[:1] or parsed[-1:]
+                where = "first sample after the timed region began"
+        reasons = sorted({r for p in inside for r in p[3]})
+        return {"sm_mhz": statistics.median(p[1] for p in inside),
+                "sm_max_mhz": max(p[2] for p in parsed), "samples": len(inside),
+                "sampled": where, "reasons": reasons}
 
 
 def dist_setup():
@@ -293,12 +319,14 @@ def run_ours(args, rank, local, world):
     clocks = ClockSampler(local)
     barrier(world)
     torch.cuda.synchronize(dev)
+    host_t0 = time.monotonic()
     evs = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
     evs[0].record(stream)
     for i in range(args.steps):
         step()
         evs[i + 1].record(stream)
     torch.cuda.synchronize(dev)
+    clocks.mark(host_t0, time.monotonic())
     barrier(world)
     clk = clocks.stop()
     ms = evs[0].elapsed_time(evs[-1])
