@@ -90,6 +90,49 @@ def _ptr(x) -> int | None:
     return x.data_ptr()
 
 
+def _tensor_ptrs(*args) -> list:
+    """_ptr over (buffer, name, dtypes, min_numel) tuples, with the checks a
+    torch tensor allows: the dtype, contiguous, large enough -- for every
+    buffer first -- then on a CUDA device.  Raw addresses pass unchecked."""
+    import torch
+    tensors = [a for a in args if isinstance(a[0], torch.Tensor)]
+    for t, what, dtypes, min_numel in tensors:
+        if t.dtype not in dtypes:
+            raise ValueError(f"{what}: dtype {t.dtype}, expected {' or '.join(map(str, dtypes))}")
+        if not t.is_contiguous():
+            raise ValueError(f"{what}: tensor must be contiguous")
+        if t.numel() < min_numel:
+            raise ValueError(f"{what}: {t.numel()} elements, at least {min_numel} needed")
+    for t, what, _, _ in tensors:
+        if not t.is_cuda:
+            raise ValueError(f"{what}: tensor must be on a CUDA device")
+    return [_ptr(a[0]) for a in args]
+
+
+def _buffers(P: int, n: int, ins, outs, comp_state, state_fmt: int):
+    """Checked pointers of one call's P inputs, P outputs and state."""
+    if len(ins) != P or len(outs) != P:
+        raise ValueError(f"expected {P} input and {P} output buffers")
+    bf = _bf16()
+    args = ([(t, f"in[{p}]", bf, n) for p, t in enumerate(ins)]
+            + [(t, f"out[{p}]", bf, n) for p, t in enumerate(outs)]
+            + [(None if comp_state is COMP_DEFAULT else comp_state, "comp_state",
+                _state_dtypes(state_fmt), P * n)])
+    ptrs = _tensor_ptrs(*args)
+    comp = COMP_DEFAULT if comp_state is COMP_DEFAULT else ptrs[2 * P]
+    return (_vp * P)(*ptrs[:P]), (_vp * P)(*ptrs[P:2 * P]), comp
+
+
+def _bf16():
+    import torch
+    return (torch.bfloat16,)
+
+
+def _state_dtypes(fmt: int):
+    import torch
+    return ((torch.float32,), (torch.bfloat16,), (torch.float16,))[fmt]
+
+
 def _stream(stream) -> int | None:
     if stream is None:
         import torch
@@ -105,6 +148,7 @@ class Plan:
     def __init__(self, handle: int, P: int, n: int, g: int, bits: int):
         self.handle = handle
         self.P, self.n, self.g, self.bits = P, n, g, bits
+        self.state_fmt = ECHO_STATE_F32          # kept in step with echo_set_state
 
     def __del__(self):
         h, self.handle = getattr(self, "handle", None), None
@@ -126,12 +170,7 @@ def echo_allreduce(plan: Plan, ins, outs, comp_state=None, stream=None) -> None:
     """ins/outs: sequences of P device tensors (or int addresses); comp_state:
     None (uncompensated), COMP_DEFAULT (the plan's own state) or a device
     buffer of echo_comp_bytes(plan) bytes."""
-    P = plan.P
-    if len(ins) != P or len(outs) != P:
-        raise ValueError(f"expected {P} input and {P} output buffers")
-    arr_in = (_vp * P)(*[_ptr(t) for t in ins])
-    arr_out = (_vp * P)(*[_ptr(t) for t in outs])
-    comp = COMP_DEFAULT if comp_state is COMP_DEFAULT else _ptr(comp_state)
+    arr_in, arr_out, comp = _buffers(plan.P, plan.n, ins, outs, comp_state, plan.state_fmt)
     _check(_lib.echo_allreduce(plan, arr_in, arr_out, comp, _stream(stream)), "echo_allreduce")
 
 
@@ -140,7 +179,8 @@ def echo_reset_comp(plan: Plan) -> None:
 
 
 def echo_reset_comp_async(plan: Plan, comp_state=COMP_DEFAULT, stream=None) -> None:
-    comp = COMP_DEFAULT if comp_state is COMP_DEFAULT else _ptr(comp_state)
+    comp = COMP_DEFAULT if comp_state is COMP_DEFAULT else _tensor_ptrs(
+        (comp_state, "comp_state", _state_dtypes(plan.state_fmt), plan.P * plan.n))[0]
     _check(_lib.echo_reset_comp_async(plan, comp, _stream(stream)), "echo_reset_comp_async")
 
 
@@ -182,6 +222,7 @@ def echo_set_quantizer(plan: Plan, mode: int) -> None:
 
 def echo_set_state(plan: Plan, fmt: int = ECHO_STATE_F32, decay: float = 1.0) -> None:
     _check(_lib.echo_set_state(plan, fmt, decay), "echo_set_state")
+    plan.state_fmt = fmt
 
 
 def echo_set_persistent(plan: Plan, on: bool) -> None:
@@ -215,11 +256,8 @@ def echo_allreduce_noalloc(P: int, n: int, bits: int, ins, outs, comp_state=None
                            stream=None) -> None:
     """The no-allocation call (see include/echo.h): no plan, receive slots in
     the library's fixed device array; comp_state is None or a caller buffer."""
-    if len(ins) != P or len(outs) != P:
-        raise ValueError(f"expected {P} input and {P} output buffers")
-    arr_in = (_vp * P)(*[_ptr(t) for t in ins])
-    arr_out = (_vp * P)(*[_ptr(t) for t in outs])
-    _check(_lib.echo_allreduce_noalloc(P, n, bits, arr_in, arr_out, _ptr(comp_state),
+    arr_in, arr_out, comp = _buffers(P, n, ins, outs, comp_state, ECHO_STATE_F32)
+    _check(_lib.echo_allreduce_noalloc(P, n, bits, arr_in, arr_out, comp,
                                        _stream(stream)), "echo_allreduce_noalloc")
 
 

@@ -79,3 +79,36 @@ def test_comp_default_sentinel_matches_header():
                  "ECHO_STATE_BF16", "ECHO_STATE_F16"):
         m = re.search(rf"#define {name}\s+(\d+)", text)
         assert m and int(m.group(1)) == getattr(echo, name), name
+
+
+def test_binding_checks_tensors_before_the_call(lib):
+    """The binding turns a tensor into a pointer only when the pointer means
+    what the C call assumes: the dtype of the buffer's role, contiguous, at
+    least n (state: P*n) elements, on a CUDA device.  A stand-in plan with a
+    null handle shows the checks come before any call into the library."""
+    import torch
+    from bit_error_compensated_gb300 import echo
+    P, n = 2, 256
+    plan = echo.Plan(0, P, n, 128, 4)
+    good = [torch.zeros(n, dtype=torch.bfloat16) for _ in range(P)]
+
+    def rejects(word, ins=good, outs=good, comp=None, noalloc=False):
+        with pytest.raises(ValueError, match=word):
+            if noalloc:
+                echo.echo_allreduce_noalloc(P, n, 4, ins, outs, comp)
+            else:
+                echo.echo_allreduce(plan, ins, outs, comp)
+
+    rejects("dtype", ins=[torch.zeros(n), good[1]])
+    rejects("contiguous", outs=[good[0], torch.zeros(2 * n, dtype=torch.bfloat16)[::2]])
+    rejects("at least 256", ins=[good[0], torch.zeros(n - 1, dtype=torch.bfloat16)])
+    rejects("CUDA device")                                  # right in every other way
+    rejects("expected 2", ins=good[:1])
+    rejects("dtype", comp=torch.zeros(P * n, dtype=torch.bfloat16))   # plan holds fp32
+    rejects("at least 512", comp=torch.zeros(P * n - 1))
+    rejects("dtype", comp=torch.zeros(P * n, dtype=torch.float16), noalloc=True)
+    plan.state_fmt = echo.ECHO_STATE_F16                   # as echo_set_state records it
+    rejects("dtype", comp=torch.zeros(P * n))
+    rejects("CUDA device", comp=torch.zeros(P * n, dtype=torch.float16))
+    with pytest.raises(ValueError, match="dtype"):
+        echo.echo_reset_comp_async(plan, torch.zeros(P * n))
