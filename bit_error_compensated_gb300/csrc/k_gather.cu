@@ -31,6 +31,12 @@ gather_kernel(const CallArgs a) {
 #endif
 constexpr int kGatherUnroll = ECHO_GATHER_UNROLL;  // warp runs in flight per warp
 
+// 1: one pass of kGatherUnroll runs per warp, as many blocks as that takes;
+// 0: one resident wave of blocks striding over the segment.
+#ifndef ECHO_GATHER_ONE_PASS
+#define ECHO_GATHER_ONE_PASS 1
+#endif
+
 template <int BITS, int MODE, int G>
 cudaError_t launch_t(const CallArgs& a, cudaStream_t s, bool pdl) {
   static CachedInt grid_cache[64];
@@ -46,11 +52,11 @@ cudaError_t launch_t(const CallArgs& a, cudaStream_t s, bool pdl) {
     grid = sms * (per_sm > 0 ? per_sm : 1);
     cached.set(grid);
   }
-  // Blocks per owner segment: enough to fill the GPU once across the P
-  // segments, but no more than the segment has warp runs for.
+  // Blocks per owner segment: one pass per warp (or one resident wave across
+  // the P segments), but no more than the segment has warp runs for.
   const int64_t per_block = (int64_t)(kThreads / 32) * kGatherUnroll * (256 / G);
   const int64_t need = (a.Gs + per_block - 1) / per_block;
-  int64_t bx = (grid + a.P - 1) / a.P;
+  int64_t bx = ECHO_GATHER_ONE_PASS ? need : (grid + a.P - 1) / a.P;
   if (bx > need) bx = need;
   if (a.grid_cap > 0 && bx > a.grid_cap) bx = a.grid_cap;
   if (bx < 1) bx = 1;

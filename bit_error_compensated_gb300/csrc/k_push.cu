@@ -8,18 +8,21 @@
 // element is added before quantizing, and the error this quantization reveals,
 // v - deq(q), replaces it (the update changes nothing this call computes).
 //
-// Grid: blockIdx.y is a (sender p, owner o) segment pair, blockIdx.x strides
-// over the segment's groups, so no division is needed per group.  g/16 lanes
+// Grid: blockIdx.y is a (sender p, owner o) segment pair, blockIdx.x and the
+// warp pick units of the segment's groups, so no division is needed per group.  g/16 lanes
 // per group of g elements (quant.cuh); a warp works on 512 adjacent elements
 // at a time (a "unit": 512/g groups, 1 KB of bf16 input and 2 KB of fp32 or
 // 1 KB of bf16 state, contiguous).
 //
-// Each warp runs its own kPushStages-deep pipeline: lane 0 issues 1-D bulk
-// copies (cp.async.bulk, the TMA engine) of the next units' input and state
-// into the warp's shared-memory stages, each stage completing on its own
-// mbarrier, while the warp quantizes the current unit from shared memory and
-// stores codes, meta and the new state straight to global memory.  Loads stay
-// in flight during compute without holding registers.  The waits are bounded
+// Each warp takes a few units (push_units): lane 0 issues 1-D
+// bulk copies (cp.async.bulk, the TMA engine) of the unit's input and state
+// into the warp's shared-memory stage, completing on the stage's mbarrier,
+// then the warp quantizes the unit from shared memory and stores codes, meta
+// and the new state straight to global memory.  With more units per warp,
+// push_stages stages keep the next units' copies in flight during compute
+// without holding registers.  Many short blocks, placed by the hardware as SMs
+// free up, keep HBM busy to the end of the grid: measured faster than one
+// resident wave of blocks striding over the segment.  The waits are bounded
 // and their outcome is the same for the whole warp: on timeout the warp
 // records ECHO_ERR_TIMEOUT, waits once more (bounded) for each copy it still
 // has in flight, and returns.  HBM-bound: per element 2 B of input and the
@@ -29,22 +32,50 @@
 namespace echo {
 namespace {
 
+// Units per warp: each block's warps take push_units<SF>() units each (0: one
+// resident wave of blocks striding over the segment).  An fp32-state unit
+// moves 3 KB and one per warp measured fastest; a 2-byte-state (or stateless)
+// unit moves 2 KB (1 KB) and four per warp did, two in flight at a time.
+#ifndef ECHO_PUSH_UNITS_F32
+#define ECHO_PUSH_UNITS_F32 1
+#endif
+#ifndef ECHO_PUSH_UNITS_2B
+#define ECHO_PUSH_UNITS_2B 4
+#endif
 #ifndef ECHO_PUSH_STAGES
 #define ECHO_PUSH_STAGES 2
 #endif
-constexpr int kPushStages = ECHO_PUSH_STAGES;      // units in flight per warp
+template <int SF>
+constexpr int push_units() { return SF == kStateF32 ? ECHO_PUSH_UNITS_F32 : ECHO_PUSH_UNITS_2B; }
+
+// Units in flight per warp: no more stages than units.
+template <int SF>
+constexpr int push_stages() {
+  return push_units<SF>() > 0 && push_units<SF>() < ECHO_PUSH_STAGES ? push_units<SF>()
+                                                                       : ECHO_PUSH_STAGES;
+}
 
 template <int SF>
 constexpr size_t push_smem_bytes() {
-  return (size_t)(kThreads / 32) * kPushStages * push_unit_bytes<SF>();
+  return (size_t)(kThreads / 32) * push_stages<SF>() * push_unit_bytes<SF>();
 }
 
+// Resident blocks per SM the compiler must allow for (0: its own choice).
+#ifndef ECHO_PUSH_MIN_BLOCKS
+#define ECHO_PUSH_MIN_BLOCKS 0
+#endif
+#if ECHO_PUSH_MIN_BLOCKS > 0
+#define ECHO_PUSH_BOUNDS __launch_bounds__(kThreads, ECHO_PUSH_MIN_BLOCKS)
+#else
+#define ECHO_PUSH_BOUNDS __launch_bounds__(kThreads)
+#endif
+
 template <int BITS, int SF, int MODE, int G>
-__global__ void __launch_bounds__(kThreads)
+__global__ void ECHO_PUSH_BOUNDS
 push_kernel(const CallArgs a) {
   constexpr int NL = G / 16;                        // lanes per group
   constexpr int GPW = 32 / NL;                      // groups per unit
-  constexpr int S = kPushStages;
+  constexpr int S = push_stages<SF>();
   constexpr int SB = push_unit_bytes<SF>();
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(8) uint64_t bars[kThreads / 32][S];
@@ -142,11 +173,13 @@ cudaError_t launch_t(const CallArgs& a, cudaStream_t s, bool pdl) {
     cached.set(resident);
   }
   const int pairs = a.P * (a.P - 1);
-  // Blocks per segment: enough to fill the GPU once across all segments, but
-  // no more than the segment has units for (8 warps x 1 unit each).
+  // Blocks per segment: push_units units for each warp, or one resident wave
+  // across all segments; no more than the segment has units for (8 warps x 1
+  // unit each).
   const int64_t per_block = (int64_t)(kThreads / 32) * (32 / (G / 16));
   const int64_t need = (a.Gs + per_block - 1) / per_block;
-  int64_t bx = (resident + pairs - 1) / pairs;
+  constexpr int U = push_units<SF>();
+  int64_t bx = U > 0 ? (need + U - 1) / U : (resident + pairs - 1) / pairs;
   if (bx > need) bx = need;
   if (a.grid_cap > 0 && bx > a.grid_cap) bx = a.grid_cap;
   if (bx < 1) bx = 1;

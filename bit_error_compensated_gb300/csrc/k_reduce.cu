@@ -7,17 +7,18 @@
 // The entry pass of the compensator (adding the owner's held error to its own
 // segment) is fused in as well.
 //
-// Blocks walk owner tiles of kReduceTileElems elements (kReduceTileElems / g
-// groups) through a ring of kReduceRing shared-memory stages.  Thread 0 fills
-// a stage with 1-D bulk copies (cp.async.bulk, the TMA engine) of the tile's
-// P-1 received code tiles, their meta words, the owner's bf16 tile and its
-// state tile, all completing on the stage's mbarrier; the block works from
-// shared memory (g/16 lanes per group) and stores its results straight to
-// global memory,
-// and thread 0 refills the stage with the block's next tile as soon as every
-// thread is done reading it, so the next tile loads while this one is
-// computed.  With a ring of 1 every block takes exactly one tile.  The waits
-// on the mbarriers are bounded and their outcome is the same for the whole
+// Each block takes one owner tile of kReduceTileElems elements
+// (kReduceTileElems / g groups).  Thread 0 fills a shared-memory stage with
+// 1-D bulk copies (cp.async.bulk, the TMA engine) of the tile's P-1 received
+// code tiles, their meta words, the owner's bf16 tile and its state tile, all
+// completing on the stage's mbarrier; the block works from shared memory
+// (g/16 lanes per group) and stores its results straight to global memory.
+// Many short blocks, placed by the hardware as SMs free up, keep the copy
+// engines and HBM busy to the end of the grid; with ECHO_REDUCE_RING = R > 1
+// a single resident wave of blocks walks the tiles instead, through a ring of
+// R stages that thread 0 refills as soon as every thread is done reading one
+// (measured slower: the last tiles of the wave leave HBM idle).  The waits on
+// the mbarriers are bounded and their outcome is the same for the whole
 // block: if one gives up, the block records ECHO_ERR_TIMEOUT in the status
 // word, waits once more (also bounded) for its copies in flight, and returns.
 //
@@ -26,7 +27,7 @@
 #include "stages.cuh"
 
 #ifndef ECHO_REDUCE_RING
-#define ECHO_REDUCE_RING 2
+#define ECHO_REDUCE_RING 1
 #endif
 
 namespace echo {
@@ -37,8 +38,18 @@ constexpr int kReduceRing = ECHO_REDUCE_RING;   // tiles in flight per block
 constexpr int kTE = kReduceTileElems;
 constexpr int kRThreads = 32 * kReduceWarps;
 
+// Resident blocks per SM the compiler must allow for: the fused kernels fit
+// 8 blocks (64 registers a thread) without spilling, the unfused ones 6.
+#ifndef ECHO_REDUCE_MIN_BLOCKS_FUSED
+#define ECHO_REDUCE_MIN_BLOCKS_FUSED 4
+#endif
+template <bool FUSED>
+constexpr int reduce_min_blocks() {
+  return (FUSED ? ECHO_REDUCE_MIN_BLOCKS_FUSED : ECHO_REDUCE_MIN_BLOCKS) * kThreads / kRThreads;
+}
+
 template <int BITS, int SF, bool FUSED, int MODE, int G>
-__global__ void __launch_bounds__(kRThreads, ECHO_REDUCE_MIN_BLOCKS * kThreads / kRThreads)
+__global__ void __launch_bounds__(kRThreads, reduce_min_blocks<FUSED>())
 reduce_kernel(const CallArgs a, int64_t tiles_per_seg, int64_t ntiles) {
   constexpr int T = tile_groups<G, kTE>();
   constexpr int R = kReduceRing;

@@ -68,7 +68,8 @@ def test_noalloc_allocates_nothing_per_call():
 def test_noalloc_rejects_sizes_beyond_its_scratch_and_the_plan_state():
     from bit_error_compensated_gb300 import echo
     P, n = 4, 4 * G * 16384 * 2          # 4096 x 4096 per rank: slots ~36 MB > 32 MiB
-    dummy = [torch.empty(8, dtype=torch.bfloat16, device="cuda") for _ in range(P)]
+    keep = [torch.empty(8, dtype=torch.bfloat16, device="cuda") for _ in range(P)]
+    dummy = [t.data_ptr() for t in keep]   # raw addresses: the library's own check decides
     with pytest.raises(echo.EchoError) as ei:
         echo.echo_allreduce_noalloc(P, n, 4, dummy, dummy, None)
     assert ei.value.status == echo.ECHO_ERR_TOO_LARGE
