@@ -22,23 +22,23 @@ constexpr bool group_supported(int g) { return g == 64 || g == 128 || g == 256; 
 // supported g, so that every tile's meta words form a 16-byte-aligned copy.
 // Warps per reduce block: each takes 512 elements of a tile per pass.
 #ifndef ECHO_REDUCE_TILE
-#define ECHO_REDUCE_TILE 16   // in groups of 128
+#define ECHO_REDUCE_TILE 8    // in groups of 128
 #endif
 #ifndef ECHO_REDUCE_WARPS
-#define ECHO_REDUCE_WARPS 4
+#define ECHO_REDUCE_WARPS 2
 #endif
 constexpr int kReduceTileElems = ECHO_REDUCE_TILE * 128;
 constexpr int kReduceWarps = ECHO_REDUCE_WARPS;
 static_assert(kReduceTileElems % (4 * 256) == 0, "reduce tile: a multiple of 4 groups of 256");
 // Elements per tile of the persistent kernel: one 512-element unit per warp.
 constexpr int kCallTileElems = 4096;
-// Threads per block of every kernel.
+// Threads per block of the push, gather and persistent kernels (the reduce
+// kernel's blocks have kReduceWarps warps).
 constexpr int kThreads = 256;
-// Blocks of 256 threads per SM the register allocation of the reduce and
-// persistent kernels must allow (the reduce kernel scales it to its block
-// size).  Their shared-memory stages already cap residency near this (about
-// 62 KB per 256 threads at 4 ranks), so a lower figure buys registers
-// without costing occupancy.
+// Blocks of 256 threads per SM the register allocation of the unfused reduce
+// kernel and the persistent kernel must allow (the reduce kernel scales it to
+// its block size; the fused one has its own, higher bound).  3 leaves them up
+// to 80 registers a thread, which they use without spilling.
 #ifndef ECHO_REDUCE_MIN_BLOCKS
 #define ECHO_REDUCE_MIN_BLOCKS 3
 #endif

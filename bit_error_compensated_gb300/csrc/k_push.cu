@@ -55,9 +55,22 @@ constexpr int push_stages() {
                                                                        : ECHO_PUSH_STAGES;
 }
 
+// Warps per push block: small blocks, so that the hardware can fill SMs as
+// they free up, but not so many blocks that launching them limits the rate.
+#ifndef ECHO_PUSH_WARPS_F32
+#define ECHO_PUSH_WARPS_F32 2
+#endif
+#ifndef ECHO_PUSH_WARPS_2B
+#define ECHO_PUSH_WARPS_2B 1
+#endif
+template <int SF>
+constexpr int push_threads() {
+  return 32 * (SF == kStateF32 ? ECHO_PUSH_WARPS_F32 : ECHO_PUSH_WARPS_2B);
+}
+
 template <int SF>
 constexpr size_t push_smem_bytes() {
-  return (size_t)(kThreads / 32) * push_stages<SF>() * push_unit_bytes<SF>();
+  return (size_t)(push_threads<SF>() / 32) * push_stages<SF>() * push_unit_bytes<SF>();
 }
 
 // Resident blocks per SM the compiler must allow for (0: its own choice).
@@ -65,9 +78,9 @@ constexpr size_t push_smem_bytes() {
 #define ECHO_PUSH_MIN_BLOCKS 0
 #endif
 #if ECHO_PUSH_MIN_BLOCKS > 0
-#define ECHO_PUSH_BOUNDS __launch_bounds__(kThreads, ECHO_PUSH_MIN_BLOCKS)
+#define ECHO_PUSH_BOUNDS __launch_bounds__(push_threads<SF>(), ECHO_PUSH_MIN_BLOCKS)
 #else
-#define ECHO_PUSH_BOUNDS __launch_bounds__(kThreads)
+#define ECHO_PUSH_BOUNDS __launch_bounds__(push_threads<SF>())
 #endif
 
 template <int BITS, int SF, int MODE, int G>
@@ -78,7 +91,7 @@ push_kernel(const CallArgs a) {
   constexpr int S = push_stages<SF>();
   constexpr int SB = push_unit_bytes<SF>();
   extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ __align__(8) uint64_t bars[kThreads / 32][S];
+  __shared__ __align__(8) uint64_t bars[push_threads<SF>() / 32][S];
 
   const int P = a.P;
   const int p = (int)blockIdx.y / (P - 1);          // sender
@@ -91,8 +104,8 @@ push_kernel(const CallArgs a) {
   const int lane = threadIdx.x & 31;
   const int sub = lane / NL;                        // group within the unit
   const int q = lane % NL;                          // lane within the group
-  const int64_t wg = (int64_t)blockIdx.x * (kThreads / 32) + warp;
-  const int64_t nw = (int64_t)gridDim.x * (kThreads / 32);
+  const int64_t wg = (int64_t)blockIdx.x * (push_threads<SF>() / 32) + warp;
+  const int64_t nw = (int64_t)gridDim.x * (push_threads<SF>() / 32);
   const int64_t nunits = (Gs + GPW - 1) / GPW;
   uint8_t* wbuf = smem + (size_t)warp * S * SB;
   const uint32_t bar0 = smem_addr(&bars[warp][0]);
@@ -167,16 +180,15 @@ cudaError_t launch_t(const CallArgs& a, cudaStream_t s, bool pdl) {
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     cudaFuncSetAttribute(push_kernel<BITS, SF, MODE, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          (int)push_smem_bytes<SF>());
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, push_kernel<BITS, SF, MODE, G>, kThreads,
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, push_kernel<BITS, SF, MODE, G>, push_threads<SF>(),
                                                   push_smem_bytes<SF>());
     resident = sms * (per_sm > 0 ? per_sm : 1);
     cached.set(resident);
   }
   const int pairs = a.P * (a.P - 1);
   // Blocks per segment: push_units units for each warp, or one resident wave
-  // across all segments; no more than the segment has units for (8 warps x 1
-  // unit each).
-  const int64_t per_block = (int64_t)(kThreads / 32) * (32 / (G / 16));
+  // across all segments; never more than one unit for each warp.
+  const int64_t per_block = (int64_t)(push_threads<SF>() / 32) * (32 / (G / 16));
   const int64_t need = (a.Gs + per_block - 1) / per_block;
   constexpr int U = push_units<SF>();
   int64_t bx = U > 0 ? (need + U - 1) / U : (resident + pairs - 1) / pairs;
@@ -186,7 +198,7 @@ cudaError_t launch_t(const CallArgs& a, cudaStream_t s, bool pdl) {
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)bx, (unsigned)pairs);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(push_threads<SF>());
   cfg.dynamicSmemBytes = push_smem_bytes<SF>();
   cfg.stream = s;
   cudaLaunchAttribute attr[1];

@@ -29,6 +29,10 @@
 #ifndef ECHO_REDUCE_RING
 #define ECHO_REDUCE_RING 1
 #endif
+// Tiles per block (0: one resident wave of blocks walking all the tiles).
+#ifndef ECHO_REDUCE_TILES_PER_BLOCK
+#define ECHO_REDUCE_TILES_PER_BLOCK 1
+#endif
 
 namespace echo {
 namespace {
@@ -38,8 +42,8 @@ constexpr int kReduceRing = ECHO_REDUCE_RING;   // tiles in flight per block
 constexpr int kTE = kReduceTileElems;
 constexpr int kRThreads = 32 * kReduceWarps;
 
-// Resident blocks per SM the compiler must allow for: the fused kernels fit
-// 8 blocks (64 registers a thread) without spilling, the unfused ones 6.
+// Resident threads per SM the compiler must allow for: the fused kernels fit
+// 1024 (64 registers a thread) without spilling, the unfused ones 768.
 #ifndef ECHO_REDUCE_MIN_BLOCKS_FUSED
 #define ECHO_REDUCE_MIN_BLOCKS_FUSED 4
 #endif
@@ -153,8 +157,8 @@ cudaError_t launch_t(const CallArgs& a, cudaStream_t s, bool pdl) {
   constexpr int T = tile_groups<G, kTE>();
   const int64_t tiles_per_seg = (a.Gs + T - 1) / T;
   const int64_t ntiles = tiles_per_seg * a.P;
-  // A ring of 1 is one tile per block; otherwise one resident wave of blocks.
-  int64_t blocks = (kReduceRing == 1 || ntiles < resident) ? ntiles : resident;
+  constexpr int64_t TPB = ECHO_REDUCE_TILES_PER_BLOCK;
+  int64_t blocks = TPB > 0 ? (ntiles + TPB - 1) / TPB : (ntiles < resident ? ntiles : resident);
   if (a.grid_cap > 0 && blocks > a.grid_cap) blocks = a.grid_cap;   // blocks stride over tiles
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)blocks);

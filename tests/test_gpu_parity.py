@@ -272,9 +272,12 @@ def test_calls_captured_in_a_cuda_graph(echo, schedule):
 
 
 @pytest.mark.parametrize("schedule", SCHEDULES)
-def test_any_grid_size_gives_the_same_bits(echo, schedule):
+@pytest.mark.parametrize("fmt", [0, 1, None])          # fp32 state, bf16 state, none
+def test_any_grid_size_gives_the_same_bits(echo, schedule, fmt):
     """The kernels stride over their work, so a 1-, 3- or 7-block grid must give
-    the same outputs, state and codes as the launchers' own grid."""
+    the same outputs, state and codes as the launchers' own grid (where a push
+    warp takes one unit with fp32 state and up to four, two in flight, with a
+    2-byte state or none)."""
     P, Gs = 4, 70
     n = P * G * Gs
     res = []
@@ -282,7 +285,10 @@ def test_any_grid_size_gives_the_same_bits(echo, schedule):
         plan = echo.echo_plan(P, n, G, 4)
         _set_schedule(echo, plan, schedule)
         echo.echo_debug_set_grid(plan, cap)
-        comp = torch.zeros((P, n), device="cuda")
+        comp = None
+        if fmt is not None:
+            echo.echo_set_state(plan, fmt, 1.0)
+            comp = torch.zeros((P, n), dtype=STATE_DTYPES[fmt], device="cuda")
         outs = []
         for k in range(3):
             x = _inputs(P, n, 5000 + k)
@@ -290,10 +296,12 @@ def test_any_grid_size_gives_the_same_bits(echo, schedule):
             echo.echo_allreduce(plan, list(x), list(out), comp)
             outs.append(bits(out))
         torch.cuda.synchronize()
-        res.append((outs, comp.cpu().numpy().view(np.uint32), echo.echo_debug_wire(plan)))
+        state = None if comp is None else comp.cpu().view(torch.uint8).numpy()
+        res.append((outs, state, echo.echo_debug_wire(plan)))
     for other in res[1:]:
         assert all(np.array_equal(a, b) for a, b in zip(res[0][0], other[0]))
-        assert np.array_equal(res[0][1], other[1])
+        assert (res[0][1] is None) == (other[1] is None)
+        assert res[0][1] is None or np.array_equal(res[0][1], other[1])
         assert res[0][2] == other[2]
 
 
