@@ -11,10 +11,11 @@
 // tile is claimed when its pushes are most likely done and pushes, reduces
 // and gathers, which load memory and ALU differently, share the GPU.  Slots
 // whose tile is out of range are skipped.  A tile is kCallTileElems elements
-// of a segment.  Blocks claim items from one atomic ticket counter.  A reduce item waits for a per-tile counter of
-// finished pushes, a gather item for a per-tile reduce flag; each consumer
-// resets what it consumed, and the last block to finish resets the ticket
-// counter, so the words are zero again for the next call.  An item only ever
+// of a segment.  Blocks claim items from one atomic ticket counter.  A reduce
+// item waits for a per-tile counter of finished pushes, a gather item for a
+// per-tile reduce flag; each consumer resets what it consumed, and the last
+// block to finish resets the ticket counter, so the words are zero again for
+// the next call.  An item only ever
 // waits on items with smaller tickets; the launch is cooperative, so all
 // blocks are co-resident.
 //
@@ -318,9 +319,9 @@ cudaError_t launch_t(const CallArgs& a, const CallSched& sch, cudaStream_t s) {
   if (resident == 0) {
     int sms = 0, per_sm = 0;
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int smem_max = (int)(2 * reduce_stage_bytes<BITS, SF, G, kCallTileElems>(ECHO_MAX_RANKS));
     cudaError_t e = cudaFuncSetAttribute(call_kernel<BITS, SF, MODE, G, FUSED>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)(2 * reduce_stage_bytes<BITS, SF, G, kCallTileElems>(ECHO_MAX_RANKS)));
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max);
     if (e != cudaSuccess) return e;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, call_kernel<BITS, SF, MODE, G, FUSED>,
                                                       kThreads, smem);

@@ -8,25 +8,26 @@
 // element is added before quantizing, and the error this quantization reveals,
 // v - deq(q), replaces it (the update changes nothing this call computes).
 //
-// Grid: blockIdx.y is a (sender p, owner o) segment pair, blockIdx.x and the
-// warp pick units of the segment's groups, so no division is needed per group.  g/16 lanes
-// per group of g elements (quant.cuh); a warp works on 512 adjacent elements
-// at a time (a "unit": 512/g groups, 1 KB of bf16 input and 2 KB of fp32 or
-// 1 KB of bf16 state, contiguous).
+// Grid: blockIdx.y is a (sender p, owner o) segment pair; blockIdx.x and the
+// warp pick units of the segment's groups, so no division is needed per
+// group.  g/16 lanes per group of g elements (quant.cuh); a warp works on 512
+// adjacent elements at a time (a "unit": 512/g groups, 1 KB of bf16 input and
+// 2 KB of fp32 or 1 KB of 2-byte state, contiguous).
 //
-// Each warp takes a few units (push_units): lane 0 issues 1-D
-// bulk copies (cp.async.bulk, the TMA engine) of the unit's input and state
-// into the warp's shared-memory stage, completing on the stage's mbarrier,
-// then the warp quantizes the unit from shared memory and stores codes, meta
-// and the new state straight to global memory.  With more units per warp,
-// push_stages stages keep the next units' copies in flight during compute
-// without holding registers.  Many short blocks, placed by the hardware as SMs
-// free up, keep HBM busy to the end of the grid: measured faster than one
-// resident wave of blocks striding over the segment.  The waits are bounded
-// and their outcome is the same for the whole warp: on timeout the warp
-// records ECHO_ERR_TIMEOUT, waits once more (bounded) for each copy it still
-// has in flight, and returns.  HBM-bound: per element 2 B of input and the
-// state read, the state and b/8 B of codes written, plus 4 B of meta a group.
+// Blocks are small and short: 2 warps taking one unit each with fp32 state,
+// 1 warp taking four units with a 2-byte state or none.  Lane 0 issues 1-D
+// bulk copies (cp.async.bulk, the TMA engine) of a unit's input and state into
+// the warp's shared-memory stage, completing on the stage's mbarrier; the warp
+// quantizes the unit from shared memory and stores codes, meta and the new
+// state straight to global memory.  With several units per warp, push_stages
+// stages keep the next units' copies in flight during compute without holding
+// registers.  Many short blocks, placed by the hardware as SMs free up, keep
+// HBM busy to the end of the grid: measured faster than one resident wave of
+// blocks striding over the segment.  The waits are bounded and their outcome
+// is the same for the whole warp: on timeout the warp records
+// ECHO_ERR_TIMEOUT, waits once more (bounded) for each copy it still has in
+// flight, and returns.  HBM-bound: per element 2 B of input and the state
+// read, the state and b/8 B of codes written, plus 4 B of meta a group.
 #include "stages.cuh"
 
 namespace echo {
@@ -180,8 +181,8 @@ cudaError_t launch_t(const CallArgs& a, cudaStream_t s, bool pdl) {
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     cudaFuncSetAttribute(push_kernel<BITS, SF, MODE, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          (int)push_smem_bytes<SF>());
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, push_kernel<BITS, SF, MODE, G>, push_threads<SF>(),
-                                                  push_smem_bytes<SF>());
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, push_kernel<BITS, SF, MODE, G>,
+                                                  push_threads<SF>(), push_smem_bytes<SF>());
     resident = sms * (per_sm > 0 ? per_sm : 1);
     cached.set(resident);
   }
