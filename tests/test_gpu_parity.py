@@ -325,9 +325,14 @@ def test_guard_bands_stay_intact(echo, case, schedule):
     assert echo.echo_debug_check_guards(plan)
 
 
-@pytest.mark.parametrize("Gs", [1, 4, 31, 32, 33, 64, 129])
-def test_tile_boundaries(echo, Gs):
-    _run_sequence(echo, 4, Gs, 4, "caller", 0, calls=2, seed=Gs)
+@pytest.mark.parametrize("Gs", [1, 4, 7, 8, 9, 31, 32, 33, 64, 129])
+@pytest.mark.parametrize("fmt", [0, 1])
+@pytest.mark.parametrize("fused", [0, 1])
+def test_tile_boundaries(echo, Gs, fmt, fused):
+    """Segments of one group up to past several reduce tiles (8 groups of 128)
+    and push blocks (8 groups with fp32 state, 16 with a 2-byte state), ending
+    on and beside their edges."""
+    _run_sequence(echo, 4, Gs, 4, "caller", fused, calls=2, seed=Gs, fmt=fmt)
 
 
 @pytest.mark.parametrize("fused", [0, 1])
