@@ -100,16 +100,23 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(kernel: str, workload: str):
-    """DRAM bytes per launch of `kernel` from the committed ncu summary, or None
-    when there is none or the kernel sources changed since it was taken."""
+def traffic_key(workload: str, bits: int, g: int, state: str, quantizer: int, schedule: str) -> str:
+    """The configuration an ncu traffic figure belongs to: everything that picks
+    a different kernel instantiation or grid (the decay does neither)."""
+    return f"{workload} bits={bits} g={g} state={state} quantizer={quantizer} schedule={schedule}"
+
+
+def profiled_traffic(kernel: str, key: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary of the
+    configuration `key` (traffic_key), or None when there is none or the
+    kernel sources changed since it was taken."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             rec = json.load(f)
     except Exception:
         return None
-    ent = rec.get(workload, {}).get(kernel)
+    ent = rec.get(key, {}).get(kernel)
     if not ent or ent.get("source_hash") != kernel_source_hash():
         return None
     return ent.get("dram_bytes_per_launch")
@@ -377,7 +384,8 @@ def run_ours(args, rank, local, world):
     achieved = kbytes / (avg_us[dominant] / 1e6) / 1e9
     kname = {"push": "push_kernel", "reduce": "reduce_kernel", "gather": "gather_kernel",
              "call": "call_kernel"}[dominant]
-    traffic = profiled_traffic(kname, w.name)
+    schedule = "persistent" if args.persistent else "fused" if fused else "unfused"
+    traffic = profiled_traffic(kname, traffic_key(w.name, bits, g, args.state, args.quantizer, schedule))
     roofline = {"bound": "hbm", "kernel": kname, "achieved": round(achieved, 1), "peak": hbm,
                 "unit": "GB/s", "frac": round(achieved / hbm, 4), "traffic": traffic,
                 "algorithmic_bytes_per_launch": int(kbytes), "avg_launch_us": round(avg_us[dominant], 2),

@@ -69,3 +69,29 @@ def test_byte_model_matches_the_per_element_totals():
     assert bench.call_model_bytes(P, n, 4, True, False, 2) == pytest.approx(P * n * (8 + 2 * c))
     assert (bench.call_model_bytes(P, n, 4, True, False) -
             bench.call_model_bytes(P, n, 4, True, False, 2)) == pytest.approx(4 * P * n)
+
+
+def test_profiled_traffic_belongs_to_one_configuration(tmp_path, monkeypatch):
+    """A DRAM-traffic figure from ncu is reported only for the configuration it
+    was captured on, and only while the kernel sources are unchanged."""
+    import json
+    import bench
+    (tmp_path / "profiles").mkdir()
+    f32 = bench.traffic_key("p4_2048x4096", 4, 128, "f32", 0, "fused")
+    bf16 = bench.traffic_key("p4_2048x4096", 4, 128, "bf16", 0, "fused")
+    rec = {f32: {"push_kernel": {"dram_bytes_per_launch": 100, "source_hash": "h1"}},
+           bf16: {"push_kernel": {"dram_bytes_per_launch": 60, "source_hash": "h1"}}}
+    (tmp_path / "profiles" / "traffic.json").write_text(json.dumps(rec))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda: "h1")
+    assert bench.profiled_traffic("push_kernel", f32) == 100
+    assert bench.profiled_traffic("push_kernel", bf16) == 60
+    assert bench.profiled_traffic("reduce_kernel", f32) is None
+    for other in (bench.traffic_key("p4_2048x4096", 8, 128, "f32", 0, "fused"),
+                  bench.traffic_key("p4_2048x4096", 4, 64, "f32", 0, "fused"),
+                  bench.traffic_key("p4_2048x4096", 4, 128, "f32", 1, "fused"),
+                  bench.traffic_key("p4_2048x4096", 4, 128, "f32", 0, "unfused"),
+                  bench.traffic_key("p4_8192x4096", 4, 128, "f32", 0, "fused")):
+        assert bench.profiled_traffic("push_kernel", other) is None
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda: "h2")   # sources changed
+    assert bench.profiled_traffic("push_kernel", f32) is None
