@@ -164,7 +164,10 @@ push_kernel(const CallArgs a) {
       fence_proxy_async();
       issue(i + S, st);
     }
-    push_finish<BITS, SF, MODE, G>(a, v, valid, j, q, pl.es, pl.cs, pl.ms, codes_pol);
+    if (SF != kNoState && a.decay != 1.0f)           // uniform: decayed error feedback
+      push_finish<BITS, SF, MODE, G, true>(a, v, valid, j, q, pl.es, pl.cs, pl.ms, codes_pol);
+    else
+      push_finish<BITS, SF, MODE, G, false>(a, v, valid, j, q, pl.es, pl.cs, pl.ms, codes_pol);
   }
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }

@@ -51,6 +51,12 @@ __device__ __forceinline__ float max3_nan(float a, float b, float c) {
   asm("max.NaN.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
   return r;
 }
+// The largest of three, NaN operands ignored (NaN only if all three are).
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
 
 // Butterfly over the NL lanes of a group (aligned lane blocks of NL).
 template <int NL>
@@ -228,9 +234,11 @@ __device__ __forceinline__ void quantize8(const float v[8], const GroupGrid& gg,
     sub2(r[k], r[k + 1], r[k], r[k + 1], M, M);
   }
   sub_n<8>(e, t, r);
-  float dev = 0.0f;
-#pragma unroll
-  for (int k = 0; k < 8; ++k) dev = fmaxf(dev, fabsf(e[k]));
+  // max |e| (NaN operands ignored, as by fmaxf), three at a time
+  float dev = max3(fabsf(e[0]), fabsf(e[1]), fabsf(e[2]));
+  dev = max3(dev, fabsf(e[3]), fabsf(e[4]));
+  dev = max3(dev, fabsf(e[5]), fabsf(e[6]));
+  dev = fmaxf(dev, fabsf(e[7]));
   if (dev >= kFastRintLimit) {
     // (+ 0 turns a -0 from rintf into +0, as the fast path gives, so that
     // cm * s below is +0 where (q - z) * s is.)
@@ -474,14 +482,20 @@ __device__ __forceinline__ void state_load8(const uint8_t* base, int i, float e[
 
 // Keeps the revealed errors r of a half in global memory at element index i
 // (a multiple of 8; the state buffer is 32-byte aligned): decay * r, stored
-// as fp32 (one 32-byte store) or rounded to bf16 (one 16-byte store).  With
-// decay 1 the product is r itself (exact for every non-NaN value), so plain
-// error feedback takes the same code.
-template <int SF>
+// as fp32 (one 32-byte store) or rounded to bf16 or fp16 (one 16-byte
+// store).  With DECAY false the multiply is skipped, for decay 1: r * 1 is r
+// itself for every value (a NaN from the subtraction is already the
+// canonical one a multiply would give).
+template <int SF, bool DECAY = true>
 __device__ __forceinline__ void state_store8(uint8_t* base, int64_t i, const float r[8],
                                              float decay) {
   float t[8];
-  mul_ns<8>(t, r, decay);
+  if constexpr (DECAY) {
+    mul_ns<8>(t, r, decay);
+  } else {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) t[k] = r[k];
+  }
   if constexpr (SF == kStateF32) {
     asm volatile("st.global.v8.f32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
                  :: "l"(base + 4 * i), "f"(t[0]), "f"(t[1]), "f"(t[2]), "f"(t[3]), "f"(t[4]),

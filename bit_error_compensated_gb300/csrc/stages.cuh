@@ -63,7 +63,7 @@ __device__ __forceinline__ void store_codes8(uint8_t* p, const float c[8], uint6
 // Quantizes group j of a sender's segment (all 32 lanes call it; lanes whose
 // group is not `valid` compute on zeros and store nothing).  cs, ms: the
 // receive slot's codes and meta; es: the sender's state of the segment.
-template <int BITS, int SF, int MODE, int G>
+template <int BITS, int SF, int MODE, int G, bool DECAY = true>
 __device__ __forceinline__ void push_finish(const CallArgs& a, const float v[16], bool valid,
                                             int64_t j, int q, uint8_t* es, uint8_t* cs,
                                             uint32_t* ms, uint64_t codes_pol) {
@@ -80,7 +80,7 @@ __device__ __forceinline__ void push_finish(const CallArgs& a, const float v[16]
       if constexpr (SF != kNoState) {
         float r[8];
         sub_n<8>(r, v + 8 * hh, d);
-        state_store8<SF>(es, j * G + half_at<NL>(hh, q), r, a.decay);
+        state_store8<SF, DECAY>(es, j * G + half_at<NL>(hh, q), r, a.decay);
       }
     }
   }
@@ -180,7 +180,7 @@ __device__ __forceinline__ void reduce_issue_codes(const CallArgs& a, uint8_t* s
 // Computes one owner tile (t groups from j0 of segment o) held in a stage,
 // writing the gather codes, meta, new owner state and (FUSED) all P outputs
 // to global memory.  The NW warps of the block take part; no block barrier.
-template <int BITS, int SF, bool FUSED, int MODE, int G, int TE, int NW>
+template <int BITS, int SF, bool FUSED, int MODE, int G, int TE, int NW, bool DECAY = true>
 __device__ __forceinline__ void reduce_tile(const CallArgs& a, const uint8_t* stage, int o,
                                             int64_t j0, int t) {
   constexpr float L = (float)((1 << BITS) - 1);
@@ -274,7 +274,7 @@ __device__ __forceinline__ void reduce_tile(const CallArgs& a, const uint8_t* st
         uint8_t* eo = reinterpret_cast<uint8_t*>(a.comp) + (int64_t)o * a.n * EB;
         float r[8];
         sub_n<8>(r, acc + 8 * hh, yb);
-        state_store8<SF>(eo, e, r, a.decay);
+        state_store8<SF, DECAY>(eo, e, r, a.decay);
       }
       if (FUSED) {
         for (int r = 0; r < P; ++r) __stcs(reinterpret_cast<uint4*>(a.out[r] + e), y);
