@@ -570,11 +570,13 @@ class OracleSample:
                        f"positions ({pos.size} of {w.P * Gs}), 4 distinct inputs cycled, state carried; "
                        f"single-threaded")
         self.i = 0
+        self.ties = 0          # values whose v/s the oracle found exactly on a half-integer
 
     def step(self):
         import oracle
-        oracle.group_positions(self.P, self.owners, self.bits, self.inputs[self.i % len(self.inputs)], self.e,
-                               **self.opts)
+        r = oracle.group_positions(self.P, self.owners, self.bits, self.inputs[self.i % len(self.inputs)],
+                                   self.e, **self.opts)
+        self.ties += r["ties"]
         self.i += 1
 
 
@@ -595,7 +597,8 @@ def cpu_baseline_oracle(args, budget_s=12.0):
         steps += 1
     sec = time.perf_counter() - t
     return {"value": round(s.bytes_per_step * steps / sec / 1e9, 4), "unit": "GB/s", "cores": 1,
-            "kind": "oracle", "sample": f"{steps} steps; " + s.sample}
+            "kind": "oracle", "sample": f"{steps} steps; " + s.sample,
+            "exact_rounding_ties": s.ties, "ties_counted_over_calls": s.i}
 
 
 def run_reference(args, rank, world):
@@ -620,7 +623,8 @@ def run_reference(args, rank, world):
                        "state": {"format": STATE_NAME[args.state],
                                  "decay": args.decay}},
             "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                             "sample": s.sample},
+                             "sample": s.sample, "exact_rounding_ties": s.ties,
+                             "ties_counted_over_calls": s.i},
             "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
 
