@@ -112,3 +112,28 @@ def test_binding_checks_tensors_before_the_call(lib):
     rejects("CUDA device", comp=torch.zeros(P * n, dtype=torch.float16))
     with pytest.raises(ValueError, match="dtype"):
         echo.echo_reset_comp_async(plan, torch.zeros(P * n))
+
+
+def test_binding_passes_raw_addresses_and_the_default_state_through(lib, monkeypatch):
+    """Integer addresses are the caller's responsibility and reach the C call
+    unchanged, as does the ECHO_COMP_DEFAULT sentinel; a stand-in for the C
+    entry point records what it was given (no GPU call is made)."""
+    from bit_error_compensated_gb300 import echo
+    P, n = 2, 256
+    plan = echo.Plan(0, P, n, 128, 4)
+    seen = {}
+
+    class FakeLib:
+        def echo_allreduce(self, plan_, ins, outs, comp, stream):
+            seen.update(ins=[ins[i] for i in range(P)], outs=[outs[i] for i in range(P)],
+                        comp=comp)
+            return 0
+
+    monkeypatch.setattr(echo, "_lib", FakeLib())
+    echo.echo_allreduce(plan, [4096, 8192], [12288, 16384], echo.COMP_DEFAULT, stream=0)
+    assert seen["ins"] == [4096, 8192] and seen["outs"] == [12288, 16384]
+    assert seen["comp"] is echo.COMP_DEFAULT
+    echo.echo_allreduce(plan, [4096, 8192], [12288, 16384], 1 << 20, stream=0)
+    assert seen["comp"] == 1 << 20
+    echo.echo_allreduce(plan, [4096, 8192], [12288, 16384], None, stream=0)
+    assert seen["comp"] is None
