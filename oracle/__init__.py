@@ -150,7 +150,10 @@ STATE_F32, STATE_BF16, STATE_F16 = 0, 1, 2
 
 def quantize_group(v: np.ndarray, bits: int, mode: int = ZERO_AWARE):
     """Q_b on one group.  Returns (codes uint8, s_bits, z_bits, flagged, ties);
-    for the naive zero-point mode z_bits is the fp16 offset m."""
+    for the naive zero-point mode z_bits is the fp16 offset m.  ``ties`` counts
+    the exact rounding ties met: every rint whose fp32 argument lies exactly on
+    a half-integer (a code's v/s -- (v - m)/s for the naive zero point -- and
+    the zero-aware zero point's -lo/s), negative or positive, before any clamp."""
     lib = _load()
     v = np.ascontiguousarray(v, dtype=np.float32)
     q = np.zeros(v.size, dtype=np.uint8)

@@ -208,7 +208,11 @@ enum { kZeroAware = 0, kNaiveZeroPoint = 1, kSymmetric = 2 };
 //
 // Returns 1 when the group holds a non-finite value or its scale does not fit
 // fp16 (the results are then unspecified), else 0.  Writes the codes q[i] in
-// [0, 2^b-1], the fp16 scale bits and the fp16 zero-point bits.
+// [0, 2^b-1], the fp16 scale bits and the fp16 zero-point bits.  When `ties`
+// is not NULL, adds the number of exact rounding ties met: each rint whose
+// fp32 argument lies exactly on a half-integer (both neighbours equally near,
+// settled half-to-even), whether that argument is negative or positive and
+// whether or not the code is clamped afterwards.
 // ---------------------------------------------------------------------------
 static int quantize_naive(const float* v, int len, int bits, uint8_t* q, uint16_t* s_bits,
                           uint16_t* z_bits, int64_t* ties);
@@ -240,8 +244,11 @@ int oracle_quantize_group(const float* v, int len, int bits, uint8_t* q,
   }
   if (!std::isfinite(s)) bad = 1;
 
-  // Step 4: integer zero point, the code that decodes to exactly 0.
-  float zf = std::rint(-lo / s);
+  // Step 4: integer zero point, the code that decodes to exactly 0.  Its
+  // rint is a rounding decision like a code's, so an exact tie here counts too.
+  const float rz = -lo / s;
+  if (ties && std::isfinite(rz) && (rz - std::floor(rz)) == 0.5f) ++*ties;
+  float zf = std::rint(rz);
   zf = std::fmin(std::fmax(zf, 0.0f), Lf);
   const int z = (int)zf;
 
@@ -382,7 +389,10 @@ void oracle_pack_codes(const uint8_t* q, int64_t count, int bits, uint8_t* out) 
 //   acc    [len]     the owner's fp32 sum, or NULL
 //   nq     [P][len]  number of quantizations each rank's contribution went
 //                    through before reaching y, or NULL
-//   ties   counter of exact rounding ties (v/s exactly k + 1/2), or NULL
+//   ties   counter of exact rounding ties, or NULL: every rint of the two
+//          quantizations whose fp32 argument is exactly k + 1/2 (a code's v/s,
+//          or (v - m)/s for the naive zero point, and the zero-aware zero
+//          point's -lo/s), counted before any clamp
 // Returns the number of quantizations flagged non-finite (0 when all is fine).
 // ---------------------------------------------------------------------------
 // The value the state keeps for a revealed error r: decay * r (one fp32

@@ -541,3 +541,35 @@ def test_exact_and_near_rounding_ties(echo, bits_, schedule):
     assert np.array_equal(bits(out), ref["out"])
     assert_wire_equal(wire_to_canonical(echo.echo_debug_wire(plan), lay, P, n, bits_), ref, P)
     assert_state_close(comp.cpu().numpy(), e_ref)
+
+
+@pytest.mark.parametrize("schedule", SCHEDULES)
+@pytest.mark.parametrize("P", [2, 4])
+@pytest.mark.parametrize("bits_", [4, 8])
+def test_tie_count_by_construction(echo, bits_, P, schedule):
+    """Inputs whose number of exact rounding ties is fixed by construction
+    (tests/test_oracle_ties.py): half-step grids at stage 1 in some groups and
+    at stage 2 in others, zero-point ties, and near ties within 2^-10..2^-22 of
+    a step.  The values ride in the caller's fp32 state over bf16 zeros, so
+    v = x + e is exact.  The oracle must count exactly the constructed ties,
+    and the GPU must produce the same codes, outputs and state on them."""
+    from test_oracle_ties import _whole_call_values
+    Gs = 36                                      # more than one reduce tile, ragged
+    n = P * G * Gs
+    rng = np.random.default_rng(60 + 10 * P + bits_)
+    e0, expected = _whole_call_values(rng, P, bits_, G, Gs, 0.25)
+    x = torch.zeros((P, n), dtype=torch.bfloat16, device="cuda")
+    comp = torch.from_numpy(e0.copy()).cuda()
+    plan = echo.echo_plan(P, n, G, bits_)
+    _set_schedule(echo, plan, schedule)
+    lay = echo.echo_wire_layout(plan)
+    out = torch.empty_like(x)
+    echo.echo_allreduce(plan, list(x), list(out), comp)
+    torch.cuda.synchronize()
+    assert echo.echo_get_status(plan) == 0
+    e_ref = e0.copy()
+    ref = oracle.allreduce(bits(x), G, bits_, e=e_ref, want_wire=True)
+    assert ref["ties"] == expected
+    assert np.array_equal(bits(out), ref["out"])
+    assert_wire_equal(wire_to_canonical(echo.echo_debug_wire(plan), lay, P, n, bits_), ref, P)
+    assert_state_close(comp.cpu().numpy(), e_ref)
