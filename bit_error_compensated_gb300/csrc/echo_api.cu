@@ -451,7 +451,7 @@ const char* echo_strerror(int status) {
     case ECHO_OK: return "ok";
     case ECHO_ERR_ARG: return "invalid argument";
     case ECHO_ERR_SHAPE: return "n must be a non-negative multiple of P*g";
-    case ECHO_ERR_UNSUPPORTED: return "unsupported configuration (bits must be 4 or 8, g must be 128)";
+    case ECHO_ERR_UNSUPPORTED: return "unsupported configuration (bits must be 4 or 8, g must be 64, 128 or 256)";
     case ECHO_ERR_ALIGN: return "device pointer not 16-byte aligned (32 for a compensator state)";
     case ECHO_ERR_CUDA: return cudaGetErrorString(g_last_cuda);
     case ECHO_ERR_OVERFLOW: return "non-finite input or fp16 step overflow in some group";

@@ -59,6 +59,10 @@ extern "C" int echo_allreduce_noalloc(int P, int64_t n, int bits, const void* co
   if (bits != 4 && bits != 8) return ECHO_ERR_UNSUPPORTED;
   if (n < 0 || n % ((int64_t)P * echo::kGroup) != 0) return ECHO_ERR_SHAPE;
   if (comp_state == ECHO_COMP_DEFAULT) return ECHO_ERR_ARG;
+  // Every element needs at least b/8 bytes of gather codes in the array, so a
+  // larger n can never fit; rejecting it first also keeps the layout sums
+  // below far from any overflow.
+  if (n > (int64_t)(ECHO_NOALLOC_SCRATCH_BYTES * 8 / bits)) return ECHO_ERR_TOO_LARGE;
 
   // Receive-slot layout, the same as a plan's (see echo_wire_layout).
   const int64_t Gs = n / P / echo::kGroup;

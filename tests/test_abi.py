@@ -137,3 +137,20 @@ def test_binding_passes_raw_addresses_and_the_default_state_through(lib, monkeyp
     assert seen["comp"] == 1 << 20
     echo.echo_allreduce(plan, [4096, 8192], [12288, 16384], None, stream=0)
     assert seen["comp"] is None
+
+
+def test_noalloc_rejects_huge_n_before_any_layout_arithmetic(lib):
+    """n so large that the receive-slot sums would wrap around 2^64 must come
+    back as ECHO_ERR_TOO_LARGE from the host checks (no CUDA call is made)."""
+    from bit_error_compensated_gb300 import echo
+    fn = lib.echo_allreduce_noalloc
+    fn.argtypes = [ctypes.c_int, ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
+                   ctypes.c_void_p, ctypes.c_void_p]
+    fn.restype = ctypes.c_int
+    P = 16
+    ptrs = (ctypes.c_void_p * P)(*[0x100000 * (p + 1) for p in range(P)])
+    limit = (32 << 20) * 8
+    for bits_ in (4, 8):
+        for n in (1 << 61, (1 << 62) + P * 128 * 7, (limit // bits_ // (P * 128) + 1) * P * 128):
+            assert n % (P * 128) == 0
+            assert fn(P, n, bits_, ptrs, ptrs, None, None) == echo.ECHO_ERR_TOO_LARGE
