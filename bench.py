@@ -4,12 +4,15 @@
 Metric: bf16-input GB/s per emulated all-reduce call (P ranks x n bf16
 elements per call / time per call), with the fraction of the HBM roofline.
 
-A step is one pass of the whole hot path over the workload's call sequence:
-for the default workload (P=4, 2048 x 4096 per rank, per-channel LogNormal
-scales with 1% x20 outlier channels) that is 64 compensated calls (32 layers x
-attention+MLP sites), each on its own inputs, all resident in HBM before the
-timed region.  Every call runs the push, reduce and gather kernels of
-libecho.so through its C ABI.
+A step is one pass of the whole hot path over the workload's call sequence.
+The default workload is the largest: P=8 ranks of 1 GiB bf16 each (512 Mi
+elements per rank, i.i.d. N(0, 0.02^2)), one compensated call with 4-bit codes
+and g=128 (the pages quote their throughput figure for 1 GB messages), inputs
+resident in HBM before the timed region.  Every call runs the push and reduce
+kernels of libecho.so (the reduce writes the P outputs) through its C ABI.
+The same line also times, under "also", the 8-bit variant of that workload,
+the other workloads of 64 MiB per rank, and the latency of the smallest one
+(P=2, n=4096), plain and replayed as a CUDA graph.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -18,7 +21,8 @@ independent replica of the workload on its own GPU (the emulated all-reduce
 has no cross-GPU exchange); the value is the work of all ranks over the
 slowest rank's time.  `--impl reference` times the CPU oracle (the plain
 single-threaded restatement the GPU path is checked against) on the host
-cores, on a sample of the same workload.
+cores, its group positions split over all of them, on a sample of the same
+workload.
 """
 from __future__ import annotations
 
@@ -106,20 +110,28 @@ def traffic_key(workload: str, bits: int, g: int, state: str, quantizer: int, sc
     return f"{workload} bits={bits} g={g} state={state} quantizer={quantizer} schedule={schedule}"
 
 
-def profiled_traffic(kernel: str, key: str):
+def profiled_traffic(kernel: str, key: str, elements: int):
     """DRAM bytes per launch of `kernel` from the committed ncu summary of the
-    configuration `key` (traffic_key), or None when there is none or the
-    kernel sources changed since it was taken."""
+    configuration `key` (traffic_key), as (bytes, note); (None, None) when there
+    is none or the kernel sources changed since it was taken.  A capture taken
+    on a smaller case of the same configuration (`captured_elements` input
+    elements per call instead of `elements`) is scaled by the element ratio,
+    since every byte these streaming kernels move is proportional to it."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             rec = json.load(f)
     except Exception:
-        return None
+        return None, None
     ent = rec.get(key, {}).get(kernel)
     if not ent or ent.get("source_hash") != kernel_source_hash():
-        return None
-    return ent.get("dram_bytes_per_launch")
+        return None, None
+    dram = ent.get("dram_bytes_per_launch")
+    cap = ent.get("captured_elements")
+    if dram is None or not cap or cap == elements:
+        return dram, None
+    return int(dram * elements / cap), (f"scaled by {elements / cap:g} from an ncu capture of "
+                                         f"{cap} input elements per call ({ent.get('capture')})")
 
 
 class ClockSampler:
@@ -256,32 +268,66 @@ def set_state(echo, plan, args):
     return 4 if args.state == "f32" else 2
 
 
-def build_inputs(number, seq, distinct, device):
-    import torch
-    from bit_error_compensated_gb300.workloads import WORKLOADS, rank_inputs
+def shape_of(number, tokens=None):
+    """(name, P, n) of a workload, with the token count overridden for
+    profiling runs on a smaller case of the same shape family."""
+    from bit_error_compensated_gb300.workloads import WORKLOADS
     w = WORKLOADS[number]
-    xs = torch.empty((distinct, w.P, w.n), dtype=torch.bfloat16, device=device)
+    if not tokens or tokens == w.tokens:
+        return w.name, w.P, w.n
+    return f"{w.name}@{tokens}x{w.hidden}", w.P, tokens * w.hidden
+
+
+def build_inputs(number, seq, distinct, device, tokens=None):
+    import torch
+    from bit_error_compensated_gb300.workloads import rank_inputs
+    _, P, n = shape_of(number, tokens)
+    xs = torch.empty((distinct, P, n), dtype=torch.bfloat16, device=device)
     for k in range(distinct):
-        rank_inputs(number, seq[k], device, out=xs[k])
+        rank_inputs(number, seq[k], device, tokens=tokens or None, out=xs[k])
     return xs
+
+
+def workload_config(args, world, seq):
+    """The workload a line measures: the same dict for the GPU arm and for the
+    reference arm (the oracle on the host cores), so the two can be paired."""
+    from bit_error_compensated_gb300.workloads import WORKLOADS
+    name, P, n = shape_of(args.workload, args.tokens)
+    sb = 4 if args.state == "f32" else 2
+    calls = len(seq)
+    comp = sum(1 for c in seq if c.state != "none")
+    distinct = calls
+    return {"workload": name, "description": WORKLOADS[args.workload].description,
+            "P": P, "n_per_rank": n, "bits": args.bits, "g": args.g,
+            "calls_per_step": calls, "compensated": comp == calls,
+            "fused_gather": bool(args.fused), "quantizer": QUANTIZERS[args.quantizer],
+            "schedule": ("one persistent kernel" if args.persistent else
+                         "two kernels" if args.fused else "three kernels")
+                        + (", CUDA graph of the call sequence" if args.graph else ""),
+            "state": {"format": STATE_NAME[args.state], "decay": args.decay},
+            "io": "bf16 in/out, fp32 arithmetic, "
+                  f"{args.bits}-bit codes, {STATE_NAME[args.state]} state",
+            "l2": f"inputs distinct per call ({distinct} x {P * n * 2 >> 20} MiB resident); "
+                  f"per-call working set {(P * n * (2 + 2 + 2 * sb)) >> 20} MiB > L2 "
+                  f"({L2_BYTES >> 20} MiB)",
+            "parallelism": f"replicas x{world}" if world > 1 else "1 GPU, P ranks emulated"}
 
 
 def run_ours(args, rank, local, world):
     import torch
     from bit_error_compensated_gb300 import echo
-    from bit_error_compensated_gb300.workloads import WORKLOADS, call_sequence
+    from bit_error_compensated_gb300.workloads import call_sequence
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     stream = torch.cuda.current_stream(dev)
     number, bits, fused = args.workload, args.bits, args.fused
-    w = WORKLOADS[number]
-    P, n = w.P, w.n
+    wname, P, n = shape_of(number, args.tokens)
     seq = call_sequence(number, steps=1)
     if args.calls:
         seq = seq[:args.calls]
     calls = len(seq)
-    xs = build_inputs(number, seq, calls, dev)
+    xs = build_inputs(number, seq, calls, dev, args.tokens)
     out = torch.empty((P, n), dtype=torch.bfloat16, device=dev)
     g = args.g
     plan = echo.echo_plan(P, n, g, bits)
@@ -339,6 +385,8 @@ def run_ours(args, rank, local, world):
     ms = evs[0].elapsed_time(evs[-1])
     step_ms = sorted(evs[i].elapsed_time(evs[i + 1]) for i in range(args.steps))
     max_ms = max_over_ranks(ms, world)
+    if echo.echo_get_status(plan, stream) != 0:
+        raise RuntimeError("device status word set during the timed steps")
 
     bytes_in_per_call = P * n * 2
     value = whole_job_gbs(bytes_in_per_call * calls, args.steps, world, max_ms)
@@ -379,35 +427,31 @@ def run_ours(args, rank, local, world):
     else:
         ran = [k for k in ("push", "reduce", "gather") if k in kb_comp and (k != "push" or P > 1)]
     avg_us = {k: per_kernel_ms[k] / nlaunch * 1e3 for k in ran}
+    kb_avg = {k: (compensated_calls * kb_comp[k] + (calls - compensated_calls) * kb_unc[k]) / calls
+              for k in ran}
+    per_kernel_frac = {k: round(kb_avg[k] / (avg_us[k] / 1e6) / 1e9 / hbm, 4) for k in ran}
     dominant = max(avg_us, key=lambda k: avg_us[k])
-    kbytes = (compensated_calls * kb_comp[dominant] + (calls - compensated_calls) * kb_unc[dominant]) / calls
+    kbytes = kb_avg[dominant]
     achieved = kbytes / (avg_us[dominant] / 1e6) / 1e9
     kname = {"push": "push_kernel", "reduce": "reduce_kernel", "gather": "gather_kernel",
              "call": "call_kernel"}[dominant]
     schedule = "persistent" if args.persistent else "fused" if fused else "unfused"
-    traffic = profiled_traffic(kname, traffic_key(w.name, bits, g, args.state, args.quantizer, schedule))
+    traffic, traffic_note = profiled_traffic(
+        kname, traffic_key(shape_of(number)[0], bits, g, args.state, args.quantizer, schedule),
+        P * n)
     roofline = {"bound": "hbm", "kernel": kname, "achieved": round(achieved, 1), "peak": hbm,
                 "unit": "GB/s", "frac": round(achieved / hbm, 4), "traffic": traffic,
                 "algorithmic_bytes_per_launch": int(kbytes), "avg_launch_us": round(avg_us[dominant], 2),
                 "peak_source": hbm_src}
+    if traffic_note:
+        roofline["traffic_note"] = traffic_note
 
     result = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(max_ms / args.steps, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded; shapes and distributions of the workload, no dataset)",
-        "config": {"workload": w.name, "P": P, "n_per_rank": n, "bits": bits, "g": g,
-                   "calls_per_step": calls, "compensated": compensated_calls == calls,
-                   "fused_gather": bool(fused), "quantizer": QUANTIZERS[args.quantizer],
-                   "schedule": ("one persistent kernel" if args.persistent else
-                                "two kernels" if fused else "three kernels")
-                               + (", CUDA graph of the call sequence" if args.graph else ""),
-                   "state": {"format": STATE_NAME[args.state], "decay": args.decay},
-                   "io": "bf16 in/out, fp32 arithmetic, "
-                   f"{bits}-bit codes, {STATE_NAME[args.state]} state",
-                   "l2": f"inputs distinct per call ({calls} x {P * n * 2 >> 20} MiB resident); "
-                         f"per-call working set {(P * n * (2 + 2 + 2 * sb)) >> 20} MiB > L2",
-                   "parallelism": f"replicas x{world}" if world > 1 else "1 GPU, P ranks emulated"},
+        "config": workload_config(args, world, seq),
         "hbm_roofline_frac": round(model / per_call_s / 1e9 / hbm, 4),
         "hbm_roofline_frac_spec": round(model / per_call_s / 1e9 / SPEC_HBM_GBS, 4),
         "model_bytes_per_call": int(model),
@@ -415,6 +459,7 @@ def run_ours(args, rank, local, world):
         "step_ms": {"median": round(step_ms[len(step_ms) // 2], 4), "min": round(step_ms[0], 4),
                     "max": round(step_ms[-1], 4)},
         "per_kernel_us": {k: round(v, 2) for k, v in avg_us.items()},
+        "per_kernel_frac": per_kernel_frac,
         "roofline": roofline,
         "gpu_launches": launches_per_call * calls * args.steps,
         "clocks": clk,
@@ -422,29 +467,48 @@ def run_ours(args, rank, local, world):
 
     if not args.no_e2e:
         result["e2e"] = run_e2e(args, echo, plan, xs, seq, states, dev, world)
+        torch.cuda.empty_cache()
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        # the oracle's sample is gathered from the inputs already on the device
+        result["cpu_baseline"] = cpu_baseline_oracle(args, budget_s=args.cpu_budget, xs=xs, seq=seq)
     if args.also:
         result["also"] = {}
-        for num in [int(v) for v in args.also.split(",") if v]:
-            result["also"][WORKLOADS[num].name] = time_other(echo, num, bits, fused, dev, args)
-        if not args.persistent:
+        for spec in [v for v in args.also.split(",") if v]:
+            num, b = parse_also(spec, bits)
+            label = shape_of(num)[0] + (f" ({b}-bit codes)" if b != bits else "")
+            result["also"][label] = time_other(echo, num, b, fused, dev, args)
+        if not args.persistent and not args.tokens:
             # the same workload with the other gather variant, for comparison
             other = "separate gather kernel" if fused else "gather fused into reduce"
-            result["also"][f"{w.name} ({other})"] = time_other(echo, number, bits, not fused, dev, args)
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        result["cpu_baseline"] = cpu_baseline_oracle(args, budget_s=args.cpu_budget)
+            del xs, call_args, out_rows, out
+            torch.cuda.empty_cache()
+            result["also"][f"{wname} ({other})"] = time_other(echo, number, bits, not fused, dev, args)
     del plan
     return result
 
 
+def parse_also(spec: str, default_bits: int):
+    """'4' -> (4, default bits); '3b8' -> workload 3 with 8-bit codes."""
+    if "b" in spec:
+        num, b = spec.split("b")
+        return int(num), int(b)
+    return int(spec), default_bits
+
+
 def run_e2e(args, echo, plan, xs, seq, states, dev, world):
     """The same call sequence from pinned host memory: every call copies its
-    inputs host->device and its result (the reduced tensor, identical on every
-    rank) device->host inside the timed region.  Copies run on their own
-    streams, double-buffered, so the copy of call k+1 overlaps call k."""
+    inputs host->device and one of its P output rows (all P rows hold the same
+    bits: the result every rank receives) device->host, inside the timed
+    region.  Copies run on their own streams, double-buffered, so the copy of
+    call k+1 overlaps call k."""
     import torch
     P, n = xs.shape[1], xs.shape[2]
     distinct = min(8, xs.shape[0])
-    host_in = [xs[k].cpu().pin_memory() for k in range(distinct)]
+    host_in = []
+    for k in range(distinct):
+        h = torch.empty((P, n), dtype=torch.bfloat16, pin_memory=True)
+        h.copy_(xs[k])
+        host_in.append(h)
     host_out = torch.empty((2, n), dtype=torch.bfloat16).pin_memory()
     dev_in = [torch.empty((P, n), dtype=torch.bfloat16, device=dev) for _ in range(2)]
     dev_out = [torch.empty((P, n), dtype=torch.bfloat16, device=dev) for _ in range(2)]
@@ -490,13 +554,17 @@ def run_e2e(args, echo, plan, xs, seq, states, dev, world):
     return {"value": round(v, 2), "unit": "GB/s", "h2d_bytes_per_step": P * n * 2 * calls,
             "d2h_bytes_per_step": n * 2 * calls, "ms_per_step": round(max_ms / args.steps, 3),
             "timing": "host wall clock around K steps, synchronized at both ends",
+            "d2h": "one of the P output rows per call: every rank receives the same bits, "
+                   "so one row is the call's whole result",
             "host_inputs": f"{distinct} distinct pinned input sets cycled over the {calls} calls"}
 
 
-def time_other(echo, number, bits, fused, dev, args, reps=3):
-    """Time another workload's call sequence (8 distinct inputs cycled): GB/s
-    and the pipeline's fraction of the HBM roofline.  No parity here: the
-    GPU tests check these workloads against the oracle."""
+def time_other(echo, number, bits, fused, dev, args):
+    """Time another workload's call sequence (8 distinct inputs cycled, at
+    least 20 calls): GB/s and the pipeline's fraction of the HBM roofline.
+    For the launch-bound P=2, n=4096 workload also the time per call with the
+    sequence replayed as a CUDA graph.  No parity here: the GPU tests check
+    these workloads against the oracle."""
     import torch
     from bit_error_compensated_gb300.workloads import WORKLOADS, call_sequence
     w = WORKLOADS[number]
@@ -509,121 +577,227 @@ def time_other(echo, number, bits, fused, dev, args, reps=3):
     echo.echo_set_quantizer(plan, args.quantizer)
     echo.echo_set_persistent(plan, args.persistent)
     sb = set_state(echo, plan, args)
-    bwd = torch.zeros((w.P, w.n), dtype=state_dtype(args), device=dev)
+    bwd = torch.zeros((w.P, w.n), dtype=state_dtype(args), device=dev) if any(
+        c.state == "bwd" for c in seq) else None
     comps = [{"fwd": echo.COMP_DEFAULT, "bwd": bwd, "none": None}[c.state] for c in seq]
     rows = [list(xs[k]) for k in range(distinct)]
     out_rows = list(out)
     stream = torch.cuda.current_stream(dev)
+    launch_bound = w.P * w.n * 2 < (1 << 20)
+    reps = max(3, -(-(2000 if launch_bound else 20) // len(seq)))
 
-    def step():
+    def step(s=stream):
         for k in range(len(seq)):
-            echo.echo_allreduce(plan, rows[k % distinct], out_rows, comps[k], stream)
+            echo.echo_allreduce(plan, rows[k % distinct], out_rows, comps[k], s)
 
-    step()
-    torch.cuda.synchronize(dev)
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    for _ in range(reps):
-        step()
-    b.record(stream)
-    torch.cuda.synchronize(dev)
-    per_call_s = a.elapsed_time(b) / 1e3 / (reps * len(seq))
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize(dev)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        return a.elapsed_time(b) / 1e3 / (reps * len(seq))
+
+    per_call_s = timed(step)
+    if echo.echo_get_status(plan, stream) != 0:
+        raise RuntimeError(f"device status word set while timing {w.name}")
     hbm, _ = load_peaks()
     comp_calls = sum(1 for c in seq if c.state != "none")
     model = (comp_calls * call_model_bytes(w.P, w.n, bits, True, fused, sb, args.g) +
              (len(seq) - comp_calls) * call_model_bytes(w.P, w.n, bits, False, fused, g=args.g)) / len(seq)
-    del plan, xs
+    res = {"gbs": round(w.P * w.n * 2 / per_call_s / 1e9, 2), "us_per_call": round(per_call_s * 1e6, 2),
+           "hbm_roofline_frac": round(model / per_call_s / 1e9 / hbm, 4), "bits": bits,
+           "calls": len(seq) * reps, "calls_per_step": len(seq),
+           "states": sorted({c.state for c in seq})}
+    if launch_bound:
+        res["note"] = "launch-bound (a few KiB per call): the time per call is the figure"
+        graph = torch.cuda.CUDAGraph()
+        gstream = torch.cuda.Stream(dev)
+        gstream.wait_stream(stream)
+        with torch.cuda.graph(graph, stream=gstream):
+            step(gstream)
+        torch.cuda.synchronize(dev)
+        res["us_per_call_cuda_graph"] = round(timed(graph.replay) * 1e6, 2)
+        del graph
+    del plan, xs, bwd
     torch.cuda.empty_cache()
-    return {"gbs": round(w.P * w.n * 2 / per_call_s / 1e9, 2), "us_per_call": round(per_call_s * 1e6, 2),
-            "hbm_roofline_frac": round(model / per_call_s / 1e9 / hbm, 4), "calls": len(seq) * reps}
+    return res
 
 
 # ------------------------------------------------------------- the oracle ----
 
+def host_cpu_info() -> dict:
+    """Usable host cores and the CPU model (lscpu, else /proc/cpuinfo)."""
+    try:
+        nproc = len(os.sched_getaffinity(0))
+    except Exception:
+        nproc = os.cpu_count() or 1
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        names = [ln.split(":", 1)[1].strip() for ln in out.splitlines()
+                 if ln.strip().lower().startswith("model name")]
+        model = "; ".join(dict.fromkeys(names)) or None
+    except Exception:
+        pass
+    if model is None:
+        try:
+            with open("/proc/cpuinfo") as f:
+                for ln in f:
+                    if ln.lower().startswith(("model name", "cpu part")):
+                        model = ln.split(":", 1)[1].strip()
+                        break
+        except Exception:
+            pass
+    return {"nproc": nproc, "cpu_model": model or "unknown"}
+
+
 class OracleSample:
-    """The oracle on a fixed 1/8 sample of one workload's group positions.
+    """The oracle on a fixed sample of one workload's group positions (1/8 of
+    them; 1/64 for the 1 GiB-per-rank workload).
 
     Each step is one call of the workload's sequence restricted to those
     positions -- exactly the oracle's work on them, since positions are
-    independent -- with 4 distinct inputs cycled and the state carried."""
+    independent -- with up to 4 distinct inputs cycled and the state carried.
+    The inputs are the GPU arm's own (gathered from `xs` on the device) when
+    given, else drawn from the workload's generator on the GPU when there is
+    one (the same bits the GPU arm draws), else on the CPU (same distribution,
+    other bits)."""
 
-    def __init__(self, number, bits, g=G, mode=0, state_fmt=0, decay=1.0):
+    def __init__(self, number, bits, g=G, mode=0, state_fmt=0, decay=1.0, tokens=None,
+                 xs=None, seq=None):
         import numpy as np
         import torch
-        from bit_error_compensated_gb300.workloads import WORKLOADS, call_sequence, rank_inputs
-        w = WORKLOADS[number]
-        self.w, self.bits, self.P = w, bits, w.P
+        from bit_error_compensated_gb300.workloads import call_sequence, rank_inputs
+        name, P, n = shape_of(number, tokens)
+        self.name, self.bits, self.P = name, bits, P
         self.opts = dict(mode=mode, state_fmt=state_fmt, decay=decay)
-        seq = call_sequence(number, steps=1)
-        Gs = w.n // w.P // g
+        seq = seq if seq is not None else call_sequence(number, steps=1)
+        Gs = n // P // g
+        frac = 64 if P * n * 2 > (4 << 30) else 8
         rng = np.random.default_rng(number)
-        pos = np.sort(rng.choice(w.P * Gs, size=max(1, w.P * Gs // 8), replace=False))
+        pos = np.sort(rng.choice(P * Gs, size=max(1, P * Gs // frac), replace=False))
         self.owners = (pos // Gs).astype(np.int32)
         idx = (pos[:, None] * g + np.arange(g)[None, :]).ravel()
-        self.e = np.zeros((pos.size, w.P, g), np.float32)
+        self.e = np.zeros((pos.size, P, g), np.float32)
         self.inputs = []
-        for k in range(min(len(seq), 4)):
-            x = rank_inputs(number, seq[k], "cpu").view(torch.int16).numpy().view(np.uint16)
-            self.inputs.append(np.ascontiguousarray(x[:, idx].reshape(w.P, pos.size, g).transpose(1, 0, 2)))
-        self.bytes_per_step = pos.size * w.P * g * 2
-        self.sample = (f"each step: one call of {w.name} on a fixed 1/8 sample of its group "
-                       f"positions ({pos.size} of {w.P * Gs}), 4 distinct inputs cycled, state carried; "
-                       f"single-threaded")
+        distinct = min(len(seq), 4)
+        if xs is not None:
+            src = "the GPU arm's inputs"
+        elif torch.cuda.is_available():
+            src = "the workload's generator on the GPU"
+        else:
+            src = "the workload's generator on the CPU"
+        dev = xs.device if xs is not None else torch.device("cuda" if torch.cuda.is_available() else "cpu")
+        idx_t = torch.from_numpy(idx).to(dev)
+        for k in range(distinct):
+            if xs is not None:
+                x = xs[k % xs.shape[0]]
+            else:
+                x = rank_inputs(number, seq[k], dev, tokens=tokens or None)
+            sel = x.index_select(1, idx_t).view(torch.int16).cpu().numpy().view(np.uint16)
+            self.inputs.append(np.ascontiguousarray(sel.reshape(P, pos.size, g).transpose(1, 0, 2)))
+            del x
+        self.bytes_per_step = pos.size * P * g * 2
+        self.sample = (f"each step: one call of {name} on a fixed 1/{frac} sample of its group "
+                       f"positions ({pos.size} of {P * Gs}), {distinct} distinct input(s) cycled "
+                       f"(from {src}), state carried")
         self.i = 0
-        self.ties = 0          # values whose v/s the oracle found exactly on a half-integer
+        self.ties = 0          # exact rounding ties the oracle met (codes and zero points)
 
-    def step(self):
+    def _chunk(self, x, a, b):
         import oracle
-        r = oracle.group_positions(self.P, self.owners, self.bits, self.inputs[self.i % len(self.inputs)],
-                                   self.e, **self.opts)
-        self.ties += r["ties"]
+        return oracle.group_positions(self.P, self.owners[a:b], self.bits, x[a:b], self.e[a:b],
+                                      **self.opts)["ties"]
+
+    def step(self, pool=None, threads=1):
+        """One call over all sampled positions: on this thread, or split into
+        `threads` contiguous chunks run by `pool` (the oracle call releases
+        the interpreter lock, so the chunks run on separate cores)."""
+        x = self.inputs[self.i % len(self.inputs)]
+        npos = self.owners.size
+        if pool is None or threads <= 1:
+            self.ties += self._chunk(x, 0, npos)
+        else:
+            cuts = [npos * t // threads for t in range(threads + 1)]
+            futs = [pool.submit(self._chunk, x, cuts[t], cuts[t + 1]) for t in range(threads)
+                    if cuts[t + 1] > cuts[t]]
+            self.ties += sum(f.result() for f in futs)
         self.i += 1
 
 
-def oracle_sample(args):
+def oracle_sample(args, xs=None, seq=None):
     """OracleSample of the workload and options the GPU arm runs."""
     return OracleSample(args.workload, args.bits, args.g, args.quantizer, STATE_FMT[args.state],
-                        args.decay)
+                        args.decay, args.tokens, xs=xs, seq=seq)
 
 
-def cpu_baseline_oracle(args, budget_s=12.0):
-    """The oracle as it stands, single-threaded on one host core, for about
-    `budget_s` seconds of steps of OracleSample."""
-    s = oracle_sample(args)
-    s.step()
+def _time_steps(s, budget_s, pool=None, threads=1):
+    s.step(pool, threads)                  # untimed first step
     steps, t = 0, time.perf_counter()
-    while time.perf_counter() - t < budget_s:
-        s.step()
+    while time.perf_counter() - t < budget_s or steps == 0:
+        s.step(pool, threads)
         steps += 1
-    sec = time.perf_counter() - t
-    return {"value": round(s.bytes_per_step * steps / sec / 1e9, 4), "unit": "GB/s", "cores": 1,
-            "kind": "oracle", "sample": f"{steps} steps; " + s.sample,
+    return steps, time.perf_counter() - t
+
+
+def cpu_baseline_oracle(args, budget_s=12.0, xs=None, seq=None):
+    """The oracle as it stands (single-threaded code) on a sample of the
+    workload, timed for about budget_s / 2 seconds on one host core and as long
+    again with the sampled positions split over every usable core."""
+    from concurrent.futures import ThreadPoolExecutor
+    info = host_cpu_info()
+    s = oracle_sample(args, xs, seq)
+    steps1, sec1 = _time_steps(s, budget_s / 2)
+    v1 = s.bytes_per_step * steps1 / sec1 / 1e9
+    threads = info["nproc"]
+    with ThreadPoolExecutor(threads) as pool:
+        stepsN, secN = _time_steps(s, budget_s / 2, pool, threads)
+    vN = s.bytes_per_step * stepsN / secN / 1e9
+    return {"value": round(vN, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": f"{stepsN} steps on {threads} threads, {steps1} on one; " + s.sample,
+            "nproc": info["nproc"], "cpu_model": info["cpu_model"],
+            "single_core": {"value": round(v1, 4), "cores": 1, "steps": steps1,
+                            "seconds": round(sec1, 2)},
+            "all_cores": {"value": round(vN, 4), "cores": threads, "steps": stepsN,
+                          "seconds": round(secN, 2)},
             "exact_rounding_ties": s.ties, "ties_counted_over_calls": s.i}
 
 
 def run_reference(args, rank, world):
-    """`--impl reference`: the oracle on the host cores, K timed steps of
-    OracleSample after W warm-up steps."""
+    """`--impl reference`: the oracle on the host cores (its sampled group
+    positions split over all of them), K timed steps of OracleSample after W
+    warm-up steps, on the workload and options of the GPU arm."""
+    from concurrent.futures import ThreadPoolExecutor
+    from bit_error_compensated_gb300.workloads import call_sequence
+    seq = call_sequence(args.workload, steps=1)
+    if args.calls:
+        seq = seq[:args.calls]
+    info = host_cpu_info()
+    threads = info["nproc"]
     s = oracle_sample(args)
-    for _ in range(args.warmup):
-        s.step()
-    t = time.perf_counter()
-    for _ in range(args.steps):
-        s.step()
-    sec = time.perf_counter() - t
+    with ThreadPoolExecutor(threads) as pool:
+        for _ in range(args.warmup):
+            s.step(pool, threads)
+        t = time.perf_counter()
+        for _ in range(args.steps):
+            s.step(pool, threads)
+        sec = time.perf_counter() - t
     v = s.bytes_per_step * args.steps / sec / 1e9
-    w = s.w
     return {"impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": "GB/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(sec / args.steps * 1e3, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic (seeded; shapes and distributions of the workload, no dataset)",
-            "config": {"workload": w.name, "P": w.P, "n_per_rank": w.n, "bits": args.bits, "g": args.g,
-                       "compensated": True, "quantizer": QUANTIZERS[args.quantizer],
-                       "state": {"format": STATE_NAME[args.state],
-                                 "decay": args.decay}},
-            "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                             "sample": s.sample, "exact_rounding_ties": s.ties,
+            "config": workload_config(args, world, seq),
+            "sample": s.sample,
+            "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                             "sample": s.sample, "nproc": info["nproc"],
+                             "cpu_model": info["cpu_model"], "exact_rounding_ties": s.ties,
                              "ties_counted_over_calls": s.i},
             "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
@@ -698,7 +872,10 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", type=int, default=2, help="1..5 (default 2: P=4, 2048x4096, 64 calls)")
+    ap.add_argument("--workload", type=int, default=3,
+                    help="1..5 (default 3: P=8, 1 GiB bf16 per rank, one call)")
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="profiling runs: the workload's shape with this many tokens per rank")
     ap.add_argument("--bits", type=int, default=4, choices=[4, 8])
     ap.add_argument("--g", type=int, default=G, choices=[64, 128, 256], help="elements per group")
     ap.add_argument("--unfused", action="store_true",
@@ -715,7 +892,9 @@ def main(argv=None):
                     help="compensator state storage (bf16 or fp16 halve its traffic)")
     ap.add_argument("--decay", type=float, default=1.0,
                     help="kept error = decay x revealed error (1 = plain error feedback)")
-    ap.add_argument("--also", default="4", help="other workloads to time, comma-separated ('' for none)")
+    ap.add_argument("--also", default="3b8,4,5,1",
+                    help="other workloads to time, comma-separated, NbB for workload N with B-bit "
+                         "codes ('' for none)")
     ap.add_argument("--calls", type=int, default=0,
                     help="time only the first N calls of the sequence (profiling runs)")
     ap.add_argument("--accuracy", action="store_true",

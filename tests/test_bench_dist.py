@@ -73,25 +73,61 @@ def test_byte_model_matches_the_per_element_totals():
 
 def test_profiled_traffic_belongs_to_one_configuration(tmp_path, monkeypatch):
     """A DRAM-traffic figure from ncu is reported only for the configuration it
-    was captured on, and only while the kernel sources are unchanged."""
+    was captured on, and only while the kernel sources are unchanged; a capture
+    of a smaller case of that configuration is scaled by the element ratio."""
     import json
     import bench
     (tmp_path / "profiles").mkdir()
     f32 = bench.traffic_key("p4_2048x4096", 4, 128, "f32", 0, "fused")
     bf16 = bench.traffic_key("p4_2048x4096", 4, 128, "bf16", 0, "fused")
+    big = bench.traffic_key("p8_1gib", 4, 128, "f32", 0, "fused")
     rec = {f32: {"push_kernel": {"dram_bytes_per_launch": 100, "source_hash": "h1"}},
-           bf16: {"push_kernel": {"dram_bytes_per_launch": 60, "source_hash": "h1"}}}
+           bf16: {"push_kernel": {"dram_bytes_per_launch": 60, "source_hash": "h1"}},
+           big: {"push_kernel": {"dram_bytes_per_launch": 1000, "source_hash": "h1",
+                                 "captured_elements": 8 * 2048 * 4096, "capture": "x.md"}}}
     (tmp_path / "profiles" / "traffic.json").write_text(json.dumps(rec))
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     monkeypatch.setattr(bench, "kernel_source_hash", lambda: "h1")
-    assert bench.profiled_traffic("push_kernel", f32) == 100
-    assert bench.profiled_traffic("push_kernel", bf16) == 60
-    assert bench.profiled_traffic("reduce_kernel", f32) is None
+    n2 = 4 * 2048 * 4096
+    assert bench.profiled_traffic("push_kernel", f32, n2) == (100, None)
+    assert bench.profiled_traffic("push_kernel", bf16, n2) == (60, None)
+    assert bench.profiled_traffic("reduce_kernel", f32, n2) == (None, None)
+    scaled, note = bench.profiled_traffic("push_kernel", big, 8 * 131072 * 4096)
+    assert scaled == 64 * 1000 and "scaled by 64" in note
+    assert bench.profiled_traffic("push_kernel", big, 8 * 2048 * 4096) == (1000, None)
     for other in (bench.traffic_key("p4_2048x4096", 8, 128, "f32", 0, "fused"),
                   bench.traffic_key("p4_2048x4096", 4, 64, "f32", 0, "fused"),
                   bench.traffic_key("p4_2048x4096", 4, 128, "f32", 1, "fused"),
                   bench.traffic_key("p4_2048x4096", 4, 128, "f32", 0, "unfused"),
                   bench.traffic_key("p4_8192x4096", 4, 128, "f32", 0, "fused")):
-        assert bench.profiled_traffic("push_kernel", other) is None
+        assert bench.profiled_traffic("push_kernel", other, n2) == (None, None)
     monkeypatch.setattr(bench, "kernel_source_hash", lambda: "h2")   # sources changed
-    assert bench.profiled_traffic("push_kernel", f32) is None
+    assert bench.profiled_traffic("push_kernel", f32, n2) == (None, None)
+
+
+def test_also_specs_and_host_cpu_info():
+    import bench
+    assert bench.parse_also("4", 4) == (4, 4)
+    assert bench.parse_also("3b8", 4) == (3, 8)
+    info = bench.host_cpu_info()
+    assert info["nproc"] >= 1 and isinstance(info["cpu_model"], str)
+    assert bench.shape_of(3) == ("p8_1gib", 8, 512 * 2 ** 20)
+    assert bench.shape_of(3, 2048) == ("p8_1gib@2048x4096", 8, 2048 * 4096)
+
+
+def test_oracle_sample_threads_give_the_single_thread_result():
+    """Splitting the sampled positions over threads changes nothing but the time:
+    same state and the same tie count as one thread."""
+    import numpy as np
+    from concurrent.futures import ThreadPoolExecutor
+    import bench
+
+    class A:
+        workload, bits, g, quantizer, state, decay, tokens = 1, 4, 128, 0, "f32", 1.0, 0
+    one, many = bench.oracle_sample(A()), bench.oracle_sample(A())
+    with ThreadPoolExecutor(3) as pool:
+        for _ in range(3):
+            one.step()
+            many.step(pool, 3)
+    assert np.array_equal(one.e.view(np.uint32), many.e.view(np.uint32))
+    assert one.ties == many.ties
