@@ -398,38 +398,10 @@ def run_ours(args, rank, local, world):
 
     # Per-kernel durations: the same K steps again, with events around each
     # kernel of every call (this makes each launch stream-serialised).
-    per_kernel_ms = {"push": 0.0, "reduce": 0.0, "gather": 0.0}
-    ev_sets = []
-    torch.cuda.synchronize(dev)
-    for _ in range(args.steps):
-        for ins, comp in call_args:
-            evs = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
-            for e in evs:
-                e.record(stream)
-            echo.echo_set_timing(plan, evs)
-            echo.echo_allreduce(plan, ins, out_rows, comp, stream)
-            ev_sets.append(evs)
-    echo.echo_set_timing(plan, None)
-    torch.cuda.synchronize(dev)
-    for evs in ev_sets:
-        per_kernel_ms["push"] += evs[0].elapsed_time(evs[1])
-        per_kernel_ms["reduce"] += evs[1].elapsed_time(evs[2])
-        per_kernel_ms["gather"] += evs[2].elapsed_time(evs[3])
-    nlaunch = len(ev_sets)
-    kb_comp = kernel_bytes(P, n, bits, True, fused, sb, g)
-    kb_unc = kernel_bytes(P, n, bits, False, fused, g=g)
-    if args.persistent:
-        # one kernel does the whole call: its events span push, reduce and gather
-        kb_comp = {"call": sum(kb_comp.values())}
-        kb_unc = {"call": sum(kb_unc.values())}
-        per_kernel_ms = {"call": per_kernel_ms["push"]}
-        ran = ["call"]
-    else:
-        ran = [k for k in ("push", "reduce", "gather") if k in kb_comp and (k != "push" or P > 1)]
-    avg_us = {k: per_kernel_ms[k] / nlaunch * 1e3 for k in ran}
-    kb_avg = {k: (compensated_calls * kb_comp[k] + (calls - compensated_calls) * kb_unc[k]) / calls
-              for k in ran}
-    per_kernel_frac = {k: round(kb_avg[k] / (avg_us[k] / 1e6) / 1e9 / hbm, 4) for k in ran}
+    raw_us = kernel_event_times(echo, plan, [(ins, out_rows, comp) for ins, comp in call_args],
+                                stream, args.steps)
+    avg_us, kb_avg, per_kernel_frac = kernel_fracs(raw_us, P, n, bits, fused, sb, g,
+                                                   compensated_calls, calls, args.persistent, hbm)
     dominant = max(avg_us, key=lambda k: avg_us[k])
     kbytes = kb_avg[dominant]
     achieved = kbytes / (avg_us[dominant] / 1e6) / 1e9
@@ -487,6 +459,49 @@ def run_ours(args, rank, local, world):
     return result
 
 
+def kernel_event_times(echo, plan, calls, stream, steps):
+    """Average device time of each kernel of a call, in microseconds: `steps`
+    passes over `calls` (a list of (ins, outs, comp)), with events recorded
+    around every kernel (which serialises the launches)."""
+    import torch
+    ev_sets = []
+    torch.cuda.synchronize()
+    for _ in range(steps):
+        for ins, outs, comp in calls:
+            evs = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+            for e in evs:
+                e.record(stream)
+            echo.echo_set_timing(plan, evs)
+            echo.echo_allreduce(plan, ins, outs, comp, stream)
+            ev_sets.append(evs)
+    echo.echo_set_timing(plan, None)
+    torch.cuda.synchronize()
+    tot = {"push": 0.0, "reduce": 0.0, "gather": 0.0}
+    for evs in ev_sets:
+        tot["push"] += evs[0].elapsed_time(evs[1])
+        tot["reduce"] += evs[1].elapsed_time(evs[2])
+        tot["gather"] += evs[2].elapsed_time(evs[3])
+    return {k: v / len(ev_sets) * 1e3 for k, v in tot.items()}
+
+
+def kernel_fracs(avg_us, P, n, bits, fused, sb, g, comp_calls, calls, persistent, hbm):
+    """Per-kernel achieved GB/s over the byte model, as fractions of `hbm`, and
+    the kernels that ran."""
+    kb_comp = kernel_bytes(P, n, bits, True, fused, sb, g)
+    kb_unc = kernel_bytes(P, n, bits, False, fused, g=g)
+    if persistent:
+        kb_comp = {"call": sum(kb_comp.values())}
+        kb_unc = {"call": sum(kb_unc.values())}
+        avg_us = {"call": avg_us["push"]}
+        ran = ["call"]
+    else:
+        ran = [k for k in ("push", "reduce", "gather") if k in kb_comp and (k != "push" or P > 1)]
+    kb = {k: (comp_calls * kb_comp[k] + (calls - comp_calls) * kb_unc[k]) / calls for k in ran}
+    avg = {k: avg_us[k] for k in ran}
+    frac = {k: round(kb[k] / (avg[k] / 1e6) / 1e9 / hbm, 4) for k in ran}
+    return avg, kb, frac
+
+
 def parse_also(spec: str, default_bits: int):
     """'4' -> (4, default bits); '3b8' -> workload 3 with 8-bit codes."""
     if "b" in spec:
@@ -521,16 +536,19 @@ def run_e2e(args, echo, plan, xs, seq, states, dev, world):
     calls = len(seq)
     comps = [states[c.state] for c in seq]
 
-    def step(first):
+    issued = [0]                                          # calls issued so far, all steps
+
+    def step():
         for k in range(calls):
-            b = k & 1
+            b = issued[0] & 1                             # alternates across steps too
+            reused = issued[0] >= 2
             with torch.cuda.stream(s_h2d):
-                if not (first and k < 2):
+                if reused:
                     s_h2d.wait_event(ev_done[b])          # dev_in[b] no longer read
                 dev_in[b].copy_(host_in[k % distinct], non_blocking=True)
                 ev_loaded[b].record(s_h2d)
             s_comp.wait_event(ev_loaded[b])
-            if not (first and k < 2):
+            if reused:
                 s_comp.wait_event(ev_read[b])             # dev_out[b] copied out
             echo.echo_allreduce(plan, list(dev_in[b]), list(dev_out[b]), comps[k], s_comp)
             ev_done[b].record(s_comp)
@@ -538,14 +556,15 @@ def run_e2e(args, echo, plan, xs, seq, states, dev, world):
                 s_d2h.wait_event(ev_done[b])
                 host_out[b].copy_(dev_out[b][0], non_blocking=True)
                 ev_read[b].record(s_d2h)
+            issued[0] += 1
 
-    for i in range(max(1, args.warmup)):
-        step(i == 0)
+    for _ in range(max(1, args.warmup)):
+        step()
     torch.cuda.synchronize(dev)
     barrier(world)
     t = time.perf_counter()
     for _ in range(args.steps):
-        step(False)
+        step()
     torch.cuda.synchronize(dev)
     barrier(world)
     wall_ms = (time.perf_counter() - t) * 1e3
@@ -607,12 +626,18 @@ def time_other(echo, number, bits, fused, dev, args):
         raise RuntimeError(f"device status word set while timing {w.name}")
     hbm, _ = load_peaks()
     comp_calls = sum(1 for c in seq if c.state != "none")
+    raw_us = kernel_event_times(echo, plan, [(rows[k % distinct], out_rows, comps[k])
+                                             for k in range(len(seq))], stream, reps)
+    k_us, _, k_frac = kernel_fracs(raw_us, w.P, w.n, bits, fused, sb, args.g, comp_calls, len(seq),
+                                   args.persistent, hbm)
     model = (comp_calls * call_model_bytes(w.P, w.n, bits, True, fused, sb, args.g) +
              (len(seq) - comp_calls) * call_model_bytes(w.P, w.n, bits, False, fused, g=args.g)) / len(seq)
     res = {"gbs": round(w.P * w.n * 2 / per_call_s / 1e9, 2), "us_per_call": round(per_call_s * 1e6, 2),
            "hbm_roofline_frac": round(model / per_call_s / 1e9 / hbm, 4), "bits": bits,
            "calls": len(seq) * reps, "calls_per_step": len(seq),
-           "states": sorted({c.state for c in seq})}
+           "states": sorted({c.state for c in seq}),
+           "per_kernel_us": {k: round(v, 2) for k, v in k_us.items()},
+           "per_kernel_frac": k_frac}
     if launch_bound:
         res["note"] = "launch-bound (a few KiB per call): the time per call is the figure"
         graph = torch.cuda.CUDAGraph()
@@ -892,7 +917,7 @@ def main(argv=None):
                     help="compensator state storage (bf16 or fp16 halve its traffic)")
     ap.add_argument("--decay", type=float, default=1.0,
                     help="kept error = decay x revealed error (1 = plain error feedback)")
-    ap.add_argument("--also", default="3b8,4,5,1",
+    ap.add_argument("--also", default="3b8,2,4,5,1",
                     help="other workloads to time, comma-separated, NbB for workload N with B-bit "
                          "codes ('' for none)")
     ap.add_argument("--calls", type=int, default=0,
