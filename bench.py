@@ -96,9 +96,14 @@ def load_peaks():
 
 
 def kernel_source_hash() -> str:
+    """Hash of the sources that define the kernels (device code and the
+    constants they are compiled with), so that host-only changes keep the
+    committed ncu figures valid and any kernel change drops them."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "bit_error_compensated_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
+        if not (name.startswith("k_") or name.endswith(".cuh") or name == "echo_internal.h"):
+            continue
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
