@@ -41,11 +41,12 @@ __device__ __forceinline__ void push_load(const uint8_t* sx, const uint8_t* se, 
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     const int i = sub * G + half_at<NL>(h, q);
-    bf16x8_to_f32(x8[i / 8], v + 8 * h);
     if constexpr (SF != kNoState) {
       float e[8];
       state_load8<SF>(se, i, e);
-      add_n<8>(v + 8 * h, v + 8 * h, e);
+      entry8(x8[i / 8], e, v + 8 * h);
+    } else {
+      bf16x8_to_f32(x8[i / 8], v + 8 * h);
     }
   }
 }
@@ -53,9 +54,9 @@ __device__ __forceinline__ void push_load(const uint8_t* sx, const uint8_t* se, 
 // The 8 codes of a half (integer-valued floats) packed into one word and
 // stored with an L2 policy: 32 bits for 4-bit codes, 64 for 8-bit.
 template <int BITS>
-__device__ __forceinline__ void store_codes8(uint8_t* p, const float c[8], uint64_t pol) {
+__device__ __forceinline__ void store_codes8(uint8_t* p, const float c[8], float zo, uint64_t pol) {
   uint32_t w0, w1;
-  pack8<BITS>(c, w0, w1);
+  pack8<BITS>(c, w0, w1, zo);
   if (BITS == 4) st_hint_u32(p, w0 | (w1 << 16), pol);
   else st_hint_u64(p, (uint64_t)w0 | ((uint64_t)w1 << 32), pol);
 }
@@ -76,7 +77,8 @@ __device__ __forceinline__ void push_finish(const CallArgs& a, const float v[16]
     float c[8], d[8];
     quantize8_mode<MODE>(v + 8 * hh, gg, L, c, d);
     if (valid) {
-      store_codes8<BITS>(cs + j * CB + half_code_byte<BITS, NL>(hh, q), c, codes_pol);
+      store_codes8<BITS>(cs + j * CB + half_code_byte<BITS, NL>(hh, q), c, code_offset<MODE>(gg),
+                         codes_pol);
       if constexpr (SF != kNoState) {
         float r[8];
         sub_n<8>(r, v + 8 * hh, d);
@@ -231,11 +233,12 @@ __device__ __forceinline__ void reduce_tile(const CallArgs& a, const uint8_t* st
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const int i = gs * G + half_at<NL>(h, q);
-        bf16x8_to_f32(s_x[i / 8], term + 8 * h);
         if constexpr (COMP) {
           float e[8];
           state_load8<SF>(s_e, i, e);
-          add_n<8>(term + 8 * h, term + 8 * h, e);
+          entry8(s_x[i / 8], e, term + 8 * h);
+        } else {
+          bf16x8_to_f32(s_x[i / 8], term + 8 * h);
         }
       }
     };
@@ -266,7 +269,8 @@ __device__ __forceinline__ void reduce_tile(const CallArgs& a, const uint8_t* st
       float c[8], deq[8];
       quantize8_mode<MODE>(acc + 8 * hh, gg, L, c, deq);
       if (!valid) continue;
-      store_codes8<BITS>(a.codes2 + grp * CB + half_code_byte<BITS, NL>(hh, q), c, codes_pol);
+      store_codes8<BITS>(a.codes2 + grp * CB + half_code_byte<BITS, NL>(hh, q), c,
+                         code_offset<MODE>(gg), codes_pol);
       float yb[8];
       const uint4 y = f32x8_to_bf16(deq, yb);
       const int64_t e = grp * G + half_at<NL>(hh, q);
