@@ -211,14 +211,6 @@ __device__ __forceinline__ GroupGrid make_grid(float lo, float hi, float L) {
   return gg;
 }
 
-// With ECHO_PACK_Z the quantizers hand back each code minus a per-group
-// offset (code_offset: the zero point, where the code is an offset from it)
-// and the packing adds the offset once per word, folded into the constant it
-// adds anyway; otherwise the codes themselves.  The packed words are the same.
-#ifndef ECHO_PACK_Z
-#define ECHO_PACK_Z 0
-#endif
-
 // Codes (as integer-valued floats in [0, L]) and decoded values of 8 values:
 // c = clamp(rint(v / s) + z, 0, L), d = (c - z) * s.
 //
@@ -257,13 +249,8 @@ __device__ __forceinline__ void quantize8(const float v[8], const GroupGrid& gg,
   float cm[8];
 #pragma unroll
   for (int k = 0; k < 8; ++k) cm[k] = fminf(r[k], lz);
-#if ECHO_PACK_Z
-#pragma unroll
-  for (int k = 0; k < 8; ++k) c[k] = cm[k];        // the packing adds z (code_offset)
-#else
 #pragma unroll
   for (int k = 0; k < 8; k += 2) add2(c[k], c[k + 1], cm[k], cm[k + 1], gg.zf, gg.zf);
-#endif
   mul_ns<8>(d, cm, gg.s);
 }
 
@@ -357,9 +344,8 @@ __device__ __forceinline__ void quantize8_mode(const float v[8], const GroupGrid
     for (int k = 0; k < 8; ++k) {
       if constexpr (MODE == kSymmetric) {
         const float lh = __fsub_rn(gg.zf, 1.0f);
-        const float cm = fminf(fmaxf(r[k], -lh), lh);
-        c[k] = ECHO_PACK_Z ? cm : __fadd_rn(cm, gg.zf);
-        d[k] = __fmul_rn(cm, gg.s);                     // (c - z) * s: c - z is cm exactly
+        c[k] = __fadd_rn(fminf(fmaxf(r[k], -lh), lh), gg.zf);
+        d[k] = __fmul_rn(__fsub_rn(c[k], gg.zf), gg.s);
       } else {
         c[k] = fminf(fmaxf(r[k], 0.0f), L);
         d[k] = __fadd_rn(__fmul_rn(c[k], gg.s), gg.zf);   // m + s*q
@@ -380,35 +366,23 @@ __device__ __forceinline__ void unpack_meta(uint32_t meta, float& s, float& zf) 
 // built with exact fp arithmetic (every intermediate is an integer below
 // 2^16) and read out of the mantissa of 2^23 + word.  Two runs of 4 (c[0..3]
 // into w0, c[4..7] into w1) at once, on pairs.
-// The offset the packing adds to each value a quantizer hands back (see
-// ECHO_PACK_Z): 0 when the quantizers return the codes themselves.
-template <int MODE>
-__device__ __forceinline__ float code_offset(const GroupGrid& gg) {
-  return (ECHO_PACK_Z && MODE != kNaiveZeroPoint) ? gg.zf : 0.0f;
-}
-
-// With an offset zo added to each of the 8 values (every code is value + zo):
-// the words are sum_k (c_k + zo) W^k = sum_k c_k W^k + zo sum_k W^k, so zo
-// joins the 2^23 added at the end (all exact: integers below 2^24).
 template <int BITS>
-__device__ __forceinline__ void pack8(const float c[8], uint32_t& w0, uint32_t& w1, float zo = 0.0f) {
+__device__ __forceinline__ void pack8(const float c[8], uint32_t& w0, uint32_t& w1) {
   constexpr float B = 8388608.0f;                  // 2^23
   float a0, a1;
   if (BITS == 4) {
-    const float bias = __fmaf_rn(zo, 4369.0f, B);  // 4369 = 1 + 16 + 256 + 4096
     fma2(a0, a1, c[1], c[5], 16.0f, 16.0f, c[0], c[4]);
     fma2(a0, a1, c[2], c[6], 256.0f, 256.0f, a0, a1);
     fma2(a0, a1, c[3], c[7], 4096.0f, 4096.0f, a0, a1);
-    add2(a0, a1, a0, a1, bias, bias);
+    add2(a0, a1, a0, a1, B, B);
     w0 = __float_as_uint(a0) & 0xFFFFu;
     w1 = __float_as_uint(a1) & 0xFFFFu;
   } else {
-    const float bias = __fmaf_rn(zo, 257.0f, B);   // 257 = 1 + 256
     float b0, b1;
     fma2(a0, a1, c[1], c[5], 256.0f, 256.0f, c[0], c[4]);   // bytes 0, 1
     fma2(b0, b1, c[3], c[7], 256.0f, 256.0f, c[2], c[6]);   // bytes 2, 3
-    add2(a0, a1, a0, a1, bias, bias);
-    add2(b0, b1, b0, b1, bias, bias);
+    add2(a0, a1, a0, a1, B, B);
+    add2(b0, b1, b0, b1, B, B);
     w0 = __byte_perm(__float_as_uint(a0), __float_as_uint(b0), 0x5410);
     w1 = __byte_perm(__float_as_uint(a1), __float_as_uint(b1), 0x5410);
   }
@@ -456,11 +430,13 @@ __device__ __forceinline__ void bf16x8_to_f32(uint4 r, float f[8]) {
 
 // The entry pass of 8 values: v[k] = float(x_k) + e[k] for 8 bf16 values in
 // 16 bytes and their fp32 held errors, one IEEE fp32 add each (the bf16 value
-// widens exactly).  With ECHO_MIXED_ADD the sm_100 family's mixed-precision
-// add takes the bf16 half of a register as it is, with no separate widening
-// instruction; otherwise the values are widened and added in pairs.
+// widens exactly).  With ECHO_MIXED_ADD (the default) the sm_100 family's
+// mixed-precision add (add.rn.f32.bf16) takes the bf16 half of a register as
+// it is, with no separate widening instruction: 2 instructions per pair
+// instead of 3 (measured +0.9% on a call with 2-byte state, +0.1% with fp32
+// state); 0 widens the values and adds them in pairs.
 #ifndef ECHO_MIXED_ADD
-#define ECHO_MIXED_ADD 0
+#define ECHO_MIXED_ADD 1
 #endif
 __device__ __forceinline__ float add_bf16_f32(uint32_t w, int half, float e) {
   float r;

@@ -54,9 +54,9 @@ __device__ __forceinline__ void push_load(const uint8_t* sx, const uint8_t* se, 
 // The 8 codes of a half (integer-valued floats) packed into one word and
 // stored with an L2 policy: 32 bits for 4-bit codes, 64 for 8-bit.
 template <int BITS>
-__device__ __forceinline__ void store_codes8(uint8_t* p, const float c[8], float zo, uint64_t pol) {
+__device__ __forceinline__ void store_codes8(uint8_t* p, const float c[8], uint64_t pol) {
   uint32_t w0, w1;
-  pack8<BITS>(c, w0, w1, zo);
+  pack8<BITS>(c, w0, w1);
   if (BITS == 4) st_hint_u32(p, w0 | (w1 << 16), pol);
   else st_hint_u64(p, (uint64_t)w0 | ((uint64_t)w1 << 32), pol);
 }
@@ -77,8 +77,7 @@ __device__ __forceinline__ void push_finish(const CallArgs& a, const float v[16]
     float c[8], d[8];
     quantize8_mode<MODE>(v + 8 * hh, gg, L, c, d);
     if (valid) {
-      store_codes8<BITS>(cs + j * CB + half_code_byte<BITS, NL>(hh, q), c, code_offset<MODE>(gg),
-                         codes_pol);
+      store_codes8<BITS>(cs + j * CB + half_code_byte<BITS, NL>(hh, q), c, codes_pol);
       if constexpr (SF != kNoState) {
         float r[8];
         sub_n<8>(r, v + 8 * hh, d);
@@ -269,8 +268,7 @@ __device__ __forceinline__ void reduce_tile(const CallArgs& a, const uint8_t* st
       float c[8], deq[8];
       quantize8_mode<MODE>(acc + 8 * hh, gg, L, c, deq);
       if (!valid) continue;
-      store_codes8<BITS>(a.codes2 + grp * CB + half_code_byte<BITS, NL>(hh, q), c,
-                         code_offset<MODE>(gg), codes_pol);
+      store_codes8<BITS>(a.codes2 + grp * CB + half_code_byte<BITS, NL>(hh, q), c, codes_pol);
       float yb[8];
       const uint4 y = f32x8_to_bf16(deq, yb);
       const int64_t e = grp * G + half_at<NL>(hh, q);

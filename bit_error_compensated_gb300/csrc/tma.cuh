@@ -78,28 +78,13 @@ __device__ __forceinline__ uint64_t policy_evict_last() {
   return p;
 }
 
-// Suspend-time hint of each try_wait, in nanoseconds (0: none, the hardware's
-// own limit): how long a thread whose phase is not yet complete may sleep in
-// one try before it is woken to check its bound.
-#ifndef ECHO_MBAR_HINT_NS
-#define ECHO_MBAR_HINT_NS 0
-#endif
-
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t done;
-#if ECHO_MBAR_HINT_NS > 0
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(done) : "r"(bar), "r"(parity), "r"((uint32_t)ECHO_MBAR_HINT_NS) : "memory");
-#else
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(done) : "r"(bar), "r"(parity) : "memory");
-#endif
   return done != 0;
 }
 

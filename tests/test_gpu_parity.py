@@ -573,3 +573,45 @@ def test_tie_count_by_construction(echo, bits_, P, schedule):
     assert np.array_equal(bits(out), ref["out"])
     assert_wire_equal(wire_to_canonical(echo.echo_debug_wire(plan), lay, P, n, bits_), ref, P)
     assert_state_close(comp.cpu().numpy(), e_ref)
+
+
+@pytest.mark.parametrize("fmt", [0, 1, 2])
+@pytest.mark.parametrize("schedule", SCHEDULES)
+def test_subnormal_inputs_and_state(echo, fmt, schedule):
+    """The entry pass, the quantizers and the state update keep subnormal
+    numbers exactly as the oracle's IEEE fp32 arithmetic does (no flush to
+    zero): bf16 inputs and held errors that are subnormal, values that cancel
+    exactly (x + e = +0), and groups whose whole range is subnormal, over three
+    compensated calls, against the oracle bit for bit."""
+    P, Gs = 2, 40
+    n = P * G * Gs
+    rng = np.random.default_rng(90 + fmt)
+    tiny = np.float32(2.0 ** -130)                     # fp32 subnormal
+    x32 = (rng.standard_normal((P, n)) * 2.0 ** -128).astype(np.float32)   # bf16 subnormals
+    x32[:, ::3] = rng.standard_normal((P, -(-n // 3))).astype(np.float32)  # mixed with normals
+    groups = x32.reshape(P, -1, G)
+    groups[:, ::4] = (rng.standard_normal((P, groups[:, ::4].shape[1], G)) * 2.0 ** -132
+                      ).astype(np.float32)             # all-subnormal groups
+    x = torch.from_numpy(x32).to(torch.bfloat16)
+    xf = x.float().numpy()
+    e0 = (rng.standard_normal((P, n)) * tiny).astype(np.float32)
+    cancel = rng.random((P, n)) < 0.1
+    e0[cancel] = -xf[cancel]                           # x + e = +0 exactly
+    if fmt != 0:                                       # a 2-byte state holds only its own values
+        e0 = torch.from_numpy(e0).to(STATE_DTYPES[fmt]).float().numpy()
+        assert (np.abs(e0[e0 != 0]) < 2.0 ** -126).any() or fmt == 2
+    plan = echo.echo_plan(P, n, G, 4)
+    _set_schedule(echo, plan, schedule)
+    echo.echo_set_state(plan, fmt, 1.0)
+    comp = torch.from_numpy(e0).to(STATE_DTYPES[fmt]).cuda()
+    e_ref = e0.copy()
+    x = x.cuda()
+    for k in range(3):
+        xk = x if k == 0 else torch.roll(x, k, dims=1)
+        out = torch.empty_like(xk)
+        echo.echo_allreduce(plan, list(xk), list(out), comp)
+        torch.cuda.synchronize()
+        assert echo.echo_get_status(plan) == 0
+        ref = oracle.allreduce(bits(xk), G, 4, e=e_ref, state_fmt=fmt)
+        assert np.array_equal(bits(out), ref["out"]), f"outputs differ at call {k}"
+        assert_state_close(comp.float().cpu().numpy(), e_ref, f"state after call {k}")
