@@ -7,31 +7,40 @@
 // Work items, in ticket order, come in rounds: round r holds the push of
 // tile r from every sender to every owner, the reduce of tile r - D of every
 // owner and (unless the reduce writes the outputs itself) the gather of tile
-// r - 2D, where the lag D is about two waves of items in flight, so a reduce
+// r - 2D, where the lag D is about a wave of items in flight, so a reduce
 // tile is claimed when its pushes are most likely done and pushes, reduces
 // and gathers, which load memory and ALU differently, share the GPU.  Slots
 // whose tile is out of range are skipped.  A tile is kCallTileElems elements
-// of a segment.  Blocks claim items from one atomic ticket counter.  A reduce
-// item waits for a per-tile counter of finished pushes, a gather item for a
-// per-tile reduce flag; each consumer resets what it consumed, and the last
-// block to finish resets the ticket counter, so the words are zero again for
-// the next call.  An item only ever
-// waits on items with smaller tickets; the launch is cooperative, so all
-// blocks are co-resident.
+// of a segment.  A reduce item waits for a per-tile counter of finished
+// pushes, a gather item for a per-tile reduce flag; each consumer resets what
+// it consumed, and the last block to finish resets the ticket counter, so the
+// words are zero again for the next call.
 //
-// Each block pipelines two items: while it computes one, thread 0 has
-// already claimed the next and, if that item's inputs are final, started its
-// bulk copies (cp.async.bulk) into the other shared-memory stage.  If they
-// are not, the block first finishes and signals the current item and only
-// then waits, so a block never waits while holding an item it has not
-// signalled: the waiting item with the smallest ticket always has all its
-// inputs on their way, and every wait ends.
+// A block is kThreads/32 compute warps and one control warp, which share a
+// ring of two shared-memory stages, each with a "full" and an "empty"
+// mbarrier.  The control warp's lane 0 does all the scheduling: it claims
+// tickets from one atomic counter (the next one fetched ahead), waits for an
+// item's inputs, fills a stage with the item's bulk copies (cp.async.bulk)
+// completing on its full barrier, and, once the compute warps have arrived on
+// the stage's empty barrier, publishes the item's completion to the other
+// blocks (a release add or store) and refills the stage.  The compute warps
+// only wait on full barriers, compute, and arrive on empty barriers: no block
+// barrier and no memory fence is ever on their path, so the latencies of the
+// claims, the flags and the release fences overlap the arithmetic.
+//
+// Deadlock freedom: an item only ever waits on items with smaller tickets,
+// the launch is cooperative (all blocks co-resident), and the control warp
+// never waits for an item's inputs while it holds an item it has not
+// published: when the next item's inputs are not final it first lets the
+// compute warps finish what it issued and publishes it.  So the waiting item
+// with the smallest ticket always has all its inputs on their way, and every
+// wait ends.
 //
 // Every wait is bounded (kWaitLimitNs) and also gives up when another block
-// has set the abort word; a block that gives up records ECHO_ERR_TIMEOUT in
-// the status word, sets the abort word, lets its copies in flight land
-// (bounded) and stops.  echo_get_status clears the schedule words after a
-// timeout.
+// has set the abort word; whoever gives up records ECHO_ERR_TIMEOUT in the
+// status word and sets the abort word; the control warp lets the copies it
+// issued land (bounded) before the block exits.  echo_get_status clears the
+// schedule words after a timeout.
 #include "stages.cuh"
 
 namespace echo {
@@ -44,7 +53,7 @@ static_assert(kCallTileElems == kUnit * (kThreads / 32), "tile: one push unit pe
 static_assert(kCallTileElems % (kRun * (kThreads / 32)) == 0, "tile: whole gather runs per warp");
 
 #ifndef ECHO_CALL_LAG_WAVES
-#define ECHO_CALL_LAG_WAVES 1
+#define ECHO_CALL_LAG_WAVES 3
 #endif
 constexpr int kCallLagWaves = ECHO_CALL_LAG_WAVES;
 
@@ -105,19 +114,56 @@ __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
-// Thread 0: waits until *w == want, or gives up (bounded, or when the abort
-// word is set).  Returns false on giving up.
+// A wait that has lasted this long starts reading the abort word (ns).
+#ifndef ECHO_ABORT_POLL_NS
+#define ECHO_ABORT_POLL_NS 20000
+#endif
+constexpr uint64_t kAbortPollNs = ECHO_ABORT_POLL_NS;
+
+// The control thread: waits until *w == want, or gives up (bounded, or when
+// the abort word is set).  Returns false on giving up.
 __device__ __forceinline__ bool wait_word(const uint32_t* w, uint32_t want, const uint32_t* abort) {
   if (ld_acquire(w) == want) return true;
   const uint64_t t0 = global_ns();
   for (;;) {
     if (ld_acquire(w) == want) return true;
-    if (ld_relaxed(abort) != 0 || global_ns() - t0 > kWaitLimitNs) return false;
+    const uint64_t dt = global_ns() - t0;
+    if (dt > kWaitLimitNs || (dt > kAbortPollNs && ld_relaxed(abort) != 0)) return false;
+  }
+}
+
+// Compute warps per block and the block size (plus the control warp).
+constexpr int kCallWarps = kThreads / 32;
+constexpr int kCallBlockThreads = kThreads + 32;
+// Resident blocks per SM the register allocation must allow: 3 blocks of 288
+// threads leave 72 registers a thread.
+#ifndef ECHO_CALL_MIN_BLOCKS
+#define ECHO_CALL_MIN_BLOCKS 3
+#endif
+constexpr int64_t kSentinel = -1;              // no ticket held in a stage
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(bar) : "memory");
+}
+
+// Bounded wait on a barrier phase that also gives up once the abort word is
+// set.  The abort word is read only once a wait has lasted kAbortPollNs (no
+// wait of a healthy call comes near it): thousands of waiting warps reading
+// it on every try would load the L2 slice that also serves the ticket
+// counter next to it.
+__device__ __forceinline__ bool mbar_wait_or_abort(uint32_t bar, uint32_t parity,
+                                                   const uint32_t* abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (;;) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t dt = global_ns() - t0;
+    if (dt > kWaitLimitNs || (dt > kAbortPollNs && ld_relaxed(abort) != 0)) return false;
   }
 }
 
 template <int BITS, int SF, int MODE, int G, bool FUSED>
-__global__ void __launch_bounds__(kThreads, ECHO_REDUCE_MIN_BLOCKS)
+__global__ void __launch_bounds__(kCallBlockThreads, ECHO_CALL_MIN_BLOCKS)
 call_kernel(const CallArgs a, const CallSched sch) {
   constexpr int T = tile_groups<G, kCallTileElems>();
   constexpr int NL = G / 16;
@@ -125,134 +171,215 @@ call_kernel(const CallArgs a, const CallSched sch) {
   constexpr int EB = state_bytes<SF>();
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(8) uint64_t full[2];
-  __shared__ int64_t s_item[2];                  // the item of each stage
-  __shared__ int s_pending[2];                   // its inputs still to be waited for
+  __shared__ __align__(8) uint64_t empty[2];
+  __shared__ Item s_item[2];                     // the item in each stage (kEmptyItem: stop)
 
   const int P = a.P;
   const int64_t Gs = a.Gs;
   const uint32_t sbytes = reduce_stage_bytes<BITS, SF, G, kCallTileElems>(P);
   const uint32_t full0 = smem_addr(&full[0]);
+  const uint32_t empty0 = smem_addr(&empty[0]);
   uint32_t* const ticket = sch.ctrl;
   uint32_t* const finished = sch.ctrl + 1;
   uint32_t* const abort = sch.ctrl + 2;
-  const int64_t runs_total = (Gs * G + kRun - 1) / kRun;
-
-  uint64_t pol = 0;
-  // Thread 0: is the input of item `it` final?  1 yes (and consumed: the
-  // counter or flag is reset for the next call), 0 not yet (only when not
-  // `blocking`), -1 gave up (the abort word is then set).
-  auto inputs_ready = [&](const Item& it, bool blocking) -> int {
-    if (it.kind == kPushItem || (it.kind == kReduceItem && P == 1)) return 1;
-    const int64_t tile = (int64_t)it.o * sch.tiles + it.k;
-    uint32_t* w = it.kind == kReduceItem ? sch.push_done + tile : sch.reduce_done + tile;
-    const uint32_t want = it.kind == kReduceItem ? (uint32_t)(P - 1) : 1u;
-    if (blocking) {
-      if (!wait_word(w, want, abort)) {
-        atomicOr(a.status, kStatusTimeout);
-        atomicExch(abort, 1u);
-        return -1;
-      }
-    } else if (ld_acquire(w) != want) {
-      return 0;
-    }
-    *w = 0;                                      // consumed; zero for the next call
-    fence_proxy_async_global();                  // before bulk copies of what it guards
-    return 1;
-  };
-  // Thread 0: starts the copies of item `it` into stage st.
-  auto issue = [&](const Item& it, int st) {
-    const int64_t j0 = it.k * T;
-    const int tg = (int)((Gs - j0) < T ? (Gs - j0) : T);     // groups in the tile
-    uint8_t* stage = smem + (size_t)st * sbytes;
-    const uint32_t bar = full0 + 8 * st;
-    if (it.kind == kPushItem) {
-      const PushPlace pl = push_place<BITS, SF, G>(a, it.p, it.o);
-      mbar_expect_tx(bar, (uint32_t)tg * G * (2u + EB));
-      bulk_g2s(smem_addr(stage), pl.xs + j0 * G, (uint32_t)tg * G * 2u, bar, pol);
-      if (SF != kNoState)
-        bulk_g2s(smem_addr(stage + T * G * 2), pl.es + j0 * G * EB, (uint32_t)tg * G * EB, bar, pol);
-    } else if (it.kind == kReduceItem) {
-      reduce_issue_own<BITS, SF, G, kCallTileElems>(a, stage, bar, it.o, j0, tg, pol);
-      reduce_issue_codes<BITS, SF, G, kCallTileElems>(a, stage, bar, it.o, j0, tg, pol);
-    }
-  };
-  // Thread 0: the next non-empty ticket, or sch.total when there is none.
-  // The ticket after it is fetched right away and used next time, so the
-  // atomic's latency passes while the block computes.
-  int64_t pre = 0;
-  auto take = [&]() -> int64_t {
-    int64_t t = pre;
-    for (;;) {
-      if (t >= sch.total) {                      // (the abort word is read only by waits)
-        pre = sch.total;
-        return sch.total;
-      }
-      if (item_of(a, sch, t).kind != kEmptyItem) break;
-      t = (int64_t)atomicAdd(ticket, 1u);
-    }
-    pre = (int64_t)atomicAdd(ticket, 1u);
-    return t;
-  };
-
-  if (threadIdx.x == 0) {
-    mbar_init(full0, 1);
-    mbar_init(full0 + 8, 1);
-    fence_barrier_init();
-    pol = policy_evict_first();                  // inputs and state are read once per call
-    if (ld_relaxed(abort) != 0) atomicOr(a.status, kStatusTimeout);   // an earlier call gave up
-    // The block holds no item yet, so it may wait.
-    pre = (int64_t)atomicAdd(ticket, 1u);
-    int64_t t = take();
-    if (t < sch.total) {
-      const Item it = item_of(a, sch, t);
-      if (inputs_ready(it, true) < 0) t = sch.total;
-      else issue(it, 0);
-    }
-    s_item[0] = t;
-  }
-  __syncthreads();
-
-  const uint64_t codes_pol = kCodesPolicyLast ? policy_evict_last() : policy_evict_normal();
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  uint32_t phase0 = 0u, phase1 = 0u;             // mbarrier phase of each stage
-  for (int i = 0;; ++i) {
-    const int st = i & 1;
-    const int64_t t = s_item[st];
-    if (t >= sch.total) break;                   // block-uniform
-    const Item it = item_of(a, sch, t);
-    const int64_t j0 = it.k * T;
-    const int tg = (int)((Gs - j0) < T ? (Gs - j0) : T);
-    uint8_t* stage = smem + (size_t)st * sbytes;
-    if (it.kind != kGatherItem) {
-      const uint32_t ph = st ? phase1 : phase0;
-      if (!mbar_wait_block(full0 + 8 * st, ph)) {                  // same outcome for all
-        if (threadIdx.x == 0) {
-          atomicOr(a.status, kStatusTimeout);
-          atomicExch(abort, 1u);
-          mbar_wait_bounded(full0 + 8 * st, ph);                   // let the copies land
+
+  if (threadIdx.x == 0) {
+    for (int st = 0; st < 2; ++st) {
+      mbar_init(full0 + 8 * st, 1);
+      mbar_init(empty0 + 8 * st, kCallWarps);
+    }
+    fence_barrier_init();
+  }
+  __syncthreads();                               // the block's only barrier
+
+  if (warp == kCallWarps) {
+    // ------------------------------------------------------------ control ----
+    if (lane != 0) return;
+    const uint64_t pol = policy_evict_first();   // inputs and state are read once per call
+    if (ld_relaxed(abort) != 0) atomicOr(a.status, kStatusTimeout);   // an earlier call gave up
+    // Is the input of item `it` final?  1 yes (and consumed: the counter or
+    // flag is reset for the next call), 0 not yet (only when not `blocking`),
+    // -1 gave up (the abort word is then set).
+    auto inputs_ready = [&](const Item& it, bool blocking) -> int {
+      if (it.kind == kPushItem || (it.kind == kReduceItem && P == 1)) return 1;
+      const int64_t tile = (int64_t)it.o * sch.tiles + it.k;
+      uint32_t* w = it.kind == kReduceItem ? sch.push_done + tile : sch.reduce_done + tile;
+      const uint32_t want = it.kind == kReduceItem ? (uint32_t)(P - 1) : 1u;
+      if (blocking) {
+        if (!wait_word(w, want, abort)) return -1;
+      } else if (ld_acquire(w) != want) {
+        return 0;
+      }
+      *w = 0;                                    // consumed; zero for the next call
+      fence_proxy_async_global();                // before bulk copies of what it guards
+      return 1;
+    };
+    // Fills stage st with item `it`: its bulk copies, or for a
+    // gather item (which reads the codes from global memory) a plain arrival.
+    auto issue = [&](const Item& it, int st) {
+      s_item[st] = it;
+      const uint32_t bar = full0 + 8 * st;
+      uint8_t* stage = smem + (size_t)st * sbytes;
+      const int64_t j0 = it.k * T;
+      const int tg = (int)((Gs - j0) < T ? (Gs - j0) : T);     // groups in the tile
+      if (it.kind == kPushItem) {
+        const PushPlace pl = push_place<BITS, SF, G>(a, it.p, it.o);
+        mbar_expect_tx(bar, (uint32_t)tg * G * (2u + EB));
+        bulk_g2s(smem_addr(stage), pl.xs + j0 * G, (uint32_t)tg * G * 2u, bar, pol);
+        if (SF != kNoState)
+          bulk_g2s(smem_addr(stage + T * G * 2), pl.es + j0 * G * EB, (uint32_t)tg * G * EB, bar, pol);
+      } else if (it.kind == kReduceItem) {
+        reduce_issue_own<BITS, SF, G, kCallTileElems>(a, stage, bar, it.o, j0, tg, pol);
+        reduce_issue_codes<BITS, SF, G, kCallTileElems>(a, stage, bar, it.o, j0, tg, pol);
+      } else {
+        mbar_arrive(bar);
+      }
+    };
+    // Publishes the completion of ticket t to the other blocks: the compute
+    // warps' writes, ordered before their arrival on the empty barrier that
+    // this thread has waited for, are made visible at GPU scope first.
+    auto publish = [&](int64_t t) {
+      const Item it = item_of(a, sch, t);
+      if (it.kind == kGatherItem || t == sch.hold) return;
+      const int64_t tile = (int64_t)it.o * sch.tiles + it.k;
+      if (it.kind == kPushItem) add_release(sch.push_done + tile, 1u);
+      else if (!FUSED) st_release(sch.reduce_done + tile, 1u);
+    };
+    // Per stage (scalars, not arrays, so that nothing goes to local memory):
+    // the ticket issued into it and not yet published, and the parity of its
+    // next empty and next full phase.
+    int64_t held0 = kSentinel, held1 = kSentinel;
+    uint32_t ep0 = 0u, ep1 = 0u, fp0 = 0u, fp1 = 0u;
+    // Waits until the compute warps are done with stage st, which is then
+    // free; `done` receives the ticket they finished there (kSentinel if the
+    // stage held none or the wait gave up), still to be published.  False if
+    // the wait gave up.
+    auto free_stage = [&](int st, int64_t& done) -> bool {
+      const int64_t h = st ? held1 : held0;
+      done = kSentinel;
+      if (h == kSentinel) return true;
+      if (!mbar_wait_or_abort(empty0 + 8 * st, st ? ep1 : ep0, abort)) return false;
+      done = h;
+      if (st) {
+        ep1 ^= 1u;
+        held1 = kSentinel;
+      } else {
+        ep0 ^= 1u;
+        held0 = kSentinel;
+      }
+      return true;
+    };
+    // The next non-empty ticket, or sch.total when there is none.  The ticket
+    // after it is fetched right away and used next time, so the atomic's
+    // latency passes while the compute warps work.
+    int64_t pre = (int64_t)atomicAdd(ticket, 1u);
+    auto take = [&]() -> int64_t {
+      int64_t t = pre;
+      for (;;) {
+        if (t >= sch.total) {
+          pre = sch.total;
+          return sch.total;
         }
+        if (item_of(a, sch, t).kind != kEmptyItem) break;
+        t = (int64_t)atomicAdd(ticket, 1u);
+      }
+      pre = (int64_t)atomicAdd(ticket, 1u);
+      return t;
+    };
+
+    bool ok = true;
+    int64_t i = 0;                               // items issued so far
+    int64_t done = kSentinel;                    // finished, not yet published
+    for (;;) {
+      const int st = (int)(i & 1);
+      if (!(ok = free_stage(st, done))) break;
+      const int64_t t = take();
+      if (t >= sch.total) break;
+      const Item it = item_of(a, sch, t);
+      int r = inputs_ready(it, false);
+      if (r == 0) {
+        // Not final yet: publish everything this block holds before waiting,
+        // so that no block waits while holding an item it has not published.
+        if (done != kSentinel) publish(done);
+        if (!(ok = free_stage(st ^ 1, done))) break;
+        if (done != kSentinel) publish(done);
+        done = kSentinel;
+        r = inputs_ready(it, true);
+      }
+      if (r < 0) {
+        ok = false;
         break;
       }
-      if (st) phase1 ^= 1u; else phase0 ^= 1u;
-    }
-    // Thread 0 takes the next item now and, if its inputs are final, starts
-    // its copies into the other stage (free: its last item was finished
-    // before the barrier that ended the previous iteration).  If they are
-    // not, it waits only after this item is done and signalled: a block never
-    // waits while it holds an item it has not signalled.
-    if (threadIdx.x == 0) {
-      const int64_t t1 = take();
-      int pend = 0;
-      if (t1 < sch.total) {
-        const Item it1 = item_of(a, sch, t1);
-        if (inputs_ready(it1, false) == 1) issue(it1, st ^ 1);
-        else pend = 1;
+      // Publish the freed stage's item, then refill the stage.  (Refilling
+      // first, so that the release fence waits beside the new copies, measured
+      // 4-6% slower: consumers in other blocks then see the item later.)
+      if (done != kSentinel) publish(done);
+      done = kSentinel;
+      issue(it, st);
+      if (st) {
+        fp1 ^= 1u;
+        held1 = t;
+      } else {
+        fp0 ^= 1u;
+        held0 = t;
       }
-      s_item[st ^ 1] = t1;
-      s_pending[st ^ 1] = pend;
+      ++i;
     }
+    if (done != kSentinel) publish(done);        // freed at the top of the last pass
+    if (ok) {
+      ok = free_stage((int)((i + 1) & 1), done);   // the last item issued
+      if (ok && done != kSentinel) publish(done);
+    }
+    if (ok) {
+      // Stop the compute warps: a sentinel in the stage they wait on next
+      // (free: its item was freed at the top of the loop's last pass).
+      const int st = (int)(i & 1);
+      s_item[st].kind = kEmptyItem;
+      mbar_arrive(full0 + 8 * st);
+      if (st) fp1 ^= 1u;
+      else fp0 ^= 1u;
+    } else {
+      atomicOr(a.status, kStatusTimeout);
+      atomicExch(abort, 1u);
+    }
+    // Copies still in flight land before the block can exit (bounded).
+    mbar_wait_bounded(full0, fp0 ^ 1u);
+    mbar_wait_bounded(full0 + 8, fp1 ^ 1u);
+    // The last block to stop claiming resets the ticket counter for the next call.
+    __threadfence();
+    if (atomicAdd(finished, 1u) == gridDim.x - 1) {
+      atomicExch(ticket, 0u);
+      atomicExch(finished, 0u);
+    }
+    return;
+  }
 
+  // -------------------------------------------------------------- compute ----
+  const uint64_t codes_pol = kCodesPolicyLast ? policy_evict_last() : policy_evict_normal();
+  const int64_t runs_total = (Gs * G + kRun - 1) / kRun;
+  for (int64_t i = 0;; ++i) {
+    const int st = (int)(i & 1);
+    const uint32_t par = (uint32_t)((i >> 1) & 1);
+    const bool got = __all_sync(kFull, mbar_wait_or_abort(full0 + 8 * st, par, abort)) != 0;
+    if (!got) {
+      if (lane == 0) {
+        atomicOr(a.status, kStatusTimeout);
+        atomicExch(abort, 1u);
+      }
+      break;
+    }
+    const volatile Item& vi = s_item[st];
+    Item it;
+    it.kind = vi.kind;
+    if (it.kind == kEmptyItem) break;
+    it.p = vi.p;
+    it.o = vi.o;
+    it.k = vi.k;
+    const int64_t j0 = it.k * T;
+    const int tg = (int)((Gs - j0) < T ? (Gs - j0) : T);
+    const uint8_t* stage = smem + (size_t)st * sbytes;
     if (it.kind == kPushItem) {
       // One 512-element unit per warp: groups [j0 + warp*GPW, +GPW) of the tile.
       const PushPlace pl = push_place<BITS, SF, G>(a, it.p, it.o);
@@ -269,42 +396,15 @@ call_kernel(const CallArgs a, const CallSched sch) {
       }
       push_finish<BITS, SF, MODE, G>(a, v, valid, j0 + gl, q, pl.es, pl.cs, pl.ms, codes_pol);
     } else if (it.kind == kReduceItem) {
-      reduce_tile<BITS, SF, FUSED, MODE, G, kCallTileElems, kThreads / 32>(a, stage, it.o, j0, tg);
+      reduce_tile<BITS, SF, FUSED, MODE, G, kCallTileElems, kCallWarps>(a, stage, it.o, j0, tg);
     } else {
       const int64_t r0 = it.k * (T * G / kRun);
       const int64_t r1 = r0 + T * G / kRun < runs_total ? r0 + T * G / kRun : runs_total;
-      gather_runs<BITS, (T * G / kRun) / (kThreads / 32), MODE, G>(a, it.o, r0 + warp,
-                                                                   kThreads / 32, r1);
+      gather_runs<BITS, (T * G / kRun) / kCallWarps, MODE, G>(a, it.o, r0 + warp, kCallWarps, r1);
     }
-
-    fence_proxy_async();                         // this thread's stage reads before a refill
-    __syncthreads();                             // the item is done; s_item, s_pending set
-    const bool pend = s_pending[st ^ 1] != 0;    // block-uniform
-    if (threadIdx.x == 0) {
-      if (it.kind != kGatherItem && t != sch.hold) {
-        const int64_t tile = (int64_t)it.o * sch.tiles + it.k;
-        if (it.kind == kPushItem)
-          add_release(sch.push_done + tile, 1u);
-        else if (!FUSED)
-          st_release(sch.reduce_done + tile, 1u);
-      }
-      if (pend) {                                // now the block holds nothing unsignalled
-        const int64_t t1 = s_item[st ^ 1];
-        const Item it1 = item_of(a, sch, t1);
-        if (inputs_ready(it1, true) < 0) s_item[st ^ 1] = sch.total;
-        else issue(it1, st ^ 1);
-      }
-    }
-    if (pend) __syncthreads();                   // s_item[st ^ 1] final
-  }
-
-  // The last block to stop claiming resets the ticket counter for the next call.
-  if (threadIdx.x == 0) {
-    __threadfence();
-    if (atomicAdd(finished, 1u) == gridDim.x - 1) {
-      atomicExch(ticket, 0u);
-      atomicExch(finished, 0u);
-    }
+    fence_proxy_async();                         // this lane's stage reads before a refill
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty0 + 8 * st);
   }
 }
 
@@ -324,7 +424,7 @@ cudaError_t launch_t(const CallArgs& a, const CallSched& sch, cudaStream_t s) {
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max);
     if (e != cudaSuccess) return e;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, call_kernel<BITS, SF, MODE, G, FUSED>,
-                                                      kThreads, smem);
+                                                      kCallBlockThreads, smem);
     if (e != cudaSuccess) return e;
     if (per_sm < 1) return cudaErrorInvalidConfiguration;
     resident = sms * per_sm;
@@ -346,7 +446,7 @@ cudaError_t launch_t(const CallArgs& a, const CallSched& sch, cudaStream_t s) {
   if (a.grid_cap > 0 && blocks > a.grid_cap) blocks = a.grid_cap;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)blocks);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(kCallBlockThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
