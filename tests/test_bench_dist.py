@@ -131,3 +131,22 @@ def test_oracle_sample_threads_give_the_single_thread_result():
             many.step(pool, 3)
     assert np.array_equal(one.e.view(np.uint32), many.e.view(np.uint32))
     assert one.ties == many.ties
+
+
+def test_reference_arm_reports_the_gpu_arms_config():
+    """`--impl reference` times the oracle on the host cores for the GPU arm's
+    workload and options, and reports the same config dict, with its sample
+    described beside it, so the two lines pair up."""
+    import bench
+    from bit_error_compensated_gb300.workloads import call_sequence
+    args = bench.main.__globals__["argparse"].Namespace(
+        workload=1, bits=4, g=128, quantizer=0, state="f32", decay=1.0, tokens=0, calls=0,
+        fused=True, persistent=False, graph=False, steps=2, warmup=1)
+    line = bench.run_reference(args, 0, 1)
+    assert line["impl"] == "reference" and line["value"] > 0
+    assert line["config"] == bench.workload_config(args, 1, call_sequence(1, steps=1))
+    assert "sample" in line and line["sample"] == line["cpu_baseline"]["sample"]
+    cb = line["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] == cb["nproc"] >= 1 and cb["cpu_model"]
+    assert line["e2e"] == {"value": line["value"], "unit": "GB/s", "h2d_bytes_per_step": 0,
+                           "d2h_bytes_per_step": 0}
