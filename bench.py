@@ -96,16 +96,22 @@ def load_peaks():
 
 
 def kernel_source_hash() -> str:
-    """Hash of the sources that define the kernels (device code and the
-    constants they are compiled with), so that host-only changes keep the
-    committed ncu figures valid and any kernel change drops them."""
+    """Hash of the code of the sources that define the kernels (device code and
+    the constants they are compiled with), comments and blank space removed,
+    so that host-only or comment-only changes keep the committed ncu figures
+    valid and any change to the kernels' code drops them."""
+    import re
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "bit_error_compensated_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
         if not (name.startswith("k_") or name.endswith(".cuh") or name == "echo_internal.h"):
             continue
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(name.encode() + f.read())
+        with open(os.path.join(csrc, name), encoding="utf-8") as f:
+            code = f.read()
+        code = re.sub(r"/\*.*?\*/", " ", code, flags=re.S)
+        code = re.sub(r"//[^\n]*", " ", code)
+        code = " ".join(code.split())
+        h.update(name.encode() + b"\0" + code.encode())
     return h.hexdigest()[:16]
 
 
