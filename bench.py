@@ -19,10 +19,11 @@ the other workloads of 64 MiB per rank, and the latency of the smallest one
 With --gpus N > 1 (one process per GPU under torchrun) every rank runs an
 independent replica of the workload on its own GPU (the emulated all-reduce
 has no cross-GPU exchange); the value is the work of all ranks over the
-slowest rank's time.  `--impl reference` times the CPU oracle (the plain
-single-threaded restatement the GPU path is checked against) on the host
-cores, its group positions split over all of them, on a sample of the same
-workload.
+slowest rank's time.  Each call's buffers are checked and marshalled once
+(echo.prepare_allreduce), outside the timed loops.  `--impl reference` times
+the CPU oracle (the plain single-threaded restatement the GPU path is
+checked against) on the host cores, its group positions split over all of
+them, on a sample of the same workload.
 """
 from __future__ import annotations
 
@@ -353,10 +354,12 @@ def run_ours(args, rank, local, world):
               "none": None}
     out_rows = list(out)
     call_args = [(list(xs[k]), states[c.state]) for k, c in enumerate(seq)]
+    # each call's buffers are checked and marshalled once, outside the timed loop
+    prepared = [echo.prepare_allreduce(plan, ins, out_rows, comp) for ins, comp in call_args]
 
     def step():
-        for ins, comp in call_args:
-            echo.echo_allreduce(plan, ins, out_rows, comp, stream)
+        for call in prepared:
+            call(stream)
 
     launches_per_call = 1 if args.persistent else (2 if fused else 3) - (1 if P == 1 else 0)
     for _ in range(args.warmup):
@@ -371,8 +374,8 @@ def run_ours(args, rank, local, world):
         gstream = torch.cuda.Stream(dev)
         gstream.wait_stream(stream)
         with torch.cuda.graph(graph, stream=gstream):
-            for ins, comp in call_args:
-                echo.echo_allreduce(plan, ins, out_rows, comp, gstream)
+            for call in prepared:
+                call(gstream)
         torch.cuda.synchronize(dev)
         step = graph.replay
         for _ in range(args.warmup):
@@ -463,7 +466,7 @@ def run_ours(args, rank, local, world):
         if not args.persistent and not args.tokens:
             # the same workload with the other gather variant, for comparison
             other = "separate gather kernel" if fused else "gather fused into reduce"
-            del xs, call_args, out_rows, out
+            del xs, call_args, prepared, out_rows, out
             torch.cuda.empty_cache()
             result["also"][f"{wname} ({other})"] = time_other(echo, number, bits, not fused, dev, args)
     del plan
@@ -546,7 +549,8 @@ def run_e2e(args, echo, plan, xs, seq, states, dev, world):
     ev_read = [torch.cuda.Event() for _ in range(2)]
     calls = len(seq)
     comps = [states[c.state] for c in seq]
-
+    prepared = [[echo.prepare_allreduce(plan, list(dev_in[b]), list(dev_out[b]), comps[k])
+                 for k in range(calls)] for b in range(2)]
     issued = [0]                                          # calls issued so far, all steps
 
     def step():
@@ -561,7 +565,7 @@ def run_e2e(args, echo, plan, xs, seq, states, dev, world):
             s_comp.wait_event(ev_loaded[b])
             if reused:
                 s_comp.wait_event(ev_read[b])             # dev_out[b] copied out
-            echo.echo_allreduce(plan, list(dev_in[b]), list(dev_out[b]), comps[k], s_comp)
+            prepared[b][k](s_comp)
             ev_done[b].record(s_comp)
             with torch.cuda.stream(s_d2h):
                 s_d2h.wait_event(ev_done[b])
@@ -616,9 +620,12 @@ def time_other(echo, number, bits, fused, dev, args):
     launch_bound = w.P * w.n * 2 < (1 << 20)
     reps = max(3, -(-(2000 if launch_bound else 20) // len(seq)))
 
+    prepared = [echo.prepare_allreduce(plan, rows[k % distinct], out_rows, comps[k])
+                for k in range(len(seq))]
+
     def step(s=stream):
-        for k in range(len(seq)):
-            echo.echo_allreduce(plan, rows[k % distinct], out_rows, comps[k], s)
+        for call in prepared:
+            call(s)
 
     def timed(fn):
         for _ in range(3):
@@ -659,7 +666,7 @@ def time_other(echo, number, bits, fused, dev, args):
         torch.cuda.synchronize(dev)
         res["us_per_call_cuda_graph"] = round(timed(graph.replay) * 1e6, 2)
         del graph
-    del plan, xs, bwd
+    del prepared, plan, xs, bwd
     torch.cuda.empty_cache()
     return res
 

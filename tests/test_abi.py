@@ -154,3 +154,43 @@ def test_noalloc_rejects_huge_n_before_any_layout_arithmetic(lib):
         for n in (1 << 61, (1 << 62) + P * 128 * 7, (limit // bits_ // (P * 128) + 1) * P * 128):
             assert n % (P * 128) == 0
             assert fn(P, n, bits_, ptrs, ptrs, None, None) == echo.ECHO_ERR_TOO_LARGE
+
+
+def test_prepared_call_checks_once_and_passes_the_same_arguments(lib, monkeypatch):
+    """A prepared call checks its buffers when it is made (the same checks as
+    echo_allreduce) and then hands the C call the same pointers every time;
+    it refuses to run after the plan's state format changed or the plan is
+    gone.  A stand-in for the C entry point records the calls."""
+    import torch
+    from bit_error_compensated_gb300 import echo
+    P, n = 2, 256
+    plan = echo.Plan(0x1000, P, n, 128, 4)
+    seen = []
+
+    class FakeLib:
+        def echo_allreduce(self, plan_, ins, outs, comp, stream):
+            seen.append((plan_.value, [ins[i] for i in range(P)], [outs[i] for i in range(P)],
+                         comp, stream))
+            return 0
+
+        def echo_plan_destroy(self, h):
+            pass
+
+        def echo_strerror(self, status):
+            return b"x"
+
+    with pytest.raises(ValueError, match="dtype"):
+        echo.prepare_allreduce(plan, [torch.zeros(n), torch.zeros(n)], [4096, 8192])
+    monkeypatch.setattr(echo, "_lib", FakeLib())
+    call = echo.prepare_allreduce(plan, [4096, 8192], [12288, 16384], echo.COMP_DEFAULT)
+    call(stream=7)
+    call(stream=7)
+    assert seen[0] == seen[1] == (0x1000, [4096, 8192], [12288, 16384], echo.COMP_DEFAULT, 7)
+    plan.state_fmt = echo.ECHO_STATE_BF16
+    with pytest.raises(ValueError, match="state format"):
+        call(stream=7)
+    plan.state_fmt = echo.ECHO_STATE_F32
+    echo.echo_plan_destroy(plan)
+    with pytest.raises(ValueError, match="destroyed"):
+        call(stream=7)
+    assert len(seen) == 2
