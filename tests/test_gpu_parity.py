@@ -615,3 +615,27 @@ def test_subnormal_inputs_and_state(echo, fmt, schedule):
         ref = oracle.allreduce(bits(xk), G, 4, e=e_ref, state_fmt=fmt)
         assert np.array_equal(bits(out), ref["out"]), f"outputs differ at call {k}"
         assert_state_close(comp.float().cpu().numpy(), e_ref, f"state after call {k}")
+
+
+@pytest.mark.parametrize("schedule", SCHEDULES)
+def test_prepared_call_matches_oracle(echo, schedule):
+    """echo.prepare_allreduce marshals the buffers once; calling it three times
+    on inputs rewritten in place between calls gives the oracle's results
+    (outputs bit for bit, the carried state within STATE_RTOL)."""
+    P, Gs = 4, 37
+    n = P * G * Gs
+    plan = echo.echo_plan(P, n, G, 4)
+    _set_schedule(echo, plan, schedule)
+    x = torch.empty((P, n), dtype=torch.bfloat16, device="cuda")
+    out = torch.empty_like(x)
+    comp = torch.zeros((P, n), device="cuda")
+    call = echo.prepare_allreduce(plan, list(x), list(out), comp)
+    e_ref = np.zeros((P, n), np.float32)
+    for k in range(3):
+        x.copy_(_inputs(P, n, 300 + k))              # new inputs, same buffers
+        call()
+        torch.cuda.synchronize()
+        ref = oracle.allreduce(bits(x), G, 4, e=e_ref)
+        assert np.array_equal(bits(out), ref["out"]), f"outputs differ at call {k}"
+        assert_state_close(comp.cpu().numpy(), e_ref, f"state after call {k}")
+    assert echo.echo_get_status(plan) == 0
