@@ -62,13 +62,19 @@ constexpr int kCallLagWaves = ECHO_CALL_LAG_WAVES;
 struct Item {
   int kind, p, o;
   int64_t k;
+  int64_t t;        // its ticket
 };
 
+// Tickets and rounds fit 32 bits (echo_set_persistent refuses a problem with
+// 2^31 or more work items), so the decoding divides in 32 bits, a few times
+// cheaper than the 64-bit division on the control thread's path.
 __device__ __forceinline__ Item item_of(const CallArgs& a, const CallSched& sch, int64_t t) {
   const int P = a.P;
   const int pairs = P * (P - 1);
-  const int64_t r = t / sch.round;
-  const int slot = (int)(t - r * sch.round);
+  const uint32_t rd = (uint32_t)sch.round;
+  const uint32_t r32 = (uint32_t)t / rd;
+  const int64_t r = r32;
+  const int slot = (int)((uint32_t)t - r32 * rd);
   Item it;
   if (slot < pairs) {
     it.kind = kPushItem;
@@ -86,6 +92,7 @@ __device__ __forceinline__ Item item_of(const CallArgs& a, const CallSched& sch,
     it.o = it.p = slot - pairs - P;
   }
   if (it.k < 0 || it.k >= sch.tiles) it.kind = kEmptyItem;
+  it.t = t;
   return it;
 }
 
@@ -146,6 +153,24 @@ constexpr int64_t kSentinel = -1;              // no ticket held in a stage
 
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(bar) : "memory");
+}
+
+// Finished items the control thread publishes together, behind one GPU-scope
+// fence (1: each item by its own release add or store).
+#ifndef ECHO_CALL_PUBLISH_BATCH
+#define ECHO_CALL_PUBLISH_BATCH 1
+#endif
+constexpr int kPublishBatch = ECHO_CALL_PUBLISH_BATCH;
+static_assert(kPublishBatch >= 1 && kPublishBatch <= 4, "publish batch: 1 to 4 items");
+
+__device__ __forceinline__ void fence_acq_rel_gpu() {
+  asm volatile("fence.acq_rel.gpu;" ::: "memory");
+}
+__device__ __forceinline__ void add_relaxed(uint32_t* p, uint32_t v) {
+  asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ void st_relaxed(uint32_t* p, uint32_t v) {
+  asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
 }
 
 // Bounded wait on a barrier phase that also gives up once the abort word is
@@ -242,12 +267,32 @@ call_kernel(const CallArgs a, const CallSched sch) {
     // Publishes the completion of ticket t to the other blocks: the compute
     // warps' writes, ordered before their arrival on the empty barrier that
     // this thread has waited for, are made visible at GPU scope first.
+    // Items finished and not yet published, published kPublishBatch at a
+    // time behind one fence (a fence, then relaxed writes, is a release of
+    // each of them).
+    int64_t pend[kPublishBatch];
+    int npend = 0;
+    auto flush = [&]() {
+      if (npend == 0) return;
+      if (kPublishBatch > 1) fence_acq_rel_gpu();
+      for (int b = 0; b < npend; ++b) {
+        const int64_t t = pend[b];
+        const Item it = item_of(a, sch, t);
+        if (it.kind == kGatherItem || t == sch.hold) continue;
+        const int64_t tile = (int64_t)it.o * sch.tiles + it.k;
+        if (kPublishBatch == 1) {
+          if (it.kind == kPushItem) add_release(sch.push_done + tile, 1u);
+          else if (!FUSED) st_release(sch.reduce_done + tile, 1u);
+        } else {
+          if (it.kind == kPushItem) add_relaxed(sch.push_done + tile, 1u);
+          else if (!FUSED) st_relaxed(sch.reduce_done + tile, 1u);
+        }
+      }
+      npend = 0;
+    };
     auto publish = [&](int64_t t) {
-      const Item it = item_of(a, sch, t);
-      if (it.kind == kGatherItem || t == sch.hold) return;
-      const int64_t tile = (int64_t)it.o * sch.tiles + it.k;
-      if (it.kind == kPushItem) add_release(sch.push_done + tile, 1u);
-      else if (!FUSED) st_release(sch.reduce_done + tile, 1u);
+      pend[npend++] = t;
+      if (npend == kPublishBatch) flush();
     };
     // Per stage (scalars, not arrays, so that nothing goes to local memory):
     // the ticket issued into it and not yet published, and the parity of its
@@ -277,14 +322,15 @@ call_kernel(const CallArgs a, const CallSched sch) {
     // after it is fetched right away and used next time, so the atomic's
     // latency passes while the compute warps work.
     int64_t pre = (int64_t)atomicAdd(ticket, 1u);
-    auto take = [&]() -> int64_t {
+    auto take = [&](Item& it) -> int64_t {
       int64_t t = pre;
       for (;;) {
         if (t >= sch.total) {
           pre = sch.total;
           return sch.total;
         }
-        if (item_of(a, sch, t).kind != kEmptyItem) break;
+        it = item_of(a, sch, t);
+        if (it.kind != kEmptyItem) break;
         t = (int64_t)atomicAdd(ticket, 1u);
       }
       pre = (int64_t)atomicAdd(ticket, 1u);
@@ -297,9 +343,9 @@ call_kernel(const CallArgs a, const CallSched sch) {
     for (;;) {
       const int st = (int)(i & 1);
       if (!(ok = free_stage(st, done))) break;
-      const int64_t t = take();
+      Item it;
+      const int64_t t = take(it);
       if (t >= sch.total) break;
-      const Item it = item_of(a, sch, t);
       int r = inputs_ready(it, false);
       if (r == 0) {
         // Not final yet: publish everything this block holds before waiting,
@@ -308,6 +354,7 @@ call_kernel(const CallArgs a, const CallSched sch) {
         if (!(ok = free_stage(st ^ 1, done))) break;
         if (done != kSentinel) publish(done);
         done = kSentinel;
+        flush();
         r = inputs_ready(it, true);
       }
       if (r < 0) {
@@ -334,6 +381,7 @@ call_kernel(const CallArgs a, const CallSched sch) {
       ok = free_stage((int)((i + 1) & 1), done);   // the last item issued
       if (ok && done != kSentinel) publish(done);
     }
+    flush();
     if (ok) {
       // Stop the compute warps: a sentinel in the stage they wait on next
       // (free: its item was freed at the top of the loop's last pass).
@@ -379,6 +427,7 @@ call_kernel(const CallArgs a, const CallSched sch) {
     it.p = vi.p;
     it.o = vi.o;
     it.k = vi.k;
+    it.t = vi.t;
     const int64_t j0 = it.k * T;
     const int tg = (int)((Gs - j0) < T ? (Gs - j0) : T);
     const uint8_t* stage = smem + (size_t)st * sbytes;
