@@ -96,16 +96,23 @@ def load_peaks():
         return FALLBACK_HBM_GBS, "fallback 6.8 TB/s (MEASURED_PEAKS.json absent)"
 
 
-def kernel_source_hash() -> str:
-    """Hash of the code of the sources that define the kernels (device code and
-    the constants they are compiled with), comments and blank space removed,
-    so that host-only or comment-only changes keep the committed ncu figures
-    valid and any change to the kernels' code drops them."""
+KERNEL_SOURCES = {"push_kernel": "k_push.cu", "reduce_kernel": "k_reduce.cu",
+                  "gather_kernel": "k_gather.cu", "call_kernel": "k_call.cu"}
+
+
+def kernel_source_hash(kernel: str = "") -> str:
+    """Hash of the code that defines `kernel` (its own source, the shared
+    device headers and echo_internal.h), comments and blank space removed, so
+    that host-only, comment-only or other kernels' changes keep a committed ncu
+    figure valid and any change to the kernel's own code drops it.  Without a
+    kernel name: every kernel source."""
     import re
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "bit_error_compensated_gb300", "csrc")
+    own = KERNEL_SOURCES.get(kernel)
     for name in sorted(os.listdir(csrc)):
-        if not (name.startswith("k_") or name.endswith(".cuh") or name == "echo_internal.h"):
+        shared = name.endswith(".cuh") or name == "echo_internal.h"
+        if not (shared or (name == own if own else name.startswith("k_"))):
             continue
         with open(os.path.join(csrc, name), encoding="utf-8") as f:
             code = f.read()
@@ -136,7 +143,7 @@ def profiled_traffic(kernel: str, key: str, elements: int):
     except Exception:
         return None, None
     ent = rec.get(key, {}).get(kernel)
-    if not ent or ent.get("source_hash") != kernel_source_hash():
+    if not ent or ent.get("source_hash") != kernel_source_hash(kernel):
         return None, None
     dram = ent.get("dram_bytes_per_launch")
     cap = ent.get("captured_elements")

@@ -87,7 +87,7 @@ def test_profiled_traffic_belongs_to_one_configuration(tmp_path, monkeypatch):
                                  "captured_elements": 8 * 2048 * 4096, "capture": "x.md"}}}
     (tmp_path / "profiles" / "traffic.json").write_text(json.dumps(rec))
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
-    monkeypatch.setattr(bench, "kernel_source_hash", lambda: "h1")
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda kernel="": "h1")
     n2 = 4 * 2048 * 4096
     assert bench.profiled_traffic("push_kernel", f32, n2) == (100, None)
     assert bench.profiled_traffic("push_kernel", bf16, n2) == (60, None)
@@ -101,7 +101,7 @@ def test_profiled_traffic_belongs_to_one_configuration(tmp_path, monkeypatch):
                   bench.traffic_key("p4_2048x4096", 4, 128, "f32", 0, "unfused"),
                   bench.traffic_key("p4_8192x4096", 4, 128, "f32", 0, "fused")):
         assert bench.profiled_traffic("push_kernel", other, n2) == (None, None)
-    monkeypatch.setattr(bench, "kernel_source_hash", lambda: "h2")   # sources changed
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda kernel="": "h2")   # sources changed
     assert bench.profiled_traffic("push_kernel", f32, n2) == (None, None)
 
 
@@ -150,3 +150,23 @@ def test_reference_arm_reports_the_gpu_arms_config():
     assert cb["kind"] == "oracle" and cb["cores"] == cb["nproc"] >= 1 and cb["cpu_model"]
     assert line["e2e"] == {"value": line["value"], "unit": "GB/s", "h2d_bytes_per_step": 0,
                            "d2h_bytes_per_step": 0}
+
+
+def test_kernel_source_hash_follows_code_not_comments(tmp_path, monkeypatch):
+    """A committed ncu figure stays valid through comment-only edits and edits
+    to other kernels, and is dropped by any change to its kernel's code."""
+    import shutil
+    import bench
+    csrc = tmp_path / "bit_error_compensated_gb300" / "csrc"
+    shutil.copytree(os.path.join(bench.ROOT, "bit_error_compensated_gb300", "csrc"), csrc)
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    push0, reduce0 = bench.kernel_source_hash("push_kernel"), bench.kernel_source_hash("reduce_kernel")
+    f = csrc / "k_push.cu"
+    f.write_text(f.read_text() + "\n// a comment\n/* and a block\n comment */\n")
+    assert bench.kernel_source_hash("push_kernel") == push0
+    f.write_text(f.read_text() + "\nnamespace echo { constexpr int kUnused = 1; }\n")
+    assert bench.kernel_source_hash("push_kernel") != push0
+    assert bench.kernel_source_hash("reduce_kernel") == reduce0
+    q = csrc / "quant.cuh"
+    q.write_text(q.read_text() + "\nnamespace echo { constexpr int kAlsoUnused = 2; }\n")
+    assert bench.kernel_source_hash("reduce_kernel") != reduce0
