@@ -8,8 +8,10 @@ A step is one pass of the whole hot path over the workload's call sequence.
 The default workload is the largest: P=8 ranks of 1 GiB bf16 each (512 Mi
 elements per rank, i.i.d. N(0, 0.02^2)), one compensated call with 4-bit codes
 and g=128 (the pages quote their throughput figure for 1 GB messages), inputs
-resident in HBM before the timed region.  Every call runs the push and reduce
-kernels of libecho.so (the reduce writes the P outputs) through its C ABI.
+resident in HBM before the timed region.  Every call runs libecho.so's default
+schedule through its C ABI: one kernel whose blocks each take a whole owner
+tile (the push of every sender, the owner's sum and the gather); the two- and
+three-kernel schedules of the same call are timed beside it.
 The same line also times, under "also", the 8-bit variant of that workload,
 the other workloads of 64 MiB per rank, and the latency of the smallest one
 (P=2, n=4096), plain and replayed as a CUDA graph.
@@ -84,6 +86,15 @@ def call_model_bytes(P, n, bits, compensated, fused, state_bytes=4, g=G):
     return sum(kernel_bytes(P, n, bits, compensated, fused, state_bytes, g).values())
 
 
+def tile_kernel_bytes(P, n, bits, compensated, state_bytes=4, g=G):
+    """Bytes the tile-fused kernel must move per call: the fused call's model
+    without the owner's read of the push codes ((P-1) n c), which it decodes
+    from the values it has just encoded: P n (2 + 2e) + (P-1) n c + n c + 2 P n."""
+    c = code_bytes_per_elem(bits, g)
+    st = 2 * state_bytes if compensated else 0
+    return P * n * (2 + st) + (P - 1) * n * c + n * c + 2 * P * n
+
+
 # ---------------------------------------------------------------- helpers ----
 
 def load_peaks():
@@ -97,7 +108,8 @@ def load_peaks():
 
 
 KERNEL_SOURCES = {"push_kernel": "k_push.cu", "reduce_kernel": "k_reduce.cu",
-                  "gather_kernel": "k_gather.cu", "call_kernel": "k_call.cu"}
+                  "gather_kernel": "k_gather.cu", "call_kernel": "k_call.cu",
+                  "tile_kernel": "k_tile.cu"}
 
 
 def kernel_source_hash(kernel: str = "") -> str:
@@ -320,7 +332,8 @@ def workload_config(args, world, seq):
             "P": P, "n_per_rank": n, "bits": args.bits, "g": args.g,
             "calls_per_step": calls, "compensated": comp == calls,
             "fused_gather": bool(args.fused), "quantizer": QUANTIZERS[args.quantizer],
-            "schedule": ("one persistent kernel" if args.persistent else
+            "schedule": ("one kernel, a block per owner tile" if args.tile else
+                         "one persistent kernel" if args.persistent else
                          "two kernels" if args.fused else "three kernels")
                         + (", CUDA graph of the call sequence" if args.graph else ""),
             "state": {"format": STATE_NAME[args.state], "decay": args.decay},
@@ -353,6 +366,7 @@ def run_ours(args, rank, local, world):
     echo.echo_set_fused(plan, fused)
     echo.echo_set_quantizer(plan, args.quantizer)
     echo.echo_set_persistent(plan, args.persistent)
+    echo.echo_set_tile_fused(plan, args.tile)
     sb = set_state(echo, plan, args)
     sdt = state_dtype(args)
     states = {"fwd": echo.COMP_DEFAULT,
@@ -368,7 +382,8 @@ def run_ours(args, rank, local, world):
         for call in prepared:
             call(stream)
 
-    launches_per_call = 1 if args.persistent else (2 if fused else 3) - (1 if P == 1 else 0)
+    launches_per_call = (1 if args.persistent or args.tile
+                         else (2 if fused else 3) - (1 if P == 1 else 0))
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize(dev)
@@ -422,13 +437,15 @@ def run_ours(args, rank, local, world):
     raw_us = kernel_event_times(echo, plan, [(ins, out_rows, comp) for ins, comp in call_args],
                                 stream, args.steps)
     avg_us, kb_avg, per_kernel_frac = kernel_fracs(raw_us, P, n, bits, fused, sb, g,
-                                                   compensated_calls, calls, args.persistent, hbm)
+                                                   compensated_calls, calls, args.persistent, hbm,
+                                                   args.tile)
     dominant = max(avg_us, key=lambda k: avg_us[k])
     kbytes = kb_avg[dominant]
     achieved = kbytes / (avg_us[dominant] / 1e6) / 1e9
     kname = {"push": "push_kernel", "reduce": "reduce_kernel", "gather": "gather_kernel",
-             "call": "call_kernel"}[dominant]
-    schedule = "persistent" if args.persistent else "fused" if fused else "unfused"
+             "call": "call_kernel", "tile": "tile_kernel"}[dominant]
+    schedule = ("tile" if args.tile else "persistent" if args.persistent
+                else "fused" if fused else "unfused")
     traffic, traffic_note = profiled_traffic(
         kname, traffic_key(shape_of(number)[0], bits, g, args.state, args.quantizer, schedule),
         P * n)
@@ -471,11 +488,15 @@ def run_ours(args, rank, local, world):
             label = shape_of(num)[0] + (f" ({b}-bit codes)" if b != bits else "")
             result["also"][label] = time_other(echo, num, b, fused, dev, args)
         if not args.persistent and not args.tokens:
-            # the same workload with the other gather variant, for comparison
-            other = "separate gather kernel" if fused else "gather fused into reduce"
+            # the same workload with the other schedules, for comparison
             del xs, call_args, prepared, out_rows, out
             torch.cuda.empty_cache()
-            result["also"][f"{wname} ({other})"] = time_other(echo, number, bits, not fused, dev, args)
+            others = [("two kernels", True, False), ("separate gather kernel", False, False),
+                      ("one kernel, a block per owner tile", True, True)]
+            for label, f, t in others:
+                if (f, t) != (fused, args.tile):
+                    result["also"][f"{wname} ({label})"] = time_other(echo, number, bits, f, dev,
+                                                                      args, tile=t)
     del plan
     return result
 
@@ -505,12 +526,17 @@ def kernel_event_times(echo, plan, calls, stream, steps):
     return {k: v / len(ev_sets) * 1e3 for k, v in tot.items()}
 
 
-def kernel_fracs(avg_us, P, n, bits, fused, sb, g, comp_calls, calls, persistent, hbm):
+def kernel_fracs(avg_us, P, n, bits, fused, sb, g, comp_calls, calls, persistent, hbm, tile=False):
     """Per-kernel achieved GB/s over the byte model, as fractions of `hbm`, and
     the kernels that ran."""
     kb_comp = kernel_bytes(P, n, bits, True, fused, sb, g)
     kb_unc = kernel_bytes(P, n, bits, False, fused, g=g)
-    if persistent:
+    if tile:
+        kb_comp = {"tile": tile_kernel_bytes(P, n, bits, True, sb, g)}
+        kb_unc = {"tile": tile_kernel_bytes(P, n, bits, False, g=g)}
+        avg_us = {"tile": avg_us["push"]}
+        ran = ["tile"]
+    elif persistent:
         kb_comp = {"call": sum(kb_comp.values())}
         kb_unc = {"call": sum(kb_unc.values())}
         avg_us = {"call": avg_us["push"]}
@@ -600,7 +626,7 @@ def run_e2e(args, echo, plan, xs, seq, states, dev, world):
             "host_inputs": f"{distinct} distinct pinned input sets cycled over the {calls} calls"}
 
 
-def time_other(echo, number, bits, fused, dev, args):
+def time_other(echo, number, bits, fused, dev, args, tile=None):
     """Time another workload's call sequence (8 distinct inputs cycled, at
     least 20 calls): GB/s and the pipeline's fraction of the HBM roofline.
     For the launch-bound P=2, n=4096 workload also the time per call with the
@@ -616,7 +642,9 @@ def time_other(echo, number, bits, fused, dev, args):
     plan = echo.echo_plan(w.P, w.n, args.g, bits)
     echo.echo_set_fused(plan, fused)
     echo.echo_set_quantizer(plan, args.quantizer)
+    tile = args.tile if tile is None else tile
     echo.echo_set_persistent(plan, args.persistent)
+    echo.echo_set_tile_fused(plan, tile)
     sb = set_state(echo, plan, args)
     bwd = torch.zeros((w.P, w.n), dtype=state_dtype(args), device=dev) if any(
         c.state == "bwd" for c in seq) else None
@@ -654,7 +682,7 @@ def time_other(echo, number, bits, fused, dev, args):
     raw_us = kernel_event_times(echo, plan, [(rows[k % distinct], out_rows, comps[k])
                                              for k in range(len(seq))], stream, reps)
     k_us, _, k_frac = kernel_fracs(raw_us, w.P, w.n, bits, fused, sb, args.g, comp_calls, len(seq),
-                                   args.persistent, hbm)
+                                   args.persistent, hbm, tile and fused and not args.persistent)
     model = (comp_calls * call_model_bytes(w.P, w.n, bits, True, fused, sb, args.g) +
              (len(seq) - comp_calls) * call_model_bytes(w.P, w.n, bits, False, fused, g=args.g)) / len(seq)
     res = {"gbs": round(w.P * w.n * 2 / per_call_s / 1e9, 2), "us_per_call": round(per_call_s * 1e6, 2),
@@ -934,6 +962,9 @@ def main(argv=None):
     ap.add_argument("--fused", action="store_true", help=argparse.SUPPRESS)   # the default
     ap.add_argument("--persistent", action="store_true",
                     help="one persistent kernel per call instead of two or three")
+    ap.add_argument("--two-kernels", action="store_true",
+                    help="push then reduce, two kernels per call, instead of one kernel whose "
+                         "blocks each take a whole owner tile (the default)")
     ap.add_argument("--graph", action="store_true",
                     help="time replays of the call sequence captured as a CUDA graph")
     ap.add_argument("--quantizer", type=int, default=0, choices=[0, 1, 2],
@@ -954,6 +985,7 @@ def main(argv=None):
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     args = ap.parse_args(argv)
     args.fused = not args.unfused
+    args.tile = not (args.two_kernels or args.unfused or args.persistent)
     if args.warmup < 3 and args.impl == "ours":
         ap.error("--warmup must be at least 3")
 

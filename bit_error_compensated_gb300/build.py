@@ -23,7 +23,8 @@ LIB = LIBDIR / "libecho.so"
 # compiled once per supported group size; the objects compile in parallel.
 GROUPS = (64, 128, 256)
 SOURCES = [("echo_api.cu", None), ("echo_noalloc.cu", None)] + [
-    (src, g) for src in ("k_push.cu", "k_reduce.cu", "k_gather.cu", "k_call.cu") for g in GROUPS]
+    (src, g) for src in ("k_push.cu", "k_reduce.cu", "k_gather.cu", "k_call.cu", "k_tile.cu")
+    for g in GROUPS]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

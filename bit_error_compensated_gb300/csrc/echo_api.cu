@@ -30,6 +30,7 @@ struct echo_plan_s {
   int state_fmt = ECHO_STATE_F32;   // ECHO_STATE_*
   float decay = 1.0f;
   int persistent = 0;               // one persistent kernel per call (k_call.cu)
+  int tile = 1;                     // one kernel, each block a whole owner tile (k_tile.cu)
   uint32_t* sched = nullptr;        // its schedule words, zero between calls
   int64_t tiles = 0;                // reduce tiles per segment
   int64_t hold = -1;                // test hook, see echo_debug_hold_push
@@ -112,6 +113,9 @@ cudaError_t launch_gather(const CallArgs& a, int g, int bits, cudaStream_t s, bo
 cudaError_t launch_call(const CallArgs& a, const CallSched& sch, int g, int bits, bool fused,
                         cudaStream_t s) {
   return ECHO_BY_GROUP(g, launch_call_g)(a, sch, bits, fused, s);
+}
+cudaError_t launch_tile(const CallArgs& a, int g, int bits, cudaStream_t s, bool pdl) {
+  return ECHO_BY_GROUP(g, launch_tile_g)(a, bits, s, pdl);
 }
 #undef ECHO_BY_GROUP
 
@@ -255,12 +259,21 @@ int echo_allreduce(echo_plan_t plan, const void* const* in, void* const* out,
   a.decay = plan->decay;
   a.grid_cap = plan->grid_cap;
   NvtxRange range(plan->persistent ? "echo_allreduce (persistent)"
+                  : plan->tile && plan->fused ? "echo_allreduce (tile-fused)"
                   : plan->fused ? "echo_allreduce" : "echo_allreduce (separate gather)");
 
   // Programmatic dependent launch lets each kernel's blocks be scheduled while
   // the previous kernel drains; every kernel waits (griddepcontrol.wait) before
   // touching data the previous one wrote.  Timing events in between make each
   // launch an ordinary stream-ordered one.
+  if (plan->tile && plan->fused && !plan->persistent) {
+    if (plan->timing) ECHO_CUDA(cudaEventRecord(plan->ev[0], s));
+    ECHO_CUDA(echo::launch_tile(a, plan->g, plan->bits, s, plan->timing == 0));
+    if (plan->timing) {
+      for (int k = 1; k < 4; ++k) ECHO_CUDA(cudaEventRecord(plan->ev[k], s));
+    }
+    return ECHO_OK;
+  }
   if (plan->persistent) {
     echo::CallSched sch;
     sch.tiles = plan->tiles;
@@ -352,6 +365,12 @@ int echo_debug_wire(echo_plan_t plan, void* host_dst, size_t bytes, void* stream
 int echo_set_fused(echo_plan_t plan, int fused) {
   if (plan == nullptr || (fused != 0 && fused != 1)) return ECHO_ERR_ARG;
   plan->fused = fused;
+  return ECHO_OK;
+}
+
+int echo_set_tile_fused(echo_plan_t plan, int on) {
+  if (plan == nullptr || (on != 0 && on != 1)) return ECHO_ERR_ARG;
+  plan->tile = on;
   return ECHO_OK;
 }
 

@@ -103,6 +103,7 @@ template <int G> cudaError_t prepare_reduce_g();
 template <int G>
 cudaError_t launch_call_g(const CallArgs& a, const CallSched& sch, int bits, bool fused,
                           cudaStream_t s);
+template <int G> cudaError_t launch_tile_g(const CallArgs& a, int bits, cudaStream_t s, bool pdl);
 
 // Dispatch on the group size g (defined in echo_api.cu, which sees only the
 // declarations above, so each kernel source instantiates its own g alone).
@@ -111,6 +112,7 @@ cudaError_t launch_reduce(const CallArgs& a, int g, int bits, bool fused, cudaSt
 cudaError_t launch_gather(const CallArgs& a, int g, int bits, cudaStream_t s, bool pdl);
 cudaError_t launch_call(const CallArgs& a, const CallSched& sch, int g, int bits, bool fused,
                         cudaStream_t s);
+cudaError_t launch_tile(const CallArgs& a, int g, int bits, cudaStream_t s, bool pdl);
 // Attributes of every reduce kernel, all group sizes.
 cudaError_t prepare_kernels();
 // Records `e` as the error echo_strerror(ECHO_ERR_CUDA) reports in this thread

@@ -52,6 +52,7 @@ _SIGS = {
     "echo_set_quantizer": (_i32, [_vp, _i32]),
     "echo_set_state": (_i32, [_vp, _i32, ctypes.c_float]),
     "echo_set_persistent": (_i32, [_vp, _i32]),
+    "echo_set_tile_fused": (_i32, [_vp, _i32]),
     "echo_debug_hold_push": (_i32, [_vp, _i64]),
     "echo_debug_set_grid": (_i32, [_vp, _i32]),
     "echo_debug_check_guards": (_i32, [_vp, ctypes.POINTER(_i32)]),
@@ -256,6 +257,10 @@ def echo_set_quantizer(plan: Plan, mode: int) -> None:
 def echo_set_state(plan: Plan, fmt: int = ECHO_STATE_F32, decay: float = 1.0) -> None:
     _check(_lib.echo_set_state(plan, fmt, decay), "echo_set_state")
     plan.state_fmt = fmt
+
+
+def echo_set_tile_fused(plan: Plan, on: bool) -> None:
+    _check(_lib.echo_set_tile_fused(plan, 1 if on else 0), "echo_set_tile_fused")
 
 
 def echo_set_persistent(plan: Plan, on: bool) -> None:

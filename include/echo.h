@@ -108,9 +108,10 @@ int echo_plan(int P, int64_t n, int g, int bits, echo_plan_t* out);
  *               zero before the first call of a sequence;
  *               read and updated in place.
  *   stream      cudaStream_t as void*.
- * Enqueues two kernels (push, then reduce, which also writes the outputs;
- * three with a separate gather kernel, see echo_set_fused; one with
- * echo_set_persistent) and returns.  Inputs must stay valid and
+ * Enqueues one kernel (a block per owner tile, see echo_set_tile_fused; two,
+ * push then reduce, with echo_set_tile_fused 0; three with a separate gather
+ * kernel, see echo_set_fused; one persistent kernel with echo_set_persistent)
+ * and returns.  Inputs must stay valid and
  * unmodified until the work completes.  Non-finite inputs or an fp16 step
  * overflow do not fail the call: they set the plan's status word (see
  * echo_get_status) and leave the affected groups' results unspecified.
@@ -170,12 +171,13 @@ int echo_get_status(echo_plan_t plan, void* stream, int* status);
 int echo_debug_wire(echo_plan_t plan, void* host_dst, size_t bytes, void* stream);
 
 /*
- * echo_set_fused -- 1 (default): the reduce kernel writes the P outputs
+ * echo_set_fused -- 1 (default): the block that encodes the gather codes
+ * (the tile-fused kernel's, or the reduce kernel's) writes the P outputs
  * itself from the values it has just encoded (the gather codes are still
  * written); with every rank's output in this GPU's memory, that is the
- * all-gather's decode without a second read of the codes or a third kernel.
- * 0: the gather is its own kernel, which reads the gather codes back and
- * writes all P outputs, as each receiving rank would.  Both give
+ * all-gather's decode without a second read of the codes or another kernel.
+ * 0: push, reduce and a separate gather kernel, which reads the gather codes
+ * back and writes all P outputs, as each receiving rank would.  All give
  * bit-identical outputs, state and codes.
  */
 int echo_set_fused(echo_plan_t plan, int fused);
@@ -184,7 +186,9 @@ int echo_set_fused(echo_plan_t plan, int fused);
  * echo_set_timing -- events (cudaEvent_t as void*) that echo_allreduce records
  * around its kernels: ev[0] before the push kernel, ev[1] after it, ev[2] after
  * the reduce kernel, ev[3] after the gather kernel (== after reduce when
- * fused).  count 4 enables, count 0 disables.  The caller owns the events.
+ * fused); with one kernel per call (tile-fused or persistent) ev[1..3] are
+ * all recorded after it.  count 4 enables, count 0 disables.  The caller owns
+ * the events.
  */
 int echo_set_timing(echo_plan_t plan, void* const* events, int count);
 
@@ -228,6 +232,28 @@ int echo_set_timing(echo_plan_t plan, void* const* events, int count);
 #define ECHO_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
 int echo_allreduce_noalloc(int P, int64_t n, int bits, const void* const* in,
                            void* const* out, void* comp_state, void* stream);
+
+/*
+ * echo_set_tile_fused -- 1 (the default): run each echo_allreduce of the plan
+ * as one kernel in which a block computes a whole owner tile; 0: as two
+ * kernels, the push, then the reduce (which also writes the outputs).  The
+ * push of the P-1 senders, the owner's sum and the gather of a tile of a
+ * segment (Fig. 2(a)) read and write only that tile's element positions of
+ * the P ranks, so with every rank in one GPU's memory one block can take all
+ * of them, with no block waiting on another and no kernel boundary between
+ * the push and the reduce.  The block walks the ranks in ascending order:
+ * each sender's codes and meta word are written to the owner's receive slot
+ * and its held error updated, as by the push; the owner sums the decoded
+ * values (decoding the codes it has just encoded rather than reading the slot
+ * back) with its own segment in fp32, quantizes the sum once, writes the
+ * gather codes and every rank's output and keeps its error.  Results, state
+ * and receive slots are bit-identical to the other schedules.  It applies
+ * while the gather is fused (echo_set_fused 1, the default) and the call is
+ * not persistent (echo_set_persistent 0, the default): a separate gather
+ * kernel or the persistent kernel take precedence.  ECHO_ERR_ARG for on not
+ * 0 or 1.
+ */
+int echo_set_tile_fused(echo_plan_t plan, int on);
 
 /*
  * echo_set_persistent -- run each later echo_allreduce of the plan as one

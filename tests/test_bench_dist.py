@@ -141,7 +141,7 @@ def test_reference_arm_reports_the_gpu_arms_config():
     from bit_error_compensated_gb300.workloads import call_sequence
     args = bench.main.__globals__["argparse"].Namespace(
         workload=1, bits=4, g=128, quantizer=0, state="f32", decay=1.0, tokens=0, calls=0,
-        fused=True, persistent=False, graph=False, steps=2, warmup=1)
+        fused=True, persistent=False, tile=False, graph=False, steps=2, warmup=1)
     line = bench.run_reference(args, 0, 1)
     assert line["impl"] == "reference" and line["value"] > 0
     assert line["config"] == bench.workload_config(args, 1, call_sequence(1, steps=1))

@@ -34,20 +34,22 @@ def _inputs(P, n, seed, scale=1.0):
     return (x * spread).to(torch.bfloat16)
 
 
-SCHEDULES = ["fused", "unfused", "persistent"]
+SCHEDULES = ["fused", "unfused", "persistent", "tile"]
 
 
 def _set_schedule(echo, plan, schedule):
     echo.echo_set_fused(plan, schedule != "unfused")
     echo.echo_set_persistent(plan, schedule == "persistent")
+    echo.echo_set_tile_fused(plan, schedule == "tile")
 
 
 def _run_sequence(echo, P, Gs, bits_, mode, fused, calls=3, seed=0, inplace=False, quant=0,
-                  fmt=0, decay=1.0, g=G, persistent=False):
+                  fmt=0, decay=1.0, g=G, persistent=False, tile=False):
     n = P * g * Gs
     plan = echo.echo_plan(P, n, g, bits_)
     echo.echo_set_fused(plan, fused)
     echo.echo_set_persistent(plan, persistent)
+    echo.echo_set_tile_fused(plan, tile)
     echo.echo_set_quantizer(plan, quant)
     echo.echo_set_state(plan, fmt, decay)
     assert echo.echo_comp_bytes(plan) == P * n * (4 if fmt == 0 else 2)
@@ -191,15 +193,42 @@ def test_persistent_tile_boundaries(echo, Gs):
     _run_sequence(echo, 3, Gs, 4, "caller", 0, calls=2, seed=Gs, persistent=True)
 
 
-def test_persistent_same_bits_as_three_kernels(echo):
+@pytest.mark.parametrize("mode", ["none", "default", "caller"])
+@pytest.mark.parametrize("bits_", [4, 8])
+@pytest.mark.parametrize("P", [1, 2, 3, 4, 8, 16])
+def test_tile_fused_matches_oracle(echo, P, bits_, mode):
+    """The whole call as one kernel, a block per owner tile (echo_set_tile_fused)."""
+    _run_sequence(echo, P, 37, bits_, mode, 1, seed=2200 + P * 10 + bits_, tile=True)
+
+
+@pytest.mark.parametrize("opts", [dict(g=64), dict(g=256), dict(quant=1), dict(quant=2),
+                                  dict(fmt=1, decay=0.5), dict(fmt=2), dict(g=64, quant=2),
+                                  dict(g=256, fmt=1), dict(inplace=True), dict(decay=0.75)])
+def test_tile_fused_with_options(echo, opts):
+    opts = dict(opts)
+    g = opts.pop("g", G)
+    _run_sequence(echo, 4, {64: 75, 128: 37, 256: 37}[g], 4, "caller", 1, seed=2300, g=g,
+                  tile=True, **opts)
+
+
+@pytest.mark.parametrize("P,Gs", [(3, 1), (3, 7), (3, 8), (3, 9), (5, 15), (5, 16), (5, 17),
+                                  (2, 300)])
+def test_tile_fused_tile_boundaries(echo, P, Gs):
+    """Segments of a few groups up to several tiles, with short last tiles."""
+    _run_sequence(echo, P, Gs, 4, "caller", 1, calls=2, seed=Gs, tile=True)
+
+
+def test_every_schedule_gives_the_same_bits(echo):
     """Outputs, state and every wire byte of a call sequence agree between the
-    two schedules."""
+    four schedules: one kernel a block per owner tile (the default), push and
+    reduce, push, reduce and gather, and the persistent kernel."""
     P, Gs = 4, 70
     n = P * G * Gs
     res = []
-    for persistent in (False, True):
+    for schedule in ("tile", "fused", "unfused", "persistent"):
         plan = echo.echo_plan(P, n, G, 4)
-        echo.echo_set_persistent(plan, persistent)
+        if schedule != "tile":                 # the default needs no call
+            _set_schedule(echo, plan, schedule)
         comp = torch.zeros((P, n), device="cuda")
         outs = []
         for k in range(4):
@@ -209,9 +238,10 @@ def test_persistent_same_bits_as_three_kernels(echo):
             outs.append(bits(out))
         torch.cuda.synchronize()
         res.append((outs, comp.cpu().numpy().view(np.uint32), echo.echo_debug_wire(plan)))
-    assert all(np.array_equal(a, b) for a, b in zip(res[0][0], res[1][0]))
-    assert np.array_equal(res[0][1], res[1][1])
-    assert res[0][2] == res[1][2]
+    for other in res[1:]:
+        assert all(np.array_equal(a, b) for a, b in zip(res[0][0], other[0]))
+        assert np.array_equal(res[0][1], other[1])
+        assert res[0][2] == other[2]
 
 
 def test_persistent_bounded_wait_reports_timeout(echo):
@@ -242,15 +272,14 @@ def test_persistent_bounded_wait_reports_timeout(echo):
         assert np.array_equal(bits(out), oracle.allreduce(bits(xk), G, 4)["out"])
 
 
-@pytest.mark.parametrize("schedule", ["fused", "unfused", "persistent"])
+@pytest.mark.parametrize("schedule", SCHEDULES)
 def test_calls_captured_in_a_cuda_graph(echo, schedule):
     """A sequence of calls captured once by stream capture and replayed: every
     replay continues the state, and outputs match the oracle's calls."""
     P, Gs = 4, 37
     n = P * G * Gs
     plan = echo.echo_plan(P, n, G, 4)
-    echo.echo_set_fused(plan, schedule != "unfused")
-    echo.echo_set_persistent(plan, schedule == "persistent")
+    _set_schedule(echo, plan, schedule)
     xs = [_inputs(P, n, 4000 + k) for k in range(3)]
     outs = [torch.empty_like(x) for x in xs]
     echo.echo_allreduce(plan, list(xs[0]), list(outs[0]), None)      # first use outside capture
@@ -500,6 +529,7 @@ def test_argument_errors(echo):
     assert echo.echo_comp_bytes(plan) == plan.P * plan.n * 4       # unchanged
     for bad in (2, -1):                                 # the C call takes 0 or 1 only
         assert echo._lib.echo_set_persistent(plan, bad) == echo.ECHO_ERR_ARG
+        assert echo._lib.echo_set_tile_fused(plan, bad) == echo.ECHO_ERR_ARG
     with pytest.raises(echo.EchoError) as ei:
         echo.echo_debug_hold_push(plan, -2)
     assert ei.value.status == echo.ECHO_ERR_ARG

@@ -79,11 +79,12 @@ def _full_sequence(echo, number, bits_, wire_every=1):
 
 
 def _sampled_sequence(echo, number, bits_, sample, calls=None, wire_calls=(0,), quant=0,
-                      fmt=0, decay=1.0, g=G, persistent=False, fused=False):
+                      fmt=0, decay=1.0, g=G, persistent=False, fused=False, tile=False):
     w = WORKLOADS[number]
     P, n = w.P, w.n
     plan = echo.echo_plan(P, n, g, bits_)
     echo.echo_set_persistent(plan, persistent)
+    echo.echo_set_tile_fused(plan, tile)
     echo.echo_set_fused(plan, fused)
     echo.echo_set_quantizer(plan, quant)
     echo.echo_set_state(plan, fmt, decay)
@@ -185,3 +186,18 @@ def test_p8_1gib_persistent_sampled(echo):
 def test_p4_32768x1024_persistent_sampled(echo):
     """Two states (forward and backward sites) through the persistent kernel."""
     _sampled_sequence(echo, 5, 4, sample=256, calls=24, persistent=True)
+
+
+def test_p8_1gib_tile_fused_sampled(echo):
+    """The tile-fused kernel at 1 GiB per rank, 4- and 8-bit codes."""
+    _sampled_sequence(echo, 3, 4, sample=2048, calls=1, tile=True)
+    _sampled_sequence(echo, 3, 8, sample=2048, calls=1, tile=True)
+
+
+def test_p4_32768x1024_tile_fused_sampled(echo):
+    """Two states (forward and backward sites) through the tile-fused kernel."""
+    _sampled_sequence(echo, 5, 4, sample=1024, calls=224, tile=True, fused=True)
+
+
+def test_p4_2048x4096_tile_fused_sampled(echo):
+    _sampled_sequence(echo, 2, 4, sample=512, calls=16, tile=True, fused=True)
