@@ -299,6 +299,26 @@ def set_state(echo, plan, args):
     return 4 if args.state == "f32" else 2
 
 
+def workload_sequence(args, number=None):
+    """The call sequence a run times: the workload's own (one step of it), or,
+    with --uncompensated, the same calls with no compensator state (the
+    "4-bit, no compensation" row of the paper's Table 6); --calls keeps only
+    the first calls."""
+    import dataclasses
+    from bit_error_compensated_gb300.workloads import call_sequence
+    seq = call_sequence(args.workload if number is None else number, steps=1)
+    if getattr(args, "uncompensated", False):
+        seq = [dataclasses.replace(c, state="none") for c in seq]
+    if number is None and args.calls:
+        seq = seq[:args.calls]
+    return seq
+
+
+def state_key(args) -> str:
+    """The state format a measurement ran with ("none" when uncompensated)."""
+    return "none" if getattr(args, "uncompensated", False) else args.state
+
+
 def shape_of(number, tokens=None):
     """(name, P, n) of a workload, with the token count overridden for
     profiling runs on a smaller case of the same shape family."""
@@ -324,9 +344,9 @@ def workload_config(args, world, seq):
     reference arm (the oracle on the host cores), so the two can be paired."""
     from bit_error_compensated_gb300.workloads import WORKLOADS
     name, P, n = shape_of(args.workload, args.tokens)
-    sb = 4 if args.state == "f32" else 2
-    calls = len(seq)
     comp = sum(1 for c in seq if c.state != "none")
+    sb = 0 if not comp else 4 if args.state == "f32" else 2
+    calls = len(seq)
     distinct = calls
     return {"workload": name, "description": WORKLOADS[args.workload].description,
             "P": P, "n_per_rank": n, "bits": args.bits, "g": args.g,
@@ -336,9 +356,11 @@ def workload_config(args, world, seq):
                          "one persistent kernel" if args.persistent else
                          "two kernels" if args.fused else "three kernels")
                         + (", CUDA graph of the call sequence" if args.graph else ""),
-            "state": {"format": STATE_NAME[args.state], "decay": args.decay},
+            "state": ({"format": STATE_NAME[args.state], "decay": args.decay} if comp
+                      else {"format": "none"}),
             "io": "bf16 in/out, fp32 arithmetic, "
-                  f"{args.bits}-bit codes, {STATE_NAME[args.state]} state",
+                  f"{args.bits}-bit codes, "
+                  + (f"{STATE_NAME[args.state]} state" if comp else "no compensator state"),
             "l2": f"inputs distinct per call ({distinct} x {P * n * 2 >> 20} MiB resident); "
                   f"per-call working set {(P * n * (2 + 2 + 2 * sb)) >> 20} MiB > L2 "
                   f"({L2_BYTES >> 20} MiB)",
@@ -348,16 +370,13 @@ def workload_config(args, world, seq):
 def run_ours(args, rank, local, world):
     import torch
     from bit_error_compensated_gb300 import echo
-    from bit_error_compensated_gb300.workloads import call_sequence
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     stream = torch.cuda.current_stream(dev)
     number, bits, fused = args.workload, args.bits, args.fused
     wname, P, n = shape_of(number, args.tokens)
-    seq = call_sequence(number, steps=1)
-    if args.calls:
-        seq = seq[:args.calls]
+    seq = workload_sequence(args)
     calls = len(seq)
     xs = build_inputs(number, seq, calls, dev, args.tokens)
     out = torch.empty((P, n), dtype=torch.bfloat16, device=dev)
@@ -447,7 +466,7 @@ def run_ours(args, rank, local, world):
     schedule = ("tile" if args.tile else "persistent" if args.persistent
                 else "fused" if fused else "unfused")
     traffic, traffic_note = profiled_traffic(
-        kname, traffic_key(shape_of(number)[0], bits, g, args.state, args.quantizer, schedule),
+        kname, traffic_key(shape_of(number)[0], bits, g, state_key(args), args.quantizer, schedule),
         P * n)
     roofline = {"bound": "hbm", "kernel": kname, "achieved": round(achieved, 1), "peak": hbm,
                 "unit": "GB/s", "frac": round(achieved / hbm, 4), "traffic": traffic,
@@ -633,9 +652,9 @@ def time_other(echo, number, bits, fused, dev, args, tile=None):
     sequence replayed as a CUDA graph.  No parity here: the GPU tests check
     these workloads against the oracle."""
     import torch
-    from bit_error_compensated_gb300.workloads import WORKLOADS, call_sequence
+    from bit_error_compensated_gb300.workloads import WORKLOADS
     w = WORKLOADS[number]
-    seq = call_sequence(number, steps=1)
+    seq = workload_sequence(args, number)
     distinct = min(8, len(seq))
     xs = build_inputs(number, seq, distinct, dev)
     out = torch.empty((w.P, w.n), dtype=torch.bfloat16, device=dev)
@@ -761,7 +780,11 @@ class OracleSample:
         pos = np.sort(rng.choice(P * Gs, size=max(1, P * Gs // frac), replace=False))
         self.owners = (pos // Gs).astype(np.int32)
         idx = (pos[:, None] * g + np.arange(g)[None, :]).ravel()
-        self.e = np.zeros((pos.size, P, g), np.float32)
+        # one held-error array per compensator state of the sequence; an
+        # uncompensated call reads and writes none
+        self.states = [c.state for c in seq]
+        self.e = {st: np.zeros((pos.size, P, g), np.float32)
+                  for st in sorted(set(self.states) - {"none"})}
         self.inputs = []
         distinct = min(len(seq), 4)
         if xs is not None:
@@ -787,22 +810,23 @@ class OracleSample:
         self.i = 0
         self.ties = 0          # exact rounding ties the oracle met (codes and zero points)
 
-    def _chunk(self, x, a, b):
+    def _chunk(self, x, e, a, b):
         import oracle
-        return oracle.group_positions(self.P, self.owners[a:b], self.bits, x[a:b], self.e[a:b],
-                                      **self.opts)["ties"]
+        return oracle.group_positions(self.P, self.owners[a:b], self.bits, x[a:b],
+                                      None if e is None else e[a:b], **self.opts)["ties"]
 
     def step(self, pool=None, threads=1):
         """One call over all sampled positions: on this thread, or split into
         `threads` contiguous chunks run by `pool` (the oracle call releases
         the interpreter lock, so the chunks run on separate cores)."""
         x = self.inputs[self.i % len(self.inputs)]
+        e = self.e.get(self.states[self.i % len(self.states)])
         npos = self.owners.size
         if pool is None or threads <= 1:
-            self.ties += self._chunk(x, 0, npos)
+            self.ties += self._chunk(x, e, 0, npos)
         else:
             cuts = [npos * t // threads for t in range(threads + 1)]
-            futs = [pool.submit(self._chunk, x, cuts[t], cuts[t + 1]) for t in range(threads)
+            futs = [pool.submit(self._chunk, x, e, cuts[t], cuts[t + 1]) for t in range(threads)
                     if cuts[t + 1] > cuts[t]]
             self.ties += sum(f.result() for f in futs)
         self.i += 1
@@ -851,13 +875,10 @@ def run_reference(args, rank, world):
     positions split over all of them), K timed steps of OracleSample after W
     warm-up steps, on the workload and options of the GPU arm."""
     from concurrent.futures import ThreadPoolExecutor
-    from bit_error_compensated_gb300.workloads import call_sequence
-    seq = call_sequence(args.workload, steps=1)
-    if args.calls:
-        seq = seq[:args.calls]
+    seq = workload_sequence(args)
     info = host_cpu_info()
     threads = info["nproc"]
-    s = oracle_sample(args)
+    s = oracle_sample(args, seq=seq)
     with ThreadPoolExecutor(threads) as pool:
         for _ in range(args.warmup):
             s.step(pool, threads)
@@ -971,6 +992,8 @@ def main(argv=None):
                     help="0 zero-aware (the method), 1 naive zero-point, 2 symmetric grid")
     ap.add_argument("--state", choices=["f32", "bf16", "f16"], default="f32",
                     help="compensator state storage (bf16 or fp16 halve its traffic)")
+    ap.add_argument("--uncompensated", action="store_true",
+                    help="every call without compensator state (no state read or written)")
     ap.add_argument("--decay", type=float, default=1.0,
                     help="kept error = decay x revealed error (1 = plain error feedback)")
     ap.add_argument("--also", default="3b8,2,4,5,1",

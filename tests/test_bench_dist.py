@@ -129,8 +129,47 @@ def test_oracle_sample_threads_give_the_single_thread_result():
         for _ in range(3):
             one.step()
             many.step(pool, 3)
-    assert np.array_equal(one.e.view(np.uint32), many.e.view(np.uint32))
+    assert one.e.keys() == many.e.keys() == {"fwd"}
+    assert np.array_equal(one.e["fwd"].view(np.uint32), many.e["fwd"].view(np.uint32))
     assert one.ties == many.ties
+
+
+def test_uncompensated_runs_and_oracle_sample_states():
+    """--uncompensated turns every call of the sequence into one without state;
+    the oracle sample then holds no state, and in a mixed sequence (the P=2
+    workload: one uncompensated call, then compensated ones) it leaves the
+    state untouched on the uncompensated call and keeps the forward and
+    backward states apart (the P=4, 32768x1024 workload)."""
+    import numpy as np
+    import bench
+
+    class A:
+        workload, bits, g, quantizer, state, decay, tokens, calls = 1, 4, 128, 0, "f32", 1.0, 0, 0
+        uncompensated, fused, tile, persistent, graph = False, True, True, False, False
+    a = A()
+    mixed = bench.workload_sequence(a)
+    assert [c.state for c in mixed] == ["none"] + ["fwd"] * 8
+    assert bench.state_key(a) == "f32"
+    s = bench.oracle_sample(a, seq=mixed)
+    s.step()                                   # the uncompensated call
+    assert not s.e["fwd"].any()
+    s.step()
+    assert s.e["fwd"].any()
+    a.uncompensated = True
+    none = bench.workload_sequence(a)
+    assert [c.state for c in none] == ["none"] * 9 and bench.state_key(a) == "none"
+    s = bench.oracle_sample(a, seq=none)
+    assert s.e == {}
+    s.step()
+    s.step()
+    cfg = bench.workload_config(a, 1, none)
+    assert cfg["compensated"] is False and cfg["state"] == {"format": "none"}
+    a.uncompensated, a.calls = False, 3
+    assert len(bench.workload_sequence(a)) == 3
+    assert len(bench.workload_sequence(a, 2)) == 64   # another workload: all of its calls
+    a.workload, a.calls = 5, 0
+    seq5 = bench.workload_sequence(a)
+    assert {c.state for c in seq5} == {"fwd", "bwd"}
 
 
 def test_reference_arm_reports_the_gpu_arms_config():
