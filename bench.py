@@ -314,6 +314,17 @@ def workload_sequence(args, number=None):
     return seq
 
 
+# --tile-form: the tile kernel's form (echo_set_tile_fused modes), as the
+# config names it, and as the ncu traffic records key it.
+TILE_MODE = {"auto": 1, "loop": 2, "parallel": 3}
+TILE_FORM_NOTE = {"auto": "", "loop": " (rank loop)", "parallel": " (rank-parallel)"}
+TILE_KEY = {"auto": "", "loop": "", "parallel": "_rp"}
+
+
+def tile_form(args) -> str:
+    return getattr(args, "tile_form", "auto")
+
+
 def state_key(args) -> str:
     """The state format a measurement ran with ("none" when uncompensated)."""
     return "none" if getattr(args, "uncompensated", False) else args.state
@@ -352,7 +363,8 @@ def workload_config(args, world, seq):
             "P": P, "n_per_rank": n, "bits": args.bits, "g": args.g,
             "calls_per_step": calls, "compensated": comp == calls,
             "fused_gather": bool(args.fused), "quantizer": QUANTIZERS[args.quantizer],
-            "schedule": ("one kernel, a block per owner tile" if args.tile else
+            "schedule": ("one kernel, a block per owner tile" + TILE_FORM_NOTE[tile_form(args)]
+                         if args.tile else
                          "one persistent kernel" if args.persistent else
                          "two kernels" if args.fused else "three kernels")
                         + (", CUDA graph of the call sequence" if args.graph else ""),
@@ -385,7 +397,7 @@ def run_ours(args, rank, local, world):
     echo.echo_set_fused(plan, fused)
     echo.echo_set_quantizer(plan, args.quantizer)
     echo.echo_set_persistent(plan, args.persistent)
-    echo.echo_set_tile_fused(plan, args.tile)
+    echo.echo_set_tile_fused(plan, TILE_MODE[tile_form(args)] if args.tile else 0)
     sb = set_state(echo, plan, args)
     sdt = state_dtype(args)
     states = {"fwd": echo.COMP_DEFAULT,
@@ -463,7 +475,7 @@ def run_ours(args, rank, local, world):
     achieved = kbytes / (avg_us[dominant] / 1e6) / 1e9
     kname = {"push": "push_kernel", "reduce": "reduce_kernel", "gather": "gather_kernel",
              "call": "call_kernel", "tile": "tile_kernel"}[dominant]
-    schedule = ("tile" if args.tile else "persistent" if args.persistent
+    schedule = ("tile" + TILE_KEY[tile_form(args)] if args.tile else "persistent" if args.persistent
                 else "fused" if fused else "unfused")
     traffic, traffic_note = profiled_traffic(
         kname, traffic_key(shape_of(number)[0], bits, g, state_key(args), args.quantizer, schedule),
@@ -663,7 +675,7 @@ def time_other(echo, number, bits, fused, dev, args, tile=None):
     echo.echo_set_quantizer(plan, args.quantizer)
     tile = args.tile if tile is None else tile
     echo.echo_set_persistent(plan, args.persistent)
-    echo.echo_set_tile_fused(plan, tile)
+    echo.echo_set_tile_fused(plan, TILE_MODE[tile_form(args)] if tile else 0)
     sb = set_state(echo, plan, args)
     bwd = torch.zeros((w.P, w.n), dtype=state_dtype(args), device=dev) if any(
         c.state == "bwd" for c in seq) else None
@@ -986,6 +998,9 @@ def main(argv=None):
     ap.add_argument("--two-kernels", action="store_true",
                     help="push then reduce, two kernels per call, instead of one kernel whose "
                          "blocks each take a whole owner tile (the default)")
+    ap.add_argument("--tile-form", choices=["auto", "loop", "parallel"], default="auto",
+                    help="the one-kernel schedule's form: chosen by size (default), the rank "
+                         "loop, or rank-parallel blocks")
     ap.add_argument("--graph", action="store_true",
                     help="time replays of the call sequence captured as a CUDA graph")
     ap.add_argument("--quantizer", type=int, default=0, choices=[0, 1, 2],

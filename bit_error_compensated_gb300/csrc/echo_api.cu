@@ -30,7 +30,8 @@ struct echo_plan_s {
   int state_fmt = ECHO_STATE_F32;   // ECHO_STATE_*
   float decay = 1.0f;
   int persistent = 0;               // one persistent kernel per call (k_call.cu)
-  int tile = 1;                     // one kernel, each block a whole owner tile (k_tile.cu)
+  int tile = ECHO_TILE_AUTO;        // one kernel, each block a whole owner tile (k_tile.cu)
+  int sms = 0;                      // SMs of the plan's device
   uint32_t* sched = nullptr;        // its schedule words, zero between calls
   int64_t tiles = 0;                // reduce tiles per segment
   int64_t hold = -1;                // test hook, see echo_debug_hold_push
@@ -114,8 +115,9 @@ cudaError_t launch_call(const CallArgs& a, const CallSched& sch, int g, int bits
                         cudaStream_t s) {
   return ECHO_BY_GROUP(g, launch_call_g)(a, sch, bits, fused, s);
 }
-cudaError_t launch_tile(const CallArgs& a, int g, int bits, cudaStream_t s, bool pdl) {
-  return ECHO_BY_GROUP(g, launch_tile_g)(a, bits, s, pdl);
+cudaError_t launch_tile(const CallArgs& a, int g, int bits, bool rank_parallel, cudaStream_t s,
+                        bool pdl) {
+  return ECHO_BY_GROUP(g, launch_tile_g)(a, bits, rank_parallel, s, pdl);
 }
 #undef ECHO_BY_GROUP
 
@@ -124,9 +126,29 @@ cudaError_t prepare_kernels() {
   if ((r = prepare_reduce_g<64>()) != cudaSuccess) e = r;
   if ((r = prepare_reduce_g<128>()) != cudaSuccess) e = r;
   if ((r = prepare_reduce_g<256>()) != cudaSuccess) e = r;
+  if ((r = prepare_tile_g<64>()) != cudaSuccess) e = r;
+  if ((r = prepare_tile_g<128>()) != cudaSuccess) e = r;
+  if ((r = prepare_tile_g<256>()) != cudaSuccess) e = r;
   return e;
 }
 }  // namespace echo
+
+namespace {
+// The tile schedule's form for a call of the plan: rank-parallel blocks when
+// the grid (one block per owner tile) is too small to keep the SMs busy with
+// the rank loop's small blocks, whose per-block path is P pushes long, and
+// P >= 3 (with two ranks both forms take the same time).
+#ifndef ECHO_TILE_RP_TILES_PER_SM
+#define ECHO_TILE_RP_TILES_PER_SM 4
+#endif
+bool tile_rank_parallel(const echo_plan_s* plan) {
+  if (plan->tile == ECHO_TILE_RANK_PARALLEL) return true;
+  if (plan->tile != ECHO_TILE_AUTO || plan->P < 3) return false;   // P = 2: the loop is as fast
+  const int64_t T = echo::kReduceTileElems / plan->g;
+  const int64_t blocks = (plan->Gs + T - 1) / T * plan->P;
+  return blocks <= (int64_t)ECHO_TILE_RP_TILES_PER_SM * plan->sms;
+}
+}  // namespace
 
 extern "C" {
 
@@ -165,6 +187,7 @@ int echo_plan(int P, int64_t n, int g, int bits, echo_plan_t* out) {
   const size_t sched_bytes = (size_t)echo::sched_words(P, p->tiles) * sizeof(uint32_t);
 
   cudaError_t e = cudaGetDevice(&p->device);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&p->sms, cudaDevAttrMultiProcessorCount, p->device);
   if (e == cudaSuccess && p->device >= 0 && p->device < 64) {
     std::lock_guard<std::mutex> lock(g_prepare_mutex);
     if (!g_kernels_prepared[p->device]) {
@@ -268,7 +291,8 @@ int echo_allreduce(echo_plan_t plan, const void* const* in, void* const* out,
   // launch an ordinary stream-ordered one.
   if (plan->tile && plan->fused && !plan->persistent) {
     if (plan->timing) ECHO_CUDA(cudaEventRecord(plan->ev[0], s));
-    ECHO_CUDA(echo::launch_tile(a, plan->g, plan->bits, s, plan->timing == 0));
+    ECHO_CUDA(echo::launch_tile(a, plan->g, plan->bits, tile_rank_parallel(plan), s,
+                                plan->timing == 0));
     if (plan->timing) {
       for (int k = 1; k < 4; ++k) ECHO_CUDA(cudaEventRecord(plan->ev[k], s));
     }
@@ -369,7 +393,7 @@ int echo_set_fused(echo_plan_t plan, int fused) {
 }
 
 int echo_set_tile_fused(echo_plan_t plan, int on) {
-  if (plan == nullptr || (on != 0 && on != 1)) return ECHO_ERR_ARG;
+  if (plan == nullptr || on < ECHO_TILE_OFF || on > ECHO_TILE_RANK_PARALLEL) return ECHO_ERR_ARG;
   plan->tile = on;
   return ECHO_OK;
 }

@@ -30,6 +30,11 @@ constexpr bool group_supported(int g) { return g == 64 || g == 128 || g == 256; 
 constexpr int kReduceTileElems = ECHO_REDUCE_TILE * 128;
 constexpr int kReduceWarps = ECHO_REDUCE_WARPS;
 static_assert(kReduceTileElems % (4 * 256) == 0, "reduce tile: a multiple of 4 groups of 256");
+// Ranks the rank-parallel form of the tile kernel takes (a warp group of
+// kReduceWarps warps per rank, at most 1024 threads a block); above it the
+// rank loop runs.
+constexpr int kTileRpMaxP = 1024 / (32 * kReduceWarps) < ECHO_MAX_RANKS
+                                ? 1024 / (32 * kReduceWarps) : ECHO_MAX_RANKS;
 // Elements per tile of the persistent kernel: one 512-element unit per warp.
 constexpr int kCallTileElems = 4096;
 // Threads per block of the push, gather and persistent kernels (the reduce
@@ -103,7 +108,10 @@ template <int G> cudaError_t prepare_reduce_g();
 template <int G>
 cudaError_t launch_call_g(const CallArgs& a, const CallSched& sch, int bits, bool fused,
                           cudaStream_t s);
-template <int G> cudaError_t launch_tile_g(const CallArgs& a, int bits, cudaStream_t s, bool pdl);
+template <int G>
+cudaError_t launch_tile_g(const CallArgs& a, int bits, bool rank_parallel, cudaStream_t s, bool pdl);
+// One-time per-device set-up of the rank-parallel tile kernels' attributes.
+template <int G> cudaError_t prepare_tile_g();
 
 // Dispatch on the group size g (defined in echo_api.cu, which sees only the
 // declarations above, so each kernel source instantiates its own g alone).
@@ -112,8 +120,9 @@ cudaError_t launch_reduce(const CallArgs& a, int g, int bits, bool fused, cudaSt
 cudaError_t launch_gather(const CallArgs& a, int g, int bits, cudaStream_t s, bool pdl);
 cudaError_t launch_call(const CallArgs& a, const CallSched& sch, int g, int bits, bool fused,
                         cudaStream_t s);
-cudaError_t launch_tile(const CallArgs& a, int g, int bits, cudaStream_t s, bool pdl);
-// Attributes of every reduce kernel, all group sizes.
+cudaError_t launch_tile(const CallArgs& a, int g, int bits, bool rank_parallel, cudaStream_t s,
+                        bool pdl);
+// Attributes of every reduce and rank-parallel tile kernel, all group sizes.
 cudaError_t prepare_kernels();
 // Records `e` as the error echo_strerror(ECHO_ERR_CUDA) reports in this thread
 // and returns ECHO_ERR_CUDA.

@@ -31,6 +31,10 @@ ECHO_MAX_RANKS = 16
 ECHO_QUANT_ZERO_AWARE = 0
 ECHO_QUANT_NAIVE_ZERO_POINT = 1
 ECHO_QUANT_SYMMETRIC = 2
+ECHO_TILE_OFF = 0
+ECHO_TILE_AUTO = 1
+ECHO_TILE_RANK_LOOP = 2
+ECHO_TILE_RANK_PARALLEL = 3
 ECHO_STATE_F32 = 0
 ECHO_STATE_BF16 = 1
 ECHO_STATE_F16 = 2
@@ -259,8 +263,9 @@ def echo_set_state(plan: Plan, fmt: int = ECHO_STATE_F32, decay: float = 1.0) ->
     plan.state_fmt = fmt
 
 
-def echo_set_tile_fused(plan: Plan, on: bool) -> None:
-    _check(_lib.echo_set_tile_fused(plan, 1 if on else 0), "echo_set_tile_fused")
+def echo_set_tile_fused(plan: Plan, on: int) -> None:
+    """on: ECHO_TILE_OFF/AUTO/RANK_LOOP/RANK_PARALLEL; False and True mean OFF and AUTO."""
+    _check(_lib.echo_set_tile_fused(plan, int(on)), "echo_set_tile_fused")
 
 
 def echo_set_persistent(plan: Plan, on: bool) -> None:

@@ -234,9 +234,10 @@ int echo_allreduce_noalloc(int P, int64_t n, int bits, const void* const* in,
                            void* const* out, void* comp_state, void* stream);
 
 /*
- * echo_set_tile_fused -- 1 (the default): run each echo_allreduce of the plan
- * as one kernel in which a block computes a whole owner tile; 0: as two
- * kernels, the push, then the reduce (which also writes the outputs).  The
+ * echo_set_tile_fused -- ECHO_TILE_AUTO (1, the default): run each
+ * echo_allreduce of the plan as one kernel in which a block computes a whole
+ * owner tile; ECHO_TILE_OFF (0): as two kernels, the push, then the reduce
+ * (which also writes the outputs).  The
  * push of the P-1 senders, the owner's sum and the gather of a tile of a
  * segment (Fig. 2(a)) read and write only that tile's element positions of
  * the P ranks, so with every rank in one GPU's memory one block can take all
@@ -250,9 +251,21 @@ int echo_allreduce_noalloc(int P, int64_t n, int bits, const void* const* in,
  * and receive slots are bit-identical to the other schedules.  It applies
  * while the gather is fused (echo_set_fused 1, the default) and the call is
  * not persistent (echo_set_persistent 0, the default): a separate gather
- * kernel or the persistent kernel take precedence.  ECHO_ERR_ARG for on not
- * 0 or 1.
+ * kernel or the persistent kernel take precedence.
+ * The kernel has two forms with the same results.  In the rank loop a small
+ * block walks the ranks one after another, many blocks per SM; in the
+ * rank-parallel form a block has a warp pair per rank, which push their
+ * ranks at the same time, and the sum and gather follow, so a block's path is
+ * one push long instead of P.  ECHO_TILE_AUTO takes the rank-parallel form
+ * when the call's blocks (one per 1024 elements of a rank) are at most four
+ * times the device's SMs and P >= 3, the rank loop otherwise; ECHO_TILE_RANK_LOOP (2)
+ * and ECHO_TILE_RANK_PARALLEL (3) force one form (the rank-parallel form for
+ * P up to 16).  ECHO_ERR_ARG for other values of on.
  */
+#define ECHO_TILE_OFF           0
+#define ECHO_TILE_AUTO          1
+#define ECHO_TILE_RANK_LOOP     2
+#define ECHO_TILE_RANK_PARALLEL 3
 int echo_set_tile_fused(echo_plan_t plan, int on);
 
 /*

@@ -42,7 +42,7 @@ def _sample(Gs):
     return np.array(sorted(groups), np.int64)
 
 
-@pytest.mark.parametrize("schedule", ["fused", "unfused", "persistent", "tile"])
+@pytest.mark.parametrize("schedule", ["fused", "unfused", "persistent", "tile", "tile_rp"])
 def test_rank_longer_than_2_31_elements(big_inputs, schedule):
     from bit_error_compensated_gb300 import echo
     x = big_inputs
@@ -54,7 +54,7 @@ def test_rank_longer_than_2_31_elements(big_inputs, schedule):
     plan = echo.echo_plan(P, N, G, 4)
     echo.echo_set_fused(plan, schedule != "unfused")
     echo.echo_set_persistent(plan, schedule == "persistent")
-    echo.echo_set_tile_fused(plan, schedule == "tile")
+    echo.echo_set_tile_fused(plan, {"tile": 2, "tile_rp": 3}.get(schedule, 0))
     lay = echo.echo_wire_layout(plan)
     out = torch.empty_like(x)
     for k in range(2):

@@ -34,13 +34,15 @@ def _inputs(P, n, seed, scale=1.0):
     return (x * spread).to(torch.bfloat16)
 
 
-SCHEDULES = ["fused", "unfused", "persistent", "tile"]
+SCHEDULES = ["fused", "unfused", "persistent", "tile", "tile_rp"]
+# the tile schedule's forms, forced (the default, ECHO_TILE_AUTO, picks one by size)
+TILE_FORMS = {"tile": 2, "tile_rp": 3}
 
 
 def _set_schedule(echo, plan, schedule):
     echo.echo_set_fused(plan, schedule != "unfused")
     echo.echo_set_persistent(plan, schedule == "persistent")
-    echo.echo_set_tile_fused(plan, schedule == "tile")
+    echo.echo_set_tile_fused(plan, TILE_FORMS.get(schedule, 0))
 
 
 def _run_sequence(echo, P, Gs, bits_, mode, fused, calls=3, seed=0, inplace=False, quant=0,
@@ -193,41 +195,54 @@ def test_persistent_tile_boundaries(echo, Gs):
     _run_sequence(echo, 3, Gs, 4, "caller", 0, calls=2, seed=Gs, persistent=True)
 
 
+@pytest.mark.parametrize("form", [2, 3], ids=["rank_loop", "rank_parallel"])
 @pytest.mark.parametrize("mode", ["none", "default", "caller"])
 @pytest.mark.parametrize("bits_", [4, 8])
 @pytest.mark.parametrize("P", [1, 2, 3, 4, 8, 16])
-def test_tile_fused_matches_oracle(echo, P, bits_, mode):
-    """The whole call as one kernel, a block per owner tile (echo_set_tile_fused)."""
-    _run_sequence(echo, P, 37, bits_, mode, 1, seed=2200 + P * 10 + bits_, tile=True)
+def test_tile_fused_matches_oracle(echo, P, bits_, mode, form):
+    """The whole call as one kernel, a block per owner tile (echo_set_tile_fused),
+    in each of its two forms."""
+    _run_sequence(echo, P, 37, bits_, mode, 1, seed=2200 + P * 10 + bits_, tile=form)
 
 
 @pytest.mark.parametrize("opts", [dict(g=64), dict(g=256), dict(quant=1), dict(quant=2),
                                   dict(fmt=1, decay=0.5), dict(fmt=2), dict(g=64, quant=2),
                                   dict(g=256, fmt=1), dict(inplace=True), dict(decay=0.75)])
-def test_tile_fused_with_options(echo, opts):
+@pytest.mark.parametrize("form", [2, 3], ids=["rank_loop", "rank_parallel"])
+def test_tile_fused_with_options(echo, opts, form):
     opts = dict(opts)
     g = opts.pop("g", G)
     _run_sequence(echo, 4, {64: 75, 128: 37, 256: 37}[g], 4, "caller", 1, seed=2300, g=g,
-                  tile=True, **opts)
+                  tile=form, **opts)
 
 
 @pytest.mark.parametrize("P,Gs", [(3, 1), (3, 7), (3, 8), (3, 9), (5, 15), (5, 16), (5, 17),
                                   (2, 300)])
-def test_tile_fused_tile_boundaries(echo, P, Gs):
+@pytest.mark.parametrize("form", [2, 3], ids=["rank_loop", "rank_parallel"])
+def test_tile_fused_tile_boundaries(echo, P, Gs, form):
     """Segments of a few groups up to several tiles, with short last tiles."""
-    _run_sequence(echo, P, Gs, 4, "caller", 1, calls=2, seed=Gs, tile=True)
+    _run_sequence(echo, P, Gs, 4, "caller", 1, calls=2, seed=Gs, tile=form)
+
+
+@pytest.mark.parametrize("P,Gs", [(8, 8), (8, 608), (8, 609), (4, 1216), (4, 1217), (2, 9)])
+def test_tile_fused_automatic_form(echo, P, Gs):
+    """The default picks the rank-parallel form for grids of at most four times
+    the SMs and P >= 3, the rank loop otherwise; both sides of that bound (608
+    blocks of 8 groups on a 152-SM GB300) match the oracle."""
+    _run_sequence(echo, P, Gs, 4, "default", 1, calls=2, seed=Gs + P, tile=1)
 
 
 def test_every_schedule_gives_the_same_bits(echo):
     """Outputs, state and every wire byte of a call sequence agree between the
-    four schedules: one kernel a block per owner tile (the default), push and
-    reduce, push, reduce and gather, and the persistent kernel."""
+    schedules: one kernel a block per owner tile (the default, and each of its
+    two forms forced), push and reduce, push, reduce and gather, and the
+    persistent kernel."""
     P, Gs = 4, 70
     n = P * G * Gs
     res = []
-    for schedule in ("tile", "fused", "unfused", "persistent"):
+    for schedule in ("default", "tile", "tile_rp", "fused", "unfused", "persistent"):
         plan = echo.echo_plan(P, n, G, 4)
-        if schedule != "tile":                 # the default needs no call
+        if schedule != "default":              # the default needs no call
             _set_schedule(echo, plan, schedule)
         comp = torch.zeros((P, n), device="cuda")
         outs = []
@@ -529,6 +544,7 @@ def test_argument_errors(echo):
     assert echo.echo_comp_bytes(plan) == plan.P * plan.n * 4       # unchanged
     for bad in (2, -1):                                 # the C call takes 0 or 1 only
         assert echo._lib.echo_set_persistent(plan, bad) == echo.ECHO_ERR_ARG
+    for bad in (4, -1):                                 # ECHO_TILE_OFF .. RANK_PARALLEL
         assert echo._lib.echo_set_tile_fused(plan, bad) == echo.ECHO_ERR_ARG
     with pytest.raises(echo.EchoError) as ei:
         echo.echo_debug_hold_push(plan, -2)

@@ -79,7 +79,10 @@ def _full_sequence(echo, number, bits_, wire_every=1):
 
 
 def _sampled_sequence(echo, number, bits_, sample, calls=None, wire_calls=(0,), quant=0,
-                      fmt=0, decay=1.0, g=G, persistent=False, fused=False, tile=False):
+                      fmt=0, decay=1.0, g=G, persistent=False, fused=True, tile=1):
+    """The workload's calls compared with the oracle on sampled group positions.
+    The schedule defaults to the library's (tile kernel, form chosen by size);
+    tile=0 with fused True/False gives the two- and three-kernel schedules."""
     w = WORKLOADS[number]
     P, n = w.P, w.n
     plan = echo.echo_plan(P, n, g, bits_)
@@ -134,8 +137,15 @@ def test_p4_2048x4096_full(echo):
 
 @pytest.mark.parametrize("bits_", [4, 8])
 def test_p8_1gib_sampled(echo, bits_):
+    """The default schedule, as the bench times it, on 1/64 of the positions."""
     w = WORKLOADS[3]
-    _sampled_sequence(echo, 3, bits_, sample=w.n // G // 64)          # 1/64 of the positions
+    _sampled_sequence(echo, 3, bits_, sample=w.n // G // 64)
+
+
+@pytest.mark.parametrize("fused", [True, False], ids=["two_kernels", "three_kernels"])
+def test_p8_1gib_kernel_schedules_sampled(echo, fused):
+    """Push and reduce (fused gather), or push, reduce and gather, at 1 GiB per rank."""
+    _sampled_sequence(echo, 3, 4, sample=2048, calls=1, tile=0, fused=fused)
 
 
 def test_p4_8192x4096_full(echo):
@@ -188,16 +198,24 @@ def test_p4_32768x1024_persistent_sampled(echo):
     _sampled_sequence(echo, 5, 4, sample=256, calls=24, persistent=True)
 
 
-def test_p8_1gib_tile_fused_sampled(echo):
-    """The tile-fused kernel at 1 GiB per rank, 4- and 8-bit codes."""
-    _sampled_sequence(echo, 3, 4, sample=2048, calls=1, tile=True)
-    _sampled_sequence(echo, 3, 8, sample=2048, calls=1, tile=True)
+def test_p8_1gib_tile_rank_parallel_sampled(echo):
+    """The tile kernel's rank-parallel form (which the default takes only for
+    small grids) at 1 GiB per rank, 4- and 8-bit codes."""
+    _sampled_sequence(echo, 3, 4, sample=2048, calls=1, tile=3)
+    _sampled_sequence(echo, 3, 8, sample=2048, calls=1, tile=3)
 
 
-def test_p4_32768x1024_tile_fused_sampled(echo):
-    """Two states (forward and backward sites) through the tile-fused kernel."""
-    _sampled_sequence(echo, 5, 4, sample=1024, calls=224, tile=True, fused=True)
+def test_p4_32768x1024_tile_rank_parallel_sampled(echo):
+    """Two states (forward and backward sites) through the rank-parallel form."""
+    _sampled_sequence(echo, 5, 4, sample=1024, calls=224, tile=3)
 
 
-def test_p4_2048x4096_tile_fused_sampled(echo):
-    _sampled_sequence(echo, 2, 4, sample=512, calls=16, tile=True, fused=True)
+@pytest.mark.parametrize("form", [2, 3], ids=["rank_loop", "rank_parallel"])
+def test_p4_2048x4096_tile_forms_sampled(echo, form):
+    _sampled_sequence(echo, 2, 4, sample=512, calls=16, tile=form)
+
+
+@pytest.mark.parametrize("fused", [True, False], ids=["two_kernels", "three_kernels"])
+def test_p4_2048x4096_kernel_schedules_sampled(echo, fused):
+    """The two- and three-kernel schedules over the first 16 calls, with bf16 state."""
+    _sampled_sequence(echo, 2, 4, sample=512, calls=16, tile=0, fused=fused, fmt=1)
