@@ -232,6 +232,48 @@ def test_tile_fused_automatic_form(echo, P, Gs):
     _run_sequence(echo, P, Gs, 4, "default", 1, calls=2, seed=Gs + P, tile=1)
 
 
+def _fuzz_cases(count, seed):
+    """Seeded random configurations of the call: ranks, segment length in
+    groups (short, one tile, several tiles with a ragged end), code width,
+    group size, quantizer, state format and decay, compensation mode, in-place
+    outputs, and the schedule (the tile kernel's two forms weighted up)."""
+    rng = np.random.default_rng(seed)
+    cases = []
+    for i in range(count):
+        P = int(rng.choice([1, 2, 3, 4, 5, 7, 8, 11, 16]))
+        g = int(rng.choice([64, 128, 256]))
+        per_tile = 1024 // g
+        Gs = int(rng.choice([1, per_tile - 1, per_tile, per_tile + 1, 3 * per_tile + 5,
+                             int(rng.integers(1, 6 * per_tile))]))
+        Gs = max(Gs, 1)
+        fmt = int(rng.integers(0, 3))
+        cases.append(dict(P=P, Gs=Gs, g=g, bits_=int(rng.choice([4, 8])),
+                          quant=int(rng.integers(0, 3)), fmt=fmt,
+                          decay=float(rng.choice([1.0, 1.0, 0.75])),
+                          mode=str(rng.choice(["none", "default", "caller", "caller"])),
+                          inplace=bool(rng.integers(0, 4) == 0),
+                          schedule=str(rng.choice(["tile", "tile_rp", "tile", "tile_rp",
+                                                   "fused", "unfused", "persistent",
+                                                   "default"])),
+                          seed=9000 + i))
+    return cases
+
+
+@pytest.mark.parametrize("case", _fuzz_cases(96, 20261203), ids=lambda c: (
+    f"P{c['P']}-Gs{c['Gs']}-g{c['g']}-b{c['bits_']}-q{c['quant']}-s{c['fmt']}-"
+    f"{c['mode']}-{c['schedule']}"))
+def test_random_configurations_match_oracle(echo, case):
+    """Random combinations of every option against the oracle, two calls each."""
+    c = dict(case)
+    schedule = c.pop("schedule")
+    mode = c.pop("mode")
+    P, Gs, bits_ = c.pop("P"), c.pop("Gs"), c.pop("bits_")
+    tile = {"tile": 2, "tile_rp": 3, "default": 1}.get(schedule, 0)
+    fused = 0 if schedule == "unfused" else 1
+    _run_sequence(echo, P, Gs, bits_, mode, fused, calls=2, tile=tile,
+                  persistent=schedule == "persistent", **c)
+
+
 def test_every_schedule_gives_the_same_bits(echo):
     """Outputs, state and every wire byte of a call sequence agree between the
     schedules: one kernel a block per owner tile (the default, and each of its
