@@ -237,9 +237,9 @@ int echo_allreduce_noalloc(int P, int64_t n, int bits, const void* const* in,
  * echo_set_tile_fused -- ECHO_TILE_AUTO (1, the default): run each
  * echo_allreduce of the plan as one kernel in which a block computes a whole
  * owner tile; ECHO_TILE_OFF (0): as two kernels, the push, then the reduce
- * (which also writes the outputs).  The
- * push of the P-1 senders, the owner's sum and the gather of a tile of a
- * segment (Fig. 2(a)) read and write only that tile's element positions of
+ * (which also writes the outputs).  The push of the P-1 senders, the owner's
+ * sum and the gather of a tile of a segment (Fig. 2(a)) read and write only
+ * that tile's element positions of
  * the P ranks, so with every rank in one GPU's memory one block can take all
  * of them, with no block waiting on another and no kernel boundary between
  * the push and the reduce.  The block walks the ranks in ascending order:
@@ -258,9 +258,9 @@ int echo_allreduce_noalloc(int P, int64_t n, int bits, const void* const* in,
  * ranks at the same time, and the sum and gather follow, so a block's path is
  * one push long instead of P.  ECHO_TILE_AUTO takes the rank-parallel form
  * when the call's blocks (one per 1024 elements of a rank) are at most four
- * times the device's SMs and P >= 3, the rank loop otherwise; ECHO_TILE_RANK_LOOP (2)
- * and ECHO_TILE_RANK_PARALLEL (3) force one form (the rank-parallel form for
- * P up to 16).  ECHO_ERR_ARG for other values of on.
+ * times the device's SMs and P >= 3, the rank loop otherwise;
+ * ECHO_TILE_RANK_LOOP (2) and ECHO_TILE_RANK_PARALLEL (3) force one form (the
+ * rank-parallel form for P up to 16).  ECHO_ERR_ARG for other values of on.
  */
 #define ECHO_TILE_OFF           0
 #define ECHO_TILE_AUTO          1
