@@ -361,7 +361,8 @@ def workload_config(args, world, seq):
     distinct = calls
     return {"workload": name, "description": WORKLOADS[args.workload].description,
             "P": P, "n_per_rank": n, "bits": args.bits, "g": args.g,
-            "calls_per_step": calls, "compensated": comp == calls,
+            "calls_per_step": calls * max(1, getattr(args, "repeat", 1)),
+            "compensated": comp == calls,
             "fused_gather": bool(args.fused), "quantizer": QUANTIZERS[args.quantizer],
             "schedule": ("one kernel, a block per owner tile" + TILE_FORM_NOTE[tile_form(args)]
                          if args.tile else
@@ -409,9 +410,12 @@ def run_ours(args, rank, local, world):
     # each call's buffers are checked and marshalled once, outside the timed loop
     prepared = [echo.prepare_allreduce(plan, ins, out_rows, comp) for ins, comp in call_args]
 
+    reps = max(1, getattr(args, "repeat", 1))
+
     def step():
-        for call in prepared:
-            call(stream)
+        for _ in range(reps):
+            for call in prepared:
+                call(stream)
 
     launches_per_call = (1 if args.persistent or args.tile
                          else (2 if fused else 3) - (1 if P == 1 else 0))
@@ -427,8 +431,9 @@ def run_ours(args, rank, local, world):
         gstream = torch.cuda.Stream(dev)
         gstream.wait_stream(stream)
         with torch.cuda.graph(graph, stream=gstream):
-            for call in prepared:
-                call(gstream)
+            for _ in range(reps):
+                for call in prepared:
+                    call(gstream)
         torch.cuda.synchronize(dev)
         step = graph.replay
         for _ in range(args.warmup):
@@ -456,8 +461,8 @@ def run_ours(args, rank, local, world):
         raise RuntimeError("device status word set during the timed steps")
 
     bytes_in_per_call = P * n * 2
-    value = whole_job_gbs(bytes_in_per_call * calls, args.steps, world, max_ms)
-    per_call_s = max_ms / 1e3 / (args.steps * calls)
+    value = whole_job_gbs(bytes_in_per_call * calls * reps, args.steps, world, max_ms)
+    per_call_s = max_ms / 1e3 / (args.steps * calls * reps)
     compensated_calls = sum(1 for c in seq if c.state != "none")
     model = (compensated_calls * call_model_bytes(P, n, bits, True, fused, sb, g) +
              (calls - compensated_calls) * call_model_bytes(P, n, bits, False, fused, g=g)) / calls
@@ -502,7 +507,7 @@ def run_ours(args, rank, local, world):
         "per_kernel_us": {k: round(v, 2) for k, v in avg_us.items()},
         "per_kernel_frac": per_kernel_frac,
         "roofline": roofline,
-        "gpu_launches": launches_per_call * calls * args.steps,
+        "gpu_launches": launches_per_call * calls * reps * args.steps,
         "clocks": clk,
     }
 
@@ -723,14 +728,18 @@ def time_other(echo, number, bits, fused, dev, args, tile=None):
            "per_kernel_us": {k: round(v, 2) for k, v in k_us.items()},
            "per_kernel_frac": k_frac}
     if launch_bound:
-        res["note"] = "launch-bound (a few KiB per call): the time per call is the figure"
+        res["note"] = ("launch-bound (a few KiB per call): the time per call is the figure; "
+                       "us_per_call issues each call from Python, us_per_call_cuda_graph replays "
+                       "a graph of the sequence repeated to about 200 calls (the GPU's own time)")
         graph = torch.cuda.CUDAGraph()
         gstream = torch.cuda.Stream(dev)
         gstream.wait_stream(stream)
+        seqs = max(1, 200 // len(seq))
         with torch.cuda.graph(graph, stream=gstream):
-            step(gstream)
+            for _ in range(seqs):
+                step(gstream)
         torch.cuda.synchronize(dev)
-        res["us_per_call_cuda_graph"] = round(timed(graph.replay) * 1e6, 2)
+        res["us_per_call_cuda_graph"] = round(timed(graph.replay) * 1e6 / seqs, 2)
         del graph
     del prepared, plan, xs, bwd
     torch.cuda.empty_cache()
@@ -1014,6 +1023,10 @@ def main(argv=None):
     ap.add_argument("--also", default="3b8,2,4,5,1",
                     help="other workloads to time, comma-separated, NbB for workload N with B-bit "
                          "codes ('' for none)")
+    ap.add_argument("--repeat", type=int, default=1,
+                    help="latency runs: each timed step issues the call sequence this many times "
+                         "(with --graph, one graph holds them all), so that host-side launch "
+                         "costs are spread over many calls")
     ap.add_argument("--calls", type=int, default=0,
                     help="time only the first N calls of the sequence (profiling runs)")
     ap.add_argument("--accuracy", action="store_true",

@@ -136,14 +136,13 @@ cudaError_t prepare_kernels() {
 namespace {
 // The tile schedule's form for a call of the plan: rank-parallel blocks when
 // the grid (one block per owner tile) is too small to keep the SMs busy with
-// the rank loop's small blocks, whose per-block path is P pushes long, and
-// P >= 3 (with two ranks both forms take the same time).
+// the rank loop's small blocks, whose per-block path is P pushes long.
 #ifndef ECHO_TILE_RP_TILES_PER_SM
 #define ECHO_TILE_RP_TILES_PER_SM 4
 #endif
 bool tile_rank_parallel(const echo_plan_s* plan) {
   if (plan->tile == ECHO_TILE_RANK_PARALLEL) return true;
-  if (plan->tile != ECHO_TILE_AUTO || plan->P < 3) return false;   // P = 2: the loop is as fast
+  if (plan->tile != ECHO_TILE_AUTO || plan->P < 2) return false;
   const int64_t T = echo::kReduceTileElems / plan->g;
   const int64_t blocks = (plan->Gs + T - 1) / T * plan->P;
   return blocks <= (int64_t)ECHO_TILE_RP_TILES_PER_SM * plan->sms;

@@ -258,7 +258,7 @@ int echo_allreduce_noalloc(int P, int64_t n, int bits, const void* const* in,
  * ranks at the same time, and the sum and gather follow, so a block's path is
  * one push long instead of P.  ECHO_TILE_AUTO takes the rank-parallel form
  * when the call's blocks (one per 1024 elements of a rank) are at most four
- * times the device's SMs and P >= 3, the rank loop otherwise;
+ * times the device's SMs and P >= 2, the rank loop otherwise;
  * ECHO_TILE_RANK_LOOP (2) and ECHO_TILE_RANK_PARALLEL (3) force one form (the
  * rank-parallel form for P up to 16).  ECHO_ERR_ARG for other values of on.
  */

@@ -227,7 +227,7 @@ def test_tile_fused_tile_boundaries(echo, P, Gs, form):
 @pytest.mark.parametrize("P,Gs", [(8, 8), (8, 608), (8, 609), (4, 1216), (4, 1217), (2, 9)])
 def test_tile_fused_automatic_form(echo, P, Gs):
     """The default picks the rank-parallel form for grids of at most four times
-    the SMs and P >= 3, the rank loop otherwise; both sides of that bound (608
+    the SMs and P >= 2, the rank loop otherwise; both sides of that bound (608
     blocks of 8 groups on a 152-SM GB300) match the oracle."""
     _run_sequence(echo, P, Gs, 4, "default", 1, calls=2, seed=Gs + P, tile=1)
 
