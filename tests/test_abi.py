@@ -2,6 +2,8 @@
 declares; host-side argument checks that need no GPU."""
 import ctypes
 import re
+import shutil
+import subprocess
 from pathlib import Path
 
 import pytest
@@ -194,3 +196,41 @@ def test_prepared_call_checks_once_and_passes_the_same_arguments(lib, monkeypatc
     with pytest.raises(ValueError, match="destroyed"):
         call(stream=7)
     assert len(seen) == 2
+
+
+C_CALLER = r"""
+#include <stdio.h>
+#include "echo.h"
+int main(void) {
+  echo_plan_t plan = 0;
+  /* rejected before any device work, so this runs without a GPU */
+  int rc = echo_plan(0, 0, 128, 4, &plan);
+  if (rc != ECHO_ERR_ARG || plan != 0) return 1;
+  rc = echo_plan(4, 4 * 128 + 1, 128, 4, &plan);
+  if (rc != ECHO_ERR_SHAPE) return 2;
+  if (echo_set_tile_fused(0, ECHO_TILE_AUTO) != ECHO_ERR_ARG) return 3;
+  printf("%s\n", echo_strerror(ECHO_ERR_ARG));
+  return 0;
+}
+"""
+
+
+def test_header_compiles_as_c_and_a_c_program_links(tmp_path):
+    """include/echo.h is a plain C interface: a C11 program including it builds
+    with every warning as an error, links against libecho.so and calls it."""
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    from bit_error_compensated_gb300.build import build_library
+    lib = build_library()
+    src = tmp_path / "caller.c"
+    src.write_text(C_CALLER)
+    exe = tmp_path / "caller"
+    subprocess.run([cc, "-std=c11", "-Wall", "-Wextra", "-pedantic", "-Werror",
+                    "-I", str(ROOT / "include"), str(src), "-o", str(exe),
+                    "-L", str(lib.parent), "-lecho", f"-Wl,-rpath,{lib.parent}"],
+                   check=True, capture_output=True)
+    out = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert out.returncode == 0, (out.returncode, out.stdout, out.stderr)
+    assert out.stdout.strip() == "invalid argument"
+
