@@ -19,8 +19,8 @@
 // words are zero again for the next call.
 //
 // A block is kThreads/32 compute warps and one control warp, which share a
-// ring of two shared-memory stages, each with a "full" and an "empty"
-// mbarrier.  The control warp's lane 0 does all the scheduling: it claims
+// ring of shared-memory stages (sch.stages of them, two or three, chosen at
+// launch), each with a "full" and an "empty" mbarrier.  The control warp's lane 0 does all the scheduling: it claims
 // tickets from one atomic counter (the next one fetched ahead), waits for an
 // item's inputs, fills a stage with the item's bulk copies (cp.async.bulk)
 // completing on its full barrier, and, once the compute warps have arrived on
@@ -150,6 +150,8 @@ constexpr int kCallBlockThreads = kThreads + 32;
 #define ECHO_CALL_MIN_BLOCKS 3
 #endif
 constexpr int64_t kSentinel = -1;              // no ticket held in a stage
+// Most stages a block's ring can have (the launcher picks 2 or 3).
+constexpr int kCallMaxStages = 4;
 
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(bar) : "memory");
@@ -197,11 +199,13 @@ call_kernel(const CallArgs a, const CallSched sch) {
   constexpr int GPW = 32 / NL;
   constexpr int EB = state_bytes<SF>();
   extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ __align__(8) uint64_t full[2];
-  __shared__ __align__(8) uint64_t empty[2];
-  __shared__ Item s_item[2];                     // the item in each stage (kEmptyItem: stop)
+  __shared__ __align__(8) uint64_t full[kCallMaxStages];
+  __shared__ __align__(8) uint64_t empty[kCallMaxStages];
+  __shared__ Item s_item[kCallMaxStages];        // the item in each stage (kEmptyItem: stop)
+  __shared__ int64_t s_held[kCallMaxStages];     // control: ticket issued into each stage
 
   const int P = a.P;
+  const int NS = sch.stages;
   const int64_t Gs = a.Gs;
   const uint32_t sbytes = reduce_stage_bytes<BITS, SF, G, kCallTileElems>(P);
   const uint32_t full0 = smem_addr(&full[0]);
@@ -213,9 +217,10 @@ call_kernel(const CallArgs a, const CallSched sch) {
   const int lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    for (int st = 0; st < 2; ++st) {
+    for (int st = 0; st < NS; ++st) {
       mbar_init(full0 + 8 * st, 1);
       mbar_init(empty0 + 8 * st, kCallWarps);
+      s_held[st] = kSentinel;
     }
     fence_barrier_init();
   }
@@ -294,27 +299,33 @@ call_kernel(const CallArgs a, const CallSched sch) {
       pend[npend++] = t;
       if (npend == kPublishBatch) flush();
     };
-    // Per stage (scalars, not arrays, so that nothing goes to local memory):
-    // the ticket issued into it and not yet published, and the parity of its
-    // next empty and next full phase.
-    int64_t held0 = kSentinel, held1 = kSentinel;
-    uint32_t ep0 = 0u, ep1 = 0u, fp0 = 0u, fp1 = 0u;
+    // Per stage: the ticket issued into it and not yet published (s_held,
+    // in shared memory), and the parity of its next empty and next full
+    // phase (bit st of ep and fp, in registers, so that nothing goes to
+    // local memory).
+    uint32_t ep = 0u, fp = 0u;
     // Waits until the compute warps are done with stage st, which is then
     // free; `done` receives the ticket they finished there (kSentinel if the
     // stage held none or the wait gave up), still to be published.  False if
     // the wait gave up.
     auto free_stage = [&](int st, int64_t& done) -> bool {
-      const int64_t h = st ? held1 : held0;
+      const int64_t h = s_held[st];
       done = kSentinel;
       if (h == kSentinel) return true;
-      if (!mbar_wait_or_abort(empty0 + 8 * st, st ? ep1 : ep0, abort)) return false;
+      if (!mbar_wait_or_abort(empty0 + 8 * st, (ep >> st) & 1u, abort)) return false;
       done = h;
-      if (st) {
-        ep1 ^= 1u;
-        held1 = kSentinel;
-      } else {
-        ep0 ^= 1u;
-        held0 = kSentinel;
+      ep ^= 1u << st;
+      s_held[st] = kSentinel;
+      return true;
+    };
+    // Frees the stages after st, oldest item first (st + 1, ..., st + NS - 1),
+    // publishing what they held.  False if a wait gave up.
+    auto drain_others = [&](int st) -> bool {
+      for (int k = 1; k < NS; ++k) {
+        const int s2 = st + k < NS ? st + k : st + k - NS;
+        int64_t d2;
+        if (!free_stage(s2, d2)) return false;
+        if (d2 != kSentinel) publish(d2);
       }
       return true;
     };
@@ -338,10 +349,9 @@ call_kernel(const CallArgs a, const CallSched sch) {
     };
 
     bool ok = true;
-    int64_t i = 0;                               // items issued so far
+    int st = 0;                                  // the stage of the next item issued
     int64_t done = kSentinel;                    // finished, not yet published
     for (;;) {
-      const int st = (int)(i & 1);
       if (!(ok = free_stage(st, done))) break;
       Item it;
       const int64_t t = take(it);
@@ -351,9 +361,8 @@ call_kernel(const CallArgs a, const CallSched sch) {
         // Not final yet: publish everything this block holds before waiting,
         // so that no block waits while holding an item it has not published.
         if (done != kSentinel) publish(done);
-        if (!(ok = free_stage(st ^ 1, done))) break;
-        if (done != kSentinel) publish(done);
         done = kSentinel;
+        if (!(ok = drain_others(st))) break;
         flush();
         r = inputs_ready(it, true);
       }
@@ -367,36 +376,25 @@ call_kernel(const CallArgs a, const CallSched sch) {
       if (done != kSentinel) publish(done);
       done = kSentinel;
       issue(it, st);
-      if (st) {
-        fp1 ^= 1u;
-        held1 = t;
-      } else {
-        fp0 ^= 1u;
-        held0 = t;
-      }
-      ++i;
+      fp ^= 1u << st;
+      s_held[st] = t;
+      st = st + 1 < NS ? st + 1 : 0;
     }
     if (done != kSentinel) publish(done);        // freed at the top of the last pass
-    if (ok) {
-      ok = free_stage((int)((i + 1) & 1), done);   // the last item issued
-      if (ok && done != kSentinel) publish(done);
-    }
+    if (ok) ok = drain_others(st);               // the last items issued
     flush();
     if (ok) {
       // Stop the compute warps: a sentinel in the stage they wait on next
       // (free: its item was freed at the top of the loop's last pass).
-      const int st = (int)(i & 1);
       s_item[st].kind = kEmptyItem;
       mbar_arrive(full0 + 8 * st);
-      if (st) fp1 ^= 1u;
-      else fp0 ^= 1u;
+      fp ^= 1u << st;
     } else {
       atomicOr(a.status, kStatusTimeout);
       atomicExch(abort, 1u);
     }
     // Copies still in flight land before the block can exit (bounded).
-    mbar_wait_bounded(full0, fp0 ^ 1u);
-    mbar_wait_bounded(full0 + 8, fp1 ^ 1u);
+    for (int s2 = 0; s2 < NS; ++s2) mbar_wait_bounded(full0 + 8 * s2, ((fp >> s2) & 1u) ^ 1u);
     // The last block to stop claiming resets the ticket counter for the next call.
     __threadfence();
     if (atomicAdd(finished, 1u) == gridDim.x - 1) {
@@ -409,9 +407,9 @@ call_kernel(const CallArgs a, const CallSched sch) {
   // -------------------------------------------------------------- compute ----
   const uint64_t codes_pol = kCodesPolicyLast ? policy_evict_last() : policy_evict_normal();
   const int64_t runs_total = (Gs * G + kRun - 1) / kRun;
-  for (int64_t i = 0;; ++i) {
-    const int st = (int)(i & 1);
-    const uint32_t par = (uint32_t)((i >> 1) & 1);
+  int st = 0;                                    // the next item's stage and its phase parity
+  uint32_t par = 0u;
+  for (;;) {
     const bool got = __all_sync(kFull, mbar_wait_or_abort(full0 + 8 * st, par, abort)) != 0;
     if (!got) {
       if (lane == 0) {
@@ -456,37 +454,77 @@ call_kernel(const CallArgs a, const CallSched sch) {
     fence_proxy_async();                         // this lane's stage reads before a refill
     __syncwarp();
     if (lane == 0) mbar_arrive(empty0 + 8 * st);
+    if (++st == NS) {
+      st = 0;
+      par ^= 1u;
+    }
   }
 }
 
+// Stages of a block's ring: 0 lets the launcher choose (three when that
+// leaves as many resident blocks per SM as two, else two); 2 to 4 asks for
+// that many, or as many as fit.  A third stage bought with a resident block
+// measured slower (P = 4, fp32 state: 776 against 850 GB/s on 2048 x 4096
+// per rank, 882 against 958 on 8192 x 4096): more blocks, each with its own
+// scheduling thread, keep more items moving than a deeper ring per block.
+// At no cost in blocks (P = 4 with bf16 state, three blocks either way) it
+// gained 2% (1017 against 996 GB/s).
+#ifndef ECHO_CALL_STAGES
+#define ECHO_CALL_STAGES 0
+#endif
+static_assert(ECHO_CALL_STAGES == 0 || (ECHO_CALL_STAGES >= 2 && ECHO_CALL_STAGES <= kCallMaxStages),
+              "persistent kernel: 0 (chosen at launch) or 2..kCallMaxStages stages");
+
 template <int BITS, int SF, int MODE, int G, bool FUSED>
 cudaError_t launch_t(const CallArgs& a, const CallSched& sch, cudaStream_t s) {
-  static CachedInt resident_cache[64][ECHO_MAX_RANKS + 1];
+  // Per device and P: resident blocks x 8 + stages.
+  static CachedInt layout_cache[64][ECHO_MAX_RANKS + 1];
   int dev = 0;
   cudaGetDevice(&dev);
-  const size_t smem = 2 * (size_t)reduce_stage_bytes<BITS, SF, G, kCallTileElems>(a.P);
-  CachedInt& cached = resident_cache[dev & 63][a.P];
-  int resident = cached.get();
-  if (resident == 0) {
-    int sms = 0, per_sm = 0;
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const int smem_max = (int)(2 * reduce_stage_bytes<BITS, SF, G, kCallTileElems>(ECHO_MAX_RANKS));
-    cudaError_t e = cudaFuncSetAttribute(call_kernel<BITS, SF, MODE, G, FUSED>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max);
+  const size_t stage_bytes = reduce_stage_bytes<BITS, SF, G, kCallTileElems>(a.P);
+  CachedInt& cached = layout_cache[dev & 63][a.P];
+  int layout = cached.get();
+  if (layout == 0) {
+    auto kernel = call_kernel<BITS, SF, MODE, G, FUSED>;
+    int sms = 0, optin = 0;
+    cudaError_t e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    cudaFuncAttributes fa;
+    if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, kernel);
     if (e != cudaSuccess) return e;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, call_kernel<BITS, SF, MODE, G, FUSED>,
-                                                      kCallBlockThreads, smem);
+    const int dyn_max = optin - (int)fa.sharedSizeBytes;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn_max);
     if (e != cudaSuccess) return e;
+    // Resident blocks per SM with ns stages (0 when a block does not fit).
+    auto per_sm_with = [&](int ns, int& blocks) -> cudaError_t {
+      blocks = 0;
+      if ((size_t)ns * stage_bytes > (size_t)dyn_max) return cudaSuccess;
+      return cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, kernel, kCallBlockThreads,
+                                                           (size_t)ns * stage_bytes);
+    };
+    int ns = 2, per_sm = 0;
+    if ((e = per_sm_with(2, per_sm)) != cudaSuccess) return e;
     if (per_sm < 1) return cudaErrorInvalidConfiguration;
-    resident = sms * per_sm;
-    cached.set(resident);
+    for (int want = 3; want <= (ECHO_CALL_STAGES ? ECHO_CALL_STAGES : 3); ++want) {
+      int p2 = 0;
+      if ((e = per_sm_with(want, p2)) != cudaSuccess) return e;
+      if (p2 >= (ECHO_CALL_STAGES ? 1 : per_sm)) {
+        ns = want;
+        per_sm = p2;
+      }
+    }
+    layout = sms * per_sm * 8 + ns;
+    cached.set(layout);
   }
+  const int resident = layout / 8;
+  const size_t smem = (size_t)(layout % 8) * stage_bytes;
   // Rounds of P(P-1) pushes, P reduces and (unfused) P gathers; the lag is
-  // about kCallLagWaves waves of items in flight (two per block).
+  // about kCallLagWaves waves of items in flight (one per stage of a block).
   CallSched sc = sch;
   const int P = a.P;
+  sc.stages = layout % 8;
   sc.round = (int64_t)P * (P - 1) + P + (FUSED ? 0 : P);
-  int64_t lag = (kCallLagWaves * 2 * (int64_t)resident + sc.round - 1) / sc.round;
+  int64_t lag = (kCallLagWaves * sc.stages * (int64_t)resident + sc.round - 1) / sc.round;
   if (P == 1) lag = 0;                           // nothing to wait for
   sc.lag = lag < sc.tiles ? lag : sc.tiles;
   sc.total = sc.round * (sc.tiles + (FUSED ? 1 : 2) * sc.lag);

@@ -6,10 +6,10 @@ every owner, the reduce of tile r - D of every owner and (unfused) the gather
 of tile r - 2D; slots whose tile is out of range are empty and skipped.
 Blocks take tickets from one counter, the next one fetched ahead.  A reduce
 item needs its tile's P - 1 pushes, a gather item its tile's reduce.  A block
-computes one item while it holds the next: if the next item's inputs are
-ready it starts it at once, otherwise it first signals the current item and
-only then waits.  Blocks advance in random interleavings; a state where no
-block can move is a deadlock.  The same model with the wait placed before the
+holds as many items as its ring has stages (two or three): if the next item's
+inputs are ready it issues it at once, otherwise it first signals every item
+it holds and only then waits.  Blocks advance in random interleavings; a state
+where no block can move is a deadlock.  The same model with the wait placed before the
 signal (the order to avoid) deadlocks, as a control.
 """
 import random
@@ -36,8 +36,11 @@ def _items(P, tiles, fused, D):
     return out
 
 
-def _run(P, tiles, fused, D, nblocks, seed, wait_before_signal=False):
-    """True when every item completes, False on a deadlock."""
+def _run(P, tiles, fused, D, nblocks, seed, stages=2, wait_before_signal=False):
+    """True when every item completes, False on a deadlock.  A block holds up
+    to `stages` items issued into its ring and not yet signalled; to issue one
+    more into a full ring it first lets the oldest finish (signalled at the
+    latest just before the block issues or waits)."""
     rng = random.Random(seed)
     items = _items(P, tiles, fused, D)
     total = len(items)
@@ -77,44 +80,52 @@ def _run(P, tiles, fused, D, nblocks, seed, wait_before_signal=False):
             t = fetch()
         return (None, total) if t >= total else (t, fetch())
 
-    # states: start | first t pre | run cur pre | next-pending t pre | stuck cur t pre | end
-    blocks = [("start",)] * nblocks
-    while any(b[0] != "end" for b in blocks):
+    # A block: its state ("start", "run": may take its next ticket, "pending":
+    # waits for the inputs of `nxt` holding nothing unsignalled, "stuck": waits
+    # for them holding `held` unsignalled, "end"), the tickets in its ring
+    # (oldest first), the next ticket it will use, and the one it waits for.
+    blocks = [dict(s="start", held=[], pre=None, nxt=None) for _ in range(nblocks)]
+    while any(b["s"] != "end" for b in blocks):
         movable = [i for i, b in enumerate(blocks)
-                   if b[0] in ("start", "run")
-                   or (b[0] in ("first", "pending") and ready(b[1]))
-                   or (b[0] == "stuck" and ready(b[2]))]
+                   if b["s"] in ("start", "run")
+                   or (b["s"] in ("pending", "stuck") and ready(b["nxt"]))]
         if not movable:
             return False
-        i = rng.choice(movable)
-        b = blocks[i]
-        if b[0] == "start":
-            t, pre = take(fetch())
-            blocks[i] = ("end",) if t is None else ("first", t, pre)
-        elif b[0] in ("first", "pending"):
-            consume(b[1])
-            blocks[i] = ("run", b[1], b[2])
-        elif b[0] == "stuck":
-            consume(b[2])
-            signal(b[1])
-            blocks[i] = ("run", b[2], b[3])
+        b = blocks[rng.choice(movable)]
+        if b["s"] == "start":
+            b["pre"], b["s"] = fetch(), "run"
+        elif b["s"] in ("pending", "stuck"):
+            consume(b["nxt"])
+            for t in b["held"]:
+                signal(t)
+            b["held"], b["nxt"], b["s"] = [b["nxt"]], None, "run"
         else:
-            cur, pre = b[1], b[2]
-            nxt, pre = take(pre)
-            if nxt is not None and not ready(nxt) and wait_before_signal:
-                blocks[i] = ("stuck", cur, nxt, pre)
-                continue
-            pend = nxt is not None and not ready(nxt)
-            if nxt is not None and not pend:
+            freed = b["held"].pop(0) if len(b["held"]) == stages else None
+            nxt, b["pre"] = take(b["pre"])
+            if nxt is None:
+                for t in ([] if freed is None else [freed]) + b["held"]:
+                    signal(t)
+                b["held"], b["s"] = [], "end"
+            elif ready(nxt):
                 consume(nxt)
-            signal(cur)
-            blocks[i] = ("end",) if nxt is None else (("pending" if pend else "run"), nxt, pre)
+                if freed is not None:
+                    signal(freed)
+                b["held"].append(nxt)
+            else:
+                if freed is not None:
+                    b["held"].insert(0, freed)
+                if not wait_before_signal:
+                    for t in b["held"]:
+                        signal(t)
+                    b["held"] = []
+                b["nxt"], b["s"] = nxt, ("stuck" if wait_before_signal else "pending")
     assert len(done) == sum(1 for x in items if x is not None)
     assert not any(pushes.values()) and not any(reduced.values())   # words back at zero
     return True
 
 
-def test_every_schedule_finishes():
+@pytest.mark.parametrize("stages", [2, 3, 4])
+def test_every_schedule_finishes(stages):
     for seed in range(1500):
         r = random.Random(seed)
         P = r.choice([1, 2, 3, 4, 8])
@@ -122,14 +133,16 @@ def test_every_schedule_finishes():
         fused = r.choice([False, True])
         D = min(r.choice([0, 1, 2, 4]), tiles)
         nblocks = r.choice([1, 2, 3, 5, 9, 17])
-        assert _run(P, tiles, fused, D, nblocks, seed), (P, tiles, fused, D, nblocks, seed)
+        assert _run(P, tiles, fused, D, nblocks, seed, stages), \
+            (P, tiles, fused, D, nblocks, seed, stages)
 
 
+@pytest.mark.parametrize("stages", [2, 3])
 @pytest.mark.parametrize("fused", [True, False])
-def test_waiting_before_signalling_deadlocks(fused):
+def test_waiting_before_signalling_deadlocks(fused, stages):
     """The control: with two ranks the last push of a tile (rank 1 to owner 0)
     is an input of the first reduce, which comes next; one block that waited
     for that reduce's inputs before signalling the push would block on
     itself."""
-    assert not _run(2, 1, fused, 0, 1, 0, wait_before_signal=True)
-    assert _run(2, 1, fused, 0, 1, 0)
+    assert not _run(2, 1, fused, 0, 1, 0, stages, wait_before_signal=True)
+    assert _run(2, 1, fused, 0, 1, 0, stages)
