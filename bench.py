@@ -11,7 +11,8 @@ and g=128 (the pages quote their throughput figure for 1 GB messages), inputs
 resident in HBM before the timed region.  Every call runs libecho.so's default
 schedule through its C ABI: one kernel whose blocks each take a whole owner
 tile (the push of every sender, the owner's sum and the gather); the two- and
-three-kernel schedules of the same call are timed beside it.
+three-kernel schedules of the same call, the persistent single kernel and the
+default schedule with a bf16 compensator state are timed beside it.
 The same line also times, under "also", the 8-bit variant of that workload,
 the other workloads of 64 MiB per rank, and the latency of the smallest one
 (P=2, n=4096), plain and replayed as a CUDA graph.
@@ -533,6 +534,14 @@ def run_ours(args, rank, local, world):
                 if (f, t) != (fused, args.tile):
                     result["also"][f"{wname} ({label})"] = time_other(echo, number, bits, f, dev,
                                                                       args, tile=t)
+            # the persistent single kernel, and the 2-byte compensator state in
+            # the default schedule
+            variants = [("persistent single kernel", {"persistent": True}),
+                        ("bf16 compensator state", {"state": "bf16"})]
+            for label, over in variants:
+                if all(getattr(args, k) != v for k, v in over.items()) and not args.uncompensated:
+                    result["also"][f"{wname} ({label})"] = time_other(
+                        echo, number, bits, fused, dev, argparse.Namespace(**{**vars(args), **over}))
     del plan
     return result
 

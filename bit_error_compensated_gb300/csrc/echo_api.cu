@@ -301,7 +301,6 @@ int echo_allreduce(echo_plan_t plan, const void* const* in, void* const* out,
     echo::CallSched sch;
     sch.tiles = plan->tiles;
     sch.round = sch.lag = sch.total = 0;       // set by the launcher
-    sch.stages = 0;
     sch.hold = plan->hold;
     sch.push_done = plan->sched;
     sch.reduce_done = plan->sched + (int64_t)P * plan->tiles;

@@ -91,7 +91,6 @@ struct CallSched {
   uint32_t* push_done;    // [P][tiles] pushes of the tile finished in this call
   uint32_t* reduce_done;  // [P][tiles] the tile's reduce finished in this call
   uint32_t* ctrl;         // [0] ticket counter, [1] blocks finished, [2] abort
-  int stages;             // shared-memory stages of a block's ring (launcher)
 };
 // 32-bit words of a plan's schedule area.
 inline int64_t sched_words(int P, int64_t tiles) { return 2 * (int64_t)P * tiles + 4; }

@@ -19,13 +19,14 @@
 // words are zero again for the next call.
 //
 // A block is kThreads/32 compute warps and one control warp, which share a
-// ring of shared-memory stages (sch.stages of them, two or three, chosen at
-// launch), each with a "full" and an "empty" mbarrier.  The control warp's lane 0 does all the scheduling: it claims
-// tickets from one atomic counter (the next one fetched ahead), waits for an
-// item's inputs, fills a stage with the item's bulk copies (cp.async.bulk)
-// completing on its full barrier, and, once the compute warps have arrived on
-// the stage's empty barrier, publishes the item's completion to the other
-// blocks (a release add or store) and refills the stage.  The compute warps
+// ring of shared-memory stages (NS of them, two or three, chosen at launch),
+// each with a "full" and an "empty" mbarrier.  The control warp's lane 0 does
+// all the scheduling: it claims tickets from one atomic counter (the next one
+// fetched ahead), waits for an item's inputs, fills a stage with the item's
+// bulk copies (cp.async.bulk) completing on its full barrier, and, once the
+// compute warps have arrived on the stage's empty barrier, publishes the
+// item's completion to the other blocks (a release add or store) and refills
+// the stage.  The compute warps
 // only wait on full barriers, compute, and arrive on empty barriers: no block
 // barrier and no memory fence is ever on their path, so the latencies of the
 // claims, the flags and the release fences overlap the arithmetic.
@@ -193,7 +194,7 @@ __device__ __forceinline__ bool mbar_wait_or_abort(uint32_t bar, uint32_t parity
 
 template <int BITS, int SF, int MODE, int G, bool FUSED>
 __global__ void __launch_bounds__(kCallBlockThreads, ECHO_CALL_MIN_BLOCKS)
-call_kernel(const CallArgs a, const CallSched sch) {
+call_kernel(const CallArgs a, const CallSched sch, const int NS) {
   constexpr int T = tile_groups<G, kCallTileElems>();
   constexpr int NL = G / 16;
   constexpr int GPW = 32 / NL;
@@ -205,7 +206,6 @@ call_kernel(const CallArgs a, const CallSched sch) {
   __shared__ int64_t s_held[kCallMaxStages];     // control: ticket issued into each stage
 
   const int P = a.P;
-  const int NS = sch.stages;
   const int64_t Gs = a.Gs;
   const uint32_t sbytes = reduce_stage_bytes<BITS, SF, G, kCallTileElems>(P);
   const uint32_t full0 = smem_addr(&full[0]);
@@ -517,14 +517,14 @@ cudaError_t launch_t(const CallArgs& a, const CallSched& sch, cudaStream_t s) {
     cached.set(layout);
   }
   const int resident = layout / 8;
-  const size_t smem = (size_t)(layout % 8) * stage_bytes;
+  const int NS = layout % 8;
+  const size_t smem = (size_t)NS * stage_bytes;
   // Rounds of P(P-1) pushes, P reduces and (unfused) P gathers; the lag is
   // about kCallLagWaves waves of items in flight (one per stage of a block).
   CallSched sc = sch;
   const int P = a.P;
-  sc.stages = layout % 8;
   sc.round = (int64_t)P * (P - 1) + P + (FUSED ? 0 : P);
-  int64_t lag = (kCallLagWaves * sc.stages * (int64_t)resident + sc.round - 1) / sc.round;
+  int64_t lag = (kCallLagWaves * NS * (int64_t)resident + sc.round - 1) / sc.round;
   if (P == 1) lag = 0;                           // nothing to wait for
   sc.lag = lag < sc.tiles ? lag : sc.tiles;
   sc.total = sc.round * (sc.tiles + (FUSED ? 1 : 2) * sc.lag);
@@ -543,7 +543,7 @@ cudaError_t launch_t(const CallArgs& a, const CallSched& sch, cudaStream_t s) {
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, call_kernel<BITS, SF, MODE, G, FUSED>, a, sc);
+  return cudaLaunchKernelEx(&cfg, call_kernel<BITS, SF, MODE, G, FUSED>, a, sc, NS);
 }
 
 template <int MODE, int G>
