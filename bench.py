@@ -420,6 +420,9 @@ def run_ours(args, rank, local, world):
 
     launches_per_call = (1 if args.persistent or args.tile
                          else (2 if fused else 3) - (1 if P == 1 else 0))
+    parity = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        parity = first_calls_parity(args, xs, seq, prepared, out, stream)
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize(dev)
@@ -511,6 +514,8 @@ def run_ours(args, rank, local, world):
         "gpu_launches": launches_per_call * calls * reps * args.steps,
         "clocks": clk,
     }
+    if parity is not None:
+        result["parity"] = parity
 
     if not args.no_e2e:
         result["e2e"] = run_e2e(args, echo, plan, xs, seq, states, dev, world)
@@ -825,6 +830,7 @@ class OracleSample:
             src = "the workload's generator on the CPU"
         dev = xs.device if xs is not None else torch.device("cuda" if torch.cuda.is_available() else "cpu")
         idx_t = torch.from_numpy(idx).to(dev)
+        self.idx_t = idx_t          # the sampled elements' indices within a rank
         for k in range(distinct):
             if xs is not None:
                 x = xs[k % xs.shape[0]]
@@ -842,24 +848,30 @@ class OracleSample:
 
     def _chunk(self, x, e, a, b):
         import oracle
-        return oracle.group_positions(self.P, self.owners[a:b], self.bits, x[a:b],
-                                      None if e is None else e[a:b], **self.opts)["ties"]
+        r = oracle.group_positions(self.P, self.owners[a:b], self.bits, x[a:b],
+                                   None if e is None else e[a:b], **self.opts)
+        return r["ties"], r["y"]
 
-    def step(self, pool=None, threads=1):
+    def step(self, pool=None, threads=1, want_y=False):
         """One call over all sampled positions: on this thread, or split into
         `threads` contiguous chunks run by `pool` (the oracle call releases
-        the interpreter lock, so the chunks run on separate cores)."""
+        the interpreter lock, so the chunks run on separate cores).  With
+        want_y, returns the call's output at the sampled positions, [npos, g]
+        bf16 bits."""
+        import numpy as np
         x = self.inputs[self.i % len(self.inputs)]
         e = self.e.get(self.states[self.i % len(self.states)])
         npos = self.owners.size
         if pool is None or threads <= 1:
-            self.ties += self._chunk(x, e, 0, npos)
+            parts = [self._chunk(x, e, 0, npos)]
         else:
             cuts = [npos * t // threads for t in range(threads + 1)]
             futs = [pool.submit(self._chunk, x, e, cuts[t], cuts[t + 1]) for t in range(threads)
                     if cuts[t + 1] > cuts[t]]
-            self.ties += sum(f.result() for f in futs)
+            parts = [f.result() for f in futs]
+        self.ties += sum(t for t, _ in parts)
         self.i += 1
+        return np.concatenate([y for _, y in parts]) if want_y else None
 
 
 def oracle_sample(args, xs=None, seq=None):
@@ -875,6 +887,34 @@ def _time_steps(s, budget_s, pool=None, threads=1):
         s.step(pool, threads)
         steps += 1
     return steps, time.perf_counter() - t
+
+
+def first_calls_parity(args, xs, seq, prepared, out, stream, calls=2):
+    """The first `calls` calls of the timed configuration, from its fresh state,
+    against the oracle on the sampled group positions of OracleSample: every
+    rank's output there, bit for bit.  A later call's output depends on the
+    state the earlier calls left, so the state is checked through it."""
+    from concurrent.futures import ThreadPoolExecutor
+    import numpy as np
+    import torch
+    s = oracle_sample(args, xs, seq)
+    threads = host_cpu_info()["nproc"]
+    P, npos, g = s.P, s.owners.size, args.g
+    mismatches = compared = 0
+    with ThreadPoolExecutor(threads) as pool:
+        for k in range(calls):
+            prepared[k % len(prepared)](stream)
+            if out.is_cuda:
+                torch.cuda.synchronize(out.device)
+            got = out.index_select(1, s.idx_t).view(torch.int16).cpu().numpy().view(np.uint16)
+            want = s.step(pool, threads, want_y=True).reshape(1, npos * g)
+            mismatches += int(np.count_nonzero(got != want))
+            compared += got.size
+    return {"calls": calls, "sampled_groups": npos, "outputs_compared": compared,
+            "output_mismatches": mismatches, "exact_rounding_ties": s.ties,
+            "what": "the first calls of the timed configuration from its fresh state, every "
+                    "rank's output at the sampled group positions against the oracle, bit for "
+                    "bit (the later call's outputs depend on the state the first one left)"}
 
 
 def cpu_baseline_oracle(args, budget_s=12.0, xs=None, seq=None):

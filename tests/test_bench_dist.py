@@ -209,3 +209,46 @@ def test_kernel_source_hash_follows_code_not_comments(tmp_path, monkeypatch):
     q = csrc / "quant.cuh"
     q.write_text(q.read_text() + "\nnamespace echo { constexpr int kAlsoUnused = 2; }\n")
     assert bench.kernel_source_hash("reduce_kernel") != reduce0
+
+
+def test_first_calls_parity_compares_the_sampled_outputs():
+    """The bench's check of the timed configuration's first calls against the
+    oracle on the sampled positions, driven here by a stand-in for the GPU
+    call that runs the oracle's whole call on the CPU: no mismatch, over two
+    calls that carry the state; then a stand-in that changes one output bit
+    at a sampled position is caught."""
+    import numpy as np
+    import torch
+    import bench
+    import oracle
+    from bit_error_compensated_gb300.workloads import call_sequence, rank_inputs
+
+    class A:
+        workload, bits, g, quantizer, state, decay, tokens = 2, 4, 128, 0, "f32", 1.0, 8
+    seq = call_sequence(2)[:3]
+    P, n = 4, 8 * 4096
+    xs = torch.stack([rank_inputs(2, c, "cpu", tokens=8) for c in seq])
+    out = torch.empty((P, n), dtype=torch.bfloat16)
+
+    def calls(flip=None):
+        e = np.zeros((P, n), np.float32)
+        made = []
+
+        def make(k):
+            def call(stream):
+                x = xs[k].view(torch.int16).numpy().view(np.uint16)
+                y = oracle.allreduce(x, 128, 4, e=e)["out"].copy()
+                if flip is not None and len(made) == 1:       # the second call
+                    y[:, flip] ^= 1
+                out.view(torch.int16).copy_(torch.from_numpy(y.view(np.int16)))
+                made.append(k)
+            return call
+        return [make(k) for k in range(len(seq))]
+
+    r = bench.first_calls_parity(A(), xs, seq, calls(), out, None)
+    assert r["calls"] == 2 and r["output_mismatches"] == 0
+    assert r["outputs_compared"] == 2 * P * r["sampled_groups"] * 128
+    s = bench.oracle_sample(A(), xs, seq)
+    sampled = int(s.idx_t[5])
+    r = bench.first_calls_parity(A(), xs, seq, calls(flip=sampled), out, None)
+    assert r["output_mismatches"] == P
