@@ -26,10 +26,10 @@
 // bulk copies (cp.async.bulk) completing on its full barrier, and, once the
 // compute warps have arrived on the stage's empty barrier, publishes the
 // item's completion to the other blocks (a release add or store) and refills
-// the stage.  The compute warps
-// only wait on full barriers, compute, and arrive on empty barriers: no block
-// barrier and no memory fence is ever on their path, so the latencies of the
-// claims, the flags and the release fences overlap the arithmetic.
+// the stage.  The compute warps only wait on full barriers, compute, and
+// arrive on empty barriers: no block barrier and no memory fence is ever on
+// their path, so the latencies of the claims, the flags and the release
+// fences overlap the arithmetic.
 //
 // Deadlock freedom: an item only ever waits on items with smaller tickets,
 // the launch is cooperative (all blocks co-resident), and the control warp
@@ -151,7 +151,8 @@ constexpr int kCallBlockThreads = kThreads + 32;
 #define ECHO_CALL_MIN_BLOCKS 3
 #endif
 constexpr int64_t kSentinel = -1;              // no ticket held in a stage
-// Most stages a block's ring can have (the launcher picks 2 or 3).
+// Most stages a block's ring can have (the launcher picks 2 or 3 unless
+// ECHO_CALL_STAGES asks for more).
 constexpr int kCallMaxStages = 4;
 
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
